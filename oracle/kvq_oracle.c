@@ -1,0 +1,312 @@
+/*
+ * kvq oracle: a plain, slow, obviously correct CPU restatement of the quantized
+ * KV-cache hot path (quantize-on-write and single-token decode attention).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may build, load or call this file.  It shares no
+ * code, header, table or constant with the CUDA library: every table below is
+ * generated here from the format definitions.
+ *
+ * Sources (web pages; cited by title and section):
+ *  [TGI]  "Accelerating Inference with FP8 KV Cache" (text-generation-inference
+ *         docs): intro (KV stored in FP8, computation in FP16); section
+ *         "FP8 Formats: E4M3 and E5M2" (bit layouts, per-tensor fp32 scale);
+ *         section "FP8 E4M3 KV Cache" (default scale 1.0).
+ *  [LMD]  "[Feature] TurboMind support W8A8 or FP8 KV Cache" (lmdeploy issue
+ *         1463): online KV-cache INT8 (quant-policy 8).
+ *  OCP 8-bit floating point (named by [TGI]): E4M3 bias 7, no infinities,
+ *  NaN = S.1111.111, max 448; E5M2 bias 15, IEEE-like Inf/NaN, max 57344.
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *  - quantize divides by the scale, dequantize multiplies by it;
+ *  - fp32 -> FP8 rounds to nearest, ties to even, and saturates to +-max
+ *    (Inf included); NaN encodes to 0x7F;
+ *  - INT8 is symmetric, one fp32 scale per (token, kv-head) row:
+ *    s = fl32(amax / 127), q = clamp(rint(fl32(x / s)), -127, 127); amax == 0
+ *    gives s = 0 and all-zero codes;
+ *  - attention: logits l_t = sm_scale * <q, k_t> over all t < context_len,
+ *    softmax, out = sum_t w_t v_t; q-head h reads kv-head h / (Hq / Hkv);
+ *    context_len 0 gives zeros.
+ *
+ * Floating point: compile without fast-math and with -ffp-contract=off; every
+ * fp32 step below is one IEEE operation in fp32, everything else is fp64.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_E4M3 1
+#define ORC_E5M2 2
+#define ORC_INT8 3
+
+/* ---------------------------------------------------------------- fp16 ---- */
+
+/* IEEE binary16 bits -> value (1 sign, 5 exponent bits with bias 15, 10
+ * mantissa bits).  Every binary16 value is exact in fp32 and fp64. */
+static double half_bits_to_double(uint16_t h) {
+    int s = h >> 15, e = (h >> 10) & 31, m = h & 1023;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);               /* subnormal: m/1024 * 2^-14 */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp(1024.0 + (double)m, e - 25);   /* (1 + m/1024) * 2^(e-15) */
+    return s ? -v : v;
+}
+
+double oracle_half_to_double(uint16_t h) { return half_bits_to_double(h); }
+
+/* ----------------------------------------------------------------- FP8 ---- */
+
+/* [TGI] section "FP8 Formats": E4M3 = 1 sign, 4 biased exponent, 3 mantissa
+ * bits; E5M2 = 1 sign, 5 biased exponent, 2 mantissa bits.  Values from the OCP
+ * definitions named there. */
+double oracle_fp8_decode(int fmt, uint8_t c) {
+    int s = c >> 7;
+    double v;
+    if (fmt == ORC_E4M3) {
+        int e = (c >> 3) & 15, m = c & 7;
+        if (e == 15 && m == 7) return NAN;       /* the only NaN pattern; no Inf */
+        v = (e == 0) ? ldexp((double)m, -9)      /* m/8 * 2^-6 */
+                     : ldexp(8.0 + m, e - 10);   /* (1 + m/8) * 2^(e-7) */
+    } else if (fmt == ORC_E5M2) {
+        int e = (c >> 2) & 31, m = c & 3;
+        if (e == 31) return m ? NAN : (s ? -INFINITY : INFINITY);
+        v = (e == 0) ? ldexp((double)m, -16)     /* m/4 * 2^-14 */
+                     : ldexp(4.0 + m, e - 17);   /* (1 + m/4) * 2^(e-15) */
+    } else {
+        return NAN;
+    }
+    return s ? -v : v;
+}
+
+/* Positive finite values of a format, sorted ascending, with their codes.
+ * Built by decoding all 128 sign-0 codes and sorting by value; nothing assumes
+ * that code order equals value order. */
+typedef struct { double v; uint8_t code; } fp8_entry;
+static fp8_entry g_tab[3][128];
+static int g_ntab[3];
+
+static int cmp_entry(const void* a, const void* b) {
+    double x = ((const fp8_entry*)a)->v, y = ((const fp8_entry*)b)->v;
+    return (x > y) - (x < y);
+}
+
+static const fp8_entry* fp8_table(int fmt, int* n) {
+    int i = fmt - 1;
+    if (g_ntab[i] == 0) {
+        int k = 0;
+        for (int c = 0; c < 128; ++c) {
+            double v = oracle_fp8_decode(fmt, (uint8_t)c);
+            if (isfinite(v)) { g_tab[i][k].v = v; g_tab[i][k].code = (uint8_t)c; ++k; }
+        }
+        qsort(g_tab[i], (size_t)k, sizeof(fp8_entry), cmp_entry);
+        g_ntab[i] = k;
+    }
+    *n = g_ntab[i];
+    return g_tab[i];
+}
+
+/* Must be called once before any parallel use of the encoder. */
+void oracle_init(void) {
+    int n;
+    fp8_table(ORC_E4M3, &n);
+    fp8_table(ORC_E5M2, &n);
+}
+
+/* fp32 -> FP8 code: nearest representable value, ties to the code with an even
+ * mantissa LSB, saturating to +-max (Inf too); signed zero for values that round
+ * to zero; NaN -> 0x7F. */
+uint8_t oracle_fp8_encode(int fmt, float y) {
+    if (isnan(y)) return 0x7F;
+    int n;
+    const fp8_entry* t = fp8_table(fmt, &n);
+    uint8_t sign = signbit(y) ? 0x80 : 0x00;
+    double a = fabs((double)y);
+    if (a >= t[n - 1].v) return sign | t[n - 1].code;
+    /* binary search: largest i with t[i].v <= a  (t[0].v == 0 <= a) */
+    int lo = 0, hi = n - 1;                   /* invariant: t[lo].v <= a < t[hi].v */
+    while (hi - lo > 1) {
+        int mid = (lo + hi) / 2;
+        if (t[mid].v <= a) lo = mid; else hi = mid;
+    }
+    double midpoint = 0.5 * (t[lo].v + t[hi].v);   /* exact: dyadic, few bits */
+    uint8_t code;
+    if (a < midpoint) code = t[lo].code;
+    else if (a > midpoint) code = t[hi].code;
+    else code = (t[lo].code & 1) ? t[hi].code : t[lo].code;
+    return sign | code;
+}
+
+void oracle_fp8_encode_array(int fmt, const float* y, uint8_t* out, int64_t n) {
+    oracle_init();
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_fp8_encode(fmt, y[i]);
+}
+
+/* ---------------------------------------------------------------- INT8 ---- */
+
+/* [LMD] online KV INT8, symmetric reading: one fp32 scale per row of D values.
+ * x: D fp32 values; writes D codes and returns the scale. */
+static float int8_quant_row(const float* x, int D, int8_t* q) {
+    float amax = 0.0f;
+    for (int d = 0; d < D; ++d) {
+        float ax = fabsf(x[d]);
+        if (ax > amax) amax = ax;
+    }
+    float s = amax / 127.0f;
+    for (int d = 0; d < D; ++d) {
+        if (s == 0.0f) { q[d] = 0; continue; }
+        float y = x[d] / s;
+        float r = rintf(y);                      /* ties to even (default mode) */
+        if (r > 127.0f) r = 127.0f;
+        if (r < -127.0f) r = -127.0f;
+        q[d] = (int8_t)r;
+    }
+    return s;
+}
+
+float oracle_int8_quant_row(const float* x, int D, int8_t* q) { return int8_quant_row(x, D, q); }
+
+/* -------------------------------------------------------------- append ---- */
+
+/* Quantize-on-write.  k, v: fp16 bits [T][Hkv][D].  The paged cache holds codes
+ * [NB][Hkv][BS][D] (u8 FP8 / i8 INT8) and, for INT8 only, scales [NB][Hkv][BS].
+ * Token t goes to block slot[t] / BS, row slot[t] % BS; slot -1 is skipped.
+ * scale: per-tensor fp32 scale (FP8 only; [TGI] default 1.0 applies when the
+ * caller passes none).  Returns 0, or -1 on a slot outside the cache. */
+int oracle_append(const uint16_t* k, const uint16_t* v, int64_t T, int Hkv, int D,
+                  const int64_t* slot_mapping, uint8_t* k_codes, uint8_t* v_codes,
+                  float* k_scales, float* v_scales, int64_t NB, int BS, int fmt,
+                  float scale) {
+    oracle_init();
+    int bad = 0;
+    float* x = (float*)malloc(sizeof(float) * (size_t)D);
+    for (int64_t t = 0; t < T; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot == -1) continue;
+        if (slot < 0 || slot >= NB * BS) { bad = 1; continue; }
+        int64_t blk = slot / BS, off = slot % BS;
+        for (int h = 0; h < Hkv; ++h) {
+            for (int which = 0; which < 2; ++which) {
+                const uint16_t* src = (which ? v : k) + ((size_t)t * Hkv + h) * D;
+                uint8_t* dst = (which ? v_codes : k_codes) + (((size_t)blk * Hkv + h) * BS + off) * D;
+                for (int d = 0; d < D; ++d) x[d] = (float)half_bits_to_double(src[d]);
+                if (fmt == ORC_INT8) {
+                    float* sc = which ? v_scales : k_scales;
+                    sc[((size_t)blk * Hkv + h) * BS + off] = int8_quant_row(x, D, (int8_t*)dst);
+                } else {
+                    for (int d = 0; d < D; ++d) dst[d] = oracle_fp8_encode(fmt, x[d] / scale);
+                }
+            }
+        }
+    }
+    free(x);
+    return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------- dequant ---- */
+
+/* Dequantize-on-read of one cached value: FP8 fl32(decode(c) * s) with the
+ * per-tensor scale, INT8 fl32(q * s_row). */
+static float dequant_value(int fmt, uint8_t c, float s) {
+    if (fmt == ORC_INT8) return (float)(int8_t)c * s;
+    return (float)oracle_fp8_decode(fmt, c) * s;
+}
+
+/* Gather + dequantize rows at the given slots: out [n][Hkv][D] fp32 (K and V). */
+int oracle_dequant(const uint8_t* k_codes, const uint8_t* v_codes, const float* k_scales,
+                   const float* v_scales, int64_t NB, int BS, int Hkv, int D, int fmt,
+                   const int64_t* slots, int64_t n, float scale, float* out_k, float* out_v) {
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t slot = slots[i];
+        if (slot < 0 || slot >= NB * BS) return -1;
+        int64_t blk = slot / BS, off = slot % BS;
+        for (int h = 0; h < Hkv; ++h) {
+            size_t row = ((size_t)blk * Hkv + h) * BS + off;
+            float sk = fmt == ORC_INT8 ? k_scales[row] : scale;
+            float sv = fmt == ORC_INT8 ? v_scales[row] : scale;
+            for (int d = 0; d < D; ++d) {
+                out_k[((size_t)i * Hkv + h) * D + d] = dequant_value(fmt, k_codes[row * D + d], sk);
+                out_v[((size_t)i * Hkv + h) * D + d] = dequant_value(fmt, v_codes[row * D + d], sv);
+            }
+        }
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------- attention ---- */
+
+/* Single-token decode attention over the paged quantized cache, in fp64 on the
+ * fp32-dequantized values.  q: fp16 bits [B][Hq][D], D <= 512.  block_tables int32
+ * [B][max_blocks]; context_lens int32 [B].  out: fp64 [B][Hq][D].  weights
+ * (optional, may be NULL): fp64 [B][Hq][w_stride], the softmax weights.
+ * Returns 0, or -1 on a block id / context length outside the cache or table. */
+int oracle_decode_attention(const uint16_t* q, int B, int Hq, int D,
+                            const uint8_t* k_codes, const uint8_t* v_codes,
+                            const float* k_scales, const float* v_scales,
+                            int64_t NB, int BS, int Hkv, int fmt,
+                            const int32_t* block_tables, int max_blocks,
+                            const int32_t* context_lens, float scale, double sm_scale,
+                            double* out, double* weights, int64_t w_stride) {
+    int G = Hq / Hkv;
+    int bad = 0;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1) reduction(| : bad)
+    for (int b = 0; b < B; ++b) {
+        for (int h = 0; h < Hq; ++h) {
+            int kvh = h / G;
+            int ctx = context_lens[b];
+            double* o = out + ((size_t)b * Hq + h) * D;
+            for (int d = 0; d < D; ++d) o[d] = 0.0;
+            if (ctx <= 0) continue;
+            if ((int64_t)ctx > (int64_t)max_blocks * BS) { bad = 1; continue; }
+            double qv[512];
+            for (int d = 0; d < D; ++d) qv[d] = half_bits_to_double(q[((size_t)b * Hq + h) * D + d]);
+            double* logit = (double*)malloc(sizeof(double) * (size_t)ctx);
+            int ok = 1;
+            for (int t = 0; t < ctx && ok; ++t) {
+                int32_t blk = block_tables[(size_t)b * max_blocks + t / BS];
+                if (blk < 0 || blk >= NB) { ok = 0; break; }
+                size_t row = ((size_t)blk * Hkv + kvh) * BS + t % BS;
+                float sk = fmt == ORC_INT8 ? k_scales[row] : scale;
+                double acc = 0.0;
+                for (int d = 0; d < D; ++d)
+                    acc += qv[d] * (double)dequant_value(fmt, k_codes[row * D + d], sk);
+                logit[t] = sm_scale * acc;
+            }
+            if (!ok) { bad = 1; free(logit); continue; }
+            double m = -INFINITY;
+            for (int t = 0; t < ctx; ++t) if (logit[t] > m) m = logit[t];
+            double denom = 0.0;
+            for (int t = 0; t < ctx; ++t) { logit[t] = exp(logit[t] - m); denom += logit[t]; }
+            for (int t = 0; t < ctx; ++t) {
+                double w = logit[t] / denom;
+                if (weights) weights[((size_t)b * Hq + h) * w_stride + t] = w;
+                int32_t blk = block_tables[(size_t)b * max_blocks + t / BS];
+                size_t row = ((size_t)blk * Hkv + kvh) * BS + t % BS;
+                float sv = fmt == ORC_INT8 ? v_scales[row] : scale;
+                for (int d = 0; d < D; ++d)
+                    o[d] += w * (double)dequant_value(fmt, v_codes[row * D + d], sv);
+            }
+            free(logit);
+        }
+    }
+    return bad ? -1 : 0;
+}
+
+int oracle_num_threads(void) {
+    int n = 1;
+#ifdef _OPENMP
+#pragma omp parallel
+    {
+#pragma omp single
+        n = omp_get_num_threads();
+    }
+#endif
+    return n;
+}
