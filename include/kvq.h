@@ -1,0 +1,159 @@
+/*
+ * kvq.h -- C ABI of the GB300 (sm_103a) quantized paged KV cache.
+ *
+ * Two operations make up the hot path of an LLM server's quantized KV cache:
+ *
+ *   kvq_append            quantize-on-write of fp16 K/V into the paged cache;
+ *   kvq_decode_attention  single-token decode attention that dequantizes the
+ *                         cache on read and computes in fp16/fp32.
+ *
+ * plus kvq_dequant, a debugging gather that returns the fp32 values a kernel
+ * sees.  The operations follow these pages (cited by title and section):
+ *
+ *   [TGI] "Accelerating Inference with FP8 KV Cache" (text-generation-inference
+ *         docs).  Intro: the KV cache is stored in FP8 while computation runs in
+ *         FP16.  "FP8 Formats: E4M3 and E5M2": E4M3 = 1 sign, 4 biased exponent,
+ *         3 mantissa bits; E5M2 = 1 sign, 5 biased exponent, 2 mantissa bits;
+ *         one fp32 scaling factor per quantized tensor (per-tensor scalar).
+ *         "FP8 E4M3 KV Cache": a scale of 1.0 is used when none is given.
+ *         "Checkpoint structure for KV scales": one kv_scale per attention layer,
+ *         shared by K and V.  "Current Hardware Support": NVIDIA GPUs take
+ *         E4M3 ("fp8") and E5M2 ("fp8_e5m2").
+ *   [LMD] "[Feature] TurboMind support W8A8 or FP8 KV Cache" (lmdeploy issue
+ *         1463): online KV-cache INT8 (quant-policy 8) as the alternative.
+ *
+ * Conventions for every call:
+ *   - Every pointer argument is a DEVICE pointer owned by the caller, except the
+ *     kvq_cache descriptor itself (a host struct read during the call only).
+ *     The library allocates no memory and frees none.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream) and
+ *     never synchronize the host, except kvq_device_error_check.
+ *   - Arguments are validated before any launch; a call that returns an error
+ *     status has launched nothing and written nothing.
+ *   - fp16 tensors are IEEE binary16, row-major, 16-byte aligned.
+ *   - A kernel that meets a slot or block id outside the cache skips that
+ *     access and records it in a device error word; kvq_device_error_check
+ *     reports it.  No kernel traps.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVQ_ABI_VERSION 1
+
+/* Same object as cudaStream_t; declared here so the header needs no CUDA include. */
+typedef struct CUstream_st* kvq_stream_t;
+
+/* Cache formats.  [TGI] "Current Hardware Support": "fp8" = E4M3 (OCP
+ * E4M3FN: no infinities, S.1111.111 = NaN, max 448) and "fp8_e5m2" = E5M2
+ * (max 57344); [LMD]: online INT8. */
+typedef enum {
+    KVQ_E4M3 = 1,
+    KVQ_E5M2 = 2,
+    KVQ_INT8 = 3
+} kvq_fmt;
+
+typedef enum {
+    KVQ_OK = 0,
+    KVQ_ERR_INVALID_ARG = 1,   /* null / misaligned pointer, bad size, fmt mismatch */
+    KVQ_ERR_UNSUPPORTED = 2,   /* head_dim, block_size or q-group size not built */
+    KVQ_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required */
+    KVQ_ERR_OUT_OF_RANGE = 4,  /* a kernel met a slot / block id outside the cache */
+    KVQ_ERR_TIMEOUT = 5,       /* a kernel's bounded wait ran out (never expected) */
+    KVQ_ERR_CUDA = 6           /* a CUDA runtime call or launch failed */
+} kvq_status;
+
+/* The paged cache: caller-owned device memory.
+ *   k_codes, v_codes: [num_blocks][num_kv_heads][block_size][head_dim] bytes,
+ *                     FP8 codes (u8) or INT8 codes (i8); 16-byte aligned.
+ *   k_scales, v_scales: INT8 only, fp32 [num_blocks][num_kv_heads][block_size]
+ *                     (one scale per (token, kv-head) row); NULL for FP8.
+ *   head_dim in {64, 128}; block_size in {16, 32, 64}; fmt a kvq_fmt. */
+typedef struct {
+    void* k_codes;
+    void* v_codes;
+    float* k_scales;
+    float* v_scales;
+    int32_t num_blocks;
+    int32_t block_size;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t fmt;
+} kvq_cache;
+
+/* Quantize-on-write ([TGI] intro and "FP8 Formats"; [LMD] online INT8).
+ *   k, v: fp16 [num_tokens][num_kv_heads][head_dim].
+ *   slot_mapping: int64 [num_tokens]; token t goes to block slot / block_size,
+ *     row slot % block_size; slot -1 skips the token (padding).
+ *   scale: FP8 only -- device pointer to ONE fp32 per-tensor scale shared by K
+ *     and V, or NULL for the default 1.0 ([TGI] "FP8 E4M3 KV Cache").  Each
+ *     element is stored as code = RNE-satfinite(fl32(x / scale)).  Ignored for
+ *     INT8, where each (token, kv-head) row gets s = fl32(amax / 127) and codes
+ *     clamp(rint(fl32(x / s)), -127, 127) (s = 0 and zero codes for a zero row).
+ *   fmt must equal cache->fmt.  num_tokens == 0 is a no-op. */
+kvq_status kvq_append(const void* k, const void* v, const kvq_cache* cache,
+                      const int64_t* slot_mapping, int64_t num_tokens,
+                      const float* scale, int32_t fmt, kvq_stream_t stream);
+
+/* Bytes of workspace kvq_decode_attention needs for these sizes on the
+ * current device (0 when no context split happens).  partition_size as below. */
+size_t kvq_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t max_context_len,
+                                 int32_t partition_size);
+
+/* Single-token decode attention over the paged quantized cache ([TGI] intro:
+ * stored quantized, computed in FP16; accumulation here is fp32).
+ *   q:   fp16 [batch][num_q_heads][head_dim].
+ *   block_tables: int32 [batch][max_blocks_per_seq]; entry i of sequence b is
+ *     the physical block holding its tokens i*block_size .. (i+1)*block_size-1.
+ *   context_lens: int32 [batch], each in [0, max_context_len]; every token
+ *     t < context_len attends (the new token is appended first).  A sequence
+ *     with context 0 gets a zero output.
+ *   q-head h reads kv-head h / (num_q_heads / num_kv_heads); num_q_heads must be
+ *     a multiple of num_kv_heads and the group size at most 8.
+ *   scale: FP8 per-tensor scale as in kvq_append (NULL = 1.0); ignored for INT8.
+ *   sm_scale: softmax scale; 0 selects 1 / sqrt(head_dim).
+ *   out: fp16 [batch][num_q_heads][head_dim] = softmax(sm_scale * q K^T) V.
+ *   workspace: device scratch of kvq_decode_workspace_size() bytes (may be NULL
+ *     when that size is 0), 256-byte aligned; contents are not preserved.
+ *   partition_size: tokens per context split (a multiple of 64, at most 8192),
+ *     or 0 to let the library choose from the sizes and the device's SM count. */
+kvq_status kvq_decode_attention(const void* q, const kvq_cache* cache,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* context_lens, int32_t batch,
+                                int32_t num_q_heads, int32_t max_context_len,
+                                const float* scale, int32_t fmt, float sm_scale, void* out,
+                                void* workspace, size_t workspace_bytes,
+                                int32_t partition_size, kvq_stream_t stream);
+
+/* Debug gather + dequantize-on-read: for each of num_slots slots, fp32
+ * [num_slots][num_kv_heads][head_dim] rows of K and V, each value
+ * fl32(decode(code) * scale) (FP8) or fl32(code * row_scale) (INT8). */
+kvq_status kvq_dequant(const kvq_cache* cache, const int64_t* slots, int64_t num_slots,
+                       const float* scale, int32_t fmt, float* out_k, float* out_v,
+                       kvq_stream_t stream);
+
+/* Decode kernel family used by kvq_decode_attention in this process:
+ * 0 = automatic (tensor-core kernel), 1 = CUDA-core kernel (group size <= 4),
+ * 2 = tensor-core kernel.  A tuning and cross-checking knob; returns the
+ * previous value, or -1 for an unknown kind (nothing changes). */
+int32_t kvq_set_decode_kernel(int32_t kind);
+
+/* Synchronizes `stream`, then reads and clears the current device's error word.
+ * Returns KVQ_OK, KVQ_ERR_OUT_OF_RANGE or KVQ_ERR_TIMEOUT (the first one
+ * recorded); *detail (if not NULL) receives the offending slot / block id. */
+kvq_status kvq_device_error_check(kvq_stream_t stream, int64_t* detail);
+
+const char* kvq_status_string(kvq_status status);
+int32_t kvq_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVQ_H */
