@@ -1,0 +1,76 @@
+// Debug gather + dequantize-on-read: the fp32 values the decode kernels see.
+// FP8: fl32(decode(code) * scale) with the per-tensor scale ("Accelerating
+// Inference with FP8 KV Cache", "FP8 Formats: E4M3 and E5M2"); INT8:
+// fl32(code * row_scale).  One thread per 16 values of one (slot, kv-head) row.
+#include "kvq_device.cuh"
+#include "kvq_launch.h"
+
+namespace kvq {
+namespace {
+
+constexpr int kThreads = 256;
+
+template <int FMT, int D>
+__global__ void __launch_bounds__(kThreads) dequant_kernel(DequantArgs a) {
+    constexpr int CPR = D / 16;
+    const int Hkv = a.cache.num_kv_heads;
+    const int64_t per = a.num_slots * Hkv * CPR;
+    const int64_t idx = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int which = blockIdx.y;
+    if (idx >= per) return;
+    const int c = (int)(idx % CPR);
+    const int64_t row = idx / CPR;  // slot index * Hkv + head
+    const int64_t i = row / Hkv;
+    const int h = (int)(row % Hkv);
+    const int64_t slot = a.slots[i];
+    const int64_t BS = a.cache.block_size;
+    float* out = (which ? a.out_v : a.out_k) + row * D + c * 16;
+    if (slot < 0 || slot >= (int64_t)a.cache.num_blocks * BS) {
+        if (c == 0 && which == 0 && h == 0) record_error(a.err, DEV_ERR_RANGE, slot);
+        return;
+    }
+    const int64_t src_row = ((slot / BS) * Hkv + h) * BS + slot % BS;
+    const uint4 r = *reinterpret_cast<const uint4*>((which ? a.cache.v_codes : a.cache.k_codes) +
+                                                    src_row * D + c * 16);
+    const float s = FMT == INT8 ? (which ? a.cache.v_scales : a.cache.k_scales)[src_row]
+                                : (a.scale ? __ldg(a.scale) : 1.0f);
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+    float y[16];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float2 lo = f16x2_to_f32x2(dec_x2<FMT>((uint16_t)(w[j] & 0xFFFF)));
+        float2 hi = f16x2_to_f32x2(dec_x2<FMT>((uint16_t)(w[j] >> 16)));
+        y[4 * j] = lo.x * s;
+        y[4 * j + 1] = lo.y * s;
+        y[4 * j + 2] = hi.x * s;
+        y[4 * j + 3] = hi.y * s;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        reinterpret_cast<float4*>(out)[j] = make_float4(y[4 * j], y[4 * j + 1], y[4 * j + 2], y[4 * j + 3]);
+}
+
+template <int FMT>
+cudaError_t launch_fmt(const DequantArgs& a, cudaStream_t s) {
+    const int D = a.cache.head_dim;
+    const int64_t per = a.num_slots * a.cache.num_kv_heads * (D / 16);
+    dim3 grid((unsigned)((per + kThreads - 1) / kThreads), 2);
+    if (D == 64)
+        dequant_kernel<FMT, 64><<<grid, kThreads, 0, s>>>(a);
+    else
+        dequant_kernel<FMT, 128><<<grid, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t s) {
+    if (a.num_slots == 0) return cudaSuccess;
+    switch (a.cache.fmt) {
+        case E4M3: return launch_fmt<E4M3>(a, s);
+        case E5M2: return launch_fmt<E5M2>(a, s);
+        default: return launch_fmt<INT8>(a, s);
+    }
+}
+
+}  // namespace kvq

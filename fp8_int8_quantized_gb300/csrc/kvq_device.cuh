@@ -143,8 +143,9 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
-// Bounded wait: gives up after kWaitLimitNs (or as soon as *abort is set) and
-// returns false.  Every spin in this library goes through here.
+// Bounded wait: gives up after kWaitLimitNs (or as soon as *abort is set, when
+// abort is not null) and returns false.  Every spin in this library goes
+// through here.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
@@ -153,7 +154,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 0) {
-            if (*abort) return false;
+            if (abort && *abort) return false;
             if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
         }
     }

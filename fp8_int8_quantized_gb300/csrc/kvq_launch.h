@@ -1,0 +1,75 @@
+// Internal interface between the C-ABI layer (kvq_api.cu) and the kernel
+// translation units.  Arguments arrive here already validated.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __CUDACC__
+#define KVQ_HD __host__ __device__
+#else
+#define KVQ_HD
+#endif
+
+namespace kvq {
+
+struct CacheView {
+    uint8_t* k_codes;
+    uint8_t* v_codes;
+    float* k_scales;
+    float* v_scales;
+    int32_t num_blocks, block_size, num_kv_heads, head_dim, fmt;
+};
+
+struct AppendArgs {
+    const uint16_t* k;  // fp16 bits [T][Hkv][D]
+    const uint16_t* v;
+    CacheView cache;
+    const int64_t* slot_mapping;
+    int64_t num_tokens;
+    const float* scale;  // device, may be null (= 1.0)
+    unsigned long long* err;
+};
+
+struct DequantArgs {
+    CacheView cache;
+    const int64_t* slots;
+    int64_t num_slots;
+    const float* scale;
+    float* out_k;
+    float* out_v;
+    unsigned long long* err;
+};
+
+struct DecodeArgs {
+    const uint16_t* q;  // fp16 bits [B][Hq][D]
+    CacheView cache;
+    const int32_t* block_tables;
+    int32_t max_blocks_per_seq;
+    const int32_t* context_lens;
+    int32_t batch, num_q_heads, max_context_len;
+    const float* scale;  // device, may be null (= 1.0); FP8 only
+    float sm_scale;      // resolved (> 0)
+    uint16_t* out;       // fp16 bits [B][Hq][D]
+    float* ws;           // partials, or null when num_parts == 1
+    int32_t partition_size;
+    int32_t num_parts;
+    int32_t kernel;      // 1 = CUDA-core, 2 = tensor-core
+    unsigned long long* err;
+};
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
+cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+
+// Workspace layout of the context split: acc fp32 [B][Hq][P][D] followed by
+// (m, l) fp32 pairs [B][Hq][P], the second part 256-byte aligned.
+KVQ_HD inline size_t ws_acc_bytes(int64_t B, int64_t Hq, int64_t P, int64_t D) {
+    return ((size_t)(B * Hq * P * D) * 4 + 255) / 256 * 256;
+}
+KVQ_HD inline size_t ws_bytes(int64_t B, int64_t Hq, int64_t P, int64_t D) {
+    return ws_acc_bytes(B, Hq, P, D) + ((size_t)(B * Hq * P) * 8 + 255) / 256 * 256;
+}
+
+}  // namespace kvq

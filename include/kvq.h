@@ -47,6 +47,12 @@ extern "C" {
 
 #define KVQ_ABI_VERSION 1
 
+#if defined(__GNUC__)
+#define KVQ_API __attribute__((visibility("default")))
+#else
+#define KVQ_API
+#endif
+
 /* Same object as cudaStream_t; declared here so the header needs no CUDA include. */
 typedef struct CUstream_st* kvq_stream_t;
 
@@ -97,13 +103,13 @@ typedef struct {
  *     INT8, where each (token, kv-head) row gets s = fl32(amax / 127) and codes
  *     clamp(rint(fl32(x / s)), -127, 127) (s = 0 and zero codes for a zero row).
  *   fmt must equal cache->fmt.  num_tokens == 0 is a no-op. */
-kvq_status kvq_append(const void* k, const void* v, const kvq_cache* cache,
+KVQ_API kvq_status kvq_append(const void* k, const void* v, const kvq_cache* cache,
                       const int64_t* slot_mapping, int64_t num_tokens,
                       const float* scale, int32_t fmt, kvq_stream_t stream);
 
 /* Bytes of workspace kvq_decode_attention needs for these sizes on the
  * current device (0 when no context split happens).  partition_size as below. */
-size_t kvq_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+KVQ_API size_t kvq_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                  int32_t head_dim, int32_t max_context_len,
                                  int32_t partition_size);
 
@@ -124,7 +130,7 @@ size_t kvq_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num
  *     when that size is 0), 256-byte aligned; contents are not preserved.
  *   partition_size: tokens per context split (a multiple of 64, at most 8192),
  *     or 0 to let the library choose from the sizes and the device's SM count. */
-kvq_status kvq_decode_attention(const void* q, const kvq_cache* cache,
+KVQ_API kvq_status kvq_decode_attention(const void* q, const kvq_cache* cache,
                                 const int32_t* block_tables, int32_t max_blocks_per_seq,
                                 const int32_t* context_lens, int32_t batch,
                                 int32_t num_q_heads, int32_t max_context_len,
@@ -135,7 +141,7 @@ kvq_status kvq_decode_attention(const void* q, const kvq_cache* cache,
 /* Debug gather + dequantize-on-read: for each of num_slots slots, fp32
  * [num_slots][num_kv_heads][head_dim] rows of K and V, each value
  * fl32(decode(code) * scale) (FP8) or fl32(code * row_scale) (INT8). */
-kvq_status kvq_dequant(const kvq_cache* cache, const int64_t* slots, int64_t num_slots,
+KVQ_API kvq_status kvq_dequant(const kvq_cache* cache, const int64_t* slots, int64_t num_slots,
                        const float* scale, int32_t fmt, float* out_k, float* out_v,
                        kvq_stream_t stream);
 
@@ -143,15 +149,15 @@ kvq_status kvq_dequant(const kvq_cache* cache, const int64_t* slots, int64_t num
  * 0 = automatic (tensor-core kernel), 1 = CUDA-core kernel (group size <= 4),
  * 2 = tensor-core kernel.  A tuning and cross-checking knob; returns the
  * previous value, or -1 for an unknown kind (nothing changes). */
-int32_t kvq_set_decode_kernel(int32_t kind);
+KVQ_API int32_t kvq_set_decode_kernel(int32_t kind);
 
 /* Synchronizes `stream`, then reads and clears the current device's error word.
  * Returns KVQ_OK, KVQ_ERR_OUT_OF_RANGE or KVQ_ERR_TIMEOUT (the first one
  * recorded); *detail (if not NULL) receives the offending slot / block id. */
-kvq_status kvq_device_error_check(kvq_stream_t stream, int64_t* detail);
+KVQ_API kvq_status kvq_device_error_check(kvq_stream_t stream, int64_t* detail);
 
-const char* kvq_status_string(kvq_status status);
-int32_t kvq_abi_version(void);
+KVQ_API const char* kvq_status_string(kvq_status status);
+KVQ_API int32_t kvq_abi_version(void);
 
 #ifdef __cplusplus
 }
