@@ -1,0 +1,514 @@
+#!/usr/bin/env python3
+"""Benchmark of the quantized paged KV-cache hot path on GB300.
+
+One step = one layer's serving decode step over a resident paged cache:
+kvq_append of the step's new K/V (the decode token of every sequence, or the
+workload's prefill chunk) followed by kvq_decode_attention for every sequence.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...     # the CPU oracle, timed on host cores
+
+Prints ONE JSON line (rank 0).  ``value`` is decode KV-read GB/s: the
+algorithmic bytes of the decode calls (every cached K/V byte of every context
+once, INT8 row scales, q, out, block tables) over the step time, summed over
+ranks (each rank runs its own copy of the workload: weak scaling, no
+collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "quantized-KV decode attention: KV-read GB/s and % of GB300 HBM peak; tokens/s"
+DEFAULT_WORKLOAD = "llama2-7b"
+L2_BYTES = 129 * 1024 * 1024
+DEFAULT_STEPS = {"tiny": 2000, "llama2-7b": 10000, "llama3-8b": 10000, "llama2-13b-int8": 1000,
+                 "llama3-70b": 300}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=0, help="timed steps (0: workload default)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
+    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "mma"])
+    ap.add_argument("--partition", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU-baseline sample time")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------- distributed --
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(local_ms: float, local_units: float, world: int, group=None):
+    """Whole-job numbers: the slowest rank's time and the units of all ranks."""
+    if world == 1:
+        return local_ms, local_units
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([local_ms], dtype=torch.float64, device=dev)
+    u = torch.tensor([local_units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item()), float(u.item())
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while it runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        except OSError:
+            pass
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- helpers --
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("kvq_decode.cu", "kvq_device.cuh", "kvq_launch.h"):
+        with open(os.path.join(ROOT, "fp8_int8_quantized_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """Per-launch DRAM bytes of the decode split kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.txt")
+    try:
+        for line in open(path):
+            line = line.split("#", 1)[0].split()
+            if len(line) >= 3 and line[0] == workload and line[1] == kernel_source_hash():
+                return float(line[2])
+    except OSError:
+        pass
+    return None
+
+
+class Setup:
+    """A workload's resident cache plus the step's inputs, all on the device."""
+
+    def __init__(self, wl, device, partition):
+        import torch
+
+        import fp8_int8_quantized_gb300 as kvq
+        from fp8_int8_quantized_gb300 import workloads as W
+        self.wl, self.device = wl, device
+        self.lay = W.Layout(wl)
+        ctx_max = self.lay.max_context_len
+        step_tok = wl.append_chunk if wl.append_chunk else 1
+        self.cache = kvq.KVCache(self.lay.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim, wl.fmt, device)
+        windows = W.chunk_positions(wl, 1 << 19)
+        k0, v0 = W.kv_tokens(wl, *windows[0], device=device)
+        sv = W.calibration_scale(wl, k0, v0)
+        del k0, v0
+        self.scale_value = sv
+        self.scale = None if sv is None else torch.tensor([sv], dtype=torch.float32, device=device)
+        # every position before the step's own tokens, untimed
+        cl = self.lay.context_lens
+        for p0, p1 in windows:
+            k, v = W.kv_tokens(wl, p0, p1, device)
+            slots = self.lay.slots(p0, p1)
+            pos = torch.arange(p0, p1).repeat(wl.batch)
+            keep = pos < (cl.repeat_interleave(p1 - p0) - step_tok)
+            slots = torch.where(keep, slots, torch.full_like(slots, -1)).to(device)
+            kvq.append(k, v, self.cache, slots, self.scale)
+            del k, v
+        # the step's tokens: positions [ctx - step_tok, ctx) of every sequence
+        ks, vs, ss = [], [], []
+        for b in range(wl.batch):
+            n = int(cl[b])
+            p0 = max(0, n - step_tok)
+            k, v = W.kv_tokens(wl, p0, n, device, seqs=[b]) if n > 0 else (None, None)
+            if k is not None:
+                ks.append(k)
+                vs.append(v)
+                ss.append(self.lay.slots(p0, n, seqs=[b]))
+        self.k_step = torch.cat(ks)
+        self.v_step = torch.cat(vs)
+        self.slots_step = torch.cat(ss).to(device)
+        self.q = W.query(wl, device)
+        self.bt = self.lay.block_tables.to(device)
+        self.cl = cl.to(device)
+        self.out = torch.empty_like(self.q)
+        self.partition = partition
+        need = kvq.workspace_size(wl.batch, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, ctx_max, partition)
+        self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+        self.num_parts = 1 if need == 0 else None
+        self.dec_bytes = W.decode_bytes(wl, cl)
+        self.app_bytes = W.append_bytes(wl, self.slots_step.numel())
+        torch.cuda.synchronize()
+
+    def append(self):
+        import fp8_int8_quantized_gb300 as kvq
+        kvq.append(self.k_step, self.v_step, self.cache, self.slots_step, self.scale)
+
+    def decode(self):
+        import fp8_int8_quantized_gb300 as kvq
+        kvq.decode_attention(self.q, self.cache, self.bt, self.cl, self.lay.max_context_len, self.scale,
+                             out=self.out, workspace=self.ws, partition_size=self.partition)
+
+
+# ---------------------------------------------------------------- kvq arm --
+
+def cpu_baseline(wl, target_s: float):
+    """The oracle, as it stands, on a bounded sample of the same workload: the
+    decode of a few whole sequences (all their q-heads, full context) plus the
+    append of their step tokens, on a cache the oracle itself filled."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from fp8_int8_quantized_gb300 import workloads as W
+    lay = W.Layout(wl)
+    fmt = {"e4m3": oracle.E4M3, "e5m2": oracle.E5M2, "int8": oracle.INT8}[wl.fmt]
+    order = list(range(wl.batch))
+
+    def run(seqs):
+        bs = wl.block_size
+        nblk = [(int(lay.context_lens[b]) + bs - 1) // bs for b in seqs]
+        cache = oracle.Cache(sum(nblk), wl.num_kv_heads, bs, wl.head_dim, fmt)
+        bt = np.zeros((len(seqs), max(nblk)), np.int32)
+        at = 0
+        for i, n in enumerate(nblk):
+            bt[i, :n] = np.arange(at, at + n)
+            at += n
+        cl = lay.context_lens[seqs].numpy().astype(np.int32)
+        # fill (untimed): the oracle's own append of every position
+        for i, b in enumerate(seqs):
+            n = int(cl[i])
+            k, v = W.kv_tokens(wl, 0, n, "cpu", seqs=[b])
+            pos = np.arange(n)
+            slots = (bt[i][pos // bs].astype(np.int64) * bs + pos % bs)
+            oracle.append(k.numpy(), v.numpy(), slots, cache, 1.0 if wl.fmt == "e4m3" else None)
+        q = W.query(wl, "cpu")[seqs].numpy()
+        step_tok = wl.append_chunk if wl.append_chunk else 1
+        ks, vs, ss = [], [], []
+        for i, b in enumerate(seqs):
+            n = int(cl[i])
+            p0 = max(0, n - step_tok)
+            k, v = W.kv_tokens(wl, p0, n, "cpu", seqs=[b])
+            pos = np.arange(p0, n)
+            ks.append(k.numpy())
+            vs.append(v.numpy())
+            ss.append(bt[i][pos // bs].astype(np.int64) * bs + pos % bs)
+        k, v, s = np.concatenate(ks), np.concatenate(vs), np.concatenate(ss)
+        t0 = time.perf_counter()
+        oracle.append(k, v, s, cache, 1.0 if wl.fmt == "e4m3" else None)
+        oracle.decode_attention(q, cache, bt, cl, 1.0 if wl.fmt == "e4m3" else None)
+        dt = time.perf_counter() - t0
+        return dt, W.decode_bytes(wl, torch.from_numpy(cl))
+
+    dt, by = run(order[:1])
+    n = max(1, min(wl.batch, int(target_s / max(dt, 1e-3))))
+    if n > 1:
+        dt, by = run(order[:n])
+    return {"value": by["total"] / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n} of {wl.batch} sequences (all {wl.num_q_heads} q-heads, full context, "
+                      f"{by['tokens']} cached tokens) decoded plus their step tokens appended, "
+                      f"{dt:.2f} s"}
+
+
+def run_kvq(args):
+    import torch
+
+    import fp8_int8_quantized_gb300 as kvq
+    from fp8_int8_quantized_gb300 import workloads as W
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    kvq.lib()
+    kvq.set_decode_kernel({"auto": 0, "simt": 1, "mma": 2}[args.kernel])
+    wl = W.WORKLOADS[args.workload]
+    K = args.steps or DEFAULT_STEPS.get(wl.name, 100)
+    Wm = max(3, args.warmup)
+    S = Setup(wl, dev, args.partition)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(Wm):
+        S.append()
+        S.decode()
+    torch.cuda.synchronize()
+    st, detail = kvq.device_error_check()
+    if st != 0:
+        raise RuntimeError(f"device error {st} ({detail})")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for i in range(K):
+            ev[i][0].record(stream)
+            S.append()
+            ev[i][1].record(stream)
+            S.decode()
+            ev[i][2].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = start.elapsed_time(end)
+    app_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    dec_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
+    ms_step = total_ms / K
+    max_ms, units = aggregate(ms_step, float(S.dec_bytes["total"]), world)
+    _, seqs = aggregate(ms_step, float(wl.batch), world)
+    value = units / (max_ms * 1e-3) / 1e9
+    launches_per_step = (1 if S.slots_step.numel() else 0) + 1 + (0 if S.num_parts == 1 else 1)
+
+    # end to end through the public API: pinned host inputs in, result out
+    e2e = None
+    if not args.no_e2e:
+        hq = S.q.cpu().pin_memory()
+        hk, hv = S.k_step.cpu().pin_memory(), S.v_step.cpu().pin_memory()
+        hs = S.slots_step.cpu().pin_memory()
+        hbt, hcl = S.bt.cpu().pin_memory(), S.cl.cpu().pin_memory()
+        hout = torch.empty(S.out.shape, dtype=S.out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hs, hbt, hcl))
+        d2h = hout.numel() * hout.element_size()
+        Ke = max(3, min(K, 200))
+
+        def e2e_step():
+            S.q.copy_(hq, non_blocking=True)
+            S.k_step.copy_(hk, non_blocking=True)
+            S.v_step.copy_(hv, non_blocking=True)
+            S.slots_step.copy_(hs, non_blocking=True)
+            S.bt.copy_(hbt, non_blocking=True)
+            S.cl.copy_(hcl, non_blocking=True)
+            S.append()
+            S.decode()
+            hout.copy_(S.out, non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(3):
+            e2e_step()
+        t = []
+        for _ in range(Ke):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            e2e_step()
+            b.record(stream)
+            b.synchronize()
+            t.append(a.elapsed_time(b))
+        e_ms = sum(t) / len(t)
+        e_max, e_units = aggregate(e_ms, float(S.dec_bytes["total"]), world)
+        e2e = {"value": round(e_units / (e_max * 1e-3) / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": round(e_max, 4), "steps": Ke}
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    peak, peak_kind = measured_peaks()
+    achieved = S.dec_bytes["total"] / (dec_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(wl.name)
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline(wl, args.cpu_seconds)
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": Wm,
+        "ms_per_step": round(max_ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": {"e4m3": "fp8-e4m3 storage, f16xf16->f32 compute", "e5m2": "fp8-e5m2 storage, f16xf16->f32 compute",
+                  "int8": "int8 storage, f16xf16->f32 compute"}[wl.fmt],
+        "data": "synthetic (seeded N(0,1) fp16 K/V/Q, shuffled block tables)",
+        "config": {"workload": wl.name, "description": wl.description, "batch": wl.batch,
+                   "num_q_heads": wl.num_q_heads, "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
+                   "block_size": wl.block_size, "format": wl.fmt,
+                   "context": wl.ctx if isinstance(wl.ctx, int) else list(wl.ctx),
+                   "step": f"append {S.slots_step.numel()} tokens + decode {wl.batch} sequences",
+                   "l2": f"inputs larger than L2 ({S.dec_bytes['total'] / 1e6:.0f} MB read per decode > 129 MB)"
+                   if S.dec_bytes["total"] > L2_BYTES else "inputs smaller than L2 (latency case)",
+                   "kernel": args.kernel, "partition": args.partition or "auto",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "tokens_per_s": round(seqs / (max_ms * 1e-3), 1),
+        "decode_ms": round(dec_ms, 5),
+        "append_ms": round(app_ms, 5),
+        "append_gbs": round(S.app_bytes / (app_ms * 1e-3) / 1e9, 2) if app_ms > 0 else None,
+        "decode_bytes": S.dec_bytes["total"],
+        "roofline": {"bound": "hbm", "kernel": "decode_split_kernel + decode_reduce_kernel",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "frac_of_nominal_8TBps": round(achieved / 8000.0, 4), "traffic": traffic},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ---------------------------------------------------------- reference arm --
+
+def run_reference(args):
+    """The CPU oracle timed as the reference arm: each step decodes one whole
+    sequence of the workload (all its q-heads, full context) and appends its
+    step tokens, on host cores.  Ranks other than 0 exit without work."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+
+    import oracle
+    from fp8_int8_quantized_gb300 import workloads as W
+    wl = W.WORKLOADS[args.workload]
+    lay = W.Layout(wl)
+    fmt = {"e4m3": oracle.E4M3, "e5m2": oracle.E5M2, "int8": oracle.INT8}[wl.fmt]
+    bs = wl.block_size
+    step_tok = wl.append_chunk if wl.append_chunk else 1
+    K = args.steps or 5
+    Wm = max(3, args.warmup)
+    nseq = min(wl.batch, 4)
+    caches = []
+    for b in range(nseq):
+        n = int(lay.context_lens[b])
+        nb = (n + bs - 1) // bs
+        cache = oracle.Cache(nb, wl.num_kv_heads, bs, wl.head_dim, fmt)
+        bt = np.arange(nb, dtype=np.int32)[None]
+        k, v = W.kv_tokens(wl, 0, n, "cpu", seqs=[b])
+        pos = np.arange(n)
+        oracle.append(k.numpy(), v.numpy(), (pos // bs) * bs + pos % bs, cache, None)
+        q = W.query(wl, "cpu")[b:b + 1].numpy()
+        p0 = max(0, n - step_tok)
+        sk, sv = k[p0:].numpy(), v[p0:].numpy()
+        caches.append((cache, bt, np.array([n], np.int32), q, sk, sv, np.arange(p0, n, dtype=np.int64)))
+
+    def step(i):
+        cache, bt, cl, q, sk, sv, slots = caches[i % nseq]
+        oracle.append(sk, sv, slots, cache, None)
+        oracle.decode_attention(q, cache, bt, cl, None)
+
+    for i in range(Wm):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(K):
+        step(i)
+    dt = (time.perf_counter() - t0) / K
+    # bytes of the decode of one whole sequence: the unit of one step
+    ctx_mean = sum(int(lay.context_lens[i]) for i in range(nseq)) / nseq
+    one = W.Workload(wl.name, 1, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, wl.block_size, wl.fmt,
+                     int(ctx_mean), wl.scale_rule)
+    value = W.decode_bytes(one, torch.tensor([int(ctx_mean)]))["total"] / dt / 1e9
+    cores = oracle.num_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": K, "warmup": Wm, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+            "config": {"workload": wl.name, "description": wl.description},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": f"each step: one sequence of {wl.name} (all {wl.num_q_heads} q-heads, "
+                                       f"context {int(lay.context_lens[0])}) decoded + {step_tok} tokens appended"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_kvq(args)
+
+
+if __name__ == "__main__":
+    main()

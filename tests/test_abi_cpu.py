@@ -1,0 +1,70 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads and
+exports every entry point include/kvq.h declares, with the declared status codes."""
+import os
+import re
+
+import pytest
+
+import fp8_int8_quantized_gb300 as kvq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kvq.build()
+    return kvq.lib()
+
+
+def declared():
+    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    return sorted(set(re.findall(r"KVQ_API\s+[\w\s\*]+?\b(kvq_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared() == sorted(kvq.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared():
+        assert hasattr(lib, name), name
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.kvq_abi_version() == 1
+    for code in range(7):
+        assert kvq.status_string(code)
+    assert kvq.status_string(99) == "unknown status"
+
+
+def test_status_codes_match_header():
+    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    for code, name in kvq.STATUS.items():
+        assert re.search(rf"\b{name}\s*=\s*{code}\b", src), name
+
+
+def test_decode_kernel_knob(lib):
+    prev = lib.kvq_set_decode_kernel(1)
+    assert lib.kvq_set_decode_kernel(prev) == 1
+    assert lib.kvq_set_decode_kernel(7) == -1
+
+
+def test_invalid_args_rejected_before_any_cuda_call(lib):
+    import ctypes
+    d = kvq.KvqCacheDesc(None, None, None, None, 8, 16, 2, 128, kvq.E4M3)
+    assert lib.kvq_append(None, None, ctypes.byref(d), None, 4, None, kvq.E4M3, None) == 1
+    d = kvq.KvqCacheDesc(16, 16, None, None, 8, 16, 2, 96, kvq.E4M3)
+    assert lib.kvq_append(16, 16, ctypes.byref(d), 16, 4, None, kvq.E4M3, None) == 2       # head_dim 96
+    d = kvq.KvqCacheDesc(16, 16, None, None, 8, 16, 2, 128, kvq.E4M3)
+    assert lib.kvq_append(16, 16, ctypes.byref(d), 16, 4, None, kvq.E5M2, None) == 1       # fmt mismatch
+    d8 = kvq.KvqCacheDesc(16, 16, None, None, 8, 16, 2, 128, kvq.INT8)
+    assert lib.kvq_append(16, 16, ctypes.byref(d8), 16, 4, None, kvq.INT8, None) == 1      # no scales
+    assert lib.kvq_decode_attention(16, ctypes.byref(d), 16, 4, 16, 2, 3, 64, None, kvq.E4M3, 0.0,
+                                    16, None, 0, 0, None) == 1                              # 3 % 2 != 0
+    assert lib.kvq_decode_attention(16, ctypes.byref(d), 16, 4, 16, 2, 32, 64, None, kvq.E4M3, 0.0,
+                                    16, None, 0, 0, None) == 2                              # group 16
+    assert lib.kvq_decode_attention(16, ctypes.byref(d), 16, 2, 16, 2, 4, 64, None, kvq.E4M3, 0.0,
+                                    16, None, 0, 0, None) == 1                              # table too short
+    assert lib.kvq_decode_attention(16, ctypes.byref(d), 16, 4, 16, 2, 4, 64, None, kvq.E4M3, 0.0,
+                                    16, None, 0, 100, None) == 1                            # partition % 64
+    assert lib.kvq_dequant(ctypes.byref(d), None, 3, None, kvq.E4M3, None, None, None) == 1

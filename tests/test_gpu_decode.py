@@ -1,0 +1,152 @@
+"""GPU parity of decode attention (kvq_decode_attention) against the fp64 CPU
+oracle on the same cache bytes: |o_gpu - o_ref| <= 2e-3 * max(1, |o_ref|) per
+element.  Small cases span several tiles, partitions and a ragged tail; the
+workload-sized cases run the launch configuration the benchmark times and check
+a seeded sample of sequences."""
+import numpy as np
+import pytest
+import torch
+
+import fp8_int8_quantized_gb300 as kvq
+import oracle
+from fp8_int8_quantized_gb300 import workloads as W
+from tests.gpu_util import ATOL_REL, DeviceWorkload, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    kvq.build()
+    torch.cuda.init()
+    yield
+    kvq.set_decode_kernel(kvq.KERNEL_AUTO)
+
+
+def small(fmt, B, Hq, Hkv, D, BS, ctx, seed=0, outliers=True, scale_rule=None):
+    wl = W.Workload(f"t-{fmt}", B, Hq, Hkv, D, BS, fmt, max(ctx), scale_rule or
+                    ("amax" if fmt == "e4m3" else ("row" if fmt == "int8" else "one")),
+                    outliers=outliers, seed=seed)
+    return DeviceWorkload(wl, chunk_tokens=1 << 16, ctx=torch.tensor(ctx, dtype=torch.int32))
+
+
+CASES = [
+    # fmt, B, Hq, Hkv, D, BS, contexts
+    ("e4m3", 3, 4, 4, 64, 16, [128, 1, 77]),
+    ("e4m3", 2, 8, 1, 128, 16, [300, 17]),
+    ("e5m2", 3, 32, 8, 128, 16, [1000, 512, 33]),
+    ("e5m2", 2, 6, 3, 64, 32, [95, 400]),
+    ("int8", 2, 4, 4, 128, 64, [640, 65]),
+    ("int8", 3, 8, 2, 64, 64, [129, 1, 256]),
+    ("e4m3", 2, 16, 2, 128, 32, [2050, 700]),
+    ("e5m2", 1, 7, 7, 128, 16, [16]),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}-G{c[2] // c[3]}-D{c[4]}-BS{c[5]}")
+@pytest.mark.parametrize("kernel", [kvq.KERNEL_MMA, kvq.KERNEL_SIMT])
+@pytest.mark.parametrize("partition", [0, 64, 256])
+def test_decode_small(case, kernel, partition):
+    fmt, B, Hq, Hkv, D, BS, ctx = case
+    if kernel == kvq.KERNEL_SIMT and Hq // Hkv > 4:
+        pytest.skip("CUDA-core kernel covers group size <= 4")
+    dw = small(fmt, B, Hq, Hkv, D, BS, ctx, seed=len(ctx) + D)
+    kvq.set_decode_kernel(kernel)
+    out = dw.decode(partition_size=partition)
+    torch.cuda.synchronize()
+    assert kvq.device_error_check()[0] == 0
+    ref = dw.oracle_decode(list(range(B)))
+    e = rel_err(out.float().cpu().numpy(), ref)
+    assert e <= ATOL_REL, e
+
+
+def test_kernels_and_partitions_agree():
+    dw = small("e4m3", 4, 8, 2, 128, 16, [3000, 1500, 64, 4097], seed=5)
+    outs = []
+    for kernel in (kvq.KERNEL_MMA, kvq.KERNEL_SIMT):
+        kvq.set_decode_kernel(kernel)
+        for p in (0, 64, 512, 4160):
+            outs.append(dw.decode(partition_size=p).float())
+    kvq.set_decode_kernel(kvq.KERNEL_AUTO)
+    for o in outs[1:]:
+        d = ((o - outs[0]).abs() / outs[0].abs().clamp(min=1.0)).max().item()
+        assert d <= 1e-3, d
+
+
+def test_edge_contexts_zero_one_and_max():
+    dw = small("e5m2", 4, 4, 2, 128, 16, [0, 1, 8192, 15], seed=9)
+    out = dw.decode().float().cpu().numpy()
+    assert not out[0].any()
+    ref = dw.oracle_decode([1, 2, 3])
+    assert rel_err(out[1:], ref) <= ATOL_REL
+    # context 1: the output is the single V row (times the scale, here 1.0)
+    assert np.abs(out[1] - ref[0]).max() <= 1e-3
+
+
+def test_nan_codes_past_the_context_do_not_leak():
+    """Rows of the last block past the context hold NaN codes; they must not reach
+    the output."""
+    wl = W.Workload("nan", 2, 4, 2, 128, 16, "e4m3", 40, "amax", seed=3)
+    lay = W.Layout(wl, torch.tensor([37, 40], dtype=torch.int32))
+    dev = torch.device("cuda")
+    cache = kvq.KVCache(lay.num_blocks, 2, 16, 128, "e4m3", dev, fill=0x7F)
+    k, v = W.kv_tokens(wl, 0, 40, dev)
+    slots = lay.slots(0, 40).to(dev)
+    kvq.append(k, v, cache, slots)
+    q = W.query(wl, dev)
+    out = kvq.decode_attention(q, cache, lay.block_tables.to(dev), lay.context_lens.to(dev), 40)
+    o = out.float().cpu().numpy()
+    assert np.isfinite(o).all()
+    oc = oracle.Cache(lay.num_blocks, 2, 16, 128, oracle.E4M3, k_codes=cache.k_codes.cpu().numpy(),
+                      v_codes=cache.v_codes.cpu().numpy())
+    ref = oracle.decode_attention(q.cpu().numpy(), oc, lay.block_tables.numpy(), lay.context_lens.numpy(), None)
+    assert rel_err(o, ref) <= ATOL_REL
+
+
+def test_bad_block_id_is_reported_without_fault():
+    dw = small("e4m3", 2, 4, 4, 128, 16, [64, 64], seed=1)
+    bt = dw.block_tables.clone()
+    bt[1, 2] = 10 ** 6
+    out = kvq.decode_attention(dw.q, dw.cache, bt, dw.context_lens, 64, dw.scale)
+    st, detail = kvq.device_error_check()
+    assert st == 4 and detail == 10 ** 6
+    ref = dw.oracle_decode([0])
+    assert rel_err(out[:1].float().cpu().numpy(), ref) <= ATOL_REL   # sequence 0 is untouched
+    assert kvq.device_error_check()[0] == 0
+
+
+def test_workspace_too_small_and_empty_batch():
+    dw = small("e4m3", 2, 4, 4, 128, 16, [2000, 100], seed=2)
+    need = kvq.workspace_size(2, 4, 4, 128, 2000, 256)
+    assert need > 0
+    ws = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(kvq.KvqError) as ei:
+        dw.decode(partition_size=256, out=None) if False else kvq.decode_attention(
+            dw.q, dw.cache, dw.block_tables, dw.context_lens, 2000, dw.scale, workspace=ws, partition_size=256)
+    assert ei.value.status == 3
+    q0 = dw.q[:0]
+    out = kvq.decode_attention(q0, dw.cache, dw.block_tables[:0], dw.context_lens[:0], 2000, dw.scale)
+    assert out.shape == (0, 4, 128)
+
+
+@pytest.mark.parametrize("name,seqs", [("tiny", [0]), ("llama2-7b", [0, 13, 31]),
+                                       ("llama3-8b", [0, 21, 40, 63]),
+                                       ("llama2-13b-int8", [0, 77, 127]),
+                                       ("llama3-70b", [0, 255])])
+def test_decode_workload_sampled(name, seqs):
+    wl = W.WORKLOADS[name]
+    dw = DeviceWorkload(wl)
+    kvq.set_decode_kernel(kvq.KERNEL_AUTO)
+    out = dw.decode()
+    torch.cuda.synchronize()
+    assert kvq.device_error_check()[0] == 0
+    o = out.float().cpu().numpy()
+    assert np.isfinite(o).all()
+    ref = dw.oracle_decode(seqs)
+    e = rel_err(o[seqs], ref)
+    assert e <= ATOL_REL, e
+    # the sample covers the shortest and longest sequences of ragged workloads
+    if not isinstance(wl.ctx, int):
+        cl = dw.lay.context_lens
+        extra = [int(torch.argmin(cl)), int(torch.argmax(cl))]
+        assert rel_err(o[extra], dw.oracle_decode(extra)) <= ATOL_REL
