@@ -68,9 +68,13 @@ def test_kernels_and_partitions_agree():
         for p in (0, 64, 512, 4160):
             outs.append(dw.decode(partition_size=p).float())
     kvq.set_decode_kernel(kvq.KERNEL_AUTO)
+    # different partitions / kernels sum in different fp32 orders; the fp16
+    # outputs may then round to neighbouring values: allow 2 fp16 ulps
     for o in outs[1:]:
-        d = ((o - outs[0]).abs() / outs[0].abs().clamp(min=1.0)).max().item()
-        assert d <= 1e-3, d
+        mag = torch.maximum(o.abs(), outs[0].abs()).clamp(min=2.0 ** -14)
+        ulp = torch.exp2(torch.floor(torch.log2(mag)) - 10)
+        d = ((o - outs[0]).abs() / ulp).max().item()
+        assert d <= 2.0, d
 
 
 def test_edge_contexts_zero_one_and_max():
@@ -121,8 +125,8 @@ def test_workspace_too_small_and_empty_batch():
     assert need > 0
     ws = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
     with pytest.raises(kvq.KvqError) as ei:
-        dw.decode(partition_size=256, out=None) if False else kvq.decode_attention(
-            dw.q, dw.cache, dw.block_tables, dw.context_lens, 2000, dw.scale, workspace=ws, partition_size=256)
+        kvq.decode_attention(dw.q, dw.cache, dw.block_tables, dw.context_lens, 2000, dw.scale, workspace=ws,
+                             partition_size=256)
     assert ei.value.status == 3
     q0 = dw.q[:0]
     out = kvq.decode_attention(q0, dw.cache, dw.block_tables[:0], dw.context_lens[:0], 2000, dw.scale)
