@@ -350,8 +350,14 @@ struct MmaConsumer {
             if (t2 < cx.valid) p2 *= sv[t2];
             if (t3 < cx.valid) p3 *= sv[t3];
         }
-        // P^T as the B operand of PV: k = token, n = head g.
+        // P^T as the B operand of PV: k = token, n = head g.  P is carried as
+        // an fp16 pair hi + lo (lo = the fp16 residual of p - hi), so the PV
+        // product keeps about 22 bits of each weight instead of 11: with
+        // outlier channels the weighted mean of large V values can cancel, and a
+        // single fp16 rounding of P would then show in the output.
         const uint32_t pb0 = pack_f16x2(p0, p1), pb1 = pack_f16x2(p2, p3);
+        const float2 h01 = f16x2_to_f32x2(pb0), h23 = f16x2_to_f32x2(pb1);
+        const uint32_t pl0 = pack_f16x2(p0 - h01.x, p1 - h01.y), pl1 = pack_f16x2(p2 - h23.x, p3 - h23.y);
         // rescale the accumulators: columns are heads 2c and 2c+1
         if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
             const float a0 = __shfl_sync(0xFFFFFFFFu, alpha, 8 * c);
@@ -382,8 +388,10 @@ struct MmaConsumer {
             const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
             const uint32_t x01 = prmt(v0[i >> 1], v1[i >> 1], sel);
             const uint32_t x23 = prmt(v2[i >> 1], v3[i >> 1], sel);
-            mma_16816(acc[i], dec_x2<FMT>((uint16_t)(x01 & 0xFFFFu)), dec_x2<FMT>((uint16_t)(x01 >> 16)),
-                      dec_x2<FMT>((uint16_t)(x23 & 0xFFFFu)), dec_x2<FMT>((uint16_t)(x23 >> 16)), pb0, pb1);
+            const uint32_t a0 = dec_x2<FMT>((uint16_t)(x01 & 0xFFFFu)), a1 = dec_x2<FMT>((uint16_t)(x01 >> 16));
+            const uint32_t a2 = dec_x2<FMT>((uint16_t)(x23 & 0xFFFFu)), a3 = dec_x2<FMT>((uint16_t)(x23 >> 16));
+            mma_16816(acc[i], a0, a1, a2, a3, pb0, pb1);
+            mma_16816(acc[i], a0, a1, a2, a3, pl0, pl1);
         }
     }
 
