@@ -19,10 +19,12 @@ import torch
 E4M3, E5M2, INT8 = 1, 2, 3
 FORMATS = {"e4m3": E4M3, "fp8": E4M3, "e5m2": E5M2, "fp8_e5m2": E5M2, "int8": INT8}
 STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED", 3: "KVQ_ERR_WORKSPACE",
-          4: "KVQ_ERR_OUT_OF_RANGE", 5: "KVQ_ERR_TIMEOUT", 6: "KVQ_ERR_CUDA"}
+          4: "KVQ_ERR_OUT_OF_RANGE", 5: "KVQ_ERR_TIMEOUT", 6: "KVQ_ERR_CUDA",
+          7: "KVQ_ERR_SCRATCH_LIMIT"}
 KERNEL_AUTO, KERNEL_SIMT, KERNEL_MMA = 0, 1, 2
 EXPORTS = ("kvq_append", "kvq_decode_workspace_size", "kvq_decode_attention", "kvq_dequant",
-           "kvq_set_decode_kernel", "kvq_device_error_check", "kvq_status_string", "kvq_abi_version")
+           "kvq_set_decode_kernel", "kvq_device_error_check", "kvq_status_string", "kvq_abi_version",
+           "kvq_decode_attention_static_scratch", "kvq_static_scratch_bytes")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkvq.so")
@@ -67,6 +69,10 @@ def lib():
         L.kvq_decode_attention.restype = ctypes.c_int
         L.kvq_decode_attention.argtypes = [P, P, P, i32, P, i32, i32, i32, P, i32, ctypes.c_float, P, P,
                                            ctypes.c_size_t, i32, P]
+        L.kvq_decode_attention_static_scratch.restype = ctypes.c_int
+        L.kvq_decode_attention_static_scratch.argtypes = [P, P, P, i32, P, i32, i32, i32, P, i32, ctypes.c_float,
+                                                          P, i32, P]
+        L.kvq_static_scratch_bytes.restype = ctypes.c_size_t
         L.kvq_dequant.restype = ctypes.c_int
         L.kvq_dequant.argtypes = [P, P, i64, P, i32, P, P, P]
         L.kvq_set_decode_kernel.restype = i32
@@ -181,6 +187,27 @@ def decode_attention(q: torch.Tensor, cache: KVCache, block_tables: torch.Tensor
                                     _dev(out, torch.float16, "out"), ws_ptr, ws_bytes, int(partition_size),
                                     _stream(stream))
     _check(st, "kvq_decode_attention")
+    return out
+
+
+def decode_attention_static_scratch(q: torch.Tensor, cache: KVCache, block_tables: torch.Tensor,
+                                    context_lens: torch.Tensor, max_context_len: int,
+                                    scale: torch.Tensor | None = None, sm_scale: float = 0.0,
+                                    out: torch.Tensor | None = None, partition_size: int = 0,
+                                    stream=None) -> torch.Tensor:
+    """kvq_decode_attention_static_scratch: decode attention for callers that cannot
+    allocate device memory; the split workspace comes from the library's fixed
+    device array.  ``out`` must be supplied by such callers."""
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    d = cache.desc()
+    st = lib().kvq_decode_attention_static_scratch(
+        _dev(q, torch.float16, "q"), ctypes.byref(d), _dev(block_tables, torch.int32, "block_tables"),
+        block_tables.shape[1], _dev(context_lens, torch.int32, "context_lens"), B, Hq, int(max_context_len),
+        _scale_ptr(scale), cache.fmt, float(sm_scale), _dev(out, torch.float16, "out"), int(partition_size),
+        _stream(stream))
+    _check(st, "kvq_decode_attention_static_scratch")
     return out
 
 

@@ -111,6 +111,7 @@ const char* kvq_status_string(kvq_status s) {
         case KVQ_ERR_OUT_OF_RANGE: return "a slot, block id or context length was outside the cache";
         case KVQ_ERR_TIMEOUT: return "a kernel's bounded wait ran out";
         case KVQ_ERR_CUDA: return "CUDA runtime error";
+        case KVQ_ERR_SCRATCH_LIMIT: return "needs more scratch than the library's fixed device array";
     }
     return "unknown status";
 }

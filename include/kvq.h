@@ -72,7 +72,8 @@ typedef enum {
     KVQ_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required */
     KVQ_ERR_OUT_OF_RANGE = 4,  /* a kernel met a slot / block id outside the cache */
     KVQ_ERR_TIMEOUT = 5,       /* a kernel's bounded wait ran out (never expected) */
-    KVQ_ERR_CUDA = 6           /* a CUDA runtime call or launch failed */
+    KVQ_ERR_CUDA = 6,          /* a CUDA runtime call or launch failed */
+    KVQ_ERR_SCRATCH_LIMIT = 7  /* needs more scratch than the library's fixed array */
 } kvq_status;
 
 /* The paged cache: caller-owned device memory.
@@ -137,6 +138,28 @@ KVQ_API kvq_status kvq_decode_attention(const void* q, const kvq_cache* cache,
                                 const float* scale, int32_t fmt, float sm_scale, void* out,
                                 void* workspace, size_t workspace_bytes,
                                 int32_t partition_size, kvq_stream_t stream);
+
+/* Decode attention for callers that cannot allocate device memory (no page
+ * has a counterpart: this is a deployment variant).  Plugin hosts that give an
+ * operator only its inputs and outputs while their own pool owns the rest of
+ * device memory, and serving loops that must not allocate once running, have
+ * no workspace to pass.  Same arguments and result as kvq_decode_attention
+ * without workspace / workspace_bytes: the workspace is a fixed array of
+ * kvq_static_scratch_bytes() (64 MiB) in the library's device memory, held by
+ * every GPU that loads the library until the process exits.  Sizes whose
+ * kvq_decode_workspace_size() exceeds it return KVQ_ERR_SCRATCH_LIMIT with
+ * nothing launched.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress); make that first call before any stream
+ * capture.  Calls share the array and it keeps the last call's contents;
+ * nothing in it needs to start at zero.  Calls whose kernels overlap on the GPU
+ * race on it.  Allocates nothing. */
+KVQ_API kvq_status kvq_decode_attention_static_scratch(const void* q, const kvq_cache* cache,
+                                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                                       const int32_t* context_lens, int32_t batch,
+                                                       int32_t num_q_heads, int32_t max_context_len,
+                                                       const float* scale, int32_t fmt, float sm_scale,
+                                                       void* out, int32_t partition_size, kvq_stream_t stream);
+KVQ_API size_t kvq_static_scratch_bytes(void);
 
 /* Debug gather + dequantize-on-read: for each of num_slots slots, fp32
  * [num_slots][num_kv_heads][head_dim] rows of K and V, each value

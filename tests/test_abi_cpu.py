@@ -32,7 +32,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_abi_version_and_status_strings(lib):
     assert lib.kvq_abi_version() == 1
-    for code in range(7):
+    for code in range(8):
         assert kvq.status_string(code)
     assert kvq.status_string(99) == "unknown status"
 
