@@ -45,6 +45,7 @@ def parse():
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "mma"])
     ap.add_argument("--partition", type=int, default=0)
+    ap.add_argument("--batch", type=int, default=0, help="override the batch (small profiling cases)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU-baseline sample time")
@@ -306,6 +307,9 @@ def run_kvq(args):
     kvq.lib()
     kvq.set_decode_kernel({"auto": 0, "simt": 1, "mma": 2}[args.kernel])
     wl = W.WORKLOADS[args.workload]
+    if args.batch:
+        import dataclasses
+        wl = dataclasses.replace(wl, batch=args.batch)
     K = args.steps or DEFAULT_STEPS.get(wl.name, 100)
     Wm = max(3, args.warmup)
     S = Setup(wl, dev, args.partition)
