@@ -45,7 +45,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         o = os.path.join(BUILD, os.path.basename(s)[:-3] + ".o")
         objs.append(o)
         if force or _stale(o, [s] + headers):
-            cmd = [nvcc()] + ARCH + FLAGS + ["-c", s, "-o", o]
+            cmd = [nvcc()] + ARCH + FLAGS + os.environ.get("KVQ_NVCC_FLAGS", "").split() + ["-c", s, "-o", o]
             if verbose:
                 cmd.insert(1, "-Xptxas=-v")
             jobs.append(cmd)

@@ -24,7 +24,8 @@ unsigned long long* g_err_ptr[kMaxDevices] = {};
 int g_sm_count[kMaxDevices] = {};
 std::atomic<int> g_decode_kernel{0};
 
-constexpr int kMaxPartition = 8192;
+constexpr int kMaxChunkTokens = 65536;
+constexpr int kMaxBatch = 4096;   // the decode kernel scans the context lengths in shared memory
 
 bool current_device(int* dev) {
     if (cudaGetDevice(dev) != cudaSuccess) return false;
@@ -76,24 +77,24 @@ kvq::CacheView view(const kvq_cache* c) {
                           c->v_scales, c->num_blocks, c->block_size, c->num_kv_heads, c->head_dim, c->fmt};
 }
 
-// Tokens per context partition: one partition when the (sequence, kv-head)
-// pairs alone fill the GPU several times over, else the smallest power-of-two
-// multiple of 256 tokens that still gives about eight resident waves of CTAs.
-int32_t choose_partition(int32_t batch, int32_t num_kv_heads, int32_t max_ctx, int sms) {
-    const int64_t pairs = (int64_t)batch * num_kv_heads;
-    const int64_t target = (int64_t)sms * 3 * 8;  // 3 CTAs per SM, ~8 waves
-    const int32_t whole = std::max<int32_t>(64, (max_ctx + 63) / 64 * 64);
-    if (whole <= kMaxPartition && pairs >= target / 2) return whole;
-    int64_t p = 256;
-    while (p < kMaxPartition && pairs * ((max_ctx + p - 1) / p) > target) p *= 2;
-    return (int32_t)std::min<int64_t>(p, std::max<int32_t>(whole, 256));
+// 16-token tiles per context chunk.  Every warp of the persistent decode
+// kernel streams a contiguous range of the flat tile list that is at least one
+// chunk long; chunks of about half a range keep every warp busy while the
+// partial slots stay few (two per chunk).  Assumes ~4 CTAs of 4 warps per SM.
+int32_t choose_chunk_tiles(int32_t batch, int32_t num_kv_heads, int32_t max_ctx, int sms) {
+    const int64_t tiles = (int64_t)batch * num_kv_heads * ((max_ctx + 15) / 16);
+    const int64_t warps = (int64_t)sms * 16;
+    int64_t c = tiles / (2 * warps);
+    if (c < 4) c = 4;
+    if (c > 256) c = 256;
+    return (int32_t)c;
 }
 
-int32_t resolve_partition(int32_t partition_size, int32_t batch, int32_t num_kv_heads, int32_t max_ctx) {
-    if (partition_size > 0) return partition_size;
+int32_t resolve_chunk_tiles(int32_t partition_size, int32_t batch, int32_t num_kv_heads, int32_t max_ctx) {
+    if (partition_size > 0) return partition_size / 16;
     int dev = 0;
     if (!current_device(&dev)) dev = 0;
-    return choose_partition(batch, num_kv_heads, max_ctx, sm_count(dev));
+    return choose_chunk_tiles(batch, num_kv_heads, max_ctx, sm_count(dev));
 }
 
 }  // namespace
@@ -142,11 +143,11 @@ kvq_status kvq_append(const void* k, const void* v, const kvq_cache* cache, cons
 
 size_t kvq_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                  int32_t max_context_len, int32_t partition_size) {
-    if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_context_len <= 0) return 0;
-    const int32_t P = resolve_partition(partition_size, batch, num_kv_heads, max_context_len);
-    const int64_t np = (max_context_len + P - 1) / P;
-    if (np <= 1) return 0;
-    return kvq::ws_bytes(batch, num_q_heads, np, head_dim);
+    if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_context_len < 0) return 0;
+    const int32_t C = resolve_chunk_tiles(partition_size, batch, num_kv_heads, max_context_len);
+    if (C <= 0) return 0;
+    const int64_t nch = std::max<int64_t>(1, ((max_context_len + 15) / 16 + C - 1) / C);
+    return kvq::ws_bytes(batch, num_q_heads, nch, head_dim);
 }
 
 kvq_status kvq_decode_attention(const void* q, const kvq_cache* cache, const int32_t* block_tables,
@@ -161,21 +162,21 @@ kvq_status kvq_decode_attention(const void* q, const kvq_cache* cache, const int
     const int G = num_q_heads / cache->num_kv_heads;
     if (G > 8) return KVQ_ERR_UNSUPPORTED;
     if ((int64_t)max_blocks_per_seq * cache->block_size < max_context_len) return KVQ_ERR_INVALID_ARG;
-    if (batch > 65535 || cache->num_kv_heads > 65535) return KVQ_ERR_UNSUPPORTED;
+    if (batch > 65535 || cache->num_kv_heads > 65535 || num_q_heads > 65535) return KVQ_ERR_UNSUPPORTED;
     if (batch == 0) return KVQ_OK;
     if (!q || !block_tables || !context_lens || !out || !aligned(q, 16) || !aligned(out, 16) ||
         !aligned(block_tables, 4) || !aligned(context_lens, 4))
         return KVQ_ERR_INVALID_ARG;
     if (scale && !aligned(scale, 4)) return KVQ_ERR_INVALID_ARG;
     if (!(sm_scale >= 0.f) || std::isinf(sm_scale)) return KVQ_ERR_INVALID_ARG;
-    if (partition_size < 0 || partition_size % 64 || partition_size > kMaxPartition) return KVQ_ERR_INVALID_ARG;
-    const int32_t P = resolve_partition(partition_size, batch, cache->num_kv_heads, std::max(max_context_len, 1));
-    const int32_t np = std::max<int32_t>(1, (max_context_len + P - 1) / P);
-    if (np > 65535) return KVQ_ERR_UNSUPPORTED;
-    if (np > 1) {
-        const size_t need = kvq::ws_bytes(batch, num_q_heads, np, cache->head_dim);
-        if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return KVQ_ERR_WORKSPACE;
-    }
+    if (partition_size < 0 || partition_size % 64 || partition_size > kMaxChunkTokens) return KVQ_ERR_INVALID_ARG;
+    if (batch > kMaxBatch) return KVQ_ERR_UNSUPPORTED;
+    if ((int64_t)batch * cache->num_kv_heads * ((max_context_len + 15) / 16) >= 0x7FFFFFFFll)
+        return KVQ_ERR_UNSUPPORTED;  // flat tile indices are 32-bit
+    const int32_t C = resolve_chunk_tiles(partition_size, batch, cache->num_kv_heads, max_context_len);
+    const int32_t nch = std::max<int32_t>(1, ((max_context_len + 15) / 16 + C - 1) / C);
+    const size_t need = kvq::ws_bytes(batch, num_q_heads, nch, cache->head_dim);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return KVQ_ERR_WORKSPACE;
     int kind = g_decode_kernel.load();
     if (kind == 0) kind = 2;
     if (kind == 1 && G > 4) return KVQ_ERR_UNSUPPORTED;
@@ -195,9 +196,9 @@ kvq_status kvq_decode_attention(const void* q, const kvq_cache* cache, const int
     a.scale = fmt == KVQ_INT8 ? nullptr : scale;
     a.sm_scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt((float)cache->head_dim);
     a.out = static_cast<uint16_t*>(out);
-    a.ws = np > 1 ? static_cast<float*>(workspace) : nullptr;
-    a.partition_size = P;
-    a.num_parts = np;
+    a.ws = static_cast<float*>(workspace);
+    a.chunk_tiles = C;
+    a.num_chunks = nch;
     a.kernel = kind;
     a.err = err;
     return kvq::launch_decode(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;

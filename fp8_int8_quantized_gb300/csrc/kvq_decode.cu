@@ -6,31 +6,37 @@
 // INT8 row scales ("[Feature] TurboMind support W8A8 or FP8 KV Cache", online
 // INT8) are folded out of the dot products: logits take s_K, outputs take s_V.
 //
-// Work decomposition: one CTA per (context partition, kv-head, sequence).  All
-// q-heads of a kv-head's group are processed by that CTA, so each cached byte
-// is read from HBM once.  Inside a CTA:
-//   * warp 4 (producer) copies 16-token tiles of one paged block -- K rows and
-//     V rows of one kv-head -- into an 8-stage shared-memory ring with 2-D TMA
-//     tile loads (cp.async.bulk.tensor, 128-byte swizzle for head_dim 128),
-//     completion tracked by mbarriers; INT8 row scales ride along as 1-D bulk
-//     copies;
-//   * warps 0-3 (consumers) take tiles round-robin, dequantize in registers and
-//     run QK^T, an online softmax (base-2) and PV, each warp with its own
-//     running (max, sum, accumulator);
-//   * at the end the four warp states are merged in shared memory and written
-//     either as the final fp16 output (one partition) or as a partial
-//     (max, sum, unnormalised accumulator) that decode_reduce_kernel combines.
+// Work decomposition.  Every (sequence, kv-head) pair owns ceil(ctx / 16)
+// tiles of 16 tokens; all pairs' tiles, in (sequence, kv-head, tile) order,
+// form one flat list.  A persistent grid (a few CTAs per SM, four independent
+// warps each) splits that list into equal contiguous ranges, one per warp, so
+// every warp streams the same number of bytes whatever the context lengths.
+// All q-heads of a kv-head's group are served by the warp that reads its tile,
+// so each cached byte is read from HBM once.  Contexts are cut into chunks of
+// C tiles; a warp range is never shorter than C, so a chunk is streamed by at
+// most two warps and owns two partial slots (max, sum, unnormalised acc) that
+// decode_reduce_kernel merges into the fp16 output.
+//
+// Every warp owns a ring of kSpw stages (a 16-token K tile and V tile of one
+// paged block, 128-byte swizzled for head_dim 128, plus INT8 row scales), each
+// with an mbarrier, and refills a stage with 2-D TMA tile loads
+// (cp.async.bulk.tensor, issued by lane 0) right after consuming it, so its
+// loads run kSpw - 1 tiles ahead across pair boundaries.  Block ids of the
+// next 32 tiles are held one per lane (loaded one window ahead); the first
+// tile of each (sequence, kv-head) pair also carries a bulk copy of the pair's
+// query rows into the warp's query buffer.
+//
 // Two consumer families:
-//   * kKindSimt: CUDA cores; 16 head-dim values per lane, warp-shuffle dot
-//     reductions, group size <= 4;
+//   * kKindSimt: CUDA cores; 16 head-dim values per lane, mixed-precision
+//     fma.rn.f32.f16 dot products and warp-shuffle reductions, group <= 4;
 //   * kKindMma: tensor cores via mma.sync m16n8k16 (f16 in, fp32 accumulate).
 //     QK^T is computed transposed (S^T = Q K^T with the q-group padded to 16
 //     rows, 8 tokens per n8 tile) so that its accumulator fragment is already
 //     the B operand of PV (out^T = V^T P^T, head_dim as M).  The contraction
 //     index (head_dim for QK, tokens for PV) is permuted so that every thread
 //     loads contiguous 16-byte runs; Q is permuted the same way.
-// Every wait is bounded (2 s); on timeout a kernel records the error and
-// drains its copies in flight.
+// Every wait is bounded (2 s); on timeout a warp records the error, waits for
+// its copies in flight and stops.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -39,53 +45,104 @@
 #include "kvq_device.cuh"
 #include "kvq_launch.h"
 
+#ifndef KVQ_SPW
+#define KVQ_SPW 3
+#endif
+#ifndef KVQ_MIN_BLOCKS
+#define KVQ_MIN_BLOCKS 4
+#endif
+
 namespace kvq {
 namespace {
 
-constexpr int kTile = 16;        // tokens per stage
-constexpr int kStages = 8;       // ring depth
-constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kMaxPartition = 8192;
-constexpr int kMaxBlkIds = kMaxPartition / 16;
-constexpr int kMergeHeads = 8;   // heads per kv-head the merge area holds
+constexpr int kTile = 16;                      // tokens per stage
+constexpr int kSpw = KVQ_SPW;                  // stages per warp
+constexpr int kConsumers = 4;                  // warps per CTA, each streaming its own range
+constexpr int kThreads = kConsumers * 32;
+constexpr int kMinBlocks = KVQ_MIN_BLOCKS;     // CTAs per SM the registers are sized for
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum { kKindSimt = 1, kKindMma = 2 };
 
-template <int D>
-struct Smem {
-    static constexpr int kTileBytes = kTile * D;                       // one K (or V) tile
-    static constexpr int kStageRegion = kStages * 2 * kTileBytes;      // K tiles then V tiles
-    static constexpr int kScaleOff = kStageRegion;                     // fp32 [stages][2][16]
-    static constexpr int kBarOff = kScaleOff + kStages * 2 * kTile * 4;
-    static constexpr int kBlkOff = kBarOff + 2 * kStages * 8;
-    static constexpr int kAbortOff = kBlkOff + kMaxBlkIds * 4;
-    static constexpr int kBytes = kAbortOff + 16;
-    static constexpr int kAlloc = kBytes + 1024;                       // alignment slack
-    // merge area (aliases the stage region once the ring has drained)
-    static constexpr int kMergeAcc = 0;                                // fp32 [warps][heads][D]
-    static constexpr int kMergeM = kConsumerWarps * kMergeHeads * D * 4;
-    static constexpr int kMergeL = kMergeM + kConsumerWarps * kMergeHeads * 4;
-    static_assert(kMergeL + kConsumerWarps * kMergeHeads * 4 <= kStageRegion, "merge area too large");
+// Shared-memory layout of one CTA (bytes from a 1024-aligned base).  Tiles
+// first (1024-aligned for the 128-byte swizzle), then per warp its INT8 row
+// scales, its stage barriers and the query rows of the (sequence, kv-head)
+// pair it is on, then the scan of tiles per sequence and the clamped context
+// lengths.
+struct Layout {
+    int tile_bytes, q_bytes, scales, full, qbuf, scan, total;
+    __host__ __device__ Layout(int D, int G, int B) {
+        tile_bytes = kTile * D;
+        q_bytes = (G * D * 2 + 127) / 128 * 128;
+        scales = kConsumers * kSpw * 2 * tile_bytes;            // [warp][stage][K,V][tile] before this
+        full = scales + kConsumers * kSpw * 2 * kTile * 4;      // f32 [warp][stage][2][16]
+        qbuf = (full + kConsumers * kSpw * 8 + 127) / 128 * 128;  // u64 [warp][stage], then f16 [warp][G][D]
+        scan = qbuf + kConsumers * q_bytes;                     // int S[B + 1], ctx[B]
+        total = scan + (2 * B + 1) * 4;
+    }
 };
 
-// Byte offset of the 16-byte chunk `chunk` of tile row `row` inside a stage
-// tile as the TMA wrote it: 128-byte swizzle (chunk ^ row % 8) for 128-byte
-// rows, plain row-major for 64-byte rows.
 template <int D>
 __device__ __forceinline__ int tile_off(int row, int chunk) {
     if (D == 128) return row * 128 + ((chunk ^ (row & 7)) << 4);
     return row * D + (chunk << 4);
 }
 
-struct Ctx {
-    uint8_t* k_tiles;
-    uint8_t* v_tiles;
-    float* scales;
-    int valid;   // valid tokens in the current tile
-    int stage;
+// Position in the flat tile list: sequence b, kv-head kvh, tile t of n.
+struct Walk {
+    int b, kvh, t, n;
 };
+
+// S[b] = tiles of sequences 0..b-1 (S[B] = all); pair (b, kvh) covers flat
+// tiles [Hkv*S[b] + kvh*n_b, ... + n_b).  f must be below Hkv * S[B]; the
+// largest b with Hkv * S[b] <= f then has n_b > 0.
+__device__ __forceinline__ Walk locate(const int* S, int B, int Hkv, int f) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (Hkv * S[mid] <= f) lo = mid; else hi = mid - 1;
+    }
+    Walk w;
+    w.b = lo;
+    w.n = S[lo + 1] - S[lo];
+    const int r = f - Hkv * S[lo];
+    w.kvh = r / w.n;
+    w.t = r - w.kvh * w.n;
+    return w;
+}
+
+__device__ __forceinline__ void advance(Walk& w, const int* S, int B, int Hkv) {
+    if (++w.t < w.n) return;
+    w.t = 0;
+    if (++w.kvh < Hkv) return;
+    w.kvh = 0;
+    do {
+        ++w.b;
+    } while (w.b < B && S[w.b + 1] == S[w.b]);
+    w.n = w.b < B ? S[w.b + 1] - S[w.b] : 0;
+}
+
+struct Tile {
+    const uint8_t* k;
+    const uint8_t* v;
+    const float* sk;
+    const float* sv;
+    int valid;
+};
+
+// Where a finished segment's state goes: partial slot (chunk, half) of the
+// q-heads hq0 .. hq0 + G - 1; values are multiplied by s_out.
+struct Flush {
+    float* acc;
+    float2* ml;
+    int64_t hq0;
+    int ch, half, nch;
+    float s_out;
+};
+
+__device__ __forceinline__ int64_t slot_index(int64_t hq, int nch, int ch, int half) {
+    return (hq * nch + ch) * 2 + half;
+}
 
 // ---------------------------------------------------------------- SIMT --
 
@@ -94,27 +151,26 @@ struct SimtConsumer {
     static constexpr int LPT = D / 16;     // lanes per token
     static constexpr int TPP = 32 / LPT;   // tokens per pass
     static constexpr int PASSES = kTile / TPP;
+    static constexpr int kMinCtas = GM == 4 ? 3 : kMinBlocks;  // 4 query rows need more registers
     uint32_t qh[GM][8];
     float m[GM], l[GM], acc[GM][16];
     int lane, j, grp, G;
     float qk_scale;
 
-    __device__ void init(const DecodeArgs& a, int b, int kvh, int G_, float qks) {
+    __device__ void init(int G_, float qks) {
         lane = threadIdx.x & 31;
         j = lane % LPT;
         grp = lane / LPT;
         G = G_;
         qk_scale = qks;
+    }
+    // q: the group's G query rows (shared-memory copy)
+    __device__ void set_q(const uint16_t* q) {
 #pragma unroll
         for (int h = 0; h < GM; ++h) {
-            m[h] = -INFINITY;
-            l[h] = 0.f;
-#pragma unroll
-            for (int e = 0; e < 16; ++e) acc[h][e] = 0.f;
             if (h < G) {
-                const uint4* src = reinterpret_cast<const uint4*>(
-                    a.q + ((int64_t)b * a.num_q_heads + (int64_t)kvh * G + h) * D + 16 * j);
-                uint4 x0 = __ldg(src), x1 = __ldg(src + 1);
+                const uint4* src = reinterpret_cast<const uint4*>(q + h * D + 16 * j);
+                const uint4 x0 = src[0], x1 = src[1];
                 qh[h][0] = x0.x; qh[h][1] = x0.y; qh[h][2] = x0.z; qh[h][3] = x0.w;
                 qh[h][4] = x1.x; qh[h][5] = x1.y; qh[h][6] = x1.z; qh[h][7] = x1.w;
             } else {
@@ -123,17 +179,22 @@ struct SimtConsumer {
             }
         }
     }
+    __device__ void reset() {
+#pragma unroll
+        for (int h = 0; h < GM; ++h) {
+            m[h] = -INFINITY;
+            l[h] = 0.f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) acc[h][e] = 0.f;
+        }
+    }
 
-    __device__ void tile(const Ctx& c) {
-        const uint8_t* kt = c.k_tiles + c.stage * Smem<D>::kTileBytes;
-        const uint8_t* vt = c.v_tiles + c.stage * Smem<D>::kTileBytes;
-        const float* sk = c.scales + c.stage * 2 * kTile;
-        const float* sv = sk + kTile;
+    __device__ void tile(const Tile& c) {
         float z[PASSES][GM];
 #pragma unroll
         for (int ps = 0; ps < PASSES; ++ps) {
             const int t = ps * TPP + grp;
-            const uint4 kw = *reinterpret_cast<const uint4*>(kt + tile_off<D>(t, j));
+            const uint4 kw = *reinterpret_cast<const uint4*>(c.k + tile_off<D>(t, j));
             const uint32_t w[4] = {kw.x, kw.y, kw.z, kw.w};
             uint32_t kh[8];
 #pragma unroll
@@ -141,7 +202,7 @@ struct SimtConsumer {
                 kh[2 * e] = dec_x2<FMT>((uint16_t)(w[e] & 0xFFFFu));
                 kh[2 * e + 1] = dec_x2<FMT>((uint16_t)(w[e] >> 16));
             }
-            const float ts = (FMT == INT8 ? sk[t] : 1.0f) * qk_scale;
+            const float ts = (FMT == INT8 ? c.sk[t] : 1.0f) * qk_scale;
 #pragma unroll
             for (int h = 0; h < GM; ++h) {
                 float d0 = 0.f, d1 = 0.f;
@@ -187,11 +248,11 @@ struct SimtConsumer {
 #pragma unroll
         for (int ps = 0; ps < PASSES; ++ps) {
             const int t = ps * TPP + grp;
-            uint4 vw = *reinterpret_cast<const uint4*>(vt + tile_off<D>(t, j));
+            uint4 vw = *reinterpret_cast<const uint4*>(c.v + tile_off<D>(t, j));
             // rows past the context may hold any bytes (NaN codes too): zero them
             if (t >= c.valid) vw = make_uint4(0u, 0u, 0u, 0u);
             const uint32_t w[4] = {vw.x, vw.y, vw.z, vw.w};
-            const float vs = (FMT == INT8 && t < c.valid) ? sv[t] : 1.0f;
+            const float vs = (FMT == INT8 && t < c.valid) ? c.sv[t] : 1.0f;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const float2 lo = f16x2_to_f32x2(dec_x2<FMT>((uint16_t)(w[e] & 0xFFFFu)));
@@ -208,27 +269,33 @@ struct SimtConsumer {
         }
     }
 
-    // Sum the per-group partials and store this warp's state for the merge.
-    __device__ void finish(float* macc, float* mm, float* ml, int warp) {
+    // Sum the per-group partials and write this segment's partial slot.
+    __device__ void flush(const Flush& f) {
 #pragma unroll
         for (int h = 0; h < GM; ++h) {
+            float lh = l[h];
+            float a[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) a[e] = acc[h][e];
 #pragma unroll
             for (int off = LPT; off < 32; off <<= 1) {
-                l[h] += __shfl_xor_sync(0xFFFFFFFFu, l[h], off);
+                lh += __shfl_xor_sync(0xFFFFFFFFu, lh, off);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) acc[h][e] += __shfl_xor_sync(0xFFFFFFFFu, acc[h][e], off);
+                for (int e = 0; e < 16; ++e) a[e] += __shfl_xor_sync(0xFFFFFFFFu, a[e], off);
             }
             if (h < G && grp == 0) {
-                float* dst = macc + ((warp * kMergeHeads) + h) * D + 16 * j;
+                const int64_t si = slot_index(f.hq0 + h, f.nch, f.ch, f.half);
+                float* dst = f.acc + si * D + 16 * j;
 #pragma unroll
                 for (int e = 0; e < 16; e += 4)
-                    *reinterpret_cast<float4*>(dst + e) = make_float4(acc[h][e], acc[h][e + 1], acc[h][e + 2], acc[h][e + 3]);
-                if (j == 0) {
-                    mm[warp * kMergeHeads + h] = m[h];
-                    ml[warp * kMergeHeads + h] = l[h];
-                }
+                    *reinterpret_cast<float4*>(dst + e) =
+                        make_float4(a[e] * f.s_out, a[e + 1] * f.s_out, a[e + 2] * f.s_out, a[e + 3] * f.s_out);
+                if (j == 0) f.ml[si] = make_float2(m[h], lh);
             }
         }
+    }
+    __device__ void flush_empty(const Flush& f) {
+        if (lane < G) f.ml[slot_index(f.hq0 + lane, f.nch, f.ch, f.half)] = make_float2(-INFINITY, 0.f);
     }
 };
 
@@ -242,36 +309,41 @@ struct MmaConsumer {
     static constexpr int DV = D / 8;    // V bytes per thread per token row
     static constexpr int VW = DV / 4;
     static constexpr int MT = D / 16;   // m-tiles of PV (head_dim / 16)
+    static constexpr int kMinCtas = kMinBlocks;
     uint32_t qa[2 * KS];
     float acc[MT][4];
     float m, l;
     int lane, g, c, G;
     float qk_scale;
 
-    __device__ void init(const DecodeArgs& a, int b, int kvh, int G_, float qks) {
+    __device__ void init(int G_, float qks) {
         lane = threadIdx.x & 31;
         g = lane >> 2;
         c = lane & 3;
         G = G_;
         qk_scale = qks;
-        m = -INFINITY;
-        l = 0.f;
-#pragma unroll
-        for (int i = 0; i < MT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-        // qa[2j] = Q[g][DC*c + 4j + {0,1}], qa[2j+1] = Q[g][DC*c + 4j + {2,3}]:
-        // the DC halves Q[g][DC*c ...] in order.
+    }
+    // qa[2j] = Q[g][DC*c + 4j + {0,1}], qa[2j+1] = Q[g][DC*c + 4j + {2,3}]: the
+    // DC halves Q[g][DC*c ...] in order.  q: the group's G query rows
+    // (shared-memory copy).
+    __device__ void set_q(const uint16_t* q) {
         if (g < G) {
-            const uint4* src = reinterpret_cast<const uint4*>(
-                a.q + ((int64_t)b * a.num_q_heads + (int64_t)kvh * G + g) * D + DC * c);
+            const uint4* src = reinterpret_cast<const uint4*>(q + g * D + DC * c);
 #pragma unroll
             for (int i = 0; i < (2 * KS) / 4; ++i) {
-                uint4 x = __ldg(src + i);
+                const uint4 x = src[i];
                 qa[4 * i] = x.x; qa[4 * i + 1] = x.y; qa[4 * i + 2] = x.z; qa[4 * i + 3] = x.w;
             }
         } else {
 #pragma unroll
             for (int i = 0; i < 2 * KS; ++i) qa[i] = 0u;
         }
+    }
+    __device__ void reset() {
+        m = -INFINITY;
+        l = 0.f;
+#pragma unroll
+        for (int i = 0; i < MT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     }
 
     // K words of tile row `row`: the thread's DC contiguous bytes at DC*c.
@@ -298,31 +370,28 @@ struct MmaConsumer {
         }
     }
 
-    __device__ void tile(const Ctx& cx) {
-        const uint8_t* kt = cx.k_tiles + cx.stage * Smem<D>::kTileBytes;
-        const uint8_t* vt = cx.v_tiles + cx.stage * Smem<D>::kTileBytes;
-        const float* sk = cx.scales + cx.stage * 2 * kTile;
-        const float* sv = sk + kTile;
+    __device__ void tile(const Tile& cx) {
         // S^T: rows = q-heads (g), columns = tokens; half A = tokens 0..7 (this
         // thread's B operand row is token g), half B = tokens 8..15.
         float sA[4] = {0.f, 0.f, 0.f, 0.f}, sB[4] = {0.f, 0.f, 0.f, 0.f};
         {
-            uint32_t kA[KW], kB[KW];
-            load_k(kt, g, kA);
-            load_k(kt, 8 + g, kB);
+            uint32_t kw[KW];
+            load_k(cx.k, g, kw);
 #pragma unroll
-            for (int j = 0; j < KS; ++j) {
-                mma_16816(sA, qa[2 * j], 0u, qa[2 * j + 1], 0u, dec_x2<FMT>((uint16_t)(kA[j] & 0xFFFFu)),
-                          dec_x2<FMT>((uint16_t)(kA[j] >> 16)));
-                mma_16816(sB, qa[2 * j], 0u, qa[2 * j + 1], 0u, dec_x2<FMT>((uint16_t)(kB[j] & 0xFFFFu)),
-                          dec_x2<FMT>((uint16_t)(kB[j] >> 16)));
-            }
+            for (int j = 0; j < KS; ++j)
+                mma_16816(sA, qa[2 * j], 0u, qa[2 * j + 1], 0u, dec_x2<FMT>((uint16_t)(kw[j] & 0xFFFFu)),
+                          dec_x2<FMT>((uint16_t)(kw[j] >> 16)));
+            load_k(cx.k, 8 + g, kw);
+#pragma unroll
+            for (int j = 0; j < KS; ++j)
+                mma_16816(sB, qa[2 * j], 0u, qa[2 * j + 1], 0u, dec_x2<FMT>((uint16_t)(kw[j] & 0xFFFFu)),
+                          dec_x2<FMT>((uint16_t)(kw[j] >> 16)));
         }
         // this thread's logits: head g, tokens 2c, 2c+1, 8+2c, 9+2c
         const int t0 = 2 * c, t1 = 2 * c + 1, t2 = 8 + 2 * c, t3 = 9 + 2 * c;
         float z0 = sA[0] * qk_scale, z1 = sA[1] * qk_scale, z2 = sB[0] * qk_scale, z3 = sB[1] * qk_scale;
         if (FMT == INT8) {
-            z0 *= sk[t0]; z1 *= sk[t1]; z2 *= sk[t2]; z3 *= sk[t3];
+            z0 *= cx.sk[t0]; z1 *= cx.sk[t1]; z2 *= cx.sk[t2]; z3 *= cx.sk[t3];
         }
         if (cx.valid < kTile) {
             if (t0 >= cx.valid) z0 = -INFINITY;
@@ -345,10 +414,10 @@ struct MmaConsumer {
         m = mn;
         l = l * alpha + ((p0 + p1) + (p2 + p3));
         if (FMT == INT8) {  // fold the V row scales into P (masked tokens keep p = 0)
-            if (t0 < cx.valid) p0 *= sv[t0];
-            if (t1 < cx.valid) p1 *= sv[t1];
-            if (t2 < cx.valid) p2 *= sv[t2];
-            if (t3 < cx.valid) p3 *= sv[t3];
+            if (t0 < cx.valid) p0 *= cx.sv[t0];
+            if (t1 < cx.valid) p1 *= cx.sv[t1];
+            if (t2 < cx.valid) p2 *= cx.sv[t2];
+            if (t3 < cx.valid) p3 *= cx.sv[t3];
         }
         // P^T as the B operand of PV: k = token, n = head g.  P is carried as
         // an fp16 pair hi + lo (lo = the fp16 residual of p - hi), so the PV
@@ -370,10 +439,10 @@ struct MmaConsumer {
         // out^T += V^T P^T.  A operand rows = head_dim DV*g + 2i (+1 for rows
         // g+8), columns = tokens 2c, 2c+1 | 8+2c, 9+2c.
         uint32_t v0[VW], v1[VW], v2[VW], v3[VW];
-        load_v(vt, t0, v0);
-        load_v(vt, t1, v1);
-        load_v(vt, t2, v2);
-        load_v(vt, t3, v3);
+        load_v(cx.v, t0, v0);
+        load_v(cx.v, t1, v1);
+        load_v(cx.v, t2, v2);
+        load_v(cx.v, t3, v3);
         if (cx.valid < kTile) {  // rows past the context may hold NaN codes: zero them
 #pragma unroll
             for (int e = 0; e < VW; ++e) {
@@ -395,173 +464,235 @@ struct MmaConsumer {
         }
     }
 
-    __device__ void finish(float* macc, float* mm, float* ml, int warp) {
-        l += __shfl_xor_sync(0xFFFFFFFFu, l, 1);
-        l += __shfl_xor_sync(0xFFFFFFFFu, l, 2);
-        if (c == 0 && g < G) {
-            mm[warp * kMergeHeads + g] = m;
-            ml[warp * kMergeHeads + g] = l;
-        }
+    __device__ void flush(const Flush& f) {
+        float lq = l;
+        lq += __shfl_xor_sync(0xFFFFFFFFu, lq, 1);
+        lq += __shfl_xor_sync(0xFFFFFFFFu, lq, 2);
+        if (c == 0 && g < G) f.ml[slot_index(f.hq0 + g, f.nch, f.ch, f.half)] = make_float2(m, lq);
         // acc[i][0..3] = out[head 2c | 2c+1][d = DV*g + 2i | DV*g + 2i + 1]
-        const int h0 = 2 * c, h1 = 2 * c + 1;
 #pragma unroll
-        for (int i = 0; i < MT; ++i) {
-            const int d = DV * g + 2 * i;
-            if (h0 < G) *reinterpret_cast<float2*>(macc + (warp * kMergeHeads + h0) * D + d) = make_float2(acc[i][0], acc[i][2]);
-            if (h1 < G) *reinterpret_cast<float2*>(macc + (warp * kMergeHeads + h1) * D + d) = make_float2(acc[i][1], acc[i][3]);
+        for (int e = 0; e < 2; ++e) {
+            const int h = 2 * c + e;
+            if (h >= G) continue;
+            float* dst = f.acc + slot_index(f.hq0 + h, f.nch, f.ch, f.half) * D + DV * g;
+#pragma unroll
+            for (int i = 0; i < MT; i += 2)
+                *reinterpret_cast<float4*>(dst + 2 * i) =
+                    make_float4(acc[i][e] * f.s_out, acc[i][2 + e] * f.s_out, acc[i + 1][e] * f.s_out,
+                                acc[i + 1][2 + e] * f.s_out);
         }
+    }
+    __device__ void flush_empty(const Flush& f) {
+        if (lane < G) f.ml[slot_index(f.hq0 + lane, f.nch, f.ch, f.half)] = make_float2(-INFINITY, 0.f);
     }
 };
 
 // -------------------------------------------------------------- kernel --
 
 template <int FMT, int D, class Consumer>
-__global__ void __launch_bounds__(kThreads) decode_split_kernel(const __grid_constant__ CUtensorMap tmk,
-                                                                const __grid_constant__ CUtensorMap tmv,
-                                                                const DecodeArgs a) {
-    using S = Smem<D>;
+__global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
+    decode_stream_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                         const DecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    uint8_t* k_tiles = smem;
-    uint8_t* v_tiles = smem + kStages * S::kTileBytes;
-    float* scales = reinterpret_cast<float*>(smem + S::kScaleOff);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
-    uint64_t* empty = full + kStages;
-    int* blk_ids = reinterpret_cast<int*>(smem + S::kBlkOff);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + S::kAbortOff);
-
-    const int p = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int Hkv = a.cache.num_kv_heads, BS = a.cache.block_size;
+    const int B = a.batch, Hkv = a.cache.num_kv_heads, BS = a.cache.block_size;
     const int G = a.num_q_heads / Hkv;
-    int ctx = a.context_lens[b];
-    const int cap = min(a.max_context_len, a.max_blocks_per_seq * BS);
-    if (ctx < 0 || ctx > cap) {
-        if (threadIdx.x == 0 && p == 0 && kvh == 0) record_error(a.err, DEV_ERR_RANGE, ctx);
-        ctx = ctx < 0 ? 0 : cap;
-    }
-    const int P = a.partition_size;
-    const int tok0 = p * P;
-    if (a.num_parts > 1 && tok0 >= ctx) return;  // the reduce reads no partial here
-    const int tok1 = min(tok0 + P, ctx);
-    const int ntiles = tok1 > tok0 ? (tok1 - tok0 + kTile - 1) / kTile : 0;
+    const Layout L(D, G, B);
+    int* S = reinterpret_cast<int*>(smem + L.scan);
+    int* ctx_s = S + B + 1;
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+    // ---- tiles per sequence, scanned (every CTA does this once) -------------
+    {
+        __shared__ int wsum[kConsumers];
+        const int cap = min(a.max_context_len, a.max_blocks_per_seq * BS);
+        const int per = (B + kThreads - 1) / kThreads;
+        const int b0 = threadIdx.x * per, b1 = min(B, b0 + per);
+        int local = 0;
+        for (int b = b0; b < b1; ++b) {
+            int ctx = a.context_lens[b];
+            if (ctx < 0 || ctx > cap) {
+                if (blockIdx.x == 0) record_error(a.err, DEV_ERR_RANGE, ctx);
+                ctx = ctx < 0 ? 0 : cap;
+            }
+            ctx_s[b] = ctx;
+            local += (ctx + kTile - 1) / kTile;
         }
-        *abort_flag = 0;
+        int x = local;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xFFFFFFFFu, x, off);
+            if (lane >= off) x += y;
+        }
+        if (lane == 31) wsum[warp] = x;
+        if (threadIdx.x < kConsumers * kSpw) mbar_init(reinterpret_cast<uint64_t*>(smem + L.full) + threadIdx.x, 1);
         fence_barrier_init();
-    }
-    __syncthreads();
-
-    if (warp == kConsumerWarps) {
-        // ------------------------------------------------------ producer
-        const int blk0 = tok0 / BS;
-        const int nblk = ntiles ? (tok1 - 1) / BS - blk0 + 1 : 0;
-        const int* bt = a.block_tables + (int64_t)b * a.max_blocks_per_seq + blk0;
-        for (int i = lane; i < nblk; i += 32) {
-            int id = bt[i];
-            if (id < 0 || id >= a.cache.num_blocks) {
-                record_error(a.err, DEV_ERR_RANGE, id);
-                id = 0;  // keep the pipeline going on a block that exists
-            }
-            blk_ids[i] = id;
+        __syncthreads();
+        int run = x - local;
+        for (int w = 0; w < warp; ++w) run += wsum[w];
+        for (int b = b0; b < b1; ++b) {
+            S[b] = run;
+            run += (ctx_s[b] + kTile - 1) / kTile;
         }
-        __syncwarp();
-        if (lane == 0 && ntiles > 0) {
-            prefetch_tmap(&tmk);
-            prefetch_tmap(&tmv);
-            const uint64_t pol = policy_evict_first();
-            const uint32_t bytes = 2 * S::kTileBytes + (FMT == INT8 ? 2 * kTile * 4 : 0);
-            int issued = 0;
-            for (int i = 0; i < ntiles; ++i) {
-                const int st = i % kStages;
-                if (!mbar_wait(&empty[st], ((i / kStages) & 1) ^ 1, abort_flag)) {
-                    record_error(a.err, DEV_ERR_TIMEOUT, 1);
-                    *abort_flag = 1;
-                    break;
-                }
-                const int tok = tok0 + i * kTile;
-                const int blk = blk_ids[tok / BS - blk0];
-                const int64_t row = ((int64_t)blk * Hkv + kvh) * BS + tok % BS;
-                mbar_arrive_expect_tx(&full[st], bytes);
-                tma_load_2d(k_tiles + st * S::kTileBytes, &tmk, 0, (int)row, &full[st], pol);
-                tma_load_2d(v_tiles + st * S::kTileBytes, &tmv, 0, (int)row, &full[st], pol);
-                if (FMT == INT8) {
-                    bulk_load(scales + st * 2 * kTile, a.cache.k_scales + row, kTile * 4, &full[st], pol);
-                    bulk_load(scales + st * 2 * kTile + kTile, a.cache.v_scales + row, kTile * 4, &full[st], pol);
-                }
-                issued = i + 1;
-            }
-            // let every copy this CTA started land before the CTA can exit
-            for (int i = max(0, issued - kStages); i < issued; ++i)
-                mbar_wait(&full[i % kStages], (i / kStages) & 1, nullptr);
-        }
-        return;
+        if (threadIdx.x == kThreads - 1) S[B] = run;
+        __syncthreads();
     }
+    // ---- this warp's range of the flat tile list -----------------------------
+    const int T = Hkv * S[B];  // total tiles
+    const int C = a.chunk_tiles;
+    const int nw = max(1, min((int)gridDim.x * kConsumers, T / C));  // a range is never shorter than a chunk
+    const int gw = blockIdx.x * kConsumers + warp;
+    if (T == 0 || gw >= nw) return;
+    const int base_len = T / nw, extra = T % nw;
+    const int lo = gw * base_len + min(gw, extra);
+    const int hi = lo + base_len + (gw < extra ? 1 : 0);
 
-    // --------------------------------------------------------- consumers
+    // paged blocks hold 1, 2 or 4 tiles: tile t sits in block-table entry t >> tpb_shift
+    const int tpb_shift = BS == 16 ? 0 : (BS == 32 ? 1 : 2);
+    const int tpb_mask = (1 << tpb_shift) - 1;
+    uint8_t* tiles = smem + warp * kSpw * 2 * L.tile_bytes;
+    float* scales = reinterpret_cast<float*>(smem + L.scales) + warp * kSpw * 2 * kTile;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full) + warp * kSpw;
+    uint8_t* qbuf = smem + L.qbuf + warp * L.q_bytes;
+
+    // block id of flat tile first + lane (lane-distributed; read back with a shuffle)
+    auto load_id = [&](int first) -> int {
+        const int ff = first + lane;
+        if (ff >= hi) return 0;
+        const Walk w = locate(S, B, Hkv, ff);
+        return __ldg(a.block_tables + (int64_t)w.b * a.max_blocks_per_seq + (w.t >> tpb_shift));
+    };
+    int idc = load_id(lo);       // tiles [window, window + 32)
+    int idn = load_id(lo + 32);  // the next window, loaded one window ahead
+    if (lane == 0) {
+        prefetch_tmap(&tmk);
+        prefetch_tmap(&tmv);
+    }
+    const uint64_t pol = policy_evict_first();
+    const uint32_t tile_tx = 2 * L.tile_bytes + (FMT == INT8 ? 2 * kTile * 4 : 0);
+    const uint32_t q_tx = G * D * 2;
+
     const float s_fp8 = (FMT != INT8 && a.scale) ? __ldg(a.scale) : 1.0f;
-    const float qk_scale = a.sm_scale * s_fp8 * kLog2e;
+    const float s_out = FMT == INT8 ? 1.0f : s_fp8;
+    float* ws_acc = a.ws;
+    float2* ws_ml = reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(a.ws) +
+                                              ws_acc_bytes(B, a.num_q_heads, a.num_chunks, D));
     Consumer cons;
-    cons.init(a, b, kvh, G, qk_scale);
-    Ctx cx{k_tiles, v_tiles, scales, 0, 0};
-    for (int i = warp; i < ntiles; i += kConsumerWarps) {
-        const int st = i % kStages;
-        if (!mbar_wait(&full[st], (i / kStages) & 1, abort_flag)) {
-            if (lane == 0) record_error(a.err, DEV_ERR_TIMEOUT, 2);
-            *abort_flag = 1;
+    cons.init(G, a.sm_scale * s_fp8 * kLog2e);
+
+    // issue side: next flat tile fi, its stage ist, its position iw, and the
+    // first tile of the last pair whose queries were copied (pend)
+    Walk iw = locate(S, B, Hkv, lo);
+    int fi = lo, ist = 0, pend = -1;
+    // consume side: next flat tile fc, its stage cst and barrier parity cph, its
+    // position cw, tile ctc within chunk cch, and the slot half of the segment
+    // in progress
+    Walk cw = iw;
+    int fc = lo, cst = 0;
+    uint32_t cph = 0;
+    int ctc = cw.t % C, cch = cw.t / C;
+    int seg_half = ctc == 0 ? 0 : 1;
+    cons.reset();
+
+    // Issue tiles while a stage is free.  The first tile of a pair also copies
+    // the pair's queries into this warp's query buffer, which must not happen
+    // before the previous pair's first tile has been consumed.
+    auto issue_ready = [&]() {
+        while (fi < hi && fi - fc < kSpw) {
+            const int rel = fi - lo;
+            const bool new_pair = iw.t == 0 || rel == 0;
+            if (new_pair && pend >= fc) break;
+            const int blk_raw = __shfl_sync(0xFFFFFFFFu, idc, rel & 31);
+            if (lane == 0) {
+                int blk = blk_raw;
+                if (blk < 0 || blk >= a.cache.num_blocks) {
+                    record_error(a.err, DEV_ERR_RANGE, blk);
+                    blk = 0;  // keep the pipeline going on a block that exists
+                }
+                const int row = (blk * Hkv + iw.kvh) * BS + ((iw.t & tpb_mask) << 4);
+                uint8_t* kt = tiles + ist * 2 * L.tile_bytes;
+                mbar_arrive_expect_tx(&full[ist], tile_tx + (new_pair ? q_tx : 0u));
+                tma_load_2d(kt, &tmk, 0, row, &full[ist], pol);
+                tma_load_2d(kt + L.tile_bytes, &tmv, 0, row, &full[ist], pol);
+                if (FMT == INT8) {
+                    bulk_load(scales + ist * 2 * kTile, a.cache.k_scales + row, kTile * 4, &full[ist], pol);
+                    bulk_load(scales + ist * 2 * kTile + kTile, a.cache.v_scales + row, kTile * 4, &full[ist], pol);
+                }
+                if (new_pair)
+                    bulk_load(qbuf, a.q + ((int64_t)iw.b * a.num_q_heads + (int64_t)iw.kvh * G) * D, q_tx,
+                              &full[ist], pol);
+            }
+            if (new_pair) pend = fi;
+            advance(iw, S, B, Hkv);
+            ++fi;
+            ist = ist + 1 == kSpw ? 0 : ist + 1;
+            if (((rel + 1) & 31) == 0) {  // next 32-tile window
+                idc = idn;
+                idn = load_id(fi + 32);
+            }
+        }
+    };
+    issue_ready();
+
+    bool failed = false;
+    while (fc < hi) {
+        if (!mbar_wait(&full[cst], cph, nullptr)) {
+            if (lane == 0) record_error(a.err, DEV_ERR_TIMEOUT, fc);
+            failed = true;
             break;
         }
-        cx.stage = st;
-        cx.valid = min(kTile, tok1 - (tok0 + i * kTile));
-        cons.tile(cx);
+        if (cw.t == 0 || fc == lo) cons.set_q(reinterpret_cast<const uint16_t*>(qbuf));  // came with this tile
+        const uint8_t* kt = tiles + cst * 2 * L.tile_bytes;
+        const Tile tl{kt, kt + L.tile_bytes, scales + cst * 2 * kTile, scales + cst * 2 * kTile + kTile,
+                      min(kTile, ctx_s[cw.b] - cw.t * kTile)};
+        cons.tile(tl);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
-    }
-    named_barrier_sync(1, kConsumerWarps * 32);  // every tile consumed: the ring is free
-    float* macc = reinterpret_cast<float*>(smem + S::kMergeAcc);
-    float* mm = reinterpret_cast<float*>(smem + S::kMergeM);
-    float* ml = reinterpret_cast<float*>(smem + S::kMergeL);
-    cons.finish(macc, mm, ml, warp);
-    named_barrier_sync(1, kConsumerWarps * 32);
-
-    const float s_out = FMT == INT8 ? 1.0f : s_fp8;
-    for (int idx = threadIdx.x; idx < G * D; idx += kConsumerWarps * 32) {
-        const int h = idx / D, d = idx % D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, (w < ntiles) ? mm[w * kMergeHeads + h] : -INFINITY);
-        float L = 0.f, O = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                if (w >= ntiles) continue;
-                const float mw = mm[w * kMergeHeads + h];
-                if (mw == -INFINITY) continue;
-                const float e = fast_exp2(mw - M);
-                L += e * ml[w * kMergeHeads + h];
-                O += e * macc[(w * kMergeHeads + h) * D + d];
+        const bool pair_end = cw.t == cw.n - 1;
+        const bool chunk_end = ctc == C - 1 || pair_end;
+        if (chunk_end || fc == hi - 1) {
+            Flush fl{ws_acc, ws_ml, (int64_t)cw.b * a.num_q_heads + (int64_t)cw.kvh * G, cch, seg_half,
+                     a.num_chunks, s_out};
+            cons.flush(fl);
+            if (seg_half == 0 && chunk_end) {  // the whole chunk was this warp's: its second slot is empty
+                fl.half = 1;
+                cons.flush_empty(fl);
+            }
+            cons.reset();
+            seg_half = 0;
+        }
+        ++fc;
+        cst = cst + 1 == kSpw ? 0 : cst + 1;
+        cph ^= cst == 0 ? 1u : 0u;
+        if (pair_end) {
+            cw.t = 0;
+            ctc = 0;
+            cch = 0;
+            if (++cw.kvh == Hkv) {
+                cw.kvh = 0;
+                do {
+                    ++cw.b;
+                } while (cw.b < B && S[cw.b + 1] == S[cw.b]);
+                cw.n = cw.b < B ? S[cw.b + 1] - S[cw.b] : 0;
+            }
+        } else {
+            ++cw.t;
+            if (++ctc == C) {
+                ctc = 0;
+                ++cch;
             }
         }
-        const int64_t hq = (int64_t)b * a.num_q_heads + (int64_t)kvh * G + h;
-        if (a.num_parts == 1) {
-            const float o = L > 0.f ? O * s_out / L : 0.f;
-            a.out[hq * D + d] = __half_as_ushort(__float2half_rn(o));
-        } else {
-            a.ws[(hq * a.num_parts + p) * D + d] = O * s_out;
-            if (d == 0) {
-                float2* ml2 = reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(a.ws) +
-                                                        ws_acc_bytes(a.batch, a.num_q_heads, a.num_parts, D));
-                ml2[hq * a.num_parts + p] = make_float2(M, L);
-            }
+        issue_ready();
+    }
+    if (failed) {  // let the copies this warp started land before it exits
+        for (int f = fc; f < fi; ++f) {
+            mbar_wait(&full[cst], cph, nullptr);
+            cst = cst + 1 == kSpw ? 0 : cst + 1;
+            cph ^= cst == 0 ? 1u : 0u;
         }
     }
 }
 
-// Combine the partials of every context partition of one (sequence, q-head):
+// Combine the chunk partials of one (sequence, q-head):
 // out = sum_i 2^(m_i - M) acc_i / sum_i 2^(m_i - M) l_i.
 template <int D>
 __global__ void __launch_bounds__(D) decode_reduce_kernel(const DecodeArgs a) {
@@ -570,22 +701,24 @@ __global__ void __launch_bounds__(D) decode_reduce_kernel(const DecodeArgs a) {
     int ctx = a.context_lens[b];
     const int cap = min(a.max_context_len, a.max_blocks_per_seq * a.cache.block_size);
     ctx = ctx < 0 ? 0 : min(ctx, cap);
-    const int np = min(a.num_parts, (ctx + a.partition_size - 1) / a.partition_size);
-    const float2* ml2 = reinterpret_cast<const float2*>(reinterpret_cast<const uint8_t*>(a.ws) +
-                                                        ws_acc_bytes(a.batch, a.num_q_heads, a.num_parts, D));
+    const int tiles = (ctx + kTile - 1) / kTile;
+    const int nslots = 2 * min(a.num_chunks, (tiles + a.chunk_tiles - 1) / a.chunk_tiles);
+    const float2* ml = reinterpret_cast<const float2*>(reinterpret_cast<const uint8_t*>(a.ws) +
+                                                       ws_acc_bytes(a.batch, a.num_q_heads, a.num_chunks, D));
+    const int64_t s0 = hq * a.num_chunks * 2;
     float M = -INFINITY;
-    for (int i = 0; i < np; ++i) M = fmaxf(M, ml2[hq * a.num_parts + i].x);
-    float L = 0.f, O = 0.f;
+    for (int i = 0; i < nslots; ++i) M = fmaxf(M, ml[s0 + i].x);
+    float Lsum = 0.f, O = 0.f;
     if (M != -INFINITY) {
-        for (int i = 0; i < np; ++i) {
-            const float2 v = ml2[hq * a.num_parts + i];
+        for (int i = 0; i < nslots; ++i) {
+            const float2 v = ml[s0 + i];
             if (v.x == -INFINITY) continue;
             const float e = fast_exp2(v.x - M);
-            L += e * v.y;
-            O += e * a.ws[(hq * a.num_parts + i) * D + d];
+            Lsum += e * v.y;
+            O += e * a.ws[(s0 + i) * D + d];
         }
     }
-    const float o = L > 0.f ? O / L : 0.f;
+    const float o = Lsum > 0.f ? O / Lsum : 0.f;
     a.out[hq * D + d] = __half_as_ushort(__float2half_rn(o));
 }
 
@@ -622,13 +755,25 @@ bool make_tmap(CUtensorMap* m, void* base, int64_t rows, int D) {
 }
 
 template <int FMT, int D, class Consumer>
-cudaError_t launch_split(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, cudaStream_t s) {
-    auto kern = decode_split_kernel<FMT, D, Consumer>;
-    const int smem = Smem<D>::kAlloc;
+cudaError_t launch_stream(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, cudaStream_t s) {
+    auto kern = decode_stream_kernel<FMT, D, Consumer>;
+    const int smem = Layout(D, a.num_q_heads / a.cache.num_kv_heads, a.batch).total + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.num_parts, a.cache.num_kv_heads, a.batch);
-    kern<<<grid, kThreads, smem, s>>>(tk, tv, a);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0, per_sm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem)) != cudaSuccess) return e;
+    per_sm = per_sm < 1 ? 1 : per_sm;
+    // no more warps than chunks at the largest context: a range spans a chunk
+    const int64_t max_tiles = (int64_t)a.batch * a.cache.num_kv_heads * ((a.max_context_len + kTile - 1) / kTile);
+    int64_t want = max_tiles / a.chunk_tiles;
+    want = want < 1 ? 1 : want;
+    int64_t grid = (want + kConsumers - 1) / kConsumers;
+    if (grid > (int64_t)sms * per_sm) grid = (int64_t)sms * per_sm;
+    kern<<<(unsigned)grid, kThreads, smem, s>>>(tk, tv, a);
     return cudaGetLastError();
 }
 
@@ -637,13 +782,13 @@ cudaError_t launch_fmt_d(const CUtensorMap& tk, const CUtensorMap& tv, const Dec
     const int G = a.num_q_heads / a.cache.num_kv_heads;
     cudaError_t e;
     if (a.kernel == kKindSimt) {
-        if (G == 1) e = launch_split<FMT, D, SimtConsumer<FMT, D, 1>>(tk, tv, a, s);
-        else if (G == 2) e = launch_split<FMT, D, SimtConsumer<FMT, D, 2>>(tk, tv, a, s);
-        else e = launch_split<FMT, D, SimtConsumer<FMT, D, 4>>(tk, tv, a, s);
+        if (G == 1) e = launch_stream<FMT, D, SimtConsumer<FMT, D, 1>>(tk, tv, a, s);
+        else if (G == 2) e = launch_stream<FMT, D, SimtConsumer<FMT, D, 2>>(tk, tv, a, s);
+        else e = launch_stream<FMT, D, SimtConsumer<FMT, D, 4>>(tk, tv, a, s);
     } else {
-        e = launch_split<FMT, D, MmaConsumer<FMT, D>>(tk, tv, a, s);
+        e = launch_stream<FMT, D, MmaConsumer<FMT, D>>(tk, tv, a, s);
     }
-    if (e != cudaSuccess || a.num_parts == 1) return e;
+    if (e != cudaSuccess) return e;
     decode_reduce_kernel<D><<<dim3(a.num_q_heads, a.batch), D, 0, s>>>(a);
     return cudaGetLastError();
 }

@@ -52,9 +52,9 @@ struct DecodeArgs {
     const float* scale;  // device, may be null (= 1.0); FP8 only
     float sm_scale;      // resolved (> 0)
     uint16_t* out;       // fp16 bits [B][Hq][D]
-    float* ws;           // partials, or null when num_parts == 1
-    int32_t partition_size;
-    int32_t num_parts;
+    float* ws;           // chunk partials (layout below)
+    int32_t chunk_tiles; // C: 16-token tiles per context chunk
+    int32_t num_chunks;  // chunks per sequence at max_context_len
     int32_t kernel;      // 1 = CUDA-core, 2 = tensor-core
     unsigned long long* err;
 };
@@ -63,13 +63,15 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 
-// Workspace layout of the context split: acc fp32 [B][Hq][P][D] followed by
-// (m, l) fp32 pairs [B][Hq][P], the second part 256-byte aligned.
-KVQ_HD inline size_t ws_acc_bytes(int64_t B, int64_t Hq, int64_t P, int64_t D) {
-    return ((size_t)(B * Hq * P * D) * 4 + 255) / 256 * 256;
+// Workspace layout: every context chunk of every (sequence, q-head) has two
+// partial slots (a chunk is streamed by at most two warps).  acc fp32
+// [B][Hq][chunks][2][D] followed (256-byte aligned) by (m, l) fp32 pairs
+// [B][Hq][chunks][2].
+KVQ_HD inline size_t ws_acc_bytes(int64_t B, int64_t Hq, int64_t NCH, int64_t D) {
+    return ((size_t)(B * Hq * NCH * 2 * D) * 4 + 255) / 256 * 256;
 }
-KVQ_HD inline size_t ws_bytes(int64_t B, int64_t Hq, int64_t P, int64_t D) {
-    return ws_acc_bytes(B, Hq, P, D) + ((size_t)(B * Hq * P) * 8 + 255) / 256 * 256;
+KVQ_HD inline size_t ws_bytes(int64_t B, int64_t Hq, int64_t NCH, int64_t D) {
+    return ws_acc_bytes(B, Hq, NCH, D) + ((size_t)(B * Hq * NCH * 2) * 8 + 255) / 256 * 256;
 }
 
 }  // namespace kvq
