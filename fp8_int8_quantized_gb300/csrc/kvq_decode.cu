@@ -310,9 +310,15 @@ struct MmaConsumer {
     static constexpr int VW = DV / 4;
     static constexpr int MT = D / 16;   // m-tiles of PV (head_dim / 16)
     static constexpr int kMinCtas = kMinBlocks;
+    // INT8 codes enter the tensor cores as fp16 1152 + code (exact); the
+    // constant is taken out again: 1152 * sum(q) from each logit, 1152 * sum(P')
+    // from each output.
+    static constexpr float kBias = 1152.f;
     uint32_t qa[2 * KS];
     float acc[MT][4];
     float m, l;
+    float qsum;  // INT8: sum of this head's query row (head g)
+    float psum;  // INT8: running sum of the fp16 P' weights fed to PV (head g, this thread's tokens)
     int lane, g, c, G;
     float qk_scale;
 
@@ -338,10 +344,28 @@ struct MmaConsumer {
 #pragma unroll
             for (int i = 0; i < 2 * KS; ++i) qa[i] = 0u;
         }
+        if (FMT == INT8) {
+            float sq = 0.f;
+#pragma unroll
+            for (int i = 0; i < 2 * KS; ++i) {
+                const float2 v = f16x2_to_f32x2(qa[i]);
+                sq += v.x + v.y;
+            }
+            sq += __shfl_xor_sync(0xFFFFFFFFu, sq, 1);
+            sq += __shfl_xor_sync(0xFFFFFFFFu, sq, 2);
+            qsum = sq;
+        }
+    }
+    // INT8 word (4 codes) -> the two f16x2 operands 1152 + code of bytes (0,1) and (2,3)
+    __device__ __forceinline__ static void int8_biased(uint32_t w, uint32_t& lo, uint32_t& hi) {
+        const uint32_t x = w ^ 0x80808080u;  // code + 128 as an unsigned byte
+        lo = prmt(x, 0x64646464u, 0x4140u);
+        hi = prmt(x, 0x64646464u, 0x4342u);
     }
     __device__ void reset() {
         m = -INFINITY;
         l = 0.f;
+        psum = 0.f;
 #pragma unroll
         for (int i = 0; i < MT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     }
@@ -376,22 +400,34 @@ struct MmaConsumer {
         float sA[4] = {0.f, 0.f, 0.f, 0.f}, sB[4] = {0.f, 0.f, 0.f, 0.f};
         {
             uint32_t kw[KW];
-            load_k(cx.k, g, kw);
 #pragma unroll
-            for (int j = 0; j < KS; ++j)
-                mma_16816(sA, qa[2 * j], 0u, qa[2 * j + 1], 0u, dec_x2<FMT>((uint16_t)(kw[j] & 0xFFFFu)),
-                          dec_x2<FMT>((uint16_t)(kw[j] >> 16)));
-            load_k(cx.k, 8 + g, kw);
+            for (int half = 0; half < 2; ++half) {
+                load_k(cx.k, 8 * half + g, kw);
 #pragma unroll
-            for (int j = 0; j < KS; ++j)
-                mma_16816(sB, qa[2 * j], 0u, qa[2 * j + 1], 0u, dec_x2<FMT>((uint16_t)(kw[j] & 0xFFFFu)),
-                          dec_x2<FMT>((uint16_t)(kw[j] >> 16)));
+                for (int j = 0; j < KS; ++j) {
+                    uint32_t b0, b1;
+                    if (FMT == INT8) {
+                        int8_biased(kw[j], b0, b1);
+                    } else {
+                        b0 = dec_fp8x2<FMT>((uint16_t)(kw[j] & 0xFFFFu));
+                        b1 = dec_fp8x2<FMT>((uint16_t)(kw[j] >> 16));
+                    }
+                    if (half == 0) mma_16816(sA, qa[2 * j], 0u, qa[2 * j + 1], 0u, b0, b1);
+                    else mma_16816(sB, qa[2 * j], 0u, qa[2 * j + 1], 0u, b0, b1);
+                }
+            }
         }
         // this thread's logits: head g, tokens 2c, 2c+1, 8+2c, 9+2c
         const int t0 = 2 * c, t1 = 2 * c + 1, t2 = 8 + 2 * c, t3 = 9 + 2 * c;
-        float z0 = sA[0] * qk_scale, z1 = sA[1] * qk_scale, z2 = sB[0] * qk_scale, z3 = sB[1] * qk_scale;
-        if (FMT == INT8) {
-            z0 *= cx.sk[t0]; z1 *= cx.sk[t1]; z2 *= cx.sk[t2]; z3 *= cx.sk[t3];
+        float z0, z1, z2, z3;
+        if (FMT == INT8) {  // remove the operand bias, then apply the K row scales
+            const float corr = kBias * qsum;
+            z0 = (sA[0] - corr) * (qk_scale * cx.sk[t0]);
+            z1 = (sA[1] - corr) * (qk_scale * cx.sk[t1]);
+            z2 = (sB[0] - corr) * (qk_scale * cx.sk[t2]);
+            z3 = (sB[1] - corr) * (qk_scale * cx.sk[t3]);
+        } else {
+            z0 = sA[0] * qk_scale; z1 = sA[1] * qk_scale; z2 = sB[0] * qk_scale; z3 = sB[1] * qk_scale;
         }
         if (cx.valid < kTile) {
             if (t0 >= cx.valid) z0 = -INFINITY;
@@ -427,6 +463,10 @@ struct MmaConsumer {
         const uint32_t pb0 = pack_f16x2(p0, p1), pb1 = pack_f16x2(p2, p3);
         const float2 h01 = f16x2_to_f32x2(pb0), h23 = f16x2_to_f32x2(pb1);
         const uint32_t pl0 = pack_f16x2(p0 - h01.x, p1 - h01.y), pl1 = pack_f16x2(p2 - h23.x, p3 - h23.y);
+        if (FMT == INT8) {  // the weights exactly as the tensor cores see them
+            const float2 l01 = f16x2_to_f32x2(pl0), l23 = f16x2_to_f32x2(pl1);
+            psum = psum * alpha + (((h01.x + l01.x) + (h01.y + l01.y)) + ((h23.x + l23.x) + (h23.y + l23.y)));
+        }
         // rescale the accumulators: columns are heads 2c and 2c+1
         if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
             const float a0 = __shfl_sync(0xFFFFFFFFu, alpha, 8 * c);
@@ -452,13 +492,29 @@ struct MmaConsumer {
                 if (t3 >= cx.valid) v3[e] = 0u;
             }
         }
+        if (FMT == INT8) {  // code + 128 as unsigned bytes, once per word
+#pragma unroll
+            for (int e = 0; e < VW; ++e) {
+                v0[e] ^= 0x80808080u; v1[e] ^= 0x80808080u; v2[e] ^= 0x80808080u; v3[e] ^= 0x80808080u;
+            }
+        }
 #pragma unroll
         for (int i = 0; i < MT; ++i) {
             const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
             const uint32_t x01 = prmt(v0[i >> 1], v1[i >> 1], sel);
             const uint32_t x23 = prmt(v2[i >> 1], v3[i >> 1], sel);
-            const uint32_t a0 = dec_x2<FMT>((uint16_t)(x01 & 0xFFFFu)), a1 = dec_x2<FMT>((uint16_t)(x01 >> 16));
-            const uint32_t a2 = dec_x2<FMT>((uint16_t)(x23 & 0xFFFFu)), a3 = dec_x2<FMT>((uint16_t)(x23 >> 16));
+            uint32_t a0, a1, a2, a3;
+            if (FMT == INT8) {  // fp16 1152 + code; the bias leaves with psum at the flush
+                a0 = prmt(x01, 0x64646464u, 0x4140u);
+                a1 = prmt(x01, 0x64646464u, 0x4342u);
+                a2 = prmt(x23, 0x64646464u, 0x4140u);
+                a3 = prmt(x23, 0x64646464u, 0x4342u);
+            } else {
+                a0 = dec_fp8x2<FMT>((uint16_t)(x01 & 0xFFFFu));
+                a1 = dec_fp8x2<FMT>((uint16_t)(x01 >> 16));
+                a2 = dec_fp8x2<FMT>((uint16_t)(x23 & 0xFFFFu));
+                a3 = dec_fp8x2<FMT>((uint16_t)(x23 >> 16));
+            }
             mma_16816(acc[i], a0, a1, a2, a3, pb0, pb1);
             mma_16816(acc[i], a0, a1, a2, a3, pl0, pl1);
         }
@@ -469,17 +525,26 @@ struct MmaConsumer {
         lq += __shfl_xor_sync(0xFFFFFFFFu, lq, 1);
         lq += __shfl_xor_sync(0xFFFFFFFFu, lq, 2);
         if (c == 0 && g < G) f.ml[slot_index(f.hq0 + g, f.nch, f.ch, f.half)] = make_float2(m, lq);
+        float bias[2] = {0.f, 0.f};
+        if (FMT == INT8) {  // 1152 * sum(P') of heads 2c and 2c+1
+            float ps = psum;
+            ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 1);
+            ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 2);
+            bias[0] = kBias * __shfl_sync(0xFFFFFFFFu, ps, 8 * c);
+            bias[1] = kBias * __shfl_sync(0xFFFFFFFFu, ps, 8 * c + 4);
+        }
         // acc[i][0..3] = out[head 2c | 2c+1][d = DV*g + 2i | DV*g + 2i + 1]
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int h = 2 * c + e;
             if (h >= G) continue;
             float* dst = f.acc + slot_index(f.hq0 + h, f.nch, f.ch, f.half) * D + DV * g;
+            const float bs = bias[e];
 #pragma unroll
             for (int i = 0; i < MT; i += 2)
                 *reinterpret_cast<float4*>(dst + 2 * i) =
-                    make_float4(acc[i][e] * f.s_out, acc[i][2 + e] * f.s_out, acc[i + 1][e] * f.s_out,
-                                acc[i + 1][2 + e] * f.s_out);
+                    make_float4((acc[i][e] - bs) * f.s_out, (acc[i][2 + e] - bs) * f.s_out,
+                                (acc[i + 1][e] - bs) * f.s_out, (acc[i + 1][2 + e] - bs) * f.s_out);
         }
     }
     __device__ void flush_empty(const Flush& f) {
