@@ -109,7 +109,7 @@ KVQ_API kvq_status kvq_append(const void* k, const void* v, const kvq_cache* cac
                       const float* scale, int32_t fmt, kvq_stream_t stream);
 
 /* Bytes of workspace kvq_decode_attention needs for these sizes on the
- * current device (0 when no context split happens).  partition_size as below. */
+ * current device (nonzero whenever batch > 0).  partition_size as below. */
 KVQ_API size_t kvq_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                  int32_t head_dim, int32_t max_context_len,
                                  int32_t partition_size);
@@ -124,13 +124,18 @@ KVQ_API size_t kvq_decode_workspace_size(int32_t batch, int32_t num_q_heads, int
  *     with context 0 gets a zero output.
  *   q-head h reads kv-head h / (num_q_heads / num_kv_heads); num_q_heads must be
  *     a multiple of num_kv_heads and the group size at most 8.
+ *   batch at most 4096, and batch * num_kv_heads * ceil(max_context_len / 16)
+ *     below 2^31 (KVQ_ERR_UNSUPPORTED otherwise).
  *   scale: FP8 per-tensor scale as in kvq_append (NULL = 1.0); ignored for INT8.
  *   sm_scale: softmax scale; 0 selects 1 / sqrt(head_dim).
  *   out: fp16 [batch][num_q_heads][head_dim] = softmax(sm_scale * q K^T) V.
- *   workspace: device scratch of kvq_decode_workspace_size() bytes (may be NULL
- *     when that size is 0), 256-byte aligned; contents are not preserved.
- *   partition_size: tokens per context split (a multiple of 64, at most 8192),
- *     or 0 to let the library choose from the sizes and the device's SM count. */
+ *   workspace: device scratch of kvq_decode_workspace_size() bytes, 256-byte
+ *     aligned, holding the partial results of context chunks; contents are not
+ *     preserved and nothing in it needs to be initialised.
+ *   partition_size: tokens per context chunk whose partial result is kept
+ *     (a multiple of 64, at most 65536), or 0 to let the library choose from
+ *     the sizes and the device's SM count.  Results agree across choices up to
+ *     fp32 summation order. */
 KVQ_API kvq_status kvq_decode_attention(const void* q, const kvq_cache* cache,
                                 const int32_t* block_tables, int32_t max_blocks_per_seq,
                                 const int32_t* context_lens, int32_t batch,
