@@ -24,7 +24,7 @@ STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED", 3: "K
 KERNEL_AUTO, KERNEL_SIMT, KERNEL_MMA = 0, 1, 2
 EXPORTS = ("kvq_append", "kvq_decode_workspace_size", "kvq_decode_attention", "kvq_dequant",
            "kvq_set_decode_kernel", "kvq_device_error_check", "kvq_status_string", "kvq_abi_version",
-           "kvq_decode_attention_static_scratch", "kvq_static_scratch_bytes")
+           "kvq_decode_attention_static_scratch", "kvq_static_scratch_bytes", "kvq_set_decode_timing_events")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkvq.so")
@@ -75,6 +75,8 @@ def lib():
         L.kvq_static_scratch_bytes.restype = ctypes.c_size_t
         L.kvq_dequant.restype = ctypes.c_int
         L.kvq_dequant.argtypes = [P, P, i64, P, i32, P, P, P]
+        L.kvq_set_decode_timing_events.restype = None
+        L.kvq_set_decode_timing_events.argtypes = [P, P]
         L.kvq_set_decode_kernel.restype = i32
         L.kvq_set_decode_kernel.argtypes = [i32]
         L.kvq_device_error_check.restype = ctypes.c_int
@@ -228,6 +230,15 @@ def set_decode_kernel(kind: int) -> int:
     if prev < 0:
         raise ValueError(f"unknown decode kernel kind {kind}")
     return prev
+
+
+def set_decode_timing_events(begin=None, end=None) -> None:
+    """kvq_set_decode_timing_events with two recorded torch.cuda.Event objects
+    (enable_timing=True), or no arguments to turn the hook off."""
+    if begin is None or end is None:
+        lib().kvq_set_decode_timing_events(None, None)
+    else:
+        lib().kvq_set_decode_timing_events(begin.cuda_event, end.cuda_event)
 
 
 def device_error_check(stream=None) -> tuple[int, int]:

@@ -23,6 +23,7 @@ std::mutex g_mu;
 unsigned long long* g_err_ptr[kMaxDevices] = {};
 int g_sm_count[kMaxDevices] = {};
 std::atomic<int> g_decode_kernel{0};
+cudaEvent_t g_ev_begin = nullptr, g_ev_end = nullptr;
 
 constexpr int kMaxChunkTokens = 65536;
 constexpr int kMaxBatch = 4096;   // the decode kernel scans the context lengths in shared memory
@@ -117,6 +118,15 @@ const char* kvq_status_string(kvq_status s) {
     return "unknown status";
 }
 
+void kvq_set_decode_timing_events(void* ev_begin, void* ev_end) {
+    if (ev_begin && ev_end) {
+        g_ev_begin = static_cast<cudaEvent_t>(ev_begin);
+        g_ev_end = static_cast<cudaEvent_t>(ev_end);
+    } else {
+        g_ev_begin = g_ev_end = nullptr;
+    }
+}
+
 int32_t kvq_set_decode_kernel(int32_t kind) {
     if (kind < 0 || kind > 2) return -1;
     return g_decode_kernel.exchange(kind);
@@ -201,6 +211,8 @@ kvq_status kvq_decode_attention(const void* q, const kvq_cache* cache, const int
     a.num_chunks = nch;
     a.kernel = kind;
     a.err = err;
+    a.ev_begin = g_ev_begin;
+    a.ev_end = g_ev_end;
     return kvq::launch_decode(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 

@@ -846,6 +846,7 @@ template <int FMT, int D>
 cudaError_t launch_fmt_d(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, cudaStream_t s) {
     const int G = a.num_q_heads / a.cache.num_kv_heads;
     cudaError_t e;
+    if (a.ev_begin && (e = cudaEventRecord(a.ev_begin, s)) != cudaSuccess) return e;
     if (a.kernel == kKindSimt) {
         if (G == 1) e = launch_stream<FMT, D, SimtConsumer<FMT, D, 1>>(tk, tv, a, s);
         else if (G == 2) e = launch_stream<FMT, D, SimtConsumer<FMT, D, 2>>(tk, tv, a, s);
@@ -854,6 +855,7 @@ cudaError_t launch_fmt_d(const CUtensorMap& tk, const CUtensorMap& tv, const Dec
         e = launch_stream<FMT, D, MmaConsumer<FMT, D>>(tk, tv, a, s);
     }
     if (e != cudaSuccess) return e;
+    if (a.ev_end && (e = cudaEventRecord(a.ev_end, s)) != cudaSuccess) return e;
     decode_reduce_kernel<D><<<dim3(a.num_q_heads, a.batch), D, 0, s>>>(a);
     return cudaGetLastError();
 }

@@ -57,6 +57,7 @@ struct DecodeArgs {
     int32_t num_chunks;  // chunks per sequence at max_context_len
     int32_t kernel;      // 1 = CUDA-core, 2 = tensor-core
     unsigned long long* err;
+    cudaEvent_t ev_begin, ev_end;  // optional: recorded around the main kernel
 };
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);

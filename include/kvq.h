@@ -179,6 +179,13 @@ KVQ_API kvq_status kvq_dequant(const kvq_cache* cache, const int64_t* slots, int
  * previous value, or -1 for an unknown kind (nothing changes). */
 KVQ_API int32_t kvq_set_decode_kernel(int32_t kind);
 
+/* Measurement hook.  While set (both non-NULL), every kvq_decode_attention
+ * call records ev_begin on its stream immediately before its main kernel and
+ * ev_end immediately after it, so that kernel can be timed alone (the call
+ * also launches a small reduce kernel).  Both are cudaEvent_t created by the
+ * caller; NULL, NULL turns the hook off.  Process-wide, not thread-safe. */
+KVQ_API void kvq_set_decode_timing_events(void* ev_begin, void* ev_end);
+
 /* Synchronizes `stream`, then reads and clears the current device's error word.
  * Returns KVQ_OK, KVQ_ERR_OUT_OF_RANGE or KVQ_ERR_TIMEOUT (the first one
  * recorded); *detail (if not NULL) receives the offending slot / block id. */
