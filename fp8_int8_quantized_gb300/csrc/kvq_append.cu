@@ -21,6 +21,8 @@ constexpr int kThreads = 256;
 template <int FMT, int D>
 __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
     constexpr int CPR = D / 16;  // threads per row
+    griddep_wait();
+    griddep_launch();
     const int64_t per_tensor = a.num_tokens * a.cache.num_kv_heads * CPR;
     const int64_t idx = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     const int which = blockIdx.y;  // 0 = K, 1 = V
@@ -96,11 +98,8 @@ cudaError_t launch_fmt(const AppendArgs& a, cudaStream_t s) {
     const int D = a.cache.head_dim;
     const int64_t per = a.num_tokens * a.cache.num_kv_heads * (D / 16);
     dim3 grid((unsigned)((per + kThreads - 1) / kThreads), 2);
-    if (D == 64)
-        append_kernel<FMT, 64><<<grid, kThreads, 0, s>>>(a);
-    else
-        append_kernel<FMT, 128><<<grid, kThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    if (D == 64) return launch_pdl(append_kernel<FMT, 64>, grid, dim3(kThreads), 0, s, a);
+    return launch_pdl(append_kernel<FMT, 128>, grid, dim3(kThreads), 0, s, a);
 }
 
 }  // namespace

@@ -566,6 +566,8 @@ __global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
     const Layout L(D, G, B);
     int* S = reinterpret_cast<int*>(smem + L.scan);
     int* ctx_s = S + B + 1;
+    griddep_wait();    // inputs may come from the previous kernel (an append)
+    griddep_launch();  // the reduce kernel may be scheduled as CTAs finish
 
     // ---- tiles per sequence, scanned (every CTA does this once) -------------
     {
@@ -757,12 +759,20 @@ __global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
     }
 }
 
-// Combine the chunk partials of one (sequence, q-head):
-// out = sum_i 2^(m_i - M) acc_i / sum_i 2^(m_i - M) l_i.
+// Combine the chunk partials of one (sequence, q-head), one warp each:
+// out = sum_i 2^(m_i - M) acc_i / sum_i 2^(m_i - M) l_i.  Lanes read the slots'
+// (m, l) in parallel; every lane then sums D/32 consecutive outputs over the
+// slots with independent vector loads.
+constexpr int kReduceWarps = 4;
+
 template <int D>
-__global__ void __launch_bounds__(D) decode_reduce_kernel(const DecodeArgs a) {
-    const int hq_local = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
-    const int64_t hq = (int64_t)b * a.num_q_heads + hq_local;
+__global__ void __launch_bounds__(kReduceWarps * 32) decode_reduce_kernel(const DecodeArgs a) {
+    constexpr int V = D / 32;  // outputs per lane: 4 (D = 128) or 2 (D = 64)
+    griddep_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t hq = (int64_t)blockIdx.x * kReduceWarps + (threadIdx.x >> 5);
+    if (hq >= (int64_t)a.batch * a.num_q_heads) return;
+    const int b = (int)(hq / a.num_q_heads);
     int ctx = a.context_lens[b];
     const int cap = min(a.max_context_len, a.max_blocks_per_seq * a.cache.block_size);
     ctx = ctx < 0 ? 0 : min(ctx, cap);
@@ -772,19 +782,34 @@ __global__ void __launch_bounds__(D) decode_reduce_kernel(const DecodeArgs a) {
                                                        ws_acc_bytes(a.batch, a.num_q_heads, a.num_chunks, D));
     const int64_t s0 = hq * a.num_chunks * 2;
     float M = -INFINITY;
-    for (int i = 0; i < nslots; ++i) M = fmaxf(M, ml[s0 + i].x);
-    float Lsum = 0.f, O = 0.f;
+    for (int i = lane; i < nslots; i += 32) M = fmaxf(M, ml[s0 + i].x);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
+    float Lsum = 0.f, O[V];
+#pragma unroll
+    for (int k = 0; k < V; ++k) O[k] = 0.f;
     if (M != -INFINITY) {
         for (int i = 0; i < nslots; ++i) {
             const float2 v = ml[s0 + i];
-            if (v.x == -INFINITY) continue;
+            if (v.x == -INFINITY) continue;  // empty slot: its accumulator was never written
             const float e = fast_exp2(v.x - M);
             Lsum += e * v.y;
-            O += e * a.ws[(s0 + i) * D + d];
+            const float* src = a.ws + (s0 + i) * D + V * lane;
+            if (V == 4) {
+                const float4 x = *reinterpret_cast<const float4*>(src);
+                O[0] += e * x.x; O[1] += e * x.y; O[2] += e * x.z; O[3] += e * x.w;
+            } else {
+                const float2 x = *reinterpret_cast<const float2*>(src);
+                O[0] += e * x.x; O[1] += e * x.y;
+            }
         }
     }
-    const float o = Lsum > 0.f ? O / Lsum : 0.f;
-    a.out[hq * D + d] = __half_as_ushort(__float2half_rn(o));
+    const float inv = Lsum > 0.f ? 1.0f / Lsum : 0.f;
+    uint32_t* dst = reinterpret_cast<uint32_t*>(a.out + hq * D + V * lane);
+    if (V == 4)
+        *reinterpret_cast<uint2*>(dst) = make_uint2(pack_f16x2(O[0] * inv, O[1] * inv), pack_f16x2(O[2] * inv, O[3] * inv));
+    else
+        *dst = pack_f16x2(O[0] * inv, O[1] * inv);
 }
 
 // ---------------------------------------------------------------- host --
@@ -838,8 +863,7 @@ cudaError_t launch_stream(const CUtensorMap& tk, const CUtensorMap& tv, const De
     want = want < 1 ? 1 : want;
     int64_t grid = (want + kConsumers - 1) / kConsumers;
     if (grid > (int64_t)sms * per_sm) grid = (int64_t)sms * per_sm;
-    kern<<<(unsigned)grid, kThreads, smem, s>>>(tk, tv, a);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), smem, s, tk, tv, a);
 }
 
 template <int FMT, int D>
@@ -856,8 +880,9 @@ cudaError_t launch_fmt_d(const CUtensorMap& tk, const CUtensorMap& tv, const Dec
     }
     if (e != cudaSuccess) return e;
     if (a.ev_end && (e = cudaEventRecord(a.ev_end, s)) != cudaSuccess) return e;
-    decode_reduce_kernel<D><<<dim3(a.num_q_heads, a.batch), D, 0, s>>>(a);
-    return cudaGetLastError();
+    const int64_t heads = (int64_t)a.batch * a.num_q_heads;
+    return launch_pdl(decode_reduce_kernel<D>, dim3((unsigned)((heads + kReduceWarps - 1) / kReduceWarps)),
+                      dim3(kReduceWarps * 32), 0, s, a);
 }
 
 template <int FMT>

@@ -214,6 +214,14 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel on the stream is still
+// running; griddep_wait() blocks until that kernel has completed and its
+// memory is visible, so it must precede every global read of data a previous
+// kernel may have written.  griddep_launch() lets the next kernel start early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // mma.sync m16n8k16, f16 inputs, fp32 accumulate (D = A * B + D).
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                           uint32_t b0, uint32_t b1) {

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #ifdef __CUDACC__
 #define KVQ_HD __host__ __device__
 #else
@@ -59,6 +61,27 @@ struct DecodeArgs {
     unsigned long long* err;
     cudaEvent_t ev_begin, ev_end;  // optional: recorded around the main kernel
 };
+
+#ifdef __CUDACC__
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the previous kernel on the stream finishes; it must call
+// griddep_wait() before reading anything that kernel may have written.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+#endif
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t s);
