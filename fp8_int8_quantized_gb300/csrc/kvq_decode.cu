@@ -122,13 +122,29 @@ __device__ __forceinline__ void advance(Walk& w, const int* S, int B, int Hkv) {
     w.n = w.b < B ? S[w.b + 1] - S[w.b] : 0;
 }
 
+// One staged tile, by 32-bit shared-memory address: K codes, V codes, and
+// (INT8) 16 K row scales followed by 16 V row scales.
 struct Tile {
-    const uint8_t* k;
-    const uint8_t* v;
-    const float* sk;
-    const float* sv;
+    uint32_t k, v, s;
     int valid;
 };
+
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 r;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(a));
+    return r;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+    uint2 r;
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(a));
+    return r;
+}
+__device__ __forceinline__ float2 __uint_as_float2(uint2 v) { return make_float2(__uint_as_float(v.x), __uint_as_float(v.y)); }
+__device__ __forceinline__ float ldsf(uint32_t a) {
+    float r;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(r) : "r"(a));
+    return r;
+}
 
 // Where a finished segment's state goes: partial slot (chunk, half) of the
 // q-heads hq0 .. hq0 + G - 1; values are multiplied by s_out.
@@ -194,7 +210,7 @@ struct SimtConsumer {
 #pragma unroll
         for (int ps = 0; ps < PASSES; ++ps) {
             const int t = ps * TPP + grp;
-            const uint4 kw = *reinterpret_cast<const uint4*>(c.k + tile_off<D>(t, j));
+            const uint4 kw = lds128(c.k + tile_off<D>(t, j));
             const uint32_t w[4] = {kw.x, kw.y, kw.z, kw.w};
             uint32_t kh[8];
 #pragma unroll
@@ -202,7 +218,7 @@ struct SimtConsumer {
                 kh[2 * e] = dec_x2<FMT>((uint16_t)(w[e] & 0xFFFFu));
                 kh[2 * e + 1] = dec_x2<FMT>((uint16_t)(w[e] >> 16));
             }
-            const float ts = (FMT == INT8 ? c.sk[t] : 1.0f) * qk_scale;
+            const float ts = (FMT == INT8 ? ldsf(c.s + 4 * t) : 1.0f) * qk_scale;
 #pragma unroll
             for (int h = 0; h < GM; ++h) {
                 float d0 = 0.f, d1 = 0.f;
@@ -248,11 +264,11 @@ struct SimtConsumer {
 #pragma unroll
         for (int ps = 0; ps < PASSES; ++ps) {
             const int t = ps * TPP + grp;
-            uint4 vw = *reinterpret_cast<const uint4*>(c.v + tile_off<D>(t, j));
+            uint4 vw = lds128(c.v + tile_off<D>(t, j));
             // rows past the context may hold any bytes (NaN codes too): zero them
             if (t >= c.valid) vw = make_uint4(0u, 0u, 0u, 0u);
             const uint32_t w[4] = {vw.x, vw.y, vw.z, vw.w};
-            const float vs = (FMT == INT8 && t < c.valid) ? c.sv[t] : 1.0f;
+            const float vs = (FMT == INT8 && t < c.valid) ? ldsf(c.s + 64 + 4 * t) : 1.0f;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const float2 lo = f16x2_to_f32x2(dec_x2<FMT>((uint16_t)(w[e] & 0xFFFFu)));
@@ -321,6 +337,10 @@ struct MmaConsumer {
     float psum;  // INT8: running sum of the fp16 P' weights fed to PV (head g, this thread's tokens)
     int lane, g, c, G;
     float qk_scale;
+    // this lane's byte offsets inside a stage tile (the 128-byte swizzle folded
+    // in): K row g at chunks 2c, 2c+1 (row 8+g is 8 rows further), V rows 2c
+    // and 2c+1 at chunk g (rows 8+2c, 9+2c are 8 rows further)
+    uint32_t k_off0, k_off1, v_off0, v_off1;
 
     __device__ void init(int G_, float qks) {
         lane = threadIdx.x & 31;
@@ -328,6 +348,17 @@ struct MmaConsumer {
         c = lane & 3;
         G = G_;
         qk_scale = qks;
+        if (D == 128) {
+            k_off0 = g * 128 + (((2 * c) ^ g) << 4);
+            k_off1 = g * 128 + (((2 * c + 1) ^ g) << 4);
+            v_off0 = (2 * c) * 128 + ((g ^ (2 * c)) << 4);
+            v_off1 = (2 * c + 1) * 128 + ((g ^ (2 * c + 1)) << 4);
+        } else {
+            k_off0 = g * D + c * 16;
+            k_off1 = 0;
+            v_off0 = (2 * c) * D + DV * g;
+            v_off1 = (2 * c + 1) * D + DV * g;
+        }
     }
     // qa[2j] = Q[g][DC*c + 4j + {0,1}], qa[2j+1] = Q[g][DC*c + 4j + {2,3}]: the
     // DC halves Q[g][DC*c ...] in order.  q: the group's G query rows
@@ -370,26 +401,26 @@ struct MmaConsumer {
         for (int i = 0; i < MT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     }
 
-    // K words of tile row `row`: the thread's DC contiguous bytes at DC*c.
-    __device__ __forceinline__ void load_k(const uint8_t* kt, int row, uint32_t (&w)[KW]) {
+    // K words of rows g (half 0) or 8 + g (half 1): the DC contiguous bytes at DC*c.
+    __device__ __forceinline__ void load_k(uint32_t kt, int half, uint32_t (&w)[KW]) {
+        const uint32_t rb = kt + half * 8 * D;
         if (D == 128) {
-            const uint4 x0 = *reinterpret_cast<const uint4*>(kt + tile_off<D>(row, 2 * c));
-            const uint4 x1 = *reinterpret_cast<const uint4*>(kt + tile_off<D>(row, 2 * c + 1));
+            const uint4 x0 = lds128(rb + k_off0), x1 = lds128(rb + k_off1);
             w[0] = x0.x; w[1] = x0.y; w[2] = x0.z; w[3] = x0.w;
             w[4] = x1.x; w[5] = x1.y; w[6] = x1.z; w[7] = x1.w;
         } else {
-            const uint4 x0 = *reinterpret_cast<const uint4*>(kt + tile_off<D>(row, c));
+            const uint4 x0 = lds128(rb + k_off0);
             w[0] = x0.x; w[1] = x0.y; w[2] = x0.z; w[3] = x0.w;
         }
     }
 
-    // V words of tile row `row`: the thread's DV contiguous bytes at DV*g.
-    __device__ __forceinline__ void load_v(const uint8_t* vt, int row, uint32_t (&w)[VW]) {
+    // V words of a row: the thread's DV contiguous bytes at DV*g.
+    __device__ __forceinline__ void load_v(uint32_t a, uint32_t (&w)[VW]) {
         if (D == 128) {
-            const uint4 x = *reinterpret_cast<const uint4*>(vt + tile_off<D>(row, g));
+            const uint4 x = lds128(a);
             w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
         } else {
-            const uint2 x = *reinterpret_cast<const uint2*>(vt + row * D + DV * g);
+            const uint2 x = lds64(a);
             w[0] = x.x; w[1] = x.y;
         }
     }
@@ -402,16 +433,12 @@ struct MmaConsumer {
             uint32_t kw[KW];
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                load_k(cx.k, 8 * half + g, kw);
+                load_k(cx.k, half, kw);
 #pragma unroll
                 for (int j = 0; j < KS; ++j) {
                     uint32_t b0, b1;
-                    if (FMT == INT8) {
-                        int8_biased(kw[j], b0, b1);
-                    } else {
-                        b0 = dec_fp8x2<FMT>((uint16_t)(kw[j] & 0xFFFFu));
-                        b1 = dec_fp8x2<FMT>((uint16_t)(kw[j] >> 16));
-                    }
+                    if (FMT == INT8) int8_biased(kw[j], b0, b1);
+                    else dec_fp8x4<FMT>(kw[j], b0, b1);
                     if (half == 0) mma_16816(sA, qa[2 * j], 0u, qa[2 * j + 1], 0u, b0, b1);
                     else mma_16816(sB, qa[2 * j], 0u, qa[2 * j + 1], 0u, b0, b1);
                 }
@@ -422,10 +449,11 @@ struct MmaConsumer {
         float z0, z1, z2, z3;
         if (FMT == INT8) {  // remove the operand bias, then apply the K row scales
             const float corr = kBias * qsum;
-            z0 = (sA[0] - corr) * (qk_scale * cx.sk[t0]);
-            z1 = (sA[1] - corr) * (qk_scale * cx.sk[t1]);
-            z2 = (sB[0] - corr) * (qk_scale * cx.sk[t2]);
-            z3 = (sB[1] - corr) * (qk_scale * cx.sk[t3]);
+            const float2 k01 = __uint_as_float2(lds64(cx.s + 8 * c)), k23 = __uint_as_float2(lds64(cx.s + 32 + 8 * c));
+            z0 = (sA[0] - corr) * (qk_scale * k01.x);
+            z1 = (sA[1] - corr) * (qk_scale * k01.y);
+            z2 = (sB[0] - corr) * (qk_scale * k23.x);
+            z3 = (sB[1] - corr) * (qk_scale * k23.y);
         } else {
             z0 = sA[0] * qk_scale; z1 = sA[1] * qk_scale; z2 = sB[0] * qk_scale; z3 = sB[1] * qk_scale;
         }
@@ -450,10 +478,12 @@ struct MmaConsumer {
         m = mn;
         l = l * alpha + ((p0 + p1) + (p2 + p3));
         if (FMT == INT8) {  // fold the V row scales into P (masked tokens keep p = 0)
-            if (t0 < cx.valid) p0 *= cx.sv[t0];
-            if (t1 < cx.valid) p1 *= cx.sv[t1];
-            if (t2 < cx.valid) p2 *= cx.sv[t2];
-            if (t3 < cx.valid) p3 *= cx.sv[t3];
+            const float2 s01 = __uint_as_float2(lds64(cx.s + 64 + 8 * c));
+            const float2 s23 = __uint_as_float2(lds64(cx.s + 96 + 8 * c));
+            if (t0 < cx.valid) p0 *= s01.x;
+            if (t1 < cx.valid) p1 *= s01.y;
+            if (t2 < cx.valid) p2 *= s23.x;
+            if (t3 < cx.valid) p3 *= s23.y;
         }
         // P^T as the B operand of PV: k = token, n = head g.  P is carried as
         // an fp16 pair hi + lo (lo = the fp16 residual of p - hi), so the PV
@@ -479,10 +509,10 @@ struct MmaConsumer {
         // out^T += V^T P^T.  A operand rows = head_dim DV*g + 2i (+1 for rows
         // g+8), columns = tokens 2c, 2c+1 | 8+2c, 9+2c.
         uint32_t v0[VW], v1[VW], v2[VW], v3[VW];
-        load_v(cx.v, t0, v0);
-        load_v(cx.v, t1, v1);
-        load_v(cx.v, t2, v2);
-        load_v(cx.v, t3, v3);
+        load_v(cx.v + v_off0, v0);
+        load_v(cx.v + v_off1, v1);
+        load_v(cx.v + v_off0 + 8 * D, v2);
+        load_v(cx.v + v_off1 + 8 * D, v3);
         if (cx.valid < kTile) {  // rows past the context may hold NaN codes: zero them
 #pragma unroll
             for (int e = 0; e < VW; ++e) {
@@ -510,10 +540,8 @@ struct MmaConsumer {
                 a2 = prmt(x23, 0x64646464u, 0x4140u);
                 a3 = prmt(x23, 0x64646464u, 0x4342u);
             } else {
-                a0 = dec_fp8x2<FMT>((uint16_t)(x01 & 0xFFFFu));
-                a1 = dec_fp8x2<FMT>((uint16_t)(x01 >> 16));
-                a2 = dec_fp8x2<FMT>((uint16_t)(x23 & 0xFFFFu));
-                a3 = dec_fp8x2<FMT>((uint16_t)(x23 >> 16));
+                dec_fp8x4<FMT>(x01, a0, a1);
+                dec_fp8x4<FMT>(x23, a2, a3);
             }
             mma_16816(acc[i], a0, a1, a2, a3, pb0, pb1);
             mma_16816(acc[i], a0, a1, a2, a3, pl0, pl1);
@@ -621,6 +649,7 @@ __global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
     float* scales = reinterpret_cast<float*>(smem + L.scales) + warp * kSpw * 2 * kTile;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full) + warp * kSpw;
     uint8_t* qbuf = smem + L.qbuf + warp * L.q_bytes;
+    const uint32_t tiles_u32 = smem_u32(tiles), scales_u32 = smem_u32(scales);
 
     // block id of flat tile first + lane (lane-distributed; read back with a shuffle)
     auto load_id = [&](int first) -> int {
@@ -709,9 +738,8 @@ __global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
             break;
         }
         if (cw.t == 0 || fc == lo) cons.set_q(reinterpret_cast<const uint16_t*>(qbuf));  // came with this tile
-        const uint8_t* kt = tiles + cst * 2 * L.tile_bytes;
-        const Tile tl{kt, kt + L.tile_bytes, scales + cst * 2 * kTile, scales + cst * 2 * kTile + kTile,
-                      min(kTile, ctx_s[cw.b] - cw.t * kTile)};
+        const uint32_t kt = tiles_u32 + cst * (2 * L.tile_bytes);
+        const Tile tl{kt, kt + L.tile_bytes, scales_u32 + cst * (2 * kTile * 4), min(kTile, ctx_s[cw.b] - cw.t * kTile)};
         cons.tile(tl);
         __syncwarp();
         const bool pair_end = cw.t == cw.n - 1;

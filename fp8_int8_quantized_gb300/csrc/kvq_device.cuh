@@ -48,6 +48,22 @@ __device__ __forceinline__ uint32_t dec_fp8x2(uint16_t two) {
     return r;
 }
 
+// Four FP8 codes in a 32-bit word -> two f16x2 (bytes 0,1 -> lo; bytes 2,3 -> hi),
+// both halves taken straight from the 32-bit register.
+template <int FMT>
+__device__ __forceinline__ void dec_fp8x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    if (FMT == E4M3)
+        asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+            "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+            : "=r"(lo), "=r"(hi)
+            : "r"(w));
+    else
+        asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+            "cvt.rn.f16x2.e5m2x2 %0, l;\n\tcvt.rn.f16x2.e5m2x2 %1, h;\n\t}"
+            : "=r"(lo), "=r"(hi)
+            : "r"(w));
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t r;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
