@@ -78,12 +78,13 @@ kvq::CacheView view(const kvq_cache* c) {
                           c->v_scales, c->num_blocks, c->block_size, c->num_kv_heads, c->head_dim, c->fmt};
 }
 
-// 16-token tiles per context chunk.  Every warp of the persistent decode
+// Decode tiles (kDecodeTileTokens tokens) per context chunk.  Every warp of the persistent decode
 // kernel streams a contiguous range of the flat tile list that is at least one
 // chunk long; chunks of about half a range keep every warp busy while the
 // partial slots stay few (two per chunk).  Assumes ~4 CTAs of 4 warps per SM.
 int32_t choose_chunk_tiles(int32_t batch, int32_t num_kv_heads, int32_t max_ctx, int sms) {
-    const int64_t tiles = (int64_t)batch * num_kv_heads * ((max_ctx + 15) / 16);
+    constexpr int TT = kvq::kDecodeTileTokens;
+    const int64_t tiles = (int64_t)batch * num_kv_heads * ((max_ctx + TT - 1) / TT);
     const int64_t warps = (int64_t)sms * 16;
     int64_t c = tiles / (2 * warps);
     if (c < 4) c = 4;
@@ -92,7 +93,7 @@ int32_t choose_chunk_tiles(int32_t batch, int32_t num_kv_heads, int32_t max_ctx,
 }
 
 int32_t resolve_chunk_tiles(int32_t partition_size, int32_t batch, int32_t num_kv_heads, int32_t max_ctx) {
-    if (partition_size > 0) return partition_size / 16;
+    if (partition_size > 0) return partition_size / kvq::kDecodeTileTokens;
     int dev = 0;
     if (!current_device(&dev)) dev = 0;
     return choose_chunk_tiles(batch, num_kv_heads, max_ctx, sm_count(dev));
@@ -156,7 +157,8 @@ size_t kvq_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num
     if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_context_len < 0) return 0;
     const int32_t C = resolve_chunk_tiles(partition_size, batch, num_kv_heads, max_context_len);
     if (C <= 0) return 0;
-    const int64_t nch = std::max<int64_t>(1, ((max_context_len + 15) / 16 + C - 1) / C);
+    constexpr int TT = kvq::kDecodeTileTokens;
+    const int64_t nch = std::max<int64_t>(1, ((max_context_len + TT - 1) / TT + C - 1) / C);
     return kvq::ws_bytes(batch, num_q_heads, nch, head_dim);
 }
 
@@ -181,10 +183,11 @@ kvq_status kvq_decode_attention(const void* q, const kvq_cache* cache, const int
     if (!(sm_scale >= 0.f) || std::isinf(sm_scale)) return KVQ_ERR_INVALID_ARG;
     if (partition_size < 0 || partition_size % 64 || partition_size > kMaxChunkTokens) return KVQ_ERR_INVALID_ARG;
     if (batch > kMaxBatch) return KVQ_ERR_UNSUPPORTED;
-    if ((int64_t)batch * cache->num_kv_heads * ((max_context_len + 15) / 16) >= 0x7FFFFFFFll)
+    constexpr int TT = kvq::kDecodeTileTokens;
+    if ((int64_t)batch * cache->num_kv_heads * ((max_context_len + TT - 1) / TT) >= 0x7FFFFFFFll)
         return KVQ_ERR_UNSUPPORTED;  // flat tile indices are 32-bit
     const int32_t C = resolve_chunk_tiles(partition_size, batch, cache->num_kv_heads, max_context_len);
-    const int32_t nch = std::max<int32_t>(1, ((max_context_len + 15) / 16 + C - 1) / C);
+    const int32_t nch = std::max<int32_t>(1, ((max_context_len + TT - 1) / TT + C - 1) / C);
     const size_t need = kvq::ws_bytes(batch, num_q_heads, nch, cache->head_dim);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return KVQ_ERR_WORKSPACE;
     int kind = g_decode_kernel.load();

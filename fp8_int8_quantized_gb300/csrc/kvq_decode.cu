@@ -46,18 +46,22 @@
 #include "kvq_launch.h"
 
 #ifndef KVQ_SPW
-#define KVQ_SPW 3
+#define KVQ_SPW 2
 #endif
 #ifndef KVQ_MIN_BLOCKS
-#define KVQ_MIN_BLOCKS 4
+#define KVQ_MIN_BLOCKS 2
+#endif
+#ifndef KVQ_WARPS
+#define KVQ_WARPS 6
 #endif
 
 namespace kvq {
 namespace {
 
-constexpr int kTile = 16;                      // tokens per stage
+constexpr int kTile = kDecodeTileTokens;       // tokens per stage: two boxes
+constexpr int kBox = 16;                       // rows per TMA box (a 16-token slice of one paged block)
 constexpr int kSpw = KVQ_SPW;                  // stages per warp
-constexpr int kConsumers = 4;                  // warps per CTA, each streaming its own range
+constexpr int kConsumers = KVQ_WARPS;          // warps per CTA, each streaming its own range
 constexpr int kThreads = kConsumers * 32;
 constexpr int kMinBlocks = KVQ_MIN_BLOCKS;     // CTAs per SM the registers are sized for
 constexpr float kLog2e = 1.4426950408889634f;
@@ -71,11 +75,11 @@ enum { kKindSimt = 1, kKindMma = 2 };
 // lengths.
 struct Layout {
     int tile_bytes, q_bytes, scales, full, qbuf, scan, total;
-    __host__ __device__ Layout(int D, int G, int B) {
+    __host__ __device__ Layout(int D, int G, int B, bool int8) {
         tile_bytes = kTile * D;
         q_bytes = (G * D * 2 + 127) / 128 * 128;
         scales = kConsumers * kSpw * 2 * tile_bytes;            // [warp][stage][K,V][tile] before this
-        full = scales + kConsumers * kSpw * 2 * kTile * 4;      // f32 [warp][stage][2][16]
+        full = scales + (int8 ? kConsumers * kSpw * 2 * kTile * 4 : 0);  // INT8: f32 [warp][stage][K,V][32]
         qbuf = (full + kConsumers * kSpw * 8 + 127) / 128 * 128;  // u64 [warp][stage], then f16 [warp][G][D]
         scan = qbuf + kConsumers * q_bytes;                     // int S[B + 1], ctx[B]
         total = scan + (2 * B + 1) * 4;
@@ -166,7 +170,7 @@ template <int FMT, int D, int GM>
 struct SimtConsumer {
     static constexpr int LPT = D / 16;     // lanes per token
     static constexpr int TPP = 32 / LPT;   // tokens per pass
-    static constexpr int PASSES = kTile / TPP;
+    static constexpr int PASSES = kBox / TPP;
     static constexpr int kMinCtas = GM == 4 ? 3 : kMinBlocks;  // 4 query rows need more registers
     uint32_t qh[GM][8];
     float m[GM], l[GM], acc[GM][16];
@@ -205,12 +209,13 @@ struct SimtConsumer {
         }
     }
 
-    __device__ void tile(const Tile& c) {
+    // One 16-row half of a tile: K rows at k, V rows at v, row scales at sk / sv.
+    __device__ void half(uint32_t k, uint32_t v, uint32_t sk, uint32_t sv, int valid) {
         float z[PASSES][GM];
 #pragma unroll
         for (int ps = 0; ps < PASSES; ++ps) {
             const int t = ps * TPP + grp;
-            const uint4 kw = lds128(c.k + tile_off<D>(t, j));
+            const uint4 kw = lds128(k + tile_off<D>(t, j));
             const uint32_t w[4] = {kw.x, kw.y, kw.z, kw.w};
             uint32_t kh[8];
 #pragma unroll
@@ -218,7 +223,7 @@ struct SimtConsumer {
                 kh[2 * e] = dec_x2<FMT>((uint16_t)(w[e] & 0xFFFFu));
                 kh[2 * e + 1] = dec_x2<FMT>((uint16_t)(w[e] >> 16));
             }
-            const float ts = (FMT == INT8 ? ldsf(c.s + 4 * t) : 1.0f) * qk_scale;
+            const float ts = (FMT == INT8 ? ldsf(sk + 4 * t) : 1.0f) * qk_scale;
 #pragma unroll
             for (int h = 0; h < GM; ++h) {
                 float d0 = 0.f, d1 = 0.f;
@@ -230,7 +235,7 @@ struct SimtConsumer {
                 float d = d0 + d1;
 #pragma unroll
                 for (int off = LPT / 2; off > 0; off >>= 1) d += __shfl_xor_sync(0xFFFFFFFFu, d, off);
-                z[ps][h] = t < c.valid ? d * ts : -INFINITY;
+                z[ps][h] = t < valid ? d * ts : -INFINITY;
             }
         }
         float p[PASSES][GM];
@@ -264,11 +269,11 @@ struct SimtConsumer {
 #pragma unroll
         for (int ps = 0; ps < PASSES; ++ps) {
             const int t = ps * TPP + grp;
-            uint4 vw = lds128(c.v + tile_off<D>(t, j));
+            uint4 vw = lds128(v + tile_off<D>(t, j));
             // rows past the context may hold any bytes (NaN codes too): zero them
-            if (t >= c.valid) vw = make_uint4(0u, 0u, 0u, 0u);
+            if (t >= valid) vw = make_uint4(0u, 0u, 0u, 0u);
             const uint32_t w[4] = {vw.x, vw.y, vw.z, vw.w};
-            const float vs = (FMT == INT8 && t < c.valid) ? ldsf(c.s + 64 + 4 * t) : 1.0f;
+            const float vs = (FMT == INT8 && t < valid) ? ldsf(sv + 4 * t) : 1.0f;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const float2 lo = f16x2_to_f32x2(dec_x2<FMT>((uint16_t)(w[e] & 0xFFFFu)));
@@ -283,6 +288,12 @@ struct SimtConsumer {
                 }
             }
         }
+    }
+
+    __device__ void tile(const Tile& c) {
+        half(c.k, c.v, c.s, c.s + 4 * kTile, c.valid);
+        if (c.valid > kBox)
+            half(c.k + kBox * D, c.v + kBox * D, c.s + 4 * kBox, c.s + 4 * kTile + 4 * kBox, c.valid - kBox);
     }
 
     // Sum the per-group partials and write this segment's partial slot.
@@ -425,101 +436,59 @@ struct MmaConsumer {
         }
     }
 
-    __device__ void tile(const Tile& cx) {
-        // S^T: rows = q-heads (g), columns = tokens; half A = tokens 0..7 (this
-        // thread's B operand row is token g), half B = tokens 8..15.
+    // QK^T of one 16-row box: this thread's logits, head g, box tokens
+    // 2c, 2c+1, 8+2c, 9+2c (already scaled, masked past `valid`).
+    __device__ __forceinline__ void qk_box(uint32_t kt, uint32_t sk, int valid, float (&z)[4]) {
+        // S^T: rows = q-heads (g), columns = tokens; half A = box tokens 0..7
+        // (this thread's B operand row is token g), half B = tokens 8..15.
         float sA[4] = {0.f, 0.f, 0.f, 0.f}, sB[4] = {0.f, 0.f, 0.f, 0.f};
-        {
-            uint32_t kw[KW];
+        uint32_t kw[KW];
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                load_k(cx.k, half, kw);
+        for (int hb = 0; hb < 2; ++hb) {
+            load_k(kt, hb, kw);
 #pragma unroll
-                for (int j = 0; j < KS; ++j) {
-                    uint32_t b0, b1;
-                    if (FMT == INT8) int8_biased(kw[j], b0, b1);
-                    else dec_fp8x4<FMT>(kw[j], b0, b1);
-                    if (half == 0) mma_16816(sA, qa[2 * j], 0u, qa[2 * j + 1], 0u, b0, b1);
-                    else mma_16816(sB, qa[2 * j], 0u, qa[2 * j + 1], 0u, b0, b1);
-                }
+            for (int j = 0; j < KS; ++j) {
+                uint32_t b0, b1;
+                if (FMT == INT8) int8_biased(kw[j], b0, b1);
+                else dec_fp8x4<FMT>(kw[j], b0, b1);
+                if (hb == 0) mma_16816(sA, qa[2 * j], 0u, qa[2 * j + 1], 0u, b0, b1);
+                else mma_16816(sB, qa[2 * j], 0u, qa[2 * j + 1], 0u, b0, b1);
             }
         }
-        // this thread's logits: head g, tokens 2c, 2c+1, 8+2c, 9+2c
-        const int t0 = 2 * c, t1 = 2 * c + 1, t2 = 8 + 2 * c, t3 = 9 + 2 * c;
-        float z0, z1, z2, z3;
         if (FMT == INT8) {  // remove the operand bias, then apply the K row scales
             const float corr = kBias * qsum;
-            const float2 k01 = __uint_as_float2(lds64(cx.s + 8 * c)), k23 = __uint_as_float2(lds64(cx.s + 32 + 8 * c));
-            z0 = (sA[0] - corr) * (qk_scale * k01.x);
-            z1 = (sA[1] - corr) * (qk_scale * k01.y);
-            z2 = (sB[0] - corr) * (qk_scale * k23.x);
-            z3 = (sB[1] - corr) * (qk_scale * k23.y);
+            const float2 k01 = __uint_as_float2(lds64(sk + 8 * c)), k23 = __uint_as_float2(lds64(sk + 32 + 8 * c));
+            z[0] = (sA[0] - corr) * (qk_scale * k01.x);
+            z[1] = (sA[1] - corr) * (qk_scale * k01.y);
+            z[2] = (sB[0] - corr) * (qk_scale * k23.x);
+            z[3] = (sB[1] - corr) * (qk_scale * k23.y);
         } else {
-            z0 = sA[0] * qk_scale; z1 = sA[1] * qk_scale; z2 = sB[0] * qk_scale; z3 = sB[1] * qk_scale;
+            z[0] = sA[0] * qk_scale; z[1] = sA[1] * qk_scale; z[2] = sB[0] * qk_scale; z[3] = sB[1] * qk_scale;
         }
-        if (cx.valid < kTile) {
-            if (t0 >= cx.valid) z0 = -INFINITY;
-            if (t1 >= cx.valid) z1 = -INFINITY;
-            if (t2 >= cx.valid) z2 = -INFINITY;
-            if (t3 >= cx.valid) z3 = -INFINITY;
+        if (valid < kBox) {
+            if (2 * c >= valid) z[0] = -INFINITY;
+            if (2 * c + 1 >= valid) z[1] = -INFINITY;
+            if (8 + 2 * c >= valid) z[2] = -INFINITY;
+            if (9 + 2 * c >= valid) z[3] = -INFINITY;
         }
-        float mx = fmaxf(fmaxf(z0, z1), fmaxf(z2, z3));
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
-        const float mn = fmaxf(m, mx);
-        float alpha = 1.f, p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
-        if (mn != -INFINITY) {
-            alpha = fast_exp2(m - mn);
-            p0 = fast_exp2(z0 - mn);
-            p1 = fast_exp2(z1 - mn);
-            p2 = fast_exp2(z2 - mn);
-            p3 = fast_exp2(z3 - mn);
-        }
-        m = mn;
-        l = l * alpha + ((p0 + p1) + (p2 + p3));
-        if (FMT == INT8) {  // fold the V row scales into P (masked tokens keep p = 0)
-            const float2 s01 = __uint_as_float2(lds64(cx.s + 64 + 8 * c));
-            const float2 s23 = __uint_as_float2(lds64(cx.s + 96 + 8 * c));
-            if (t0 < cx.valid) p0 *= s01.x;
-            if (t1 < cx.valid) p1 *= s01.y;
-            if (t2 < cx.valid) p2 *= s23.x;
-            if (t3 < cx.valid) p3 *= s23.y;
-        }
-        // P^T as the B operand of PV: k = token, n = head g.  P is carried as
-        // an fp16 pair hi + lo (lo = the fp16 residual of p - hi), so the PV
-        // product keeps about 22 bits of each weight instead of 11: with
-        // outlier channels the weighted mean of large V values can cancel, and a
-        // single fp16 rounding of P would then show in the output.
-        const uint32_t pb0 = pack_f16x2(p0, p1), pb1 = pack_f16x2(p2, p3);
-        const float2 h01 = f16x2_to_f32x2(pb0), h23 = f16x2_to_f32x2(pb1);
-        const uint32_t pl0 = pack_f16x2(p0 - h01.x, p1 - h01.y), pl1 = pack_f16x2(p2 - h23.x, p3 - h23.y);
-        if (FMT == INT8) {  // the weights exactly as the tensor cores see them
-            const float2 l01 = f16x2_to_f32x2(pl0), l23 = f16x2_to_f32x2(pl1);
-            psum = psum * alpha + (((h01.x + l01.x) + (h01.y + l01.y)) + ((h23.x + l23.x) + (h23.y + l23.y)));
-        }
-        // rescale the accumulators: columns are heads 2c and 2c+1
-        if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
-            const float a0 = __shfl_sync(0xFFFFFFFFu, alpha, 8 * c);
-            const float a1 = __shfl_sync(0xFFFFFFFFu, alpha, 8 * c + 4);
-#pragma unroll
-            for (int i = 0; i < MT; ++i) {
-                acc[i][0] *= a0; acc[i][1] *= a1; acc[i][2] *= a0; acc[i][3] *= a1;
-            }
-        }
-        // out^T += V^T P^T.  A operand rows = head_dim DV*g + 2i (+1 for rows
-        // g+8), columns = tokens 2c, 2c+1 | 8+2c, 9+2c.
+    }
+
+    // out^T += V^T P^T for one box.  A operand rows = head_dim DV*g + 2i (+1
+    // for rows g+8), columns = box tokens 2c, 2c+1 | 8+2c, 9+2c.
+    __device__ __forceinline__ void pv_box(uint32_t vt, int valid, uint32_t pb0, uint32_t pb1, uint32_t pl0,
+                                           uint32_t pl1) {
         uint32_t v0[VW], v1[VW], v2[VW], v3[VW];
-        load_v(cx.v + v_off0, v0);
-        load_v(cx.v + v_off1, v1);
-        load_v(cx.v + v_off0 + 8 * D, v2);
-        load_v(cx.v + v_off1 + 8 * D, v3);
-        if (cx.valid < kTile) {  // rows past the context may hold NaN codes: zero them
+        load_v(vt + v_off0, v0);
+        load_v(vt + v_off1, v1);
+        load_v(vt + v_off0 + 8 * D, v2);
+        load_v(vt + v_off1 + 8 * D, v3);
+        if (valid < kBox) {  // rows past the context may hold NaN codes: zero them
 #pragma unroll
             for (int e = 0; e < VW; ++e) {
-                if (t0 >= cx.valid) v0[e] = 0u;
-                if (t1 >= cx.valid) v1[e] = 0u;
-                if (t2 >= cx.valid) v2[e] = 0u;
-                if (t3 >= cx.valid) v3[e] = 0u;
+                if (2 * c >= valid) v0[e] = 0u;
+                if (2 * c + 1 >= valid) v1[e] = 0u;
+                if (8 + 2 * c >= valid) v2[e] = 0u;
+                if (9 + 2 * c >= valid) v3[e] = 0u;
             }
         }
         if (FMT == INT8) {  // code + 128 as unsigned bytes, once per word
@@ -545,6 +514,73 @@ struct MmaConsumer {
             }
             mma_16816(acc[i], a0, a1, a2, a3, pb0, pb1);
             mma_16816(acc[i], a0, a1, a2, a3, pl0, pl1);
+        }
+    }
+
+    // P of one box as the B operand of PV (k = token, n = head g), carried as
+    // an fp16 pair hi + lo (lo = the fp16 residual of p - hi): the PV product
+    // keeps about 22 bits of each weight instead of 11.  With outlier channels
+    // the weighted mean of large V values can cancel, and a single fp16
+    // rounding of P would then show in the output.
+    __device__ __forceinline__ void p_frags(const float (&p)[4], uint32_t& pb0, uint32_t& pb1, uint32_t& pl0,
+                                            uint32_t& pl1, float& sum_fed) {
+        pb0 = pack_f16x2(p[0], p[1]);
+        pb1 = pack_f16x2(p[2], p[3]);
+        const float2 h01 = f16x2_to_f32x2(pb0), h23 = f16x2_to_f32x2(pb1);
+        pl0 = pack_f16x2(p[0] - h01.x, p[1] - h01.y);
+        pl1 = pack_f16x2(p[2] - h23.x, p[3] - h23.y);
+        if (FMT == INT8) {  // the weights exactly as the tensor cores see them
+            const float2 l01 = f16x2_to_f32x2(pl0), l23 = f16x2_to_f32x2(pl1);
+            sum_fed += ((h01.x + l01.x) + (h01.y + l01.y)) + ((h23.x + l23.x) + (h23.y + l23.y));
+        }
+    }
+
+    __device__ void tile(const Tile& cx) {
+        const bool two = cx.valid > kBox;  // warp-uniform: the second box holds context rows
+        float z0[4], z1[4];
+        qk_box(cx.k, cx.s, cx.valid, z0);
+        if (two) qk_box(cx.k + kBox * D, cx.s + 4 * kBox, cx.valid - kBox, z1);
+        else z1[0] = z1[1] = z1[2] = z1[3] = -INFINITY;
+        float mx = fmaxf(fmaxf(fmaxf(z0[0], z0[1]), fmaxf(z0[2], z0[3])), fmaxf(fmaxf(z1[0], z1[1]), fmaxf(z1[2], z1[3])));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+        const float mn = fmaxf(m, mx);
+        float alpha = 1.f, p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
+        if (mn != -INFINITY) {
+            alpha = fast_exp2(m - mn);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                p0[e] = fast_exp2(z0[e] - mn);
+                p1[e] = fast_exp2(z1[e] - mn);
+            }
+        }
+        m = mn;
+        l = l * alpha + (((p0[0] + p0[1]) + (p0[2] + p0[3])) + ((p1[0] + p1[1]) + (p1[2] + p1[3])));
+        if (FMT == INT8) {  // fold the V row scales into P (masked tokens keep p = 0)
+            const uint32_t sv = cx.s + 4 * kTile;
+            const float2 a01 = __uint_as_float2(lds64(sv + 8 * c)), a23 = __uint_as_float2(lds64(sv + 32 + 8 * c));
+            p0[0] *= a01.x; p0[1] *= a01.y; p0[2] *= a23.x; p0[3] *= a23.y;
+            if (two) {
+                const float2 b01 = __uint_as_float2(lds64(sv + 64 + 8 * c)), b23 = __uint_as_float2(lds64(sv + 96 + 8 * c));
+                p1[0] *= b01.x; p1[1] *= b01.y; p1[2] *= b23.x; p1[3] *= b23.y;
+            }
+            psum *= alpha;
+        }
+        // rescale the accumulators: columns are heads 2c and 2c+1
+        if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
+            const float a0 = __shfl_sync(0xFFFFFFFFu, alpha, 8 * c);
+            const float a1 = __shfl_sync(0xFFFFFFFFu, alpha, 8 * c + 4);
+#pragma unroll
+            for (int i = 0; i < MT; ++i) {
+                acc[i][0] *= a0; acc[i][1] *= a1; acc[i][2] *= a0; acc[i][3] *= a1;
+            }
+        }
+        uint32_t pb0, pb1, pl0, pl1;
+        p_frags(p0, pb0, pb1, pl0, pl1, psum);
+        pv_box(cx.v, cx.valid, pb0, pb1, pl0, pl1);
+        if (two) {
+            p_frags(p1, pb0, pb1, pl0, pl1, psum);
+            pv_box(cx.v + kBox * D, cx.valid - kBox, pb0, pb1, pl0, pl1);
         }
     }
 
@@ -591,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int B = a.batch, Hkv = a.cache.num_kv_heads, BS = a.cache.block_size;
     const int G = a.num_q_heads / Hkv;
-    const Layout L(D, G, B);
+    const Layout L(D, G, B, FMT == INT8);
     int* S = reinterpret_cast<int*>(smem + L.scan);
     int* ctx_s = S + B + 1;
     griddep_wait();    // inputs may come from the previous kernel (an append)
@@ -642,30 +678,31 @@ __global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
     const int lo = gw * base_len + min(gw, extra);
     const int hi = lo + base_len + (gw < extra ? 1 : 0);
 
-    // paged blocks hold 1, 2 or 4 tiles: tile t sits in block-table entry t >> tpb_shift
-    const int tpb_shift = BS == 16 ? 0 : (BS == 32 ? 1 : 2);
-    const int tpb_mask = (1 << tpb_shift) - 1;
     uint8_t* tiles = smem + warp * kSpw * 2 * L.tile_bytes;
     float* scales = reinterpret_cast<float*>(smem + L.scales) + warp * kSpw * 2 * kTile;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full) + warp * kSpw;
     uint8_t* qbuf = smem + L.qbuf + warp * L.q_bytes;
     const uint32_t tiles_u32 = smem_u32(tiles), scales_u32 = smem_u32(scales);
 
-    // block id of flat tile first + lane (lane-distributed; read back with a shuffle)
+    // Block-table entries of the 32 boxes of flat tiles [first, first + 16):
+    // lane j holds box j % 2 of tile first + j / 2 (0 for boxes past the
+    // context, which are never loaded).  Read back with a shuffle.
     auto load_id = [&](int first) -> int {
-        const int ff = first + lane;
+        const int ff = first + (lane >> 1);
         if (ff >= hi) return 0;
         const Walk w = locate(S, B, Hkv, ff);
-        return __ldg(a.block_tables + (int64_t)w.b * a.max_blocks_per_seq + (w.t >> tpb_shift));
+        const int tok = w.t * kTile + (lane & 1) * kBox;
+        if (tok >= ctx_s[w.b]) return 0;
+        return __ldg(a.block_tables + (int64_t)w.b * a.max_blocks_per_seq + tok / BS);
     };
-    int idc = load_id(lo);       // tiles [window, window + 32)
-    int idn = load_id(lo + 32);  // the next window, loaded one window ahead
+    int idc = load_id(lo);       // tiles [window, window + 16)
+    int idn = load_id(lo + 16);  // the next window, loaded one window ahead
     if (lane == 0) {
         prefetch_tmap(&tmk);
         prefetch_tmap(&tmv);
     }
     const uint64_t pol = policy_evict_first();
-    const uint32_t tile_tx = 2 * L.tile_bytes + (FMT == INT8 ? 2 * kTile * 4 : 0);
+    const uint32_t box_tx = 2 * kBox * D + (FMT == INT8 ? 2 * kBox * 4 : 0);
     const uint32_t q_tx = G * D * 2;
 
     const float s_fp8 = (FMT != INT8 && a.scale) ? __ldg(a.scale) : 1.0f;
@@ -698,33 +735,41 @@ __global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
             const int rel = fi - lo;
             const bool new_pair = iw.t == 0 || rel == 0;
             if (new_pair && pend >= fc) break;
-            const int blk_raw = __shfl_sync(0xFFFFFFFFu, idc, rel & 31);
+            const int id0 = __shfl_sync(0xFFFFFFFFu, idc, (2 * rel) & 31);
+            const int id1 = __shfl_sync(0xFFFFFFFFu, idc, (2 * rel + 1) & 31);
             if (lane == 0) {
-                int blk = blk_raw;
-                if (blk < 0 || blk >= a.cache.num_blocks) {
-                    record_error(a.err, DEV_ERR_RANGE, blk);
-                    blk = 0;  // keep the pipeline going on a block that exists
-                }
-                const int row = (blk * Hkv + iw.kvh) * BS + ((iw.t & tpb_mask) << 4);
-                uint8_t* kt = tiles + ist * 2 * L.tile_bytes;
-                mbar_arrive_expect_tx(&full[ist], tile_tx + (new_pair ? q_tx : 0u));
-                tma_load_2d(kt, &tmk, 0, row, &full[ist], pol);
-                tma_load_2d(kt + L.tile_bytes, &tmv, 0, row, &full[ist], pol);
-                if (FMT == INT8) {
-                    bulk_load(scales + ist * 2 * kTile, a.cache.k_scales + row, kTile * 4, &full[ist], pol);
-                    bulk_load(scales + ist * 2 * kTile + kTile, a.cache.v_scales + row, kTile * 4, &full[ist], pol);
+                const int tok0 = iw.t * kTile;
+                const int nbox = ctx_s[iw.b] - tok0 > kBox ? 2 : 1;  // a box past the context is not loaded
+                uint64_t* fb = &full[ist];
+                mbar_arrive_expect_tx(fb, nbox * box_tx + (new_pair ? q_tx : 0u));
+                const uint32_t kt = tiles_u32 + ist * (2 * L.tile_bytes);
+                const uint32_t st = scales_u32 + ist * (2 * kTile * 4);
+#pragma unroll
+                for (int bx = 0; bx < 2; ++bx) {
+                    if (bx >= nbox) break;
+                    int blk = bx ? id1 : id0;
+                    if (blk < 0 || blk >= a.cache.num_blocks) {
+                        record_error(a.err, DEV_ERR_RANGE, blk);
+                        blk = 0;  // keep the pipeline going on a block that exists
+                    }
+                    const int row = (blk * Hkv + iw.kvh) * BS + ((tok0 + bx * kBox) & (BS - 1));
+                    tma_load_2d_u32(kt + bx * kBox * D, &tmk, 0, row, fb, pol);
+                    tma_load_2d_u32(kt + L.tile_bytes + bx * kBox * D, &tmv, 0, row, fb, pol);
+                    if (FMT == INT8) {
+                        bulk_load_u32(st + bx * kBox * 4, a.cache.k_scales + row, kBox * 4, fb, pol);
+                        bulk_load_u32(st + 4 * kTile + bx * kBox * 4, a.cache.v_scales + row, kBox * 4, fb, pol);
+                    }
                 }
                 if (new_pair)
-                    bulk_load(qbuf, a.q + ((int64_t)iw.b * a.num_q_heads + (int64_t)iw.kvh * G) * D, q_tx,
-                              &full[ist], pol);
+                    bulk_load(qbuf, a.q + ((int64_t)iw.b * a.num_q_heads + (int64_t)iw.kvh * G) * D, q_tx, fb, pol);
             }
             if (new_pair) pend = fi;
             advance(iw, S, B, Hkv);
             ++fi;
             ist = ist + 1 == kSpw ? 0 : ist + 1;
-            if (((rel + 1) & 31) == 0) {  // next 32-tile window
+            if (((rel + 1) & 15) == 0) {  // next 16-tile window
                 idc = idn;
-                idn = load_id(fi + 32);
+                idn = load_id(fi + 16);
             }
         }
     };
@@ -857,13 +902,13 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 
 // 2-D view [rows = blocks * kv-heads * block][head_dim] of one code array;
-// box = one 16-token tile.
+// box = 16 rows (one 16-token slice of a paged block).
 bool make_tmap(CUtensorMap* m, void* base, int64_t rows, int D) {
     auto enc = get_encode();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)D};
-    cuuint32_t box[2] = {(cuuint32_t)D, (cuuint32_t)kTile};
+    cuuint32_t box[2] = {(cuuint32_t)D, (cuuint32_t)kBox};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -875,7 +920,7 @@ bool make_tmap(CUtensorMap* m, void* base, int64_t rows, int D) {
 template <int FMT, int D, class Consumer>
 cudaError_t launch_stream(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, cudaStream_t s) {
     auto kern = decode_stream_kernel<FMT, D, Consumer>;
-    const int smem = Layout(D, a.num_q_heads / a.cache.num_kv_heads, a.batch).total + 1024;
+    const int smem = Layout(D, a.num_q_heads / a.cache.num_kv_heads, a.batch, FMT == INT8).total + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);

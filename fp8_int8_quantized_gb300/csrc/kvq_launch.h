@@ -16,6 +16,10 @@
 
 namespace kvq {
 
+// Tokens per work unit of the decode kernel (two 16-row TMA boxes); the
+// host sizes chunks and workspaces in these units.
+constexpr int kDecodeTileTokens = 32;
+
 struct CacheView {
     uint8_t* k_codes;
     uint8_t* v_codes;
@@ -55,7 +59,7 @@ struct DecodeArgs {
     float sm_scale;      // resolved (> 0)
     uint16_t* out;       // fp16 bits [B][Hq][D]
     float* ws;           // chunk partials (layout below)
-    int32_t chunk_tiles; // C: 16-token tiles per context chunk
+    int32_t chunk_tiles; // C: 32-token tiles per context chunk
     int32_t num_chunks;  // chunks per sequence at max_context_len
     int32_t kernel;      // 1 = CUDA-core, 2 = tensor-core
     unsigned long long* err;
