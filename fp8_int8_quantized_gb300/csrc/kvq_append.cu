@@ -93,10 +93,95 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
     *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// FP8 append of large batches: every CTA first tabulates the code of all
+// 65536 fp16 inputs for this call's scale -- RNE-satfinite(fl32(x / scale)),
+// the same division and conversion as append_kernel, so the result is
+// bit-identical -- into shared memory, then streams its share of (token,
+// kv-head, 16-value chunk) units, K and V together, encoding every value with
+// one shared-memory lookup instead of an IEEE division.
+constexpr int kLutThreads = 512;
+constexpr int kLutBytes = 65536;
+
+template <int FMT, int D>
+__global__ void __launch_bounds__(kLutThreads, 2) append_lut_kernel(AppendArgs a) {
+    extern __shared__ __align__(16) uint8_t lut[];
+    constexpr int CPR = D / 16;
+    griddep_wait();
+    griddep_launch();
+    const float s = a.scale ? __ldg(a.scale) : 1.0f;
+    for (int w = threadIdx.x; w < kLutBytes / 4; w += kLutThreads) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int k = 0; k < 4; k += 2) {
+            float x0 = __half2float(__ushort_as_half((uint16_t)(4 * w + k)));
+            float x1 = __half2float(__ushort_as_half((uint16_t)(4 * w + k + 1)));
+            if (s != 1.0f) {
+                x0 = __fdiv_rn(x0, s);
+                x1 = __fdiv_rn(x1, s);
+            }
+            word |= (uint32_t)enc_fp8x2<FMT>(x0, x1) << (8 * k);
+        }
+        reinterpret_cast<uint32_t*>(lut)[w] = word;
+    }
+    __syncthreads();
+    const uint32_t lut_base = smem_u32(lut);
+    const int Hkv = a.cache.num_kv_heads;
+    const int64_t BS = a.cache.block_size;
+    const int64_t units = a.num_tokens * Hkv * CPR;
+    for (int64_t idx = (int64_t)blockIdx.x * kLutThreads + threadIdx.x; idx < units;
+         idx += (int64_t)gridDim.x * kLutThreads) {
+        const int c = (int)(idx % CPR);
+        const int64_t row = idx / CPR;  // token * Hkv + head
+        const int64_t t = row / Hkv;
+        const int h = (int)(row % Hkv);
+        const int64_t slot = a.slot_mapping[t];
+        if (slot == -1) continue;
+        if (slot < 0 || slot >= (int64_t)a.cache.num_blocks * BS) {
+            if (c == 0 && h == 0) record_error(a.err, DEV_ERR_RANGE, slot);
+            continue;
+        }
+        const int64_t dst_row = ((slot / BS) * Hkv + h) * BS + slot % BS;
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+            const uint4* src = reinterpret_cast<const uint4*>((which ? a.v : a.k) + row * D + c * 16);
+            const uint4 r0 = __ldg(src), r1 = __ldg(src + 1);
+            const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint32_t b0, b1, b2, b3;
+                asm volatile("ld.shared.u8 %0, [%1];" : "=r"(b0) : "r"(lut_base + (w[2 * i] & 0xFFFFu)));
+                asm volatile("ld.shared.u8 %0, [%1];" : "=r"(b1) : "r"(lut_base + (w[2 * i] >> 16)));
+                asm volatile("ld.shared.u8 %0, [%1];" : "=r"(b2) : "r"(lut_base + (w[2 * i + 1] & 0xFFFFu)));
+                asm volatile("ld.shared.u8 %0, [%1];" : "=r"(b3) : "r"(lut_base + (w[2 * i + 1] >> 16)));
+                o[i] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+            }
+            uint8_t* dst = (which ? a.cache.v_codes : a.cache.k_codes) + dst_row * D + c * 16;
+            *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+}
+
+// Values per call from which the tabulating kernel pays off (its table costs
+// 65536 divisions per CTA).
+constexpr int64_t kLutMinValues = (int64_t)1 << 22;
+
 template <int FMT>
 cudaError_t launch_fmt(const AppendArgs& a, cudaStream_t s) {
     const int D = a.cache.head_dim;
     const int64_t per = a.num_tokens * a.cache.num_kv_heads * (D / 16);
+    if (FMT != INT8 && per * 32 >= kLutMinValues) {
+        int dev = 0, sms = 0;
+        cudaError_t e;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        auto kern = D == 64 ? append_lut_kernel<FMT, 64> : append_lut_kernel<FMT, 128>;
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kLutBytes)) != cudaSuccess)
+            return e;
+        const int64_t want = (per + kLutThreads - 1) / kLutThreads;
+        const int64_t grid = want < (int64_t)sms * 2 ? want : (int64_t)sms * 2;
+        return launch_pdl(kern, dim3((unsigned)grid), dim3(kLutThreads), kLutBytes, s, a);
+    }
     dim3 grid((unsigned)((per + kThreads - 1) / kThreads), 2);
     if (D == 64) return launch_pdl(append_kernel<FMT, 64>, grid, dim3(kThreads), 0, s, a);
     return launch_pdl(append_kernel<FMT, 128>, grid, dim3(kThreads), 0, s, a);

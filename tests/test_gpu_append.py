@@ -62,6 +62,28 @@ def test_encoder_every_fp16_pattern(fmt, scale):
     assert (ref.k_codes[nan] == 0x7F).all()
 
 
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("scale", [None, 0.0123, 3.7])
+def test_encoder_every_fp16_pattern_large_append(fmt, scale):
+    """Appends large enough for the code-table kernel (every CTA tabulates the
+    65536 fp16 codes for the call's scale): 64 copies of every fp16 bit pattern
+    in shuffled slots, bit-exact against the oracle."""
+    bits = torch.arange(65536, dtype=torch.int32).to(torch.int16).view(torch.float16)
+    g = torch.Generator().manual_seed(17)
+    k = bits.repeat(64)[torch.randperm(64 * 65536, generator=g)].reshape(-1, 1, 128).clone()
+    v = bits.repeat(64).flip(0).reshape(-1, 1, 128).clone()
+    T = k.shape[0]
+    slots = torch.randperm(T + 100, generator=g)[:T].to(torch.int64)
+    NB = (T + 100 + 15) // 16
+    c, ref = run_both(k, v, slots, NB, 1, 16, 128, fmt, scale)
+    gk, gv = c.k_codes.cpu().numpy(), c.v_codes.cpu().numpy()
+    tab = oracle.fp8_decode_table(ORACLE_FMT[fmt])
+    for got, want in ((gk, ref.k_codes), (gv, ref.v_codes)):
+        nan = np.isnan(tab[want]) & (want != 0xA5)
+        assert np.array_equal(got[~nan], want[~nan])
+        assert np.isnan(tab[got[nan]]).all()
+
+
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2", "int8"])
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("BS", [16, 32, 64])
