@@ -413,7 +413,8 @@ def run_kvq(args):
         return
     peak, peak_kind = measured_peaks()
     achieved = S.dec_bytes["total"] / (kern_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(wl.name)
+    # the recorded figures are for the workload's own batch
+    traffic = recorded_traffic(wl.name) if wl.batch == W.WORKLOADS[wl.name].batch else None
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline(wl, args.cpu_seconds)
