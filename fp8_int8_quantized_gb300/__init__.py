@@ -54,6 +54,8 @@ def build(force: bool = False) -> str:
 def lib():
     """The loaded ``libkvq.so``; raises if it has not been built."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is not None:
             return _lib
@@ -140,12 +142,20 @@ class KVCache:
             self.v_scales = torch.zeros(sshape, dtype=torch.float32, device=device)
         else:
             self.k_scales = self.v_scales = None
+        self._desc = None
 
     def desc(self) -> KvqCacheDesc:
+        """A new C descriptor of this cache."""
         return KvqCacheDesc(self.k_codes.data_ptr(), self.v_codes.data_ptr(),
                             self.k_scales.data_ptr() if self.k_scales is not None else None,
                             self.v_scales.data_ptr() if self.v_scales is not None else None,
                             self.num_blocks, self.block_size, self.num_kv_heads, self.head_dim, self.fmt)
+
+    def _cdesc(self) -> KvqCacheDesc:
+        # the binding's own descriptor, built once per format (the arrays never move)
+        if self._desc is None or self._desc.fmt != self.fmt:
+            self._desc = self.desc()
+        return self._desc
 
 
 def append(k: torch.Tensor, v: torch.Tensor, cache: KVCache, slot_mapping: torch.Tensor,
@@ -154,7 +164,7 @@ def append(k: torch.Tensor, v: torch.Tensor, cache: KVCache, slot_mapping: torch
     T = slot_mapping.shape[0]
     if k.shape != (T, cache.num_kv_heads, cache.head_dim) or v.shape != k.shape:
         raise ValueError("k/v must be [num_tokens][num_kv_heads][head_dim]")
-    d = cache.desc()
+    d = cache._cdesc()
     st = lib().kvq_append(_dev(k, torch.float16, "k"), _dev(v, torch.float16, "v"), ctypes.byref(d),
                           _dev(slot_mapping, torch.int64, "slot_mapping"), T, _scale_ptr(scale), cache.fmt,
                           _stream(stream))
@@ -176,12 +186,13 @@ def decode_attention(q: torch.Tensor, cache: KVCache, block_tables: torch.Tensor
         raise ValueError("head_dim mismatch")
     if out is None:
         out = torch.empty_like(q)
-    need = workspace_size(B, Hq, cache.num_kv_heads, D, max_context_len, partition_size)
-    if need and workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if workspace is None:  # a caller-given workspace is checked by the library
+        need = workspace_size(B, Hq, cache.num_kv_heads, D, max_context_len, partition_size)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    d = cache.desc()
+    d = cache._cdesc()
     st = lib().kvq_decode_attention(_dev(q, torch.float16, "q"), ctypes.byref(d),
                                     _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
                                     _dev(context_lens, torch.int32, "context_lens"), B, Hq, int(max_context_len),
@@ -203,7 +214,7 @@ def decode_attention_static_scratch(q: torch.Tensor, cache: KVCache, block_table
     B, Hq, D = q.shape
     if out is None:
         out = torch.empty_like(q)
-    d = cache.desc()
+    d = cache._cdesc()
     st = lib().kvq_decode_attention_static_scratch(
         _dev(q, torch.float16, "q"), ctypes.byref(d), _dev(block_tables, torch.int32, "block_tables"),
         block_tables.shape[1], _dev(context_lens, torch.int32, "context_lens"), B, Hq, int(max_context_len),
@@ -218,7 +229,7 @@ def dequant(cache: KVCache, slots: torch.Tensor, scale: torch.Tensor | None = No
     n = slots.shape[0]
     ok = torch.empty((n, cache.num_kv_heads, cache.head_dim), dtype=torch.float32, device=slots.device)
     ov = torch.empty_like(ok)
-    d = cache.desc()
+    d = cache._cdesc()
     st = lib().kvq_dequant(ctypes.byref(d), _dev(slots, torch.int64, "slots"), n, _scale_ptr(scale), cache.fmt,
                            ok.data_ptr(), ov.data_ptr(), _stream(stream))
     _check(st, "kvq_dequant")

@@ -93,23 +93,61 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
     *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// FP8 append of large batches: every CTA first tabulates the code of all
-// 65536 fp16 inputs for this call's scale -- RNE-satfinite(fl32(x / scale)),
-// the same division and conversion as append_kernel, so the result is
-// bit-identical -- into shared memory, then streams its share of (token,
-// kv-head, 16-value chunk) units, K and V together, encoding every value with
-// one shared-memory lookup instead of an IEEE division.
+// Division of 0 <= n < 2^31 by a divisor d fixed at launch, as a multiply-high
+// and a shift (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994, round-up multiplier with N = 31): with
+// l = ceil(log2 d) and m = ceil(2^(31+l) / d) < 2^32, n / d = (n * m) >> (31 + l).
+struct FastDiv {
+    uint32_t d = 1, m = 0;
+    int shift = 0;  // l - 1
+    FastDiv() = default;
+    explicit FastDiv(uint32_t d_) : d(d_) {
+        int l = 0;
+        while ((1ull << l) < d) ++l;
+        if (d > 1) {
+            m = (uint32_t)(((1ull << (31 + l)) + d - 1) / d);
+            shift = l - 1;
+        }
+    }
+    __device__ __forceinline__ uint32_t div(uint32_t n) const { return d == 1 ? n : __umulhi(n, m) >> shift; }
+};
+
+// FP8 append of large batches.  The code of x is RNE-satfinite(fl32(x /
+// scale)); negating x negates the quotient and flips only the code's sign
+// bit, so every CTA first tabulates the codes of the 32768 non-negative fp16
+// patterns for this call's scale -- the same division and conversion as
+// append_kernel, so the result is bit-identical -- in shared memory, then
+// encodes each value with one byte lookup of its magnitude and an XOR of its
+// sign into bit 7.  The CTA then streams its share of (token, kv-head,
+// 16-value chunk) units, K and V together, two units per iteration with all
+// four 32-byte loads issued before the first lookup.
 constexpr int kLutThreads = 512;
-constexpr int kLutBytes = 65536;
+constexpr int kLutEntries = 32768;
+
+// 16 fp16 values (8 words) -> 16 codes by table lookup
+__device__ __forceinline__ uint4 lut_encode16(const uint4& r0, const uint4& r1, const uint8_t* lut) {
+    const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t a = w[2 * i], b = w[2 * i + 1];
+        const uint32_t codes = (uint32_t)lut[a & 0x7FFFu] | ((uint32_t)lut[(a >> 16) & 0x7FFFu] << 8) |
+                               ((uint32_t)lut[b & 0x7FFFu] << 16) | ((uint32_t)lut[(b >> 16) & 0x7FFFu] << 24);
+        const uint32_t signs = prmt(a, b, 0x7531u) & 0x80808080u;  // bit 15 of each half -> bit 7 of its byte
+        o[i] = codes ^ signs;
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
 
 template <int FMT, int D>
-__global__ void __launch_bounds__(kLutThreads, 2) append_lut_kernel(AppendArgs a) {
+__global__ void __launch_bounds__(kLutThreads, 2) append_lut_kernel(AppendArgs a, FastDiv by_heads) {
     extern __shared__ __align__(16) uint8_t lut[];
-    constexpr int CPR = D / 16;
+    constexpr int CPR = D / 16;  // units per row
+    constexpr int LOG_CPR = D == 128 ? 3 : 2;
     griddep_wait();
     griddep_launch();
     const float s = a.scale ? __ldg(a.scale) : 1.0f;
-    for (int w = threadIdx.x; w < kLutBytes / 4; w += kLutThreads) {
+    for (int w = threadIdx.x; w < kLutEntries / 4; w += kLutThreads) {
         uint32_t word = 0;
 #pragma unroll
         for (int k = 0; k < 4; k += 2) {
@@ -124,63 +162,74 @@ __global__ void __launch_bounds__(kLutThreads, 2) append_lut_kernel(AppendArgs a
         reinterpret_cast<uint32_t*>(lut)[w] = word;
     }
     __syncthreads();
-    const uint32_t lut_base = smem_u32(lut);
     const int Hkv = a.cache.num_kv_heads;
-    const int64_t BS = a.cache.block_size;
-    const int64_t units = a.num_tokens * Hkv * CPR;
-    for (int64_t idx = (int64_t)blockIdx.x * kLutThreads + threadIdx.x; idx < units;
-         idx += (int64_t)gridDim.x * kLutThreads) {
-        const int c = (int)(idx % CPR);
-        const int64_t row = idx / CPR;  // token * Hkv + head
-        const int64_t t = row / Hkv;
-        const int h = (int)(row % Hkv);
-        const int64_t slot = a.slot_mapping[t];
-        if (slot == -1) continue;
-        if (slot < 0 || slot >= (int64_t)a.cache.num_blocks * BS) {
-            if (c == 0 && h == 0) record_error(a.err, DEV_ERR_RANGE, slot);
-            continue;
+    const int BS = a.cache.block_size;  // 16, 32 or 64
+    const int lbs = __ffs(BS) - 1;
+    const int64_t nslots = (int64_t)a.cache.num_blocks * BS;
+    const uint32_t units = (uint32_t)(a.num_tokens * Hkv * CPR);  // < 2^31 (checked by the launcher)
+    const uint32_t stride = gridDim.x * kLutThreads;
+
+    // one unit = chunk c of row (token t, head h): its K and V values and slot
+    struct Unit {
+        uint4 r[4];
+        int64_t slot;
+        uint32_t row;
+    };
+    auto load = [&](uint32_t u, Unit& x) {
+        const uint4* k = reinterpret_cast<const uint4*>(a.k) + 2 * (int64_t)u;  // 16 fp16 = two uint4
+        const uint4* v = reinterpret_cast<const uint4*>(a.v) + 2 * (int64_t)u;
+        x.r[0] = __ldg(k);
+        x.r[1] = __ldg(k + 1);
+        x.r[2] = __ldg(v);
+        x.r[3] = __ldg(v + 1);
+        x.row = u >> LOG_CPR;
+        x.slot = __ldg(a.slot_mapping + by_heads.div(x.row));
+    };
+    auto store = [&](uint32_t u, const Unit& x) {
+        const int c = (int)(u & (CPR - 1));
+        const int h = (int)(x.row - by_heads.div(x.row) * (uint32_t)Hkv);
+        if (x.slot == -1) return;
+        if (x.slot < 0 || x.slot >= nslots) {
+            if (c == 0 && h == 0) record_error(a.err, DEV_ERR_RANGE, x.slot);
+            return;
         }
-        const int64_t dst_row = ((slot / BS) * Hkv + h) * BS + slot % BS;
-#pragma unroll
-        for (int which = 0; which < 2; ++which) {
-            const uint4* src = reinterpret_cast<const uint4*>((which ? a.v : a.k) + row * D + c * 16);
-            const uint4 r0 = __ldg(src), r1 = __ldg(src + 1);
-            const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-            uint32_t o[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                uint32_t b0, b1, b2, b3;
-                asm volatile("ld.shared.u8 %0, [%1];" : "=r"(b0) : "r"(lut_base + (w[2 * i] & 0xFFFFu)));
-                asm volatile("ld.shared.u8 %0, [%1];" : "=r"(b1) : "r"(lut_base + (w[2 * i] >> 16)));
-                asm volatile("ld.shared.u8 %0, [%1];" : "=r"(b2) : "r"(lut_base + (w[2 * i + 1] & 0xFFFFu)));
-                asm volatile("ld.shared.u8 %0, [%1];" : "=r"(b3) : "r"(lut_base + (w[2 * i + 1] >> 16)));
-                o[i] = b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
-            }
-            uint8_t* dst = (which ? a.cache.v_codes : a.cache.k_codes) + dst_row * D + c * 16;
-            *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
-        }
+        const int64_t dst = ((((x.slot >> lbs) * Hkv + h) << lbs) + (x.slot & (BS - 1))) * D + c * 16;
+        *reinterpret_cast<uint4*>(a.cache.k_codes + dst) = lut_encode16(x.r[0], x.r[1], lut);
+        *reinterpret_cast<uint4*>(a.cache.v_codes + dst) = lut_encode16(x.r[2], x.r[3], lut);
+    };
+    for (uint32_t u0 = blockIdx.x * kLutThreads + threadIdx.x; u0 < units; u0 += 2 * stride) {
+        const uint32_t u1 = u0 + stride;
+        Unit x0, x1;
+        load(u0, x0);
+        if (u1 < units) load(u1, x1);
+        store(u0, x0);
+        if (u1 < units) store(u1, x1);
     }
 }
 
 // Values per call from which the tabulating kernel pays off (its table costs
-// 65536 divisions per CTA).
+// 32768 divisions per CTA).
 constexpr int64_t kLutMinValues = (int64_t)1 << 22;
 
 template <int FMT>
 cudaError_t launch_fmt(const AppendArgs& a, cudaStream_t s) {
     const int D = a.cache.head_dim;
     const int64_t per = a.num_tokens * a.cache.num_kv_heads * (D / 16);
-    if (FMT != INT8 && per * 32 >= kLutMinValues) {
-        int dev = 0, sms = 0;
-        cudaError_t e;
-        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-        auto kern = D == 64 ? append_lut_kernel<FMT, 64> : append_lut_kernel<FMT, 128>;
-        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kLutBytes)) != cudaSuccess)
-            return e;
-        const int64_t want = (per + kLutThreads - 1) / kLutThreads;
-        const int64_t grid = want < (int64_t)sms * 2 ? want : (int64_t)sms * 2;
-        return launch_pdl(kern, dim3((unsigned)grid), dim3(kLutThreads), kLutBytes, s, a);
+    if constexpr (FMT != INT8) {
+        if (per * 32 >= kLutMinValues && per < ((int64_t)1 << 31)) {
+            int dev = 0, sms = 0;
+            cudaError_t e;
+            if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+            if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+            auto kern = D == 64 ? append_lut_kernel<FMT, 64> : append_lut_kernel<FMT, 128>;
+            if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kLutEntries)) !=
+                cudaSuccess)
+                return e;
+            const int64_t want = (per + kLutThreads - 1) / kLutThreads;
+            const int64_t grid = want < (int64_t)sms * 2 ? want : (int64_t)sms * 2;
+            return launch_pdl(kern, dim3((unsigned)grid), dim3(kLutThreads), kLutEntries, s, a,
+                              FastDiv((uint32_t)a.cache.num_kv_heads));
+        }
     }
     dim3 grid((unsigned)((per + kThreads - 1) / kThreads), 2);
     if (D == 64) return launch_pdl(append_kernel<FMT, 64>, grid, dim3(kThreads), 0, s, a);

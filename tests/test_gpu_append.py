@@ -63,11 +63,12 @@ def test_encoder_every_fp16_pattern(fmt, scale):
 
 
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
-@pytest.mark.parametrize("scale", [None, 0.0123, 3.7])
+@pytest.mark.parametrize("scale", [None, 0.0123, 3.7, -0.75])
 def test_encoder_every_fp16_pattern_large_append(fmt, scale):
     """Appends large enough for the code-table kernel (every CTA tabulates the
-    65536 fp16 codes for the call's scale): 64 copies of every fp16 bit pattern
-    in shuffled slots, bit-exact against the oracle."""
+    codes of the non-negative fp16 patterns for the call's scale and takes the
+    sign from the input): 64 copies of every fp16 bit pattern in shuffled
+    slots, bit-exact against the oracle; a negative scale included."""
     bits = torch.arange(65536, dtype=torch.int32).to(torch.int16).view(torch.float16)
     g = torch.Generator().manual_seed(17)
     k = bits.repeat(64)[torch.randperm(64 * 65536, generator=g)].reshape(-1, 1, 128).clone()
@@ -82,6 +83,26 @@ def test_encoder_every_fp16_pattern_large_append(fmt, scale):
         nan = np.isnan(tab[want]) & (want != 0xA5)
         assert np.array_equal(got[~nan], want[~nan])
         assert np.isnan(tab[got[nan]]).all()
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("Hkv,D,BS", [(3, 128, 16), (5, 64, 64), (40, 128, 32), (1, 64, 16)])
+def test_large_append_bit_exact_heads_and_blocks(fmt, Hkv, D, BS):
+    """The code-table kernel (appends of 2^22 values or more) on random rows
+    for several kv-head counts -- its row-to-token division is a multiply-high
+    -- head sizes and block sizes, with skipped slots and a ragged last pass."""
+    g = torch.Generator().manual_seed(Hkv * 1000 + D + BS)
+    T = (1 << 22) // (Hkv * D) + 37
+    k = (torch.randn((T, Hkv, D), generator=g) * 2).to(torch.float16)
+    v = (torch.randn((T, Hkv, D), generator=g) * 2).to(torch.float16)
+    NB = (T + 200 + BS - 1) // BS
+    slots = torch.randperm(NB * BS, generator=g)[:T].to(torch.int64)
+    slots[::13] = -1
+    scale = 0.0173 if fmt == "e4m3" else None
+    c, ref = run_both(k, v, slots, NB, Hkv, BS, D, fmt, scale)
+    assert np.array_equal(c.k_codes.cpu().numpy(), ref.k_codes)
+    assert np.array_equal(c.v_codes.cpu().numpy(), ref.v_codes)
+    assert kvq.device_error_check()[0] == 0
 
 
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2", "int8"])
