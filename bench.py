@@ -1,9 +1,12 @@
 #!/usr/bin/env python3
 """Benchmark of the quantized paged KV-cache hot path on GB300.
 
-One step = one layer's serving decode step over a resident paged cache:
-kvq_append of the step's new K/V (the decode token of every sequence, or the
-workload's prefill chunk) followed by kvq_decode_attention for every sequence.
+One step = one layer's serving decode step over a resident paged cache: the
+step's new K/V rows go into the cache and every sequence is decoded.  When the
+step brings one token per sequence, both happen in one call,
+kvq_decode_attention_append (--unfused: kvq_append then kvq_decode_attention);
+a prefill chunk (the Llama-3-70B workload) is kvq_append followed by
+kvq_decode_attention.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...     # the CPU oracle, timed on host cores
@@ -47,6 +50,8 @@ def parse():
     ap.add_argument("--partition", type=int, default=0)
     ap.add_argument("--batch", type=int, default=0, help="override the batch (small profiling cases)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--unfused", action="store_true",
+                    help="append one-token steps with a separate kvq_append launch")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU-baseline sample time")
     return ap.parse_args()
@@ -171,7 +176,7 @@ def recorded_traffic(workload: str):
 class Setup:
     """A workload's resident cache plus the step's inputs, all on the device."""
 
-    def __init__(self, wl, device, partition):
+    def __init__(self, wl, device, partition, unfused=False):
         import torch
 
         import fp8_int8_quantized_gb300 as kvq
@@ -220,6 +225,12 @@ class Setup:
         self.num_parts = 1 if need == 0 else None
         self.dec_bytes = W.decode_bytes(wl, cl)
         self.app_bytes = W.append_bytes(wl, self.slots_step.numel())
+        # one new token per sequence: the decode launch appends it (unless --unfused)
+        self.fused = (not unfused and step_tok == 1 and self.slots_step.numel() == wl.batch
+                      and bool((cl >= 1).all()))
+        if self.fused:
+            self.k_step = self.k_step.view(wl.batch, wl.num_kv_heads, wl.head_dim)
+            self.v_step = self.v_step.view(wl.batch, wl.num_kv_heads, wl.head_dim)
         torch.cuda.synchronize()
 
     def append(self):
@@ -230,6 +241,29 @@ class Setup:
         import fp8_int8_quantized_gb300 as kvq
         kvq.decode_attention(self.q, self.cache, self.bt, self.cl, self.lay.max_context_len, self.scale,
                              out=self.out, workspace=self.ws, partition_size=self.partition)
+
+    def decode_step(self, q=None, k=None, v=None, bt=None, cl=None, out=None):
+        """The decode call of one step: with the step's new rows appended in the
+        same launch when the step is one token per sequence (fused), else the
+        plain decode (the append is a separate call)."""
+        import fp8_int8_quantized_gb300 as kvq
+        q = self.q if q is None else q
+        bt = self.bt if bt is None else bt
+        cl = self.cl if cl is None else cl
+        out = self.out if out is None else out
+        if self.fused:
+            k = self.k_step if k is None else k
+            v = self.v_step if v is None else v
+            kvq.decode_attention_append(q, k, v, self.cache, bt, cl, self.lay.max_context_len, self.scale,
+                                        out=out, workspace=self.ws, partition_size=self.partition)
+        else:
+            kvq.decode_attention(q, self.cache, bt, cl, self.lay.max_context_len, self.scale, out=out,
+                                 workspace=self.ws, partition_size=self.partition)
+
+    def step(self):
+        if not self.fused:
+            self.append()
+        self.decode_step()
 
 
 # ---------------------------------------------------------------- kvq arm --
@@ -342,10 +376,9 @@ def e2e_pipeline(S, K):
             uploaded[j].record(us)
         cs.wait_event(uploaded[j])
         with torch.cuda.stream(cs):
-            if slots.numel():
+            if slots.numel() and not S.fused:
                 kvq.append(k, v, S.cache, slots, S.scale)
-            kvq.decode_attention(q, S.cache, bt, cl, S.lay.max_context_len, S.scale, out=outs[j],
-                                 workspace=S.ws, partition_size=S.partition)
+            S.decode_step(q, k, v, bt, cl, outs[j])
             consumed[j].record(cs)
         ds.wait_event(consumed[j])
         with torch.cuda.stream(ds):
@@ -389,12 +422,11 @@ def run_kvq(args):
         wl = dataclasses.replace(wl, batch=args.batch)
     K = args.steps or DEFAULT_STEPS.get(wl.name, 100)
     Wm = max(3, args.warmup)
-    S = Setup(wl, dev, args.partition)
+    S = Setup(wl, dev, args.partition, args.unfused)
     stream = torch.cuda.current_stream()
 
     for _ in range(Wm):
-        S.append()
-        S.decode()
+        S.step()
     torch.cuda.synchronize()
     st, detail = kvq.device_error_check()
     if st != 0:
@@ -408,8 +440,7 @@ def run_kvq(args):
         # the timed region: exactly K steps, events only at its two ends
         start.record(stream)
         for _ in range(K):
-            S.append()
-            S.decode()
+            S.step()
         end.record(stream)
         torch.cuda.synchronize()
     if world > 1:
@@ -428,10 +459,11 @@ def run_kvq(args):
     for i in range(Ki):
         e = ev[i]
         e[0].record(stream)
-        S.append()
+        if not S.fused:
+            S.append()
         e[1].record(stream)
         kvq.set_decode_timing_events(e[3], e[4])
-        S.decode()
+        S.decode_step()
         e[2].record(stream)
     torch.cuda.synchronize()
     kvq.set_decode_timing_events()
@@ -443,7 +475,7 @@ def run_kvq(args):
     max_ms, units = aggregate(ms_step, float(S.dec_bytes["total"]), world)
     _, seqs = aggregate(ms_step, float(wl.batch), world)
     value = units / (max_ms * 1e-3) / 1e9
-    launches_per_step = (1 if S.slots_step.numel() else 0) + 1 + (0 if S.num_parts == 1 else 1)
+    launches_per_step = (1 if S.slots_step.numel() and not S.fused else 0) + 2  # [append], stream, reduce
 
     # end to end through the public API: pinned host inputs in, result out
     e2e = None
@@ -460,7 +492,9 @@ def run_kvq(args):
             torch.distributed.destroy_process_group()
         return
     peak, peak_kind = measured_peaks()
-    achieved = S.dec_bytes["total"] / (kern_ms * 1e-3) / 1e9
+    # the stream kernel's algorithmic bytes (with the new rows when it appends them)
+    kern_bytes = S.dec_bytes["total"] + (S.app_bytes if S.fused else 0)
+    achieved = kern_bytes / (kern_ms * 1e-3) / 1e9
     # the recorded figures are for the workload's own batch
     traffic = recorded_traffic(wl.name) if wl.batch == W.WORKLOADS[wl.name].batch else None
     cpu = None
@@ -485,7 +519,8 @@ def run_kvq(args):
                    "num_q_heads": wl.num_q_heads, "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
                    "block_size": wl.block_size, "format": wl.fmt,
                    "context": wl.ctx if isinstance(wl.ctx, int) else list(wl.ctx),
-                   "step": f"append {S.slots_step.numel()} tokens + decode {wl.batch} sequences",
+                   "step": f"append {S.slots_step.numel()} tokens + decode {wl.batch} sequences"
+                           + (" (the append fused into the decode launch)" if S.fused else ""),
                    "l2": f"inputs larger than L2 ({S.dec_bytes['total'] / 1e6:.0f} MB read per decode > 129 MB)"
                    if S.dec_bytes["total"] > L2_BYTES else "inputs smaller than L2 (latency case)",
                    "kernel": args.kernel, "partition": args.partition or "auto",
@@ -494,7 +529,8 @@ def run_kvq(args):
         "instrumented_steps": Ki,
         "decode_ms": round(dec_ms, 5),
         "append_ms": round(app_ms, 5),
-        "append_gbs": round(S.app_bytes / (app_ms * 1e-3) / 1e9, 2) if app_ms > 0 else None,
+        "append_gbs": (round(S.app_bytes / (app_ms * 1e-3) / 1e9, 2) if app_ms > 0 and not S.fused
+                       else None),
         "decode_bytes": S.dec_bytes["total"],
         "decode_kernel_ms": round(kern_ms, 5),
         "roofline": {"bound": "hbm", "kernel": "decode_stream_kernel",

@@ -22,7 +22,8 @@ STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED", 3: "K
           4: "KVQ_ERR_OUT_OF_RANGE", 5: "KVQ_ERR_TIMEOUT", 6: "KVQ_ERR_CUDA",
           7: "KVQ_ERR_SCRATCH_LIMIT"}
 KERNEL_AUTO, KERNEL_SIMT, KERNEL_MMA = 0, 1, 2
-EXPORTS = ("kvq_append", "kvq_decode_workspace_size", "kvq_decode_attention", "kvq_dequant",
+EXPORTS = ("kvq_append", "kvq_decode_workspace_size", "kvq_decode_attention", "kvq_decode_attention_append",
+           "kvq_dequant",
            "kvq_set_decode_kernel", "kvq_device_error_check", "kvq_status_string", "kvq_abi_version",
            "kvq_decode_attention_static_scratch", "kvq_static_scratch_bytes", "kvq_set_decode_timing_events")
 
@@ -71,6 +72,9 @@ def lib():
         L.kvq_decode_attention.restype = ctypes.c_int
         L.kvq_decode_attention.argtypes = [P, P, P, i32, P, i32, i32, i32, P, i32, ctypes.c_float, P, P,
                                            ctypes.c_size_t, i32, P]
+        L.kvq_decode_attention_append.restype = ctypes.c_int
+        L.kvq_decode_attention_append.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, P, i32, ctypes.c_float, P,
+                                                  P, ctypes.c_size_t, i32, P]
         L.kvq_decode_attention_static_scratch.restype = ctypes.c_int
         L.kvq_decode_attention_static_scratch.argtypes = [P, P, P, i32, P, i32, i32, i32, P, i32, ctypes.c_float,
                                                           P, i32, P]
@@ -200,6 +204,37 @@ def decode_attention(q: torch.Tensor, cache: KVCache, block_tables: torch.Tensor
                                     _dev(out, torch.float16, "out"), ws_ptr, ws_bytes, int(partition_size),
                                     _stream(stream))
     _check(st, "kvq_decode_attention")
+    return out
+
+
+def decode_attention_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, cache: KVCache,
+                            block_tables: torch.Tensor, context_lens: torch.Tensor, max_context_len: int,
+                            scale: torch.Tensor | None = None, sm_scale: float = 0.0,
+                            out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                            partition_size: int = 0, stream=None) -> torch.Tensor:
+    """kvq_decode_attention_append: one decode step with each sequence's newest
+    K/V row (fp16 [B][Hkv][D], position context_lens[b] - 1) quantized into the
+    cache in the same launch; bit-identical to ``append`` then ``decode_attention``."""
+    B, Hq, D = q.shape
+    if k_new.shape != (B, cache.num_kv_heads, D) or v_new.shape != k_new.shape:
+        raise ValueError("k_new/v_new must be [batch][num_kv_heads][head_dim]")
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        need = workspace_size(B, Hq, cache.num_kv_heads, D, max_context_len, partition_size)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    d = cache._cdesc()
+    st = lib().kvq_decode_attention_append(_dev(q, torch.float16, "q"), _dev(k_new, torch.float16, "k_new"),
+                                           _dev(v_new, torch.float16, "v_new"), ctypes.byref(d),
+                                           _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
+                                           _dev(context_lens, torch.int32, "context_lens"), B, Hq,
+                                           int(max_context_len), _scale_ptr(scale), cache.fmt, float(sm_scale),
+                                           _dev(out, torch.float16, "out"), ws_ptr, ws_bytes, int(partition_size),
+                                           _stream(stream))
+    _check(st, "kvq_decode_attention_append")
     return out
 
 

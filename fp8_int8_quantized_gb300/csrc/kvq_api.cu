@@ -99,6 +99,65 @@ int32_t resolve_chunk_tiles(int32_t partition_size, int32_t batch, int32_t num_k
     return choose_chunk_tiles(batch, num_kv_heads, max_ctx, sm_count(dev));
 }
 
+kvq_status decode_impl(const void* q, const void* k_new, const void* v_new, const kvq_cache* cache,
+                       const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* context_lens,
+                       int32_t batch, int32_t num_q_heads, int32_t max_context_len, const float* scale, int32_t fmt,
+                       float sm_scale, void* out, void* workspace, size_t workspace_bytes, int32_t partition_size,
+                       kvq_stream_t stream) {
+    kvq_status st = check_cache(cache, fmt);
+    if (st != KVQ_OK) return st;
+    if (batch < 0 || num_q_heads <= 0 || max_context_len < 0 || max_blocks_per_seq <= 0) return KVQ_ERR_INVALID_ARG;
+    if (num_q_heads % cache->num_kv_heads) return KVQ_ERR_INVALID_ARG;
+    const int G = num_q_heads / cache->num_kv_heads;
+    if (G > 8) return KVQ_ERR_UNSUPPORTED;
+    if ((int64_t)max_blocks_per_seq * cache->block_size < max_context_len) return KVQ_ERR_INVALID_ARG;
+    if (batch > 65535 || cache->num_kv_heads > 65535 || num_q_heads > 65535) return KVQ_ERR_UNSUPPORTED;
+    if (batch == 0) return KVQ_OK;
+    if (!q || !block_tables || !context_lens || !out || !aligned(q, 16) || !aligned(out, 16) ||
+        !aligned(block_tables, 4) || !aligned(context_lens, 4))
+        return KVQ_ERR_INVALID_ARG;
+    if (scale && !aligned(scale, 4)) return KVQ_ERR_INVALID_ARG;
+    if (!(sm_scale >= 0.f) || std::isinf(sm_scale)) return KVQ_ERR_INVALID_ARG;
+    if (partition_size < 0 || partition_size % 64 || partition_size > kMaxChunkTokens) return KVQ_ERR_INVALID_ARG;
+    if (batch > kMaxBatch) return KVQ_ERR_UNSUPPORTED;
+    constexpr int TT = kvq::kDecodeTileTokens;
+    if ((int64_t)batch * cache->num_kv_heads * ((max_context_len + TT - 1) / TT) >= 0x7FFFFFFFll)
+        return KVQ_ERR_UNSUPPORTED;  // flat tile indices are 32-bit
+    const int32_t C = resolve_chunk_tiles(partition_size, batch, cache->num_kv_heads, max_context_len);
+    const int32_t nch = std::max<int32_t>(1, ((max_context_len + TT - 1) / TT + C - 1) / C);
+    const size_t need = kvq::ws_bytes(batch, num_q_heads, nch, cache->head_dim);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return KVQ_ERR_WORKSPACE;
+    int kind = g_decode_kernel.load();
+    if (kind == 0) kind = 2;
+    if (kind == 1 && G > 4) return KVQ_ERR_UNSUPPORTED;
+    int dev;
+    if (!current_device(&dev)) return KVQ_ERR_CUDA;
+    unsigned long long* err = err_word(dev);
+    if (!err) return KVQ_ERR_CUDA;
+    kvq::DecodeArgs a{};
+    a.q = static_cast<const uint16_t*>(q);
+    a.cache = view(cache);
+    a.block_tables = block_tables;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.context_lens = context_lens;
+    a.batch = batch;
+    a.num_q_heads = num_q_heads;
+    a.max_context_len = max_context_len;
+    a.scale = fmt == KVQ_INT8 ? nullptr : scale;
+    a.sm_scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt((float)cache->head_dim);
+    a.out = static_cast<uint16_t*>(out);
+    a.ws = static_cast<float*>(workspace);
+    a.chunk_tiles = C;
+    a.num_chunks = nch;
+    a.kernel = kind;
+    a.err = err;
+    a.ev_begin = g_ev_begin;
+    a.ev_end = g_ev_end;
+    a.k_new = static_cast<const uint16_t*>(k_new);
+    a.v_new = static_cast<const uint16_t*>(v_new);
+    return kvq::launch_decode(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -167,56 +226,21 @@ kvq_status kvq_decode_attention(const void* q, const kvq_cache* cache, const int
                                 int32_t num_q_heads, int32_t max_context_len, const float* scale, int32_t fmt,
                                 float sm_scale, void* out, void* workspace, size_t workspace_bytes,
                                 int32_t partition_size, kvq_stream_t stream) {
-    kvq_status st = check_cache(cache, fmt);
-    if (st != KVQ_OK) return st;
-    if (batch < 0 || num_q_heads <= 0 || max_context_len < 0 || max_blocks_per_seq <= 0) return KVQ_ERR_INVALID_ARG;
-    if (num_q_heads % cache->num_kv_heads) return KVQ_ERR_INVALID_ARG;
-    const int G = num_q_heads / cache->num_kv_heads;
-    if (G > 8) return KVQ_ERR_UNSUPPORTED;
-    if ((int64_t)max_blocks_per_seq * cache->block_size < max_context_len) return KVQ_ERR_INVALID_ARG;
-    if (batch > 65535 || cache->num_kv_heads > 65535 || num_q_heads > 65535) return KVQ_ERR_UNSUPPORTED;
-    if (batch == 0) return KVQ_OK;
-    if (!q || !block_tables || !context_lens || !out || !aligned(q, 16) || !aligned(out, 16) ||
-        !aligned(block_tables, 4) || !aligned(context_lens, 4))
-        return KVQ_ERR_INVALID_ARG;
-    if (scale && !aligned(scale, 4)) return KVQ_ERR_INVALID_ARG;
-    if (!(sm_scale >= 0.f) || std::isinf(sm_scale)) return KVQ_ERR_INVALID_ARG;
-    if (partition_size < 0 || partition_size % 64 || partition_size > kMaxChunkTokens) return KVQ_ERR_INVALID_ARG;
-    if (batch > kMaxBatch) return KVQ_ERR_UNSUPPORTED;
-    constexpr int TT = kvq::kDecodeTileTokens;
-    if ((int64_t)batch * cache->num_kv_heads * ((max_context_len + TT - 1) / TT) >= 0x7FFFFFFFll)
-        return KVQ_ERR_UNSUPPORTED;  // flat tile indices are 32-bit
-    const int32_t C = resolve_chunk_tiles(partition_size, batch, cache->num_kv_heads, max_context_len);
-    const int32_t nch = std::max<int32_t>(1, ((max_context_len + TT - 1) / TT + C - 1) / C);
-    const size_t need = kvq::ws_bytes(batch, num_q_heads, nch, cache->head_dim);
-    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return KVQ_ERR_WORKSPACE;
-    int kind = g_decode_kernel.load();
-    if (kind == 0) kind = 2;
-    if (kind == 1 && G > 4) return KVQ_ERR_UNSUPPORTED;
-    int dev;
-    if (!current_device(&dev)) return KVQ_ERR_CUDA;
-    unsigned long long* err = err_word(dev);
-    if (!err) return KVQ_ERR_CUDA;
-    kvq::DecodeArgs a{};
-    a.q = static_cast<const uint16_t*>(q);
-    a.cache = view(cache);
-    a.block_tables = block_tables;
-    a.max_blocks_per_seq = max_blocks_per_seq;
-    a.context_lens = context_lens;
-    a.batch = batch;
-    a.num_q_heads = num_q_heads;
-    a.max_context_len = max_context_len;
-    a.scale = fmt == KVQ_INT8 ? nullptr : scale;
-    a.sm_scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt((float)cache->head_dim);
-    a.out = static_cast<uint16_t*>(out);
-    a.ws = static_cast<float*>(workspace);
-    a.chunk_tiles = C;
-    a.num_chunks = nch;
-    a.kernel = kind;
-    a.err = err;
-    a.ev_begin = g_ev_begin;
-    a.ev_end = g_ev_end;
-    return kvq::launch_decode(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+    return decode_impl(q, nullptr, nullptr, cache, block_tables, max_blocks_per_seq, context_lens, batch,
+                       num_q_heads, max_context_len, scale, fmt, sm_scale, out, workspace, workspace_bytes,
+                       partition_size, stream);
+}
+
+kvq_status kvq_decode_attention_append(const void* q, const void* k_new, const void* v_new, const kvq_cache* cache,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* context_lens, int32_t batch, int32_t num_q_heads,
+                                       int32_t max_context_len, const float* scale, int32_t fmt, float sm_scale,
+                                       void* out, void* workspace, size_t workspace_bytes, int32_t partition_size,
+                                       kvq_stream_t stream) {
+    if (batch > 0 && (!k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16))) return KVQ_ERR_INVALID_ARG;
+    return decode_impl(q, k_new, v_new, cache, block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads,
+                       max_context_len, scale, fmt, sm_scale, out, workspace, workspace_bytes, partition_size,
+                       stream);
 }
 
 kvq_status kvq_dequant(const kvq_cache* cache, const int64_t* slots, int64_t num_slots, const float* scale,

@@ -71,17 +71,21 @@ enum { kKindSimt = 1, kKindMma = 2 };
 // Shared-memory layout of one CTA (bytes from a 1024-aligned base).  Tiles
 // first (1024-aligned for the 128-byte swizzle), then per warp its INT8 row
 // scales, its stage barriers and the query rows of the (sequence, kv-head)
-// pair it is on, then the scan of tiles per sequence and the clamped context
+// pair it is on; when the launch appends the newest tokens, per warp the fp16
+// K and V rows of the token that ends the pending pair and the block id its
+// row goes to; then the scan of tiles per sequence and the clamped context
 // lengths.
 struct Layout {
-    int tile_bytes, q_bytes, scales, full, qbuf, scan, total;
-    __host__ __device__ Layout(int D, int G, int B, bool int8) {
+    int tile_bytes, q_bytes, scales, full, qbuf, newkv, patch, scan, total;
+    __host__ __device__ Layout(int D, int G, int B, bool int8, bool append) {
         tile_bytes = kTile * D;
         q_bytes = (G * D * 2 + 127) / 128 * 128;
         scales = kConsumers * kSpw * 2 * tile_bytes;            // [warp][stage][K,V][tile] before this
         full = scales + (int8 ? kConsumers * kSpw * 2 * kTile * 4 : 0);  // INT8: f32 [warp][stage][K,V][32]
         qbuf = (full + kConsumers * kSpw * 8 + 127) / 128 * 128;  // u64 [warp][stage], then f16 [warp][G][D]
-        scan = qbuf + kConsumers * q_bytes;                     // int S[B + 1], ctx[B]
+        newkv = qbuf + kConsumers * q_bytes;                    // f16 [warp][K,V][D]
+        patch = newkv + (append ? kConsumers * 2 * D * 2 : 0);  // int [warp]
+        scan = patch + (append ? kConsumers * 4 : 0);           // int S[B + 1], ctx[B]
         total = scan + (2 * B + 1) * 4;
     }
 };
@@ -616,6 +620,103 @@ struct MmaConsumer {
     }
 };
 
+// ------------------------------------------------------ append in decode --
+
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void sts16(uint32_t addr, uint16_t v) {
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+__device__ __forceinline__ void stsf(uint32_t addr, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// One warp quantizes the newest token's K and V rows (fp16, in shared memory
+// at nkv) exactly as the append kernels do, writes the codes (and INT8 row
+// scales) to the cache row of position `pos`, and patches them into the
+// landed stage tile (first token tok0) so this tile's attention sees them.
+// blk < 0: the block id was outside the cache (already recorded); nothing is
+// written.  Lane l handles values D/32 * l ...
+template <int FMT, int D>
+__device__ __noinline__ void append_newest(const uint16_t* nkv, int blk, int pos, int tok0, int kvh,
+                                           const DecodeArgs& a, float s_fp8, uint32_t kt, int tile_bytes,
+                                           uint32_t st, int lane) {
+    constexpr int VPL = D / 32;  // values per lane: 4 or 2
+    float x[2][VPL];
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+        const uint16_t* src = nkv + w * D + VPL * lane;
+        if (VPL == 4) {
+            const uint2 r = *reinterpret_cast<const uint2*>(src);
+            const float2 f0 = f16x2_to_f32x2(r.x), f1 = f16x2_to_f32x2(r.y);
+            x[w][0] = f0.x; x[w][1] = f0.y; x[w][VPL > 2 ? 2 : 0] = f1.x; x[w][VPL > 3 ? 3 : 1] = f1.y;
+        } else {
+            const float2 f0 = f16x2_to_f32x2(*reinterpret_cast<const uint32_t*>(src));
+            x[w][0] = f0.x; x[w][1] = f0.y;
+        }
+    }
+    uint32_t code[2];
+    float rs[2] = {0.f, 0.f};
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+        uint32_t c = 0;
+        if (FMT == INT8) {
+            float amax = 0.f;
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) amax = fmaxf(amax, fabsf(x[w][i]));
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+            const float s = __fdiv_rn(amax, 127.0f);
+            rs[w] = s;
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) {
+                int q = 0;
+                if (s != 0.f) q = max(-127, min(127, __float2int_rn(__fdiv_rn(x[w][i], s))));
+                c |= (uint32_t)(q & 0xFF) << (8 * i);
+            }
+        } else {
+            float y[VPL];
+#pragma unroll
+            for (int i = 0; i < VPL; ++i) y[i] = s_fp8 != 1.0f ? __fdiv_rn(x[w][i], s_fp8) : x[w][i];
+#pragma unroll
+            for (int i = 0; i < VPL; i += 2) c |= (uint32_t)enc_fp8x2<FMT>(y[i], y[i + 1]) << (8 * i);
+        }
+        code[w] = c;
+    }
+    if (blk >= 0) {
+        const int r = pos - tok0;  // row in the tile: box r / 16, row r % 16
+        const uint32_t kb = kt + (r / kBox) * kBox * D;
+        if (D == 128) {
+            const uint32_t off = tile_off<128>(r % kBox, lane >> 2) + 4 * (lane & 3);
+            sts32(kb + off, code[0]);
+            sts32(kb + tile_bytes + off, code[1]);
+        } else {
+            const uint32_t off = (r % kBox) * D + 2 * lane;
+            sts16(kb + off, (uint16_t)code[0]);
+            sts16(kb + tile_bytes + off, (uint16_t)code[1]);
+        }
+        const int BS = a.cache.block_size;
+        const int64_t row = ((int64_t)blk * a.cache.num_kv_heads + kvh) * BS + (pos & (BS - 1));
+        if (D == 128) {
+            reinterpret_cast<uint32_t*>(a.cache.k_codes + row * D)[lane] = code[0];
+            reinterpret_cast<uint32_t*>(a.cache.v_codes + row * D)[lane] = code[1];
+        } else {
+            reinterpret_cast<uint16_t*>(a.cache.k_codes + row * D)[lane] = (uint16_t)code[0];
+            reinterpret_cast<uint16_t*>(a.cache.v_codes + row * D)[lane] = (uint16_t)code[1];
+        }
+        if (FMT == INT8 && lane == 0) {
+            stsf(st + 4 * r, rs[0]);
+            stsf(st + 4 * kTile + 4 * r, rs[1]);
+            a.cache.k_scales[row] = rs[0];
+            a.cache.v_scales[row] = rs[1];
+        }
+        // the stage is refilled by TMA later: order these generic writes first
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncwarp();
+}
+
 // -------------------------------------------------------------- kernel --
 
 template <int FMT, int D, class Consumer>
@@ -627,7 +728,8 @@ __global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int B = a.batch, Hkv = a.cache.num_kv_heads, BS = a.cache.block_size;
     const int G = a.num_q_heads / Hkv;
-    const Layout L(D, G, B, FMT == INT8);
+    const bool append = a.k_new != nullptr;
+    const Layout L(D, G, B, FMT == INT8, append);
     int* S = reinterpret_cast<int*>(smem + L.scan);
     int* ctx_s = S + B + 1;
     griddep_wait();    // inputs may come from the previous kernel (an append)
@@ -682,6 +784,8 @@ __global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
     float* scales = reinterpret_cast<float*>(smem + L.scales) + warp * kSpw * 2 * kTile;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full) + warp * kSpw;
     uint8_t* qbuf = smem + L.qbuf + warp * L.q_bytes;
+    uint16_t* nkv = reinterpret_cast<uint16_t*>(smem + L.newkv) + warp * 2 * D;  // appending launches only
+    int* patch_blk = reinterpret_cast<int*>(smem + L.patch) + warp;
     const uint32_t tiles_u32 = smem_u32(tiles), scales_u32 = smem_u32(scales);
 
     // Block-table entries of the 32 boxes of flat tiles [first, first + 16):
@@ -713,10 +817,11 @@ __global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
     Consumer cons;
     cons.init(G, a.sm_scale * s_fp8 * kLog2e);
 
-    // issue side: next flat tile fi, its stage ist, its position iw, and the
-    // first tile of the last pair whose queries were copied (pend)
+    // issue side: next flat tile fi, its stage ist, its position iw, the
+    // first tile of the last pair whose queries were copied (pend) and the
+    // last tile of the last pair whose newest K/V row was copied (lpend)
     Walk iw = locate(S, B, Hkv, lo);
-    int fi = lo, ist = 0, pend = -1;
+    int fi = lo, ist = 0, pend = -1, lpend = -1;
     // consume side: next flat tile fc, its stage cst and barrier parity cph, its
     // position cw, tile ctc within chunk cch, and the slot half of the segment
     // in progress
@@ -729,19 +834,28 @@ __global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
 
     // Issue tiles while a stage is free.  The first tile of a pair also copies
     // the pair's queries into this warp's query buffer, which must not happen
-    // before the previous pair's first tile has been consumed.
+    // before the previous pair's first tile has been consumed.  In an
+    // appending launch the last tile of a pair also copies the fp16 K and V
+    // rows of the pair's newest token into the warp's new-row buffer, under
+    // the same rule.
     auto issue_ready = [&]() {
         while (fi < hi && fi - fc < kSpw) {
             const int rel = fi - lo;
             const bool new_pair = iw.t == 0 || rel == 0;
             if (new_pair && pend >= fc) break;
+            const bool ends = append && iw.t == iw.n - 1;
+            if (ends && lpend >= fc) break;
             const int id0 = __shfl_sync(0xFFFFFFFFu, idc, (2 * rel) & 31);
             const int id1 = __shfl_sync(0xFFFFFFFFu, idc, (2 * rel + 1) & 31);
             if (lane == 0) {
                 const int tok0 = iw.t * kTile;
                 const int nbox = ctx_s[iw.b] - tok0 > kBox ? 2 : 1;  // a box past the context is not loaded
                 uint64_t* fb = &full[ist];
-                mbar_arrive_expect_tx(fb, nbox * box_tx + (new_pair ? q_tx : 0u));
+                if (ends) {  // block of the newest row; -1 (not written) if outside the cache
+                    const int nb = ctx_s[iw.b] - 1 - tok0 >= kBox ? id1 : id0;
+                    *patch_blk = nb < 0 || nb >= a.cache.num_blocks ? -1 : nb;
+                }
+                mbar_arrive_expect_tx(fb, nbox * box_tx + (new_pair ? q_tx : 0u) + (ends ? 4u * D : 0u));
                 const uint32_t kt = tiles_u32 + ist * (2 * L.tile_bytes);
                 const uint32_t st = scales_u32 + ist * (2 * kTile * 4);
 #pragma unroll
@@ -762,8 +876,14 @@ __global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
                 }
                 if (new_pair)
                     bulk_load(qbuf, a.q + ((int64_t)iw.b * a.num_q_heads + (int64_t)iw.kvh * G) * D, q_tx, fb, pol);
+                if (ends) {
+                    const int64_t row = ((int64_t)iw.b * Hkv + iw.kvh) * D;
+                    bulk_load(nkv, a.k_new + row, 2 * D, fb, pol);
+                    bulk_load(nkv + D, a.v_new + row, 2 * D, fb, pol);
+                }
             }
             if (new_pair) pend = fi;
+            if (ends) lpend = fi;
             advance(iw, S, B, Hkv);
             ++fi;
             ist = ist + 1 == kSpw ? 0 : ist + 1;
@@ -783,6 +903,10 @@ __global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
             break;
         }
         if (cw.t == 0 || fc == lo) cons.set_q(reinterpret_cast<const uint16_t*>(qbuf));  // came with this tile
+        if (append && cw.t == cw.n - 1)
+            append_newest<FMT, D>(nkv, *patch_blk, ctx_s[cw.b] - 1, cw.t * kTile, cw.kvh, a, s_fp8,
+                                  tiles_u32 + cst * (2 * L.tile_bytes), L.tile_bytes,
+                                  scales_u32 + cst * (2 * kTile * 4), lane);
         const uint32_t kt = tiles_u32 + cst * (2 * L.tile_bytes);
         const Tile tl{kt, kt + L.tile_bytes, scales_u32 + cst * (2 * kTile * 4), min(kTile, ctx_s[cw.b] - cw.t * kTile)};
         cons.tile(tl);
@@ -920,7 +1044,8 @@ bool make_tmap(CUtensorMap* m, void* base, int64_t rows, int D) {
 template <int FMT, int D, class Consumer>
 cudaError_t launch_stream(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, cudaStream_t s) {
     auto kern = decode_stream_kernel<FMT, D, Consumer>;
-    const int smem = Layout(D, a.num_q_heads / a.cache.num_kv_heads, a.batch, FMT == INT8).total + 1024;
+    const int smem =
+        Layout(D, a.num_q_heads / a.cache.num_kv_heads, a.batch, FMT == INT8, a.k_new != nullptr).total + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);

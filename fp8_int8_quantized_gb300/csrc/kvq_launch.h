@@ -64,6 +64,8 @@ struct DecodeArgs {
     int32_t kernel;      // 1 = CUDA-core, 2 = tensor-core
     unsigned long long* err;
     cudaEvent_t ev_begin, ev_end;  // optional: recorded around the main kernel
+    const uint16_t* k_new;  // optional fp16 [B][Hkv][D]: newest token's K/V, appended in the launch
+    const uint16_t* v_new;
 };
 
 #ifdef __CUDACC__

@@ -6,6 +6,8 @@
  *   kvq_append            quantize-on-write of fp16 K/V into the paged cache;
  *   kvq_decode_attention  single-token decode attention that dequantizes the
  *                         cache on read and computes in fp16/fp32.
+ *   kvq_decode_attention_append  the same decode with each sequence's newest
+ *                         K/V row quantized into the cache in the same launch.
  *
  * plus kvq_dequant, a debugging gather that returns the fp32 values a kernel
  * sees.  The operations follow these pages (cited by title and section):
@@ -143,6 +145,28 @@ KVQ_API kvq_status kvq_decode_attention(const void* q, const kvq_cache* cache,
                                 const float* scale, int32_t fmt, float sm_scale, void* out,
                                 void* workspace, size_t workspace_bytes,
                                 int32_t partition_size, kvq_stream_t stream);
+
+/* Decode step with the newest token's K/V appended inside the same launch:
+ * the result -- cache bytes, INT8 row scales and out -- is bit-identical to
+ * kvq_append of k_new / v_new followed by kvq_decode_attention with the same
+ * arguments.  It follows the same passages as those two calls; fusing them is
+ * a scheduling choice (one launch instead of two) that no page prescribes.
+ *   k_new, v_new: fp16 [batch][num_kv_heads][head_dim], the K and V rows of
+ *     each sequence's newest token, position context_lens[b] - 1, which goes to
+ *     the cache slot block_tables[b][(ctx - 1) / block_size] * block_size +
+ *     (ctx - 1) % block_size.  A sequence with context 0 appends nothing.
+ *     The row is quantized exactly as kvq_append does (FP8 with `scale`, INT8
+ *     with its own row scale).
+ *   Every other argument, the workspace and the errors are those of
+ *   kvq_decode_attention; a block id outside the cache is recorded and its row
+ *   is not written. */
+KVQ_API kvq_status kvq_decode_attention_append(const void* q, const void* k_new, const void* v_new,
+                                       const kvq_cache* cache, const int32_t* block_tables,
+                                       int32_t max_blocks_per_seq, const int32_t* context_lens,
+                                       int32_t batch, int32_t num_q_heads, int32_t max_context_len,
+                                       const float* scale, int32_t fmt, float sm_scale, void* out,
+                                       void* workspace, size_t workspace_bytes,
+                                       int32_t partition_size, kvq_stream_t stream);
 
 /* Decode attention for callers that cannot allocate device memory (no page
  * has a counterpart: this is a deployment variant).  Plugin hosts that give an

@@ -68,3 +68,7 @@ def test_invalid_args_rejected_before_any_cuda_call(lib):
     assert lib.kvq_decode_attention(16, ctypes.byref(d), 16, 4, 16, 2, 4, 64, None, kvq.E4M3, 0.0,
                                     16, None, 0, 100, None) == 1                            # partition % 64
     assert lib.kvq_dequant(ctypes.byref(d), None, 3, None, kvq.E4M3, None, None, None) == 1
+    assert lib.kvq_decode_attention_append(16, None, 16, ctypes.byref(d), 16, 4, 16, 2, 4, 64, None, kvq.E4M3,
+                                           0.0, 16, None, 0, 0, None) == 1                  # no k_new
+    assert lib.kvq_decode_attention_append(16, 24, 16, ctypes.byref(d), 16, 4, 16, 2, 4, 64, None, kvq.E4M3,
+                                           0.0, 16, None, 0, 0, None) == 1                  # misaligned k_new
