@@ -1,4 +1,5 @@
-"""CPU oracle for the quantized paged KV cache (quantize-on-write + decode attention).
+"""CPU oracle for the quantized paged KV cache (quantize-on-write, decode attention
+and causal attention of a chunk of new queries over the cache).
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 ``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
@@ -77,6 +78,10 @@ def _load():
                                                 P, P, P, P, i64, ctypes.c_int, ctypes.c_int,
                                                 ctypes.c_int, P, ctypes.c_int, P, f32, f64,
                                                 P, P, i64]
+        lib.oracle_prefill_attention.restype = ctypes.c_int
+        lib.oracle_prefill_attention.argtypes = [P, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                 P, P, P, P, i64, ctypes.c_int, ctypes.c_int,
+                                                 ctypes.c_int, P, ctypes.c_int, P, P, f32, f64, P]
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_init()
         _lib = lib
@@ -208,3 +213,34 @@ def decode_attention(q, cache: Cache, block_tables, context_lens, scale: float |
     if rc != 0:
         raise IndexError("block table / context length outside the cache")
     return (out, w) if return_weights else out
+
+
+def prefill_attention(q, cache: Cache, block_tables, context_lens, query_start,
+                      scale: float | None = None, sm_scale: float | None = None):
+    """fp64 causal attention of chunks of new queries over the cache.
+
+    q fp16 [Tq][Hq][D]; sequence b owns rows query_start[b] .. query_start[b+1]-1,
+    the last n_b of its context_lens[b] cached positions (its own K/V already
+    appended); query i of the chunk attends to positions 0 .. ctx - n_b + i.
+    Returns out fp64 [Tq][Hq][D] (rows no chunk covers stay zero)."""
+    q = _need(np.ascontiguousarray(q), np.float16, "q")
+    Tq, Hq, D = q.shape
+    if D != cache.head_dim or Hq % cache.num_kv_heads:
+        raise ValueError("q shape does not match the cache")
+    bt = _need(np.ascontiguousarray(block_tables, dtype=np.int32), np.int32, "block_tables")
+    cl = _need(np.ascontiguousarray(context_lens, dtype=np.int32), np.int32, "context_lens")
+    qs = _need(np.ascontiguousarray(query_start, dtype=np.int32), np.int32, "query_start")
+    B = cl.shape[0]
+    if qs.shape[0] != B + 1:
+        raise ValueError("query_start needs batch + 1 entries")
+    out = np.zeros((Tq, Hq, D), np.float64)
+    s = np.float32(1.0 if scale is None else scale)
+    sm = default_sm_scale(D) if not sm_scale else float(sm_scale)
+    rc = _load().oracle_prefill_attention(_ptr(q.view(np.uint16)), Tq, B, Hq, D, _ptr(cache.k_codes),
+                                          _ptr(cache.v_codes), _ptr(cache.k_scales),
+                                          _ptr(cache.v_scales), cache.num_blocks, cache.block_size,
+                                          cache.num_kv_heads, cache.fmt, _ptr(bt), bt.shape[1],
+                                          _ptr(cl), _ptr(qs), s, sm, _ptr(out))
+    if rc != 0:
+        raise IndexError("chunk longer than its context, or block table / context outside the cache")
+    return out

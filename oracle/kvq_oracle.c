@@ -1,6 +1,7 @@
 /*
  * kvq oracle: a plain, slow, obviously correct CPU restatement of the quantized
- * KV-cache hot path (quantize-on-write and single-token decode attention).
+ * KV-cache hot path (quantize-on-write, single-token decode attention, and
+ * causal attention of a chunk of new queries over the cache).
  *
  * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
  * benchmark's CPU-baseline leg may build, load or call this file.  It shares no
@@ -26,7 +27,11 @@
  *    gives s = 0 and all-zero codes;
  *  - attention: logits l_t = sm_scale * <q, k_t> over all t < context_len,
  *    softmax, out = sum_t w_t v_t; q-head h reads kv-head h / (Hq / Hkv);
- *    context_len 0 gives zeros.
+ *    context_len 0 gives zeros;
+ *  - a chunk of n new queries of a sequence with context_len tokens (the
+ *    chunk's own K/V already appended) holds positions context_len - n ...
+ *    context_len - 1; query i attends causally to every t <= its position,
+ *    i.e. it is the decode attention above with context_len - n + i + 1.
  *
  * Floating point: compile without fast-math and with -ffp-contract=off; every
  * fp32 step below is one IEEE operation in fp32, everything else is fp64.
@@ -295,6 +300,74 @@ int oracle_decode_attention(const uint16_t* q, int B, int Hq, int D,
             }
             free(logit);
         }
+    }
+    return bad ? -1 : 0;
+}
+
+/* Causal attention of chunks of new queries over the paged quantized cache,
+ * fp64 on the fp32-dequantized values.  q: fp16 bits [Tq][Hq][D], D <= 512, the
+ * rows of sequence b at query_start[b] .. query_start[b+1]-1 (n_b of them, in
+ * position order); context_lens[b] counts every cached token of b, the chunk's
+ * own included.  Query i of sequence b sits at p = context_lens[b] - n_b + i
+ * and attends to t = 0 .. p:  l_t = sm_scale <q, k_t>, w = softmax(l),
+ * out = sum_t w_t v_t.  out: fp64 [Tq][Hq][D].  Returns 0, or -1 on a chunk
+ * longer than its context or a block id / context outside the cache or table. */
+int oracle_prefill_attention(const uint16_t* q, int64_t Tq, int B, int Hq, int D,
+                             const uint8_t* k_codes, const uint8_t* v_codes,
+                             const float* k_scales, const float* v_scales,
+                             int64_t NB, int BS, int Hkv, int fmt,
+                             const int32_t* block_tables, int max_blocks,
+                             const int32_t* context_lens, const int32_t* query_start,
+                             float scale, double sm_scale, double* out) {
+    int G = Hq / Hkv;
+    int bad = 0;
+    for (int64_t r = 0; r < Tq * Hq * D; ++r) out[r] = 0.0;
+    for (int b = 0; b < B; ++b) {
+        int n = query_start[b + 1] - query_start[b];
+        if (n < 0 || n > context_lens[b] || query_start[b] < 0 || query_start[b + 1] > Tq) bad = 1;
+        if ((int64_t)context_lens[b] > (int64_t)max_blocks * BS) bad = 1;
+    }
+    if (bad) return -1;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t row = 0; row < Tq; ++row) {
+        int b = 0;
+        while (b < B && !(row >= query_start[b] && row < query_start[b + 1])) ++b;
+        if (b == B) continue;                       /* a row no chunk covers stays zero */
+        int n = query_start[b + 1] - query_start[b];
+        int pos = context_lens[b] - n + (int)(row - query_start[b]);
+        int len = pos + 1;                          /* tokens 0 .. pos attend */
+        double* logit = (double*)malloc(sizeof(double) * (size_t)len);
+        double qv[512];
+        for (int h = 0; h < Hq; ++h) {
+            int kvh = h / G;
+            double* o = out + ((size_t)row * Hq + h) * D;
+            for (int d = 0; d < D; ++d) qv[d] = half_bits_to_double(q[((size_t)row * Hq + h) * D + d]);
+            int ok = 1;
+            for (int t = 0; t < len; ++t) {
+                int32_t blk = block_tables[(size_t)b * max_blocks + t / BS];
+                if (blk < 0 || blk >= NB) { ok = 0; break; }
+                size_t kr = ((size_t)blk * Hkv + kvh) * BS + t % BS;
+                float sk = fmt == ORC_INT8 ? k_scales[kr] : scale;
+                double acc = 0.0;
+                for (int d = 0; d < D; ++d)
+                    acc += qv[d] * (double)dequant_value(fmt, k_codes[kr * D + d], sk);
+                logit[t] = sm_scale * acc;
+            }
+            if (!ok) { bad = 1; break; }
+            double m = -INFINITY;
+            for (int t = 0; t < len; ++t) if (logit[t] > m) m = logit[t];
+            double denom = 0.0;
+            for (int t = 0; t < len; ++t) { logit[t] = exp(logit[t] - m); denom += logit[t]; }
+            for (int t = 0; t < len; ++t) {
+                double w = logit[t] / denom;
+                int32_t blk = block_tables[(size_t)b * max_blocks + t / BS];
+                size_t vr = ((size_t)blk * Hkv + kvh) * BS + t % BS;
+                float sv = fmt == ORC_INT8 ? v_scales[vr] : scale;
+                for (int d = 0; d < D; ++d)
+                    o[d] += w * (double)dequant_value(fmt, v_codes[vr * D + d], sv);
+            }
+        }
+        free(logit);
     }
     return bad ? -1 : 0;
 }
