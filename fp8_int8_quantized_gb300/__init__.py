@@ -25,7 +25,8 @@ KERNEL_AUTO, KERNEL_SIMT, KERNEL_MMA = 0, 1, 2
 EXPORTS = ("kvq_append", "kvq_decode_workspace_size", "kvq_decode_attention", "kvq_decode_attention_append",
            "kvq_dequant",
            "kvq_set_decode_kernel", "kvq_device_error_check", "kvq_status_string", "kvq_abi_version",
-           "kvq_decode_attention_static_scratch", "kvq_static_scratch_bytes", "kvq_set_decode_timing_events")
+           "kvq_decode_attention_static_scratch", "kvq_static_scratch_bytes", "kvq_set_decode_timing_events",
+           "kvq_prefill_attention")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkvq.so")
@@ -79,6 +80,9 @@ def lib():
         L.kvq_decode_attention_static_scratch.argtypes = [P, P, P, i32, P, i32, i32, i32, P, i32, ctypes.c_float,
                                                           P, i32, P]
         L.kvq_static_scratch_bytes.restype = ctypes.c_size_t
+        L.kvq_prefill_attention.restype = ctypes.c_int
+        L.kvq_prefill_attention.argtypes = [P, P, P, i32, P, P, i32, i64, i32, i32, P, i32, ctypes.c_float, P,
+                                            P]
         L.kvq_dequant.restype = ctypes.c_int
         L.kvq_dequant.argtypes = [P, P, i64, P, i32, P, P, P]
         L.kvq_set_decode_timing_events.restype = None
@@ -204,6 +208,33 @@ def decode_attention(q: torch.Tensor, cache: KVCache, block_tables: torch.Tensor
                                     _dev(out, torch.float16, "out"), ws_ptr, ws_bytes, int(partition_size),
                                     _stream(stream))
     _check(st, "kvq_decode_attention")
+    return out
+
+
+def prefill_attention(q: torch.Tensor, cache: KVCache, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                      query_start: torch.Tensor, max_query_len: int, scale: torch.Tensor | None = None,
+                      sm_scale: float = 0.0, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """kvq_prefill_attention: causal attention of chunks of new queries over the cache.
+
+    q fp16 [Tq][Hq][D]; sequence b owns rows query_start[b] .. query_start[b+1]-1, the last
+    positions of its context_lens[b] cached tokens.  Returns out fp16 [Tq][Hq][D]."""
+    Tq, Hq, D = q.shape
+    if D != cache.head_dim:
+        raise ValueError("head_dim mismatch")
+    B = context_lens.shape[0]
+    if query_start.shape[0] != B + 1:
+        raise ValueError("query_start needs batch + 1 entries")
+    if out is None:
+        out = torch.empty_like(q)
+    d = cache._cdesc()
+    st = lib().kvq_prefill_attention(_dev(q, torch.float16, "q"), ctypes.byref(d),
+                                     _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
+                                     _dev(context_lens, torch.int32, "context_lens"),
+                                     _dev(query_start, torch.int32, "query_start"), B, Tq, Hq,
+                                     int(max_query_len),
+                                     _scale_ptr(scale), cache.fmt, float(sm_scale),
+                                     _dev(out, torch.float16, "out"), _stream(stream))
+    _check(st, "kvq_prefill_attention")
     return out
 
 

@@ -243,6 +243,47 @@ kvq_status kvq_decode_attention_append(const void* q, const void* k_new, const v
                        stream);
 }
 
+kvq_status kvq_prefill_attention(const void* q, const kvq_cache* cache, const int32_t* block_tables,
+                                 int32_t max_blocks_per_seq, const int32_t* context_lens, const int32_t* query_start,
+                                 int32_t batch, int64_t num_q_tokens, int32_t num_q_heads, int32_t max_query_len,
+                                 const float* scale,
+                                 int32_t fmt, float sm_scale, void* out, kvq_stream_t stream) {
+    kvq_status st = check_cache(cache, fmt);
+    if (st != KVQ_OK) return st;
+    if (batch < 0 || num_q_tokens < 0 || num_q_heads <= 0 || max_query_len < 0 || max_blocks_per_seq <= 0)
+        return KVQ_ERR_INVALID_ARG;
+    if (num_q_heads % cache->num_kv_heads) return KVQ_ERR_INVALID_ARG;
+    if (num_q_heads / cache->num_kv_heads > kvq::prefill_rows_per_tile()) return KVQ_ERR_UNSUPPORTED;
+    if (num_q_tokens > 0x7FFFFFFFll) return KVQ_ERR_UNSUPPORTED;   // query_start entries are int32
+    if (batch > 65535 || cache->num_kv_heads > 65535) return KVQ_ERR_UNSUPPORTED;
+    if (batch == 0 || max_query_len == 0 || num_q_tokens == 0) return KVQ_OK;
+    if (!q || !block_tables || !context_lens || !query_start || !out || !aligned(q, 16) || !aligned(out, 16) ||
+        !aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(query_start, 4))
+        return KVQ_ERR_INVALID_ARG;
+    if (scale && !aligned(scale, 4)) return KVQ_ERR_INVALID_ARG;
+    if (!(sm_scale >= 0.f) || std::isinf(sm_scale)) return KVQ_ERR_INVALID_ARG;
+    int dev;
+    if (!current_device(&dev)) return KVQ_ERR_CUDA;
+    unsigned long long* err = err_word(dev);
+    if (!err) return KVQ_ERR_CUDA;
+    kvq::PrefillArgs a{};
+    a.q = static_cast<const uint16_t*>(q);
+    a.cache = view(cache);
+    a.block_tables = block_tables;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.context_lens = context_lens;
+    a.query_start = query_start;
+    a.batch = batch;
+    a.num_q_tokens = num_q_tokens;
+    a.num_q_heads = num_q_heads;
+    a.max_query_len = max_query_len;
+    a.scale = fmt == KVQ_INT8 ? nullptr : scale;
+    a.sm_scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt((float)cache->head_dim);
+    a.out = static_cast<uint16_t*>(out);
+    a.err = err;
+    return kvq::launch_prefill(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
 kvq_status kvq_dequant(const kvq_cache* cache, const int64_t* slots, int64_t num_slots, const float* scale,
                        int32_t fmt, float* out_k, float* out_v, kvq_stream_t stream) {
     kvq_status st = check_cache(cache, fmt);

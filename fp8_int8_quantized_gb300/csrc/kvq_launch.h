@@ -68,6 +68,21 @@ struct DecodeArgs {
     const uint16_t* v_new;
 };
 
+struct PrefillArgs {
+    const uint16_t* q;  // fp16 bits [num_q_tokens][Hq][D]
+    CacheView cache;
+    const int32_t* block_tables;
+    int32_t max_blocks_per_seq;
+    const int32_t* context_lens;
+    const int32_t* query_start;  // [batch + 1]
+    int64_t num_q_tokens;
+    int32_t batch, num_q_heads, max_query_len;
+    const float* scale;  // device, may be null (= 1.0); FP8 only
+    float sm_scale;      // resolved (> 0)
+    uint16_t* out;       // fp16 bits [num_q_tokens][Hq][D]
+    unsigned long long* err;
+};
+
 #ifdef __CUDACC__
 // Launch with programmatic stream serialization: the kernel may be scheduled
 // while the previous kernel on the stream finishes; it must call
@@ -92,6 +107,8 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
 cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
+int prefill_rows_per_tile();  // (query, q-head) rows per CTA of the prefill kernel
 
 // Workspace layout: every context chunk of every (sequence, q-head) has two
 // partial slots (a chunk is streamed by at most two warps).  acc fp32

@@ -202,3 +202,31 @@ def append_bytes(wl: Workload, num_tokens: int) -> int:
     if wl.fmt == "int8":
         b += 2 * num_tokens * wl.num_kv_heads * 4
     return b
+
+
+def prefill_chunks(wl: Workload, ctx: torch.Tensor, chunk: int | None = None) -> torch.Tensor:
+    """int32 [batch] new-query counts of a chunked-prefill step: ``chunk`` (default
+    the workload's append chunk) clipped to each sequence's context."""
+    n = wl.append_chunk if chunk is None else chunk
+    return torch.clamp(ctx.to(torch.int32), max=n)
+
+
+def prefill_queries(wl: Workload, chunk_lens: torch.Tensor, device="cpu", step: int = 0):
+    """fp16 Q [sum(chunk_lens)][Hq][D] ~ N(0, 1) and int32 query_start [batch + 1]
+    for chunks of ``chunk_lens`` new queries per sequence."""
+    qs = torch.zeros(chunk_lens.shape[0] + 1, dtype=torch.int32)
+    qs[1:] = torch.cumsum(chunk_lens.to(torch.int64), 0).to(torch.int32)
+    g = _gen(wl.seed + 6000 + 7919 * step, device)
+    q = torch.randn((int(qs[-1]), wl.num_q_heads, wl.head_dim), generator=g, device=device,
+                    dtype=torch.float32)
+    return q.to(torch.float16), qs
+
+
+def prefill_flops(wl: Workload, ctx: torch.Tensor, chunk_lens: torch.Tensor) -> int:
+    """Algorithmic flops of causal chunk attention: query i of an n-query chunk at
+    position ctx - n + i takes 2 * 2 * head_dim flops (QK^T and PV) per attended
+    token and q-head."""
+    tot = 0
+    for c, n in zip(ctx.tolist(), chunk_lens.tolist()):
+        tot += n * (c - n) + n * (n + 1) // 2
+    return 4 * wl.num_q_heads * wl.head_dim * tot

@@ -190,6 +190,39 @@ KVQ_API kvq_status kvq_decode_attention_static_scratch(const void* q, const kvq_
                                                        void* out, int32_t partition_size, kvq_stream_t stream);
 KVQ_API size_t kvq_static_scratch_bytes(void);
 
+/* Causal attention of chunks of new queries over the paged quantized cache
+ * (chunked prefill).  The pages define the cache formats and their scales
+ * ([TGI] "FP8 Formats: E4M3 and E5M2", intro: stored quantized, computed in
+ * FP16; [LMD] online INT8) but not the prefill step itself; this is the plain
+ * causal attention that reads that cache, with fp16 x fp16 products and fp32
+ * sums on the tensor cores.
+ *   q:   fp16 [num_q_tokens][num_q_heads][head_dim]; sequence b owns rows
+ *     query_start[b] .. query_start[b+1]-1 (n_b = query_start[b+1] -
+ *     query_start[b] new queries, in position order).
+ *   query_start: int32 [batch + 1], non-decreasing, 0 <= query_start[b] and
+ *     query_start[batch] <= num_q_tokens (the rows q and out hold).
+ *   context_lens: int32 [batch]: every cached token of b, the chunk's own
+ *     included (append the chunk's K/V first).  Query i of the chunk sits at
+ *     position context_lens[b] - n_b + i and attends to tokens 0 .. position.
+ *   block_tables, max_blocks_per_seq, scale, fmt, sm_scale: as in
+ *     kvq_decode_attention.  q-head h reads kv-head h / (num_q_heads /
+ *     num_kv_heads); the group size may be at most 128.
+ *   max_query_len: an upper bound of every n_b (sizes the launch).
+ *   out: fp16 [num_q_tokens][num_q_heads][head_dim]; rows of sequences with
+ *     n_b > context_lens[b], n_b > max_query_len, query_start[b] < 0,
+ *     query_start[b+1] > num_q_tokens or context_lens[b] >
+ *     max_blocks_per_seq * block_size are left unwritten and the sequence
+ *     index is recorded for kvq_device_error_check (KVQ_ERR_OUT_OF_RANGE), as
+ *     is a block id outside the cache (its tokens then count as zeros).
+ *   Needs no workspace. */
+KVQ_API kvq_status kvq_prefill_attention(const void* q, const kvq_cache* cache,
+                                 const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t* context_lens, const int32_t* query_start,
+                                 int32_t batch, int64_t num_q_tokens, int32_t num_q_heads,
+                                 int32_t max_query_len,
+                                 const float* scale, int32_t fmt, float sm_scale, void* out,
+                                 kvq_stream_t stream);
+
 /* Debug gather + dequantize-on-read: for each of num_slots slots, fp32
  * [num_slots][num_kv_heads][head_dim] rows of K and V, each value
  * fl32(decode(code) * scale) (FP8) or fl32(code * row_scale) (INT8). */
