@@ -50,10 +50,11 @@ namespace kvq {
 namespace {
 
 constexpr int kRows = 128;        // M tile: (query, q-head) rows
-constexpr int kKvTile = 128;      // tokens per KV tile
-constexpr int kThreads = 256;     // 4 softmax warps (thread 0 issues the MMAs), 4 dequant warps
+constexpr int kKvTile = 64;       // tokens per KV tile
+constexpr int kThreads = 256;     // 4 softmax warps, 1 MMA warp, 3 dequant warps
+constexpr int kDqThreads = 96;    // dequantizing threads (warps 5-7)
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColO = 128;   // O accumulator columns start here
+constexpr uint32_t kColO = 128;   // O accumulator columns start here (two S buffers of 64 before)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (weights < 2^8)
 
@@ -161,6 +162,22 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
                  : "memory");
 }
 
+// After tcgen05.wait::ld: ties the loaded registers to this point so that no
+// use of them is scheduled before the wait.
+__device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]));
+}
+
+__device__ __forceinline__ void reg_fence32(uint32_t (&r)[32]) {
+    uint32_t(&a)[16] = *reinterpret_cast<uint32_t(*)[16]>(&r[0]);
+    uint32_t(&b)[16] = *reinterpret_cast<uint32_t(*)[16]>(&r[16]);
+    reg_fence16(a);
+    reg_fence16(b);
+}
+
 // Four INT8 codes (one 32-bit word) -> two f16x2 words, exact.
 __device__ __forceinline__ void dec_int8x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
     const uint32_t b = w ^ 0x80808080u;
@@ -184,6 +201,20 @@ __device__ __forceinline__ void dec16(const uint4& c, uint4& h0, uint4& h1) {
     }
 }
 
+// fp16 pair (lo, hi) holding RN(p0), RN(p1) -> fp16 pair of the residuals
+// RN(p0 - h0), RN(p1 - h1); each difference is one mixed-precision FMA (exact
+// product h * -1, one rounding).
+__device__ __forceinline__ uint32_t residual_f16x2(uint32_t h, float p0, float p1) {
+    uint32_t r;
+    asm("{\n\t.reg .f16 a, b, m1;\n\t.reg .f32 r0, r1;\n\t"
+        "mov.b32 {a, b}, %1;\n\tmov.b16 m1, 0xBC00;\n\t"
+        "fma.rn.f32.f16 r0, a, m1, %2;\n\tfma.rn.f32.f16 r1, b, m1, %3;\n\t"
+        "cvt.rn.f16x2.f32 %0, r1, r0;\n\t}"
+        : "=r"(r)
+        : "r"(h), "f"(p0), "f"(p1));
+    return r;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4& v) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
@@ -199,33 +230,47 @@ __device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {
 
 // ------------------------------------------------------------- layout -----
 
-enum Bar : int { B_KFULL, B_VFULL, B_SFULL, B_PFULL, B_KFREE, B_VFREE, B_OFINAL, B_SC0, B_SC1, kNumBars };
+// Barriers.  Per-slot barriers serve tiles j with j % slots == slot; their
+// phase for tile j is (j / slots) % 2.
+enum Bar : int {
+    B_KFULL0, B_KFULL1,    // dequant -> MMA: K tile in its buffer (128 arrivals)
+    B_VFULL0, B_VFULL1,    // dequant -> MMA: V tile (128)
+    B_KFREE0, B_KFREE1,    // MMA -> dequant: S = Q K^T done reading the K buffer (commit)
+    B_VFREE0, B_VFREE1,    // MMA -> dequant, softmax: O += P V done (commit)
+    B_SFULL0, B_SFULL1,    // MMA -> softmax: S in its tensor-memory buffer (commit)
+    B_PFULL0, B_PFULL1,    // softmax -> MMA: P written over S (128)
+    B_SC0, B_SC1, B_SC2, B_SC3,  // dequant -> softmax: INT8 scales of the tile (128)
+    B_OFINAL,              // every MMA done (commit)
+    kNumBars
+};
 
 // Shared memory of one CTA (base 1024-byte aligned).  Operand tiles are
 // [rows][D] fp16 stored as D / 64 column blocks of [rows][128 B], each with the
-// 128-byte swizzle: the query tile (A of S = Q K^T, K-major), the K tile (B of
-// S, K-major) and the V tile (B of O = P V, MN-major) share one layout.
+// 128-byte swizzle: the query tile (128 rows; A of S = Q K^T, K-major), and two
+// buffers each of K (64 rows; B of S, K-major) and V (64 rows; B of O = P V,
+// MN-major).
 template <int D>
 struct SmemLayout {
-    static constexpr uint32_t kBlk = kRows * 128;          // one 64-column block of 128 rows
-    static constexpr uint32_t kTile = kBlk * (D / 64);     // a [128][D] fp16 tile
+    static constexpr uint32_t kBlkQ = kRows * 128;         // one 64-column block of the query tile
+    static constexpr uint32_t kBlkKV = kKvTile * 128;      // one 64-column block of a K / V tile
+    static constexpr uint32_t kTileQ = kBlkQ * (D / 64);
+    static constexpr uint32_t kTileKV = kBlkKV * (D / 64);
     static constexpr uint32_t kQ = 0;
-    static constexpr uint32_t kK = kQ + kTile;
-    static constexpr uint32_t kV = kK + kTile;
-    static constexpr uint32_t kKsc = kV + kTile;           // fp32 [2][128] INT8 K row scales
-    static constexpr uint32_t kVsc = kKsc + 2 * kKvTile * 4;
-    static constexpr uint32_t kBar = kVsc + 2 * kKvTile * 4;
+    static constexpr uint32_t kK = kQ + kTileQ;            // two K buffers
+    static constexpr uint32_t kV = kK + 2 * kTileKV;       // two V buffers
+    static constexpr uint32_t kKsc = kV + 2 * kTileKV;     // fp32 [4][64] INT8 logit multipliers
+    static constexpr uint32_t kVsc = kKsc + 4 * kKvTile * 4;  // fp32 [4][64] INT8 V row scales
+    static constexpr uint32_t kBar = kVsc + 4 * kKvTile * 4;
     static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
     static constexpr uint32_t kBytes = kAbort + 4;
     static constexpr uint32_t kAlloc = kBytes + 1024;      // slack for the 1024-byte alignment
 };
 
-// Byte offset, within an operand tile, of the 8 fp16 values at columns
-// 8c .. 8c+7 of row r.
-template <int D>
-__device__ __forceinline__ uint32_t tile_off(uint32_t r, uint32_t c) {
-    return (c >> 3) * SmemLayout<D>::kBlk + sw128(r, c & 7u);
+// Byte offset, within an operand tile whose 64-column blocks are `blk` bytes
+// apart, of the 8 fp16 values at columns 8c .. 8c+7 of row r.
+__device__ __forceinline__ uint32_t tile_off(uint32_t blk, uint32_t r, uint32_t c) {
+    return (c >> 3) * blk + sw128(r, c & 7u);
 }
 
 struct PrefillParams {
@@ -260,6 +305,8 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
     using L = SmemLayout<D>;
     constexpr int kChunks = D / 8;       // 16-byte fp16 chunks per row
     constexpr int kCodeVecs = D / 16;    // 16-byte code vectors per token row
+    constexpr int kTileVecs = kKvTile * kCodeVecs;  // 16-code vectors per K or V tile
+    constexpr int kVecsPerThread = (kTileVecs + kDqThreads - 1) / kDqThreads;
     constexpr uint32_t kIdescQK = idesc_f16(kRows, kKvTile, 0);
     constexpr uint32_t kIdescPV = idesc_f16(kRows, D, 1);
 
@@ -292,12 +339,21 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
     const int p_first = ctx - n + qt * TQ;          // position of its first query
     const int p_last = p_first + nq - 1;
     const int nkv = p_last / kKvTile + 1;           // KV tiles to walk
+    // The M tiles of one (sequence, kv-head) read the same K/V; each walks the
+    // tiles from its own starting point (softmax accumulation is
+    // order-free), so concurrent CTAs spread their reads over the L2 slices
+    // instead of all requesting the same lines at once.
+    const int rot = (int)(((unsigned)qt * 37u) % (unsigned)nkv);
+    auto tile_of = [&](int j) { const int x = j + rot; return x >= nkv ? x - nkv : x; };
     const float s_fp8 = (FMT != INT8 && a.scale) ? *a.scale : 1.0f;
+    // logits in log2 units: S * c_k (FP8; K carries the scale's sign) or S * c_k * s_K[t] (INT8)
+    const float c_k = a.sm_scale * kLog2e * fabsf(s_fp8);
 
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i) {
-            const uint32_t cnt = (i == B_KFULL || i == B_VFULL || i == B_PFULL || i == B_SC0 || i == B_SC1) ? 128u : 1u;
-            mbar_init(&bars[i], cnt);
+            const bool by_dq = (i >= B_KFULL0 && i <= B_VFULL1) || (i >= B_SC0 && i <= B_SC3);
+            const bool by_sm = i == B_PFULL0 || i == B_PFULL1;
+            mbar_init(&bars[i], by_dq ? (uint32_t)kDqThreads : by_sm ? 128u : 1u);
         }
         *abort = 0;
         fence_barrier_init();
@@ -313,13 +369,73 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp >= 4) {
+    if (warp == 4) {
+        // ---------------------------------------------------------- MMA ----
+        // One elected lane issues every MMA, in the order S_0, S_1, O+=P_0 V_0,
+        // S_2, O+=P_1 V_1, ...: S of tile j goes into S buffer j % 2 as soon as
+        // K_j is stored, so it runs while the softmax of tile j-1 works on the
+        // other buffer.  Descriptors are computed by the whole warp.
+        const int lane_ = tid & 31;
+        // Descriptors of the first K-step of each operand tile; every other
+        // K-step adds a constant to the 14-bit start-address field (addresses
+        // stay below 2^18 bytes, so the field never carries).
+        const uint64_t dq0 = smem_desc(sbase + L::kQ, 16, 1024);
+        const uint64_t dk0 = smem_desc(sbase + L::kK, 16, 1024);
+        const uint64_t dv0 = smem_desc(sbase + L::kV, L::kBlkKV, 1024);
+        auto issue_qk = [&](int j) {
+            const int sl = j & 1;
+            if (!wait_or_abort(&bars[B_KFULL0 + sl], (j >> 1) & 1, abort, a.err)) return false;
+            tc_fence_after();
+            const uint64_t dk = dk0 + ((sl * L::kTileKV) >> 4);
+            const uint32_t d_tmem = tmem + sl * kKvTile;
+            if (lane_ == 0) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk & 3) * 32;
+                    mma_ss(d_tmem, dq0 + (((kk >> 2) * L::kBlkQ + off) >> 4), dk + (((kk >> 2) * L::kBlkKV + off) >> 4),
+                           kIdescQK, kk > 0);
+                }
+                mma_commit(&bars[B_SFULL0 + sl]);
+                mma_commit(&bars[B_KFREE0 + sl]);
+            }
+            __syncwarp();
+            return true;
+        };
+        auto issue_pv = [&](int j) {
+            const int sl = j & 1;
+            if (!wait_or_abort(&bars[B_PFULL0 + sl], (j >> 1) & 1, abort, a.err)) return false;
+            if (!wait_or_abort(&bars[B_VFULL0 + sl], (j >> 1) & 1, abort, a.err)) return false;
+            tc_fence_after();
+            const uint64_t dv = dv0 + ((sl * L::kTileKV) >> 4);
+            const uint32_t p_tmem = tmem + sl * kKvTile;
+            if (lane_ == 0) {
+#pragma unroll
+                for (int kk = 0; kk < kKvTile / 16; ++kk) {
+                    const uint32_t a_hi = p_tmem + 16 * kk;   // P of tokens 16kk .. 16kk+15
+                    const uint64_t vd = dv + ((kk * 2048) >> 4);
+                    mma_ts(tmem + kColO, a_hi, vd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts(tmem + kColO, a_hi + 8, vd, kIdescPV, 1u);
+                }
+                mma_commit(&bars[B_VFREE0 + sl]);
+            }
+            __syncwarp();
+            return true;
+        };
+        bool mma_ok = true;
+        for (int j = 0; j < nkv && mma_ok; ++j) {
+            mma_ok = issue_qk(j);
+            if (mma_ok && j >= 1) mma_ok = issue_pv(j - 1);
+        }
+        if (mma_ok && !*abort) issue_pv(nkv - 1);
+        if (lane_ == 0) mma_commit(&bars[B_OFINAL]);   // after every MMA this CTA issued
+        __syncwarp();
+    } else if (warp >= 5) {
         // ------------------------------------------------------ dequant ----
-        const int dt = tid - 128;
+        const int dt = tid - 160;
         const size_t head_stride = (size_t)a.block_size * D;
         const int32_t* bt = a.block_tables + (size_t)b * a.max_blocks_per_seq;
         // query tile: row r = (query qt*TQ + r / G, head kvh*G + r % G)
-        for (int e = dt; e < kRows * kChunks; e += 128) {
+        for (int e = dt; e < kRows * kChunks; e += kDqThreads) {
             const int r = e / kChunks, c = e % kChunks;
             const int qi = r / G;
             uint4 v = make_uint4(0, 0, 0, 0);
@@ -327,113 +443,157 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
                 const size_t row = (size_t)(q0 + qt * TQ + qi) * Hq + kvh * G + r % G;
                 v = *reinterpret_cast<const uint4*>(a.q + row * D + c * 8);
             }
-            st_shared_v4(sbase + L::kQ + tile_off<D>(r, c), v);
+            st_shared_v4(sbase + L::kQ + tile_off(L::kBlkQ, r, c), v);
         }
-        // codes of K (which = 0) or V (which = 1) of KV tile j -> registers
-        auto load_codes = [&](int j, int which, uint4 (&cv)[kCodeVecs]) {
-            const uint8_t* codes = which ? a.v_codes : a.k_codes;
+        // Thread dt handles vectors e = it * 96 + dt (it = 0 .. kVecsPerThread-1,
+        // e below kTileVecs): the 16 codes c16 of token row u, with rows varying
+        // fastest across groups of 8 lanes: each 8-lane group stores one 16-byte
+        // column chunk of 8 consecutive rows, which the 128-byte swizzle spreads
+        // over all 32 banks, and each warp load reads whole 32-byte sectors of 8
+        // rows.
+        auto has = [&](int it) { return it * kDqThreads + dt < kTileVecs; };
+        auto row_of = [&](int it) {
+            const int e = it * kDqThreads + dt;
+            return ((e >> 3) / kCodeVecs) * 8 + (e & 7);
+        };
+        auto vec_of = [&](int it) { const int e = it * kDqThreads + dt; return (e >> 3) % kCodeVecs; };
+        const int lbs = 31 - __clz(a.block_size);   // block sizes are powers of two
+        int blk[kVecsPerThread];                    // physical block of each row, -1 = zeros
+        int blk_next[kVecsPerThread];               // the same for the tile after (loaded a tile ahead)
+        auto fetch_ids = [&](int j, int (&blk)[kVecsPerThread]) {
 #pragma unroll
-            for (int it = 0; it < kCodeVecs; ++it) {
-                const int e = it * 128 + dt;
-                const int u = e / kCodeVecs, c16 = e % kCodeVecs;
-                const int t = j * kKvTile + u;
-                cv[it] = make_uint4(0, 0, 0, 0);
-                if (t <= p_last) {
-                    const int blk = bt[t / a.block_size];
-                    if (blk >= 0 && blk < a.num_blocks) {
-                        cv[it] = ld_global_nc_v4(codes + ((size_t)blk * Hkv + kvh) * head_stride +
-                                                 (size_t)(t % a.block_size) * D + c16 * 16);
-                    } else if (c16 == 0 && which == 0) {
-                        record_error(a.err, DEV_ERR_RANGE, blk);
+            for (int it = 0; it < kVecsPerThread; ++it) {
+                const int t = tile_of(j) * kKvTile + row_of(it);
+                int id = -1;
+                if (has(it) && j < nkv && t <= p_last) {
+                    id = bt[t >> lbs];
+                    if (id < 0 || id >= a.num_blocks) {
+                        record_error(a.err, DEV_ERR_RANGE, id);
+                        id = -1;
                     }
+                }
+                blk[it] = id;
+            }
+        };
+        auto load_codes = [&](const uint8_t* codes, int j, uint4 (&cv)[kVecsPerThread]) {
+#pragma unroll
+            for (int it = 0; it < kVecsPerThread; ++it) {
+                const int t = tile_of(j) * kKvTile + row_of(it);
+                cv[it] = make_uint4(0, 0, 0, 0);
+                if (blk[it] >= 0)
+                    cv[it] = ld_global_nc_v4(codes + ((size_t)blk[it] * Hkv + kvh) * head_stride +
+                                             (size_t)(t & (a.block_size - 1)) * D + vec_of(it) * 16);
+            }
+        };
+        auto load_scales = [&](int j, float& ks, float& vs) {
+            ks = vs = 0.f;
+            const int t = tile_of(j) * kKvTile + dt;
+            if (dt < kKvTile && t <= p_last) {
+                const int id = bt[t >> lbs];
+                if (id >= 0 && id < a.num_blocks) {
+                    const size_t srow = ((size_t)id * Hkv + kvh) * a.block_size + (t & (a.block_size - 1));
+                    ks = a.k_scales[srow];
+                    vs = a.v_scales[srow];
                 }
             }
         };
-        auto store_tile = [&](uint32_t tile, const uint4 (&cv)[kCodeVecs]) {
+        // A negative FP8 scale is folded into K's fp16 signs, so the logit
+        // multiplier is never negative.
+        const uint32_t kflip = (FMT != INT8 && s_fp8 < 0.f) ? 0x80008000u : 0u;
+        auto store_tile = [&](uint32_t tile, const uint4 (&cv)[kVecsPerThread], uint32_t flip) {
 #pragma unroll
-            for (int it = 0; it < kCodeVecs; ++it) {
-                const int e = it * 128 + dt;
-                const int u = e / kCodeVecs, c16 = e % kCodeVecs;
+            for (int it = 0; it < kVecsPerThread; ++it) {
+                if (!has(it)) continue;
+                const int u = row_of(it), c16 = vec_of(it);
                 uint4 h0, h1;
                 dec16<FMT>(cv[it], h0, h1);
-                st_shared_v4(tile + tile_off<D>(u, 2 * c16), h0);
-                st_shared_v4(tile + tile_off<D>(u, 2 * c16 + 1), h1);
+                if (flip) {
+                    h0.x ^= flip; h0.y ^= flip; h0.z ^= flip; h0.w ^= flip;
+                    h1.x ^= flip; h1.y ^= flip; h1.z ^= flip; h1.w ^= flip;
+                }
+                st_shared_v4(tile + tile_off(L::kBlkKV, u, 2 * c16), h0);
+                st_shared_v4(tile + tile_off(L::kBlkKV, u, 2 * c16 + 1), h1);
             }
         };
+        // Tile j goes to buffer j % 2 once the MMAs of tile j - 2 have read it;
+        // the codes of tile j+1 are loaded into registers meanwhile, and the
+        // block ids of tile j+2 (so no code load waits for its block id).
+        uint4 kc[kVecsPerThread], vc[kVecsPerThread];
+        float ks = 0.f, vs = 0.f;
+        fetch_ids(0, blk);
+        fetch_ids(1, blk_next);
+        load_codes(a.k_codes, 0, kc);
+        load_codes(a.v_codes, 0, vc);
+        if (FMT == INT8) load_scales(0, ks, vs);
         for (int j = 0; j < nkv; ++j) {
-            uint4 cv[kCodeVecs];
-            load_codes(j, 0, cv);
-            float ks = 0.f, vs = 0.f;
-            if (FMT == INT8) {
-                const int t = j * kKvTile + dt;
-                if (t <= p_last) {
-                    const int blk = bt[t / a.block_size];
-                    if (blk >= 0 && blk < a.num_blocks) {
-                        const size_t srow = ((size_t)blk * Hkv + kvh) * a.block_size + t % a.block_size;
-                        ks = a.k_scales[srow];
-                        vs = a.v_scales[srow];
-                    }
-                }
-            }
-            if (j > 0 && !wait_or_abort(&bars[B_KFREE], (j - 1) & 1, abort, a.err)) break;
-            store_tile(sbase + L::kK, cv);
-            if (FMT == INT8) {
-                ksc[(j & 1) * kKvTile + dt] = ks;
-                vsc[(j & 1) * kKvTile + dt] = vs;
+            const int sl = j & 1;
+            if (j >= 2 && !wait_or_abort(&bars[B_KFREE0 + sl], ((j >> 1) - 1) & 1, abort, a.err)) break;
+            store_tile(sbase + L::kK + sl * L::kTileKV, kc, kflip);
+            if (FMT == INT8 && dt < kKvTile) {
+                ksc[(j & 3) * kKvTile + dt] = ks * c_k;   // the logit multiplier of token t
+                vsc[(j & 3) * kKvTile + dt] = vs;
             }
             fence_proxy_async();
-            mbar_arrive(&bars[B_KFULL]);
-            if (FMT == INT8) mbar_arrive(&bars[B_SC0 + (j & 1)]);
-            load_codes(j, 1, cv);
-            if (j > 0 && !wait_or_abort(&bars[B_VFREE], (j - 1) & 1, abort, a.err)) break;
-            store_tile(sbase + L::kV, cv);
+            mbar_arrive(&bars[B_KFULL0 + sl]);
+            if (FMT == INT8) mbar_arrive(&bars[B_SC0 + (j & 3)]);
+            const bool more = j + 1 < nkv;
+            if (more) {
+#pragma unroll
+                for (int it = 0; it < kVecsPerThread; ++it) blk[it] = blk_next[it];   // V_j's codes are loaded
+                load_codes(a.k_codes, j + 1, kc);
+                if (FMT == INT8) load_scales(j + 1, ks, vs);
+                fetch_ids(j + 2, blk_next);
+            }
+            if (j >= 2 && !wait_or_abort(&bars[B_VFREE0 + sl], ((j >> 1) - 1) & 1, abort, a.err)) break;
+            store_tile(sbase + L::kV + sl * L::kTileKV, vc, 0u);
             fence_proxy_async();
-            mbar_arrive(&bars[B_VFULL]);
+            mbar_arrive(&bars[B_VFULL0 + sl]);
+            if (more) load_codes(a.v_codes, j + 1, vc);
         }
     } else {
         // ------------------------------------------------------ softmax ----
         const int r = tid;
         const bool rv = r < TQ * G && r / G < nq;
         const int pos = rv ? p_first + r / G : p_last;
-        const float c_k = a.sm_scale * kLog2e * s_fp8;
         const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < nkv && ok; ++j) {
-            if (tid == 0 && wait_or_abort(&bars[B_KFULL], j & 1, abort, a.err)) {
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * L::kBlk + (kk & 3) * 32;
-                    mma_ss(tmem, smem_desc(sbase + L::kQ + off, 16, 1024), smem_desc(sbase + L::kK + off, 16, 1024),
-                           kIdescQK, kk > 0);
-                }
-                mma_commit(&bars[B_SFULL]);
-                mma_commit(&bars[B_KFREE]);
-            }
-            __syncwarp();
-            if (!wait_or_abort(&bars[B_SFULL], j & 1, abort, a.err)) { ok = false; break; }
+            const int sl = j & 1;
+            if (!wait_or_abort(&bars[B_SFULL0 + sl], (j >> 1) & 1, abort, a.err)) { ok = false; break; }
             tc_fence_after();
-            if (FMT == INT8 && !wait_or_abort(&bars[B_SC0 + (j & 1)], (j >> 1) & 1, abort, a.err)) {
+            if (FMT == INT8 && !wait_or_abort(&bars[B_SC0 + (j & 3)], (j >> 2) & 1, abort, a.err)) {
                 ok = false;
                 break;
             }
-            const float* ks = ksc + (j & 1) * kKvTile;
-            const float* vs = vsc + (j & 1) * kKvTile;
-            const int lim = pos - j * kKvTile;      // columns u <= lim attend
-            uint32_t s[16];
+            const float* ks = ksc + (j & 3) * kKvTile;
+            const float* vs = vsc + (j & 3) * kKvTile;
+            const uint32_t srow = trow + sl * kKvTile;   // this tile's S / P columns
+            const int lim = pos - tile_of(j) * kKvTile;   // columns u <= lim attend
+            // lane 0 holds the warp's first position: past it no column is masked
+            const bool full = __shfl_sync(0xFFFFFFFFu, lim, 0) >= kKvTile - 1;
+            // pass 1: the tile's row maximum; the second TMEM load overlaps the first chunk's work
             float mx = -INFINITY;
-#pragma unroll 1
-            for (int ch = 0; ch < kKvTile / 16; ++ch) {
-                tmem_ld16(trow + ch * 16, s);
-                tc_wait_ld();
+            auto chunk_max = [&](const uint32_t (&sv)[32], int ch) {
 #pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const int u = ch * 16 + q;
-                    const float x = __uint_as_float(s[q]) * (FMT == INT8 ? c_k * ks[u] : c_k);
-                    if (u <= lim) mx = fmaxf(mx, x);
+                for (int q = 0; q < 32; ++q) {
+                    const int u = ch * 32 + q;
+                    const float x = FMT == INT8 ? __uint_as_float(sv[q]) * ks[u] : __uint_as_float(sv[q]);
+                    if (full || u <= lim) mx = fmaxf(mx, x);
                 }
+            };
+            {
+                uint32_t sa[32], sb[32];
+                tmem_ld32(srow, sa);
+                tc_wait_ld();
+                reg_fence32(sa);
+                tmem_ld32(srow + 32, sb);
+                chunk_max(sa, 0);
+                tc_wait_ld();
+                reg_fence32(sb);
+                chunk_max(sb, 1);
             }
+            if (FMT != INT8) mx *= c_k;
             const float m_new = fmaxf(m_used, mx);
             float alpha = 1.f;
             bool resc = false;
@@ -443,21 +603,26 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
                 resc = true;
             }
             if (j > 0 && __any_sync(0xFFFFFFFFu, resc)) {
+                // O must hold every earlier tile's product before it is rescaled
+                const int jp = j - 1;
+                if (!wait_or_abort(&bars[B_VFREE0 + (jp & 1)], (jp >> 1) & 1, abort, a.err)) { ok = false; break; }
+                tc_fence_after();
 #pragma unroll 1
                 for (int ch = 0; ch < D / 32; ++ch) {
                     uint32_t o[32];
                     tmem_ld32(trow + kColO + ch * 32, o);
                     tc_wait_ld();
+                    reg_fence32(o);
 #pragma unroll
                     for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha);
                     tmem_st32(trow + kColO + ch * 32, o);
                 }
             }
             l *= alpha;
-#pragma unroll 1
-            for (int ch = 0; ch < kKvTile / 16; ++ch) {
-                tmem_ld16(trow + ch * 16, s);
-                tc_wait_ld();
+            // pass 2: weights, written over their logits as fp16 hi + residual
+            const float neg_m = -m_used;
+            float l2 = 0.f;                         // second partial sum (shorter add chains)
+            auto chunk_p = [&](const uint32_t (&sv)[16], int ch) {
                 uint32_t hi[8], lo[8];
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
@@ -465,41 +630,44 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
 #pragma unroll
                     for (int z = 0; z < 2; ++z) {
                         const int u = ch * 16 + 2 * q + z;
-                        const float x = __uint_as_float(s[2 * q + z]) * (FMT == INT8 ? c_k * ks[u] : c_k);
-                        const float p = u <= lim ? fast_exp2(x - m_used) : 0.f;
-                        l += p;
-                        pv[z] = FMT == INT8 ? p * vs[u] : p;
+                        float e = fast_exp2(fmaf(__uint_as_float(sv[2 * q + z]), FMT == INT8 ? ks[u] : c_k, neg_m));
+                        if (!full && u > lim) e = 0.f;
+                        if (z) l2 += e; else l += e;
+                        pv[z] = FMT == INT8 ? e * vs[u] : e;
                     }
-                    const __half2 h = __floats2half2_rn(pv[0], pv[1]);
-                    const float2 hf = __half22float2(h);
-                    const __half2 rl = __floats2half2_rn(pv[0] - hf.x, pv[1] - hf.y);
-                    hi[q] = *reinterpret_cast<const uint32_t*>(&h);
-                    lo[q] = *reinterpret_cast<const uint32_t*>(&rl);
+                    hi[q] = pack_f16x2(pv[0], pv[1]);
+                    lo[q] = residual_f16x2(hi[q], pv[0], pv[1]);
                 }
                 // tokens 16c .. 16c+15 (read from columns 16c .. 16c+15) -> hi in
                 // columns 16c .. 16c+7, lo in 16c+8 .. 16c+15
-                tmem_st8(trow + ch * 16, hi);
-                tmem_st8(trow + ch * 16 + 8, lo);
+                tmem_st8(srow + ch * 16, hi);
+                tmem_st8(srow + ch * 16 + 8, lo);
+            };
+            {
+                uint32_t sa[16], sb[16];
+                tmem_ld16(srow, sa);
+                tc_wait_ld();
+                reg_fence16(sa);
+                tmem_ld16(srow + 16, sb);
+                chunk_p(sa, 0);
+                tc_wait_ld();
+                reg_fence16(sb);
+                tmem_ld16(srow + 32, sa);
+                chunk_p(sb, 1);
+                tc_wait_ld();
+                reg_fence16(sa);
+                tmem_ld16(srow + 48, sb);
+                chunk_p(sa, 2);
+                tc_wait_ld();
+                reg_fence16(sb);
+                chunk_p(sb, 3);
             }
+            l += l2;
             tc_wait_st();
             tc_fence_before();
-            mbar_arrive(&bars[B_PFULL]);
-            if (tid == 0 && wait_or_abort(&bars[B_PFULL], j & 1, abort, a.err) &&
-                wait_or_abort(&bars[B_VFULL], j & 1, abort, a.err)) {
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < kKvTile / 16; ++kk) {
-                    const uint32_t a_hi = tmem + 16 * kk;   // P of tokens 16kk .. 16kk+15
-                    const uint64_t vd = smem_desc(sbase + L::kV + kk * 2048, L::kBlk, 1024);
-                    mma_ts(tmem + kColO, a_hi, vd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-                    mma_ts(tmem + kColO, a_hi + 8, vd, kIdescPV, 1u);
-                }
-                mma_commit(&bars[B_VFREE]);
-            }
-            __syncwarp();
+            mbar_arrive(&bars[B_PFULL0 + sl]);
         }
-        if (tid == 0) mma_commit(&bars[B_OFINAL]);   // after every MMA this CTA issued
-        __syncwarp();
+
         if (ok && wait_or_abort(&bars[B_OFINAL], 0, abort, a.err)) {
             tc_fence_after();
             const float inv = s_fp8 / l;
@@ -510,6 +678,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
                 uint32_t o[32];
                 tmem_ld32(trow + kColO + ch * 32, o);
                 tc_wait_ld();
+                reg_fence32(o);
                 uint32_t h[16];
 #pragma unroll
                 for (int q = 0; q < 16; ++q)

@@ -156,3 +156,25 @@ def test_prefill_workload_sampled(name, chunk, seqs):
             assert np.isfinite(o).all()
             e = rel_err(o, ref)
             assert e <= ATOL_REL, (b, i, e)
+
+
+@pytest.mark.parametrize("fmt,scale", [("e4m3", -0.0123), ("e5m2", 3.0)])
+def test_prefill_explicit_scale(fmt, scale):
+    """A scale given by the caller, negative included (dequantization multiplies
+    every code by it, so K and V both change sign)."""
+    wl = W.Workload(f"s-{fmt}", 2, 8, 2, 128, 16, fmt, 300, "one", outliers=False, seed=23)
+    lay = W.Layout(wl, torch.tensor([300, 140], dtype=torch.int32))
+    cache = kvq.KVCache(lay.num_blocks, 2, 16, 128, fmt, "cuda", fill=0xA5)
+    k, v = W.kv_tokens(wl, 0, 300, "cuda")
+    sc = torch.tensor([scale], dtype=torch.float32, device="cuda")
+    kvq.append(k, v, cache, lay.slots(0, 300).cuda(), sc)
+    n = torch.tensor([160, 140], dtype=torch.int32)
+    q, qs = W.prefill_queries(wl, n, "cuda")
+    out = kvq.prefill_attention(q, cache, lay.block_tables.cuda(), lay.context_lens.cuda(), qs.cuda(), 160, sc)
+    torch.cuda.synchronize()
+    assert kvq.device_error_check()[0] == 0
+    oc = oracle.Cache(lay.num_blocks, 2, 16, 128, {"e4m3": oracle.E4M3, "e5m2": oracle.E5M2}[fmt],
+                      k_codes=cache.k_codes.cpu().numpy(), v_codes=cache.v_codes.cpu().numpy())
+    ref = oracle.prefill_attention(q.cpu().numpy(), oc, lay.block_tables.numpy(), lay.context_lens.numpy(),
+                                   qs.numpy(), float(np.float32(scale)))
+    assert rel_err(out.float().cpu().numpy(), ref) <= ATOL_REL
