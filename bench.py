@@ -10,6 +10,7 @@ kvq_decode_attention.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...     # the CPU oracle, timed on host cores
+  python bench.py --prefill [--workload llama3-70b] [--chunk N]   # chunked prefill
 
 Prints ONE JSON line (rank 0).  ``value`` is decode KV-read GB/s: the
 algorithmic bytes of the decode calls (every cached K/V byte of every context
@@ -54,6 +55,9 @@ def parse():
                     help="append one-token steps with a separate kvq_append launch")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU-baseline sample time")
+    ap.add_argument("--prefill", action="store_true",
+                    help="time a chunked-prefill step (append of the chunk + causal attention of its queries)")
+    ap.add_argument("--chunk", type=int, default=0, help="prefill chunk per sequence (0: the workload's, else 2048)")
     return ap.parse_args()
 
 
@@ -149,6 +153,17 @@ def measured_peaks():
         return float(p["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+def measured_tensor_peak():
+    """Dense bf16 TFLOP/s (the fp16 tensor rate is the same) for a kernel timed
+    alone: the measured burst figure, else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
 
 
 def kernel_source_hash() -> str:
@@ -547,6 +562,248 @@ def run_kvq(args):
         torch.distributed.destroy_process_group()
 
 
+# ---------------------------------------------------------- prefill arm --
+
+class PrefillSetup:
+    """A workload's cache filled up to each sequence's chunk, plus the chunk:
+    its K/V rows, slots and queries (on the device) -- one chunked-prefill step."""
+
+    def __init__(self, wl, device, chunk):
+        import torch
+
+        import fp8_int8_quantized_gb300 as kvq
+        from fp8_int8_quantized_gb300 import workloads as W
+        self.wl = wl
+        self.lay = W.Layout(wl)
+        cl = self.lay.context_lens
+        self.n = W.prefill_chunks(wl, cl, chunk)
+        self.cache = kvq.KVCache(self.lay.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim, wl.fmt, device)
+        windows = W.chunk_positions(wl, 1 << 19)
+        k0, v0 = W.kv_tokens(wl, *windows[0], device=device)
+        sv = W.calibration_scale(wl, k0, v0)
+        del k0, v0
+        self.scale_value = sv
+        self.scale = None if sv is None else torch.tensor([sv], dtype=torch.float32, device=device)
+        first = (cl - self.n).to(torch.int64)           # the chunk's first position per sequence
+        for p0, p1 in windows:                           # every earlier position, untimed
+            k, v = W.kv_tokens(wl, p0, p1, device)
+            slots = self.lay.slots(p0, p1)
+            pos = torch.arange(p0, p1).repeat(wl.batch)
+            keep = pos < first.repeat_interleave(p1 - p0)
+            kvq.append(k, v, self.cache, torch.where(keep, slots, torch.full_like(slots, -1)).to(device),
+                       self.scale)
+            del k, v
+        ks, vs, ss = [], [], []
+        for b in range(wl.batch):
+            c, f = int(cl[b]), int(first[b])
+            if c > f:
+                k, v = W.kv_tokens(wl, f, c, device, seqs=[b])
+                ks.append(k)
+                vs.append(v)
+                ss.append(self.lay.slots(f, c, seqs=[b]))
+        self.k_step, self.v_step = torch.cat(ks), torch.cat(vs)
+        self.slots = torch.cat(ss).to(device)
+        self.q, qs = W.prefill_queries(wl, self.n, device)
+        self.qs = qs.to(device)
+        self.max_n = int(self.n.max())
+        self.bt = self.lay.block_tables.to(device)
+        self.cl = cl.to(device)
+        self.out = torch.empty_like(self.q)
+        self.flops = W.prefill_flops(wl, cl, self.n)
+        self.app_bytes = W.append_bytes(wl, self.slots.numel())
+        torch.cuda.synchronize()
+
+    def attend(self, q=None, out=None):
+        import fp8_int8_quantized_gb300 as kvq
+        kvq.prefill_attention(self.q if q is None else q, self.cache, self.bt, self.cl, self.qs, self.max_n,
+                              self.scale, out=self.out if out is None else out)
+
+    def step(self, k=None, v=None, slots=None, q=None, out=None):
+        import fp8_int8_quantized_gb300 as kvq
+        kvq.append(self.k_step if k is None else k, self.v_step if v is None else v, self.cache,
+                   self.slots if slots is None else slots, self.scale)
+        self.attend(q, out)
+
+
+def prefill_cpu_baseline(wl, n_chunk: int, target_s: float):
+    """The oracle, as it stands, on a bounded sample of the prefill step: the
+    last m queries of sequence 0's chunk (all q-heads, causal over the cache
+    the oracle itself filled) plus the append of those m tokens."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from fp8_int8_quantized_gb300 import workloads as W
+    lay = W.Layout(wl)
+    fmt = {"e4m3": oracle.E4M3, "e5m2": oracle.E5M2, "int8": oracle.INT8}[wl.fmt]
+    bs, c = wl.block_size, int(lay.context_lens[0])
+    nb = (c + bs - 1) // bs
+    cache = oracle.Cache(nb, wl.num_kv_heads, bs, wl.head_dim, fmt)
+    bt = np.arange(nb, dtype=np.int32)[None]
+    k, v = W.kv_tokens(wl, 0, c, "cpu", seqs=[0])
+    pos = np.arange(c)
+    slots = (pos // bs) * bs + pos % bs
+    oracle.append(k.numpy(), v.numpy(), slots, cache, None)
+    q, _ = W.prefill_queries(wl, torch.tensor([min(n_chunk, c)], dtype=torch.int32), "cpu")
+    q = q.numpy()
+
+    def run(m):
+        qs = np.array([0, m], np.int32)
+        t0 = time.perf_counter()
+        oracle.append(k.numpy()[c - m:], v.numpy()[c - m:], slots[c - m:], cache, None)
+        oracle.prefill_attention(q[-m:], cache, bt, np.array([c], np.int32), qs, None)
+        dt = time.perf_counter() - t0
+        one = W.Workload(wl.name, 1, wl.num_q_heads, wl.num_kv_heads, wl.head_dim, bs, wl.fmt, c, wl.scale_rule)
+        return dt, W.prefill_flops(one, torch.tensor([c]), torch.tensor([m]))
+
+    dt, fl = run(1)
+    m = max(1, min(q.shape[0], int(target_s / max(dt, 1e-3))))
+    if m > 1:
+        dt, fl = run(m)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"the last {m} queries of sequence 0's {q.shape[0]}-query chunk (all {wl.num_q_heads} "
+                      f"q-heads, context {c}) plus the append of their K/V, {dt:.2f} s"}
+
+
+def run_prefill_bench(args):
+    """Chunked-prefill step: kvq_append of each sequence's chunk of K/V, then
+    kvq_prefill_attention of the chunk's queries over the whole cache.
+    value = attention TFLOP/s of the step (4 * head_dim flops per attended
+    (query, q-head, token)); the roofline is the prefill kernel's own time
+    against the measured dense bf16 rate (the fp16 tensor rate)."""
+    import torch
+
+    import fp8_int8_quantized_gb300 as kvq
+    from fp8_int8_quantized_gb300 import workloads as W
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    kvq.lib()
+    name = args.workload if args.workload != DEFAULT_WORKLOAD else "llama3-70b"
+    wl = W.WORKLOADS[name]
+    if args.batch:
+        import dataclasses
+        wl = dataclasses.replace(wl, batch=args.batch)
+    chunk = args.chunk or wl.append_chunk or 2048
+    K = args.steps or 5
+    Wm = max(3, args.warmup)
+    S = PrefillSetup(wl, dev, chunk)
+    stream = torch.cuda.current_stream()
+    for _ in range(Wm):
+        S.step()
+    torch.cuda.synchronize()
+    st, detail = kvq.device_error_check()
+    if st != 0:
+        raise RuntimeError(f"device error {st} ({detail})")
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for _ in range(K):
+            S.step()
+        end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    # instrumented pass: append and attention timed apart
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    for e in ev:
+        e[0].record(stream)
+        kvq.append(S.k_step, S.v_step, S.cache, S.slots, S.scale)
+        e[1].record(stream)
+        S.attend()
+        e[2].record(stream)
+    torch.cuda.synchronize()
+    ms_step = start.elapsed_time(end) / K
+    app_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    att_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
+    max_ms, flops = aggregate(ms_step, float(S.flops), world)
+    value = flops / (max_ms * 1e-3) / 1e12
+
+    # end to end through the public API: the chunk's K/V, slots and queries
+    # uploaded from pinned host memory every step, the output read back
+    e2e = None
+    if not args.no_e2e:
+        parts = [S.k_step, S.v_step, S.slots, S.q]
+        host = [t.cpu().pin_memory() for t in parts]
+        dev_in = [torch.empty_like(t) for t in parts]
+        h_out = torch.empty(S.out.shape, dtype=S.out.dtype).pin_memory()
+        Ke = max(3, min(K, 20))
+        for i in range(Ke + 1):
+            if i == 1:
+                torch.cuda.synchronize()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+            for d, h in zip(dev_in, host):
+                d.copy_(h, non_blocking=True)
+            S.step(*dev_in, out=S.out)
+            h_out.copy_(S.out, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        e_ms = a.elapsed_time(b) / Ke
+        e_max, e_fl = aggregate(e_ms, float(S.flops), world)
+        e2e = {"value": round(e_fl / (e_max * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in parts),
+               "d2h_bytes_per_step": h_out.numel() * h_out.element_size(), "ms_per_step": round(e_max, 3),
+               "steps": Ke}
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    peak, peak_kind = measured_tensor_peak()
+    achieved = S.flops / (att_ms * 1e-3) / 1e12
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = prefill_cpu_baseline(wl, chunk, args.cpu_seconds)
+    line = {
+        "metric": "quantized-KV chunked-prefill attention: TFLOP/s (causal attention of each chunk over the cache)",
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": Wm,
+        "ms_per_step": round(max_ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": {"e4m3": "fp8-e4m3 storage, f16xf16->f32 compute", "e5m2": "fp8-e5m2 storage, f16xf16->f32 compute",
+                  "int8": "int8 storage, f16xf16->f32 compute"}[wl.fmt],
+        "data": "synthetic (seeded N(0,1) fp16 K/V/Q, shuffled block tables)",
+        "config": {"workload": wl.name + "-prefill", "description": wl.description, "batch": wl.batch,
+                   "num_q_heads": wl.num_q_heads, "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
+                   "block_size": wl.block_size, "format": wl.fmt,
+                   "context": wl.ctx if isinstance(wl.ctx, int) else list(wl.ctx),
+                   "chunk": chunk, "queries": int(S.n.sum()),
+                   "step": f"append {S.slots.numel()} tokens + causal attention of their queries over the cache",
+                   "l2": "inputs larger than L2 (cache and queries)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "attention_flops_per_step": S.flops,
+        "tokens_per_s": round(float(S.n.sum()) * world / (max_ms * 1e-3), 1),
+        "append_ms": round(app_ms, 4),
+        "append_gbs": round(S.app_bytes / (app_ms * 1e-3) / 1e9, 2),
+        "prefill_kernel_ms": round(att_ms, 4),
+        "roofline": {"bound": "tensor", "kernel": "prefill_kernel", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "executed_tensor_tflops": round(1.5 * achieved, 1),
+                     "note": "achieved counts the algorithmic QK^T and PV flops; the kernel executes PV twice "
+                             "(fp16 hi + residual weights), 1.5x the algorithmic tensor work",
+                     "traffic": None},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 2 * K,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 # ---------------------------------------------------------- reference arm --
 
 def run_reference(args):
@@ -615,6 +872,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.prefill:
+        run_prefill_bench(args)
     else:
         run_kvq(args)
 
