@@ -84,30 +84,35 @@ __host__ __device__ constexpr uint32_t idesc_f16(uint32_t m, uint32_t n, uint32_
     return (1u << 4) | (b_mn << 16) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
+// tcgen05.mma kind::f16, A and B from shared memory (mma_ss_warp) or A from
+// tensor memory (mma_ts_warp), executed by a whole converged warp: elect.sync
+// picks one lane (the lowest, the same every time) to issue, so the operands
+// can stay warp-uniform.
+__device__ __forceinline__ void mma_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
+__device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
-// Arrive once on `bar` when every tcgen05 operation this thread issued so far
-// has completed.
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     smem_u32(bar))
-                 : "memory");
+// Arrive once on `bar` (by the elected lane) when every tcgen05 operation that
+// lane issued so far has completed.
+__device__ __forceinline__ void mma_commit_warp(uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+        : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -136,15 +141,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
         "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
         "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
-            taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
 }
 
@@ -374,8 +370,8 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
         // One elected lane issues every MMA, in the order S_0, S_1, O+=P_0 V_0,
         // S_2, O+=P_1 V_1, ...: S of tile j goes into S buffer j % 2 as soon as
         // K_j is stored, so it runs while the softmax of tile j-1 works on the
-        // other buffer.  Descriptors are computed by the whole warp.
-        const int lane_ = tid & 31;
+        // other buffer.  The whole warp runs this code; elect.sync picks the
+        // issuing lane, so descriptors stay warp-uniform.
         // Descriptors of the first K-step of each operand tile; every other
         // K-step adds a constant to the 14-bit start-address field (addresses
         // stay below 2^18 bytes, so the field never carries).
@@ -388,17 +384,14 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
             tc_fence_after();
             const uint64_t dk = dk0 + ((sl * L::kTileKV) >> 4);
             const uint32_t d_tmem = tmem + sl * kKvTile;
-            if (lane_ == 0) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk & 3) * 32;
-                    mma_ss(d_tmem, dq0 + (((kk >> 2) * L::kBlkQ + off) >> 4), dk + (((kk >> 2) * L::kBlkKV + off) >> 4),
-                           kIdescQK, kk > 0);
-                }
-                mma_commit(&bars[B_SFULL0 + sl]);
-                mma_commit(&bars[B_KFREE0 + sl]);
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk & 3) * 32;
+                mma_ss_warp(d_tmem, dq0 + (((kk >> 2) * L::kBlkQ + off) >> 4), dk + (((kk >> 2) * L::kBlkKV + off) >> 4),
+                            kIdescQK, kk > 0);
             }
-            __syncwarp();
+            mma_commit_warp(&bars[B_SFULL0 + sl]);
+            mma_commit_warp(&bars[B_KFREE0 + sl]);
             return true;
         };
         auto issue_pv = [&](int j) {
@@ -408,17 +401,14 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
             tc_fence_after();
             const uint64_t dv = dv0 + ((sl * L::kTileKV) >> 4);
             const uint32_t p_tmem = tmem + sl * kKvTile;
-            if (lane_ == 0) {
 #pragma unroll
-                for (int kk = 0; kk < kKvTile / 16; ++kk) {
-                    const uint32_t a_hi = p_tmem + 16 * kk;   // P of tokens 16kk .. 16kk+15
-                    const uint64_t vd = dv + ((kk * 2048) >> 4);
-                    mma_ts(tmem + kColO, a_hi, vd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-                    mma_ts(tmem + kColO, a_hi + 8, vd, kIdescPV, 1u);
-                }
-                mma_commit(&bars[B_VFREE0 + sl]);
+            for (int kk = 0; kk < kKvTile / 16; ++kk) {
+                const uint32_t a_hi = p_tmem + 16 * kk;   // P of tokens 16kk .. 16kk+15
+                const uint64_t vd = dv + ((kk * 2048) >> 4);
+                mma_ts_warp(tmem + kColO, a_hi, vd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                mma_ts_warp(tmem + kColO, a_hi + 8, vd, kIdescPV, 1u);
             }
-            __syncwarp();
+            mma_commit_warp(&bars[B_VFREE0 + sl]);
             return true;
         };
         bool mma_ok = true;
@@ -427,8 +417,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
             if (mma_ok && j >= 1) mma_ok = issue_pv(j - 1);
         }
         if (mma_ok && !*abort) issue_pv(nkv - 1);
-        if (lane_ == 0) mma_commit(&bars[B_OFINAL]);   // after every MMA this CTA issued
-        __syncwarp();
+        mma_commit_warp(&bars[B_OFINAL]);   // after every MMA this CTA issued
     } else if (warp >= 5) {
         // ------------------------------------------------------ dequant ----
         const int dt = tid - 160;
@@ -458,8 +447,9 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
         };
         auto vec_of = [&](int it) { const int e = it * kDqThreads + dt; return (e >> 3) % kCodeVecs; };
         const int lbs = 31 - __clz(a.block_size);   // block sizes are powers of two
-        int blk[kVecsPerThread];                    // physical block of each row, -1 = zeros
-        int blk_next[kVecsPerThread];               // the same for the tile after (loaded a tile ahead)
+        int blk_k[kVecsPerThread];                  // physical block of each row of the tile whose K codes
+                                                    // are loaded next, -1 = zeros
+        int blk_v[kVecsPerThread];                  // the same for the tile whose V codes are loaded next
         auto fetch_ids = [&](int j, int (&blk)[kVecsPerThread]) {
 #pragma unroll
             for (int it = 0; it < kVecsPerThread; ++it) {
@@ -475,7 +465,8 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
                 blk[it] = id;
             }
         };
-        auto load_codes = [&](const uint8_t* codes, int j, uint4 (&cv)[kVecsPerThread]) {
+        auto load_codes = [&](const uint8_t* codes, int j, uint4 (&cv)[kVecsPerThread],
+                              const int (&blk)[kVecsPerThread]) {
 #pragma unroll
             for (int it = 0; it < kVecsPerThread; ++it) {
                 const int t = tile_of(j) * kKvTile + row_of(it);
@@ -515,40 +506,49 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
                 st_shared_v4(tile + tile_off(L::kBlkKV, u, 2 * c16 + 1), h1);
             }
         };
-        // Tile j goes to buffer j % 2 once the MMAs of tile j - 2 have read it;
-        // the codes of tile j+1 are loaded into registers meanwhile, and the
-        // block ids of tile j+2 (so no code load waits for its block id).
+        // Tile t goes to buffer t % 2 once the MMAs of tile t - 2 have read it.
+        // K runs one tile ahead of V (K_{j+1} is stored before V_j), so the next
+        // S never waits on the V side of the pipeline; the codes of the next K
+        // and V tiles are loaded into registers meanwhile.
         uint4 kc[kVecsPerThread], vc[kVecsPerThread];
         float ks = 0.f, vs = 0.f;
-        fetch_ids(0, blk);
-        fetch_ids(1, blk_next);
-        load_codes(a.k_codes, 0, kc);
-        load_codes(a.v_codes, 0, vc);
-        if (FMT == INT8) load_scales(0, ks, vs);
-        for (int j = 0; j < nkv; ++j) {
-            const int sl = j & 1;
-            if (j >= 2 && !wait_or_abort(&bars[B_KFREE0 + sl], ((j >> 1) - 1) & 1, abort, a.err)) break;
+        auto put_k = [&](int t) {
+            const int sl = t & 1;
+            if (t >= 2 && !wait_or_abort(&bars[B_KFREE0 + sl], ((t >> 1) - 1) & 1, abort, a.err)) return false;
             store_tile(sbase + L::kK + sl * L::kTileKV, kc, kflip);
             if (FMT == INT8 && dt < kKvTile) {
-                ksc[(j & 3) * kKvTile + dt] = ks * c_k;   // the logit multiplier of token t
-                vsc[(j & 3) * kKvTile + dt] = vs;
+                ksc[(t & 3) * kKvTile + dt] = ks * c_k;   // the logit multiplier of token t
+                vsc[(t & 3) * kKvTile + dt] = vs;
             }
             fence_proxy_async();
             mbar_arrive(&bars[B_KFULL0 + sl]);
-            if (FMT == INT8) mbar_arrive(&bars[B_SC0 + (j & 3)]);
+            if (FMT == INT8) mbar_arrive(&bars[B_SC0 + (t & 3)]);
+            return true;
+        };
+        fetch_ids(0, blk_k);
+        load_codes(a.k_codes, 0, kc, blk_k);
+        load_codes(a.v_codes, 0, vc, blk_k);
+        if (FMT == INT8) load_scales(0, ks, vs);
+        put_k(0);
+        fetch_ids(1, blk_k);
+        load_codes(a.k_codes, 1, kc, blk_k);
+        if (FMT == INT8) load_scales(1, ks, vs);
+        for (int j = 0; j < nkv; ++j) {
+            const int sl = j & 1;
             const bool more = j + 1 < nkv;
             if (more) {
+                if (!put_k(j + 1)) break;
 #pragma unroll
-                for (int it = 0; it < kVecsPerThread; ++it) blk[it] = blk_next[it];   // V_j's codes are loaded
-                load_codes(a.k_codes, j + 1, kc);
-                if (FMT == INT8) load_scales(j + 1, ks, vs);
-                fetch_ids(j + 2, blk_next);
+                for (int it = 0; it < kVecsPerThread; ++it) blk_v[it] = blk_k[it];   // tile j+1
+                fetch_ids(j + 2, blk_k);
+                load_codes(a.k_codes, j + 2, kc, blk_k);
+                if (FMT == INT8) load_scales(j + 2, ks, vs);
             }
             if (j >= 2 && !wait_or_abort(&bars[B_VFREE0 + sl], ((j >> 1) - 1) & 1, abort, a.err)) break;
             store_tile(sbase + L::kV + sl * L::kTileKV, vc, 0u);
             fence_proxy_async();
             mbar_arrive(&bars[B_VFULL0 + sl]);
-            if (more) load_codes(a.v_codes, j + 1, vc);
+            if (more) load_codes(a.v_codes, j + 1, vc, blk_v);
         }
     } else {
         // ------------------------------------------------------ softmax ----
