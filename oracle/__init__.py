@@ -14,7 +14,7 @@ Sources, by page title and section:
     ("FP8 Formats: E4M3 and E5M2"); scale 1.0 when none is given
     ("FP8 E4M3 KV Cache").
   * "[Feature] TurboMind support W8A8 or FP8 KV Cache" (lmdeploy issue 1463):
-    online KV-cache INT8.
+    online KV-cache INT8 (and the INT4 implementation named beside it).
 
 Parity pins for every function here live in ``tests/test_oracle_*.py``.
 """
@@ -27,8 +27,9 @@ import threading
 
 import numpy as np
 
-E4M3, E5M2, INT8 = 1, 2, 3
-FORMATS = {"e4m3": E4M3, "e5m2": E5M2, "int8": INT8}
+E4M3, E5M2, INT8, INT4 = 1, 2, 3, 4
+FORMATS = {"e4m3": E4M3, "e5m2": E5M2, "int8": INT8, "int4": INT4}
+ROW_SCALED = (INT8, INT4)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "kvq_oracle.c")
@@ -65,6 +66,8 @@ def _load():
         lib.oracle_fp8_encode_array.argtypes = [ctypes.c_int, P, P, i64]
         lib.oracle_int8_quant_row.restype = f32
         lib.oracle_int8_quant_row.argtypes = [P, ctypes.c_int, P]
+        lib.oracle_int4_quant_row.restype = f32
+        lib.oracle_int4_quant_row.argtypes = [P, ctypes.c_int, P]
         lib.oracle_half_to_double.restype = f64
         lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
         lib.oracle_append.restype = ctypes.c_int
@@ -125,6 +128,22 @@ def fp8_encode(fmt: int, y) -> np.ndarray:
     return out
 
 
+def int4_quant_row(x) -> tuple[np.ndarray, np.float32]:
+    """One INT4 row: returns (packed codes uint8 [D / 2], scale fp32)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    q = np.empty(x.shape[:-1] + (x.shape[-1] // 2,), dtype=np.uint8)
+    s = _load().oracle_int4_quant_row(_ptr(x), x.size, _ptr(q))
+    return q, np.float32(s)
+
+
+def int4_unpack(packed: np.ndarray) -> np.ndarray:
+    """Signed INT4 codes (int8 [..., 2 * n]) of packed rows uint8 [..., n]."""
+    lo = (packed & 0xF).astype(np.int16)
+    hi = (packed >> 4).astype(np.int16)
+    both = np.stack([lo, hi], axis=-1).reshape(packed.shape[:-1] + (2 * packed.shape[-1],))
+    return np.where(both >= 8, both - 16, both).astype(np.int8)
+
+
 def int8_quant_row(x) -> tuple[np.ndarray, np.float32]:
     """One INT8 row: returns (codes int8 [D], scale fp32)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
@@ -134,16 +153,17 @@ def int8_quant_row(x) -> tuple[np.ndarray, np.float32]:
 
 
 class Cache:
-    """Host copy of a paged cache: codes [NB][Hkv][BS][D], INT8 scales [NB][Hkv][BS]."""
+    """Host copy of a paged cache: codes [NB][Hkv][BS][D] ([D / 2] packed bytes for
+    INT4), INT8 / INT4 row scales [NB][Hkv][BS]."""
 
     def __init__(self, num_blocks, num_kv_heads, block_size, head_dim, fmt, fill=0xA5,
                  k_codes=None, v_codes=None, k_scales=None, v_scales=None):
         self.num_blocks, self.num_kv_heads = num_blocks, num_kv_heads
         self.block_size, self.head_dim, self.fmt = block_size, head_dim, fmt
-        shape = (num_blocks, num_kv_heads, block_size, head_dim)
+        shape = (num_blocks, num_kv_heads, block_size, head_dim // 2 if fmt == INT4 else head_dim)
         self.k_codes = k_codes if k_codes is not None else np.full(shape, fill, np.uint8)
         self.v_codes = v_codes if v_codes is not None else np.full(shape, fill, np.uint8)
-        if fmt == INT8:
+        if fmt in ROW_SCALED:
             sshape = (num_blocks, num_kv_heads, block_size)
             self.k_scales = k_scales if k_scales is not None else np.full(sshape, np.nan, np.float32)
             self.v_scales = v_scales if v_scales is not None else np.full(sshape, np.nan, np.float32)

@@ -14,7 +14,8 @@
  *         "FP8 Formats: E4M3 and E5M2" (bit layouts, per-tensor fp32 scale);
  *         section "FP8 E4M3 KV Cache" (default scale 1.0).
  *  [LMD]  "[Feature] TurboMind support W8A8 or FP8 KV Cache" (lmdeploy issue
- *         1463): online KV-cache INT8 (quant-policy 8).
+ *         1463): online KV-cache INT8 (quant-policy 8); the maintainers' reply
+ *         names the INT8 and INT4 implementations side by side.
  *  OCP 8-bit floating point (named by [TGI]): E4M3 bias 7, no infinities,
  *  NaN = S.1111.111, max 448; E5M2 bias 15, IEEE-like Inf/NaN, max 57344.
  *
@@ -25,6 +26,9 @@
  *  - INT8 is symmetric, one fp32 scale per (token, kv-head) row:
  *    s = fl32(amax / 127), q = clamp(rint(fl32(x / s)), -127, 127); amax == 0
  *    gives s = 0 and all-zero codes;
+ *  - INT4 is the same with 4 bits: s = fl32(amax / 7), q in [-7, 7], two codes
+ *    per byte (channel 2i in the low nibble, 2i+1 in the high nibble, 4-bit
+ *    two's complement), so a cached row is D / 2 bytes;
  *  - attention: logits l_t = sm_scale * <q, k_t> over all t < context_len,
  *    softmax, out = sum_t w_t v_t; q-head h reads kv-head h / (Hq / Hkv);
  *    context_len 0 gives zeros;
@@ -47,6 +51,7 @@
 #define ORC_E4M3 1
 #define ORC_E5M2 2
 #define ORC_INT8 3
+#define ORC_INT4 4
 
 /* ---------------------------------------------------------------- fp16 ---- */
 
@@ -178,10 +183,54 @@ static float int8_quant_row(const float* x, int D, int8_t* q) {
 
 float oracle_int8_quant_row(const float* x, int D, int8_t* q) { return int8_quant_row(x, D, q); }
 
+/* ---------------------------------------------------------------- INT4 ---- */
+
+/* The INT4 reading: one fp32 scale per row, s = fl32(amax / 7), codes
+ * clamp(rint(fl32(x / s)), -7, 7) packed two per byte (channel 2i low nibble,
+ * 2i+1 high nibble).  x: D fp32 values (D even); writes D / 2 bytes and returns
+ * the scale. */
+static float int4_quant_row(const float* x, int D, uint8_t* packed) {
+    float amax = 0.0f;
+    for (int d = 0; d < D; ++d) {
+        float ax = fabsf(x[d]);
+        if (ax > amax) amax = ax;
+    }
+    float s = amax / 7.0f;
+    for (int i = 0; i < D / 2; ++i) {
+        int q2[2];
+        for (int z = 0; z < 2; ++z) {
+            float r = 0.0f;
+            if (s != 0.0f) {
+                r = rintf(x[2 * i + z] / s);         /* ties to even (default mode) */
+                if (r > 7.0f) r = 7.0f;
+                if (r < -7.0f) r = -7.0f;
+            }
+            q2[z] = (int)r;
+        }
+        packed[i] = (uint8_t)((q2[0] & 0xF) | ((q2[1] & 0xF) << 4));
+    }
+    return s;
+}
+
+float oracle_int4_quant_row(const float* x, int D, uint8_t* packed) { return int4_quant_row(x, D, packed); }
+
+/* The signed 4-bit code of channel d of a packed row. */
+static int int4_code(const uint8_t* row, int d) {
+    int nib = (row[d >> 1] >> ((d & 1) * 4)) & 0xF;
+    return nib >= 8 ? nib - 16 : nib;
+}
+
+/* Bytes of one cached (token, kv-head) row. */
+static int row_bytes(int fmt, int D) { return fmt == ORC_INT4 ? D / 2 : D; }
+
+/* Formats that carry one scale per (token, kv-head) row. */
+static int row_scaled(int fmt) { return fmt == ORC_INT8 || fmt == ORC_INT4; }
+
 /* -------------------------------------------------------------- append ---- */
 
 /* Quantize-on-write.  k, v: fp16 bits [T][Hkv][D].  The paged cache holds codes
- * [NB][Hkv][BS][D] (u8 FP8 / i8 INT8) and, for INT8 only, scales [NB][Hkv][BS].
+ * [NB][Hkv][BS][D] (u8 FP8 / i8 INT8; [D / 2] packed bytes for INT4) and, for
+ * INT8 and INT4, scales [NB][Hkv][BS].
  * Token t goes to block slot[t] / BS, row slot[t] % BS; slot -1 is skipped.
  * scale: per-tensor fp32 scale (FP8 only; [TGI] default 1.0 applies when the
  * caller passes none).  Returns 0, or -1 on a slot outside the cache. */
@@ -200,11 +249,14 @@ int oracle_append(const uint16_t* k, const uint16_t* v, int64_t T, int Hkv, int 
         for (int h = 0; h < Hkv; ++h) {
             for (int which = 0; which < 2; ++which) {
                 const uint16_t* src = (which ? v : k) + ((size_t)t * Hkv + h) * D;
-                uint8_t* dst = (which ? v_codes : k_codes) + (((size_t)blk * Hkv + h) * BS + off) * D;
+                uint8_t* dst = (which ? v_codes : k_codes) + (((size_t)blk * Hkv + h) * BS + off) * row_bytes(fmt, D);
                 for (int d = 0; d < D; ++d) x[d] = (float)half_bits_to_double(src[d]);
                 if (fmt == ORC_INT8) {
                     float* sc = which ? v_scales : k_scales;
                     sc[((size_t)blk * Hkv + h) * BS + off] = int8_quant_row(x, D, (int8_t*)dst);
+                } else if (fmt == ORC_INT4) {
+                    float* sc = which ? v_scales : k_scales;
+                    sc[((size_t)blk * Hkv + h) * BS + off] = int4_quant_row(x, D, dst);
                 } else {
                     for (int d = 0; d < D; ++d) dst[d] = oracle_fp8_encode(fmt, x[d] / scale);
                 }
@@ -224,21 +276,29 @@ static float dequant_value(int fmt, uint8_t c, float s) {
     return (float)oracle_fp8_decode(fmt, c) * s;
 }
 
+/* Channel d of a cached row (row = its first byte), dequantized: INT4
+ * fl32(q * s_row), else as dequant_value. */
+static float cached_value(int fmt, const uint8_t* row, int d, float s) {
+    if (fmt == ORC_INT4) return (float)int4_code(row, d) * s;
+    return dequant_value(fmt, row[d], s);
+}
+
 /* Gather + dequantize rows at the given slots: out [n][Hkv][D] fp32 (K and V). */
 int oracle_dequant(const uint8_t* k_codes, const uint8_t* v_codes, const float* k_scales,
                    const float* v_scales, int64_t NB, int BS, int Hkv, int D, int fmt,
                    const int64_t* slots, int64_t n, float scale, float* out_k, float* out_v) {
+    const size_t rb = (size_t)row_bytes(fmt, D);
     for (int64_t i = 0; i < n; ++i) {
         int64_t slot = slots[i];
         if (slot < 0 || slot >= NB * BS) return -1;
         int64_t blk = slot / BS, off = slot % BS;
         for (int h = 0; h < Hkv; ++h) {
             size_t row = ((size_t)blk * Hkv + h) * BS + off;
-            float sk = fmt == ORC_INT8 ? k_scales[row] : scale;
-            float sv = fmt == ORC_INT8 ? v_scales[row] : scale;
+            float sk = row_scaled(fmt) ? k_scales[row] : scale;
+            float sv = row_scaled(fmt) ? v_scales[row] : scale;
             for (int d = 0; d < D; ++d) {
-                out_k[((size_t)i * Hkv + h) * D + d] = dequant_value(fmt, k_codes[row * D + d], sk);
-                out_v[((size_t)i * Hkv + h) * D + d] = dequant_value(fmt, v_codes[row * D + d], sv);
+                out_k[((size_t)i * Hkv + h) * D + d] = cached_value(fmt, k_codes + row * rb, d, sk);
+                out_v[((size_t)i * Hkv + h) * D + d] = cached_value(fmt, v_codes + row * rb, d, sv);
             }
         }
     }
@@ -260,6 +320,7 @@ int oracle_decode_attention(const uint16_t* q, int B, int Hq, int D,
                             const int32_t* context_lens, float scale, double sm_scale,
                             double* out, double* weights, int64_t w_stride) {
     int G = Hq / Hkv;
+    const size_t rb = (size_t)row_bytes(fmt, D);
     int bad = 0;
 #pragma omp parallel for collapse(2) schedule(dynamic, 1) reduction(| : bad)
     for (int b = 0; b < B; ++b) {
@@ -278,10 +339,10 @@ int oracle_decode_attention(const uint16_t* q, int B, int Hq, int D,
                 int32_t blk = block_tables[(size_t)b * max_blocks + t / BS];
                 if (blk < 0 || blk >= NB) { ok = 0; break; }
                 size_t row = ((size_t)blk * Hkv + kvh) * BS + t % BS;
-                float sk = fmt == ORC_INT8 ? k_scales[row] : scale;
+                float sk = row_scaled(fmt) ? k_scales[row] : scale;
                 double acc = 0.0;
                 for (int d = 0; d < D; ++d)
-                    acc += qv[d] * (double)dequant_value(fmt, k_codes[row * D + d], sk);
+                    acc += qv[d] * (double)cached_value(fmt, k_codes + row * rb, d, sk);
                 logit[t] = sm_scale * acc;
             }
             if (!ok) { bad = 1; free(logit); continue; }
@@ -294,9 +355,9 @@ int oracle_decode_attention(const uint16_t* q, int B, int Hq, int D,
                 if (weights) weights[((size_t)b * Hq + h) * w_stride + t] = w;
                 int32_t blk = block_tables[(size_t)b * max_blocks + t / BS];
                 size_t row = ((size_t)blk * Hkv + kvh) * BS + t % BS;
-                float sv = fmt == ORC_INT8 ? v_scales[row] : scale;
+                float sv = row_scaled(fmt) ? v_scales[row] : scale;
                 for (int d = 0; d < D; ++d)
-                    o[d] += w * (double)dequant_value(fmt, v_codes[row * D + d], sv);
+                    o[d] += w * (double)cached_value(fmt, v_codes + row * rb, d, sv);
             }
             free(logit);
         }
@@ -320,6 +381,7 @@ int oracle_prefill_attention(const uint16_t* q, int64_t Tq, int B, int Hq, int D
                              const int32_t* context_lens, const int32_t* query_start,
                              float scale, double sm_scale, double* out) {
     int G = Hq / Hkv;
+    const size_t rb = (size_t)row_bytes(fmt, D);
     int bad = 0;
     for (int64_t r = 0; r < Tq * Hq * D; ++r) out[r] = 0.0;
     for (int b = 0; b < B; ++b) {
@@ -347,10 +409,10 @@ int oracle_prefill_attention(const uint16_t* q, int64_t Tq, int B, int Hq, int D
                 int32_t blk = block_tables[(size_t)b * max_blocks + t / BS];
                 if (blk < 0 || blk >= NB) { ok = 0; break; }
                 size_t kr = ((size_t)blk * Hkv + kvh) * BS + t % BS;
-                float sk = fmt == ORC_INT8 ? k_scales[kr] : scale;
+                float sk = row_scaled(fmt) ? k_scales[kr] : scale;
                 double acc = 0.0;
                 for (int d = 0; d < D; ++d)
-                    acc += qv[d] * (double)dequant_value(fmt, k_codes[kr * D + d], sk);
+                    acc += qv[d] * (double)cached_value(fmt, k_codes + kr * rb, d, sk);
                 logit[t] = sm_scale * acc;
             }
             if (!ok) { bad = 1; break; }
@@ -362,9 +424,9 @@ int oracle_prefill_attention(const uint16_t* q, int64_t Tq, int B, int Hq, int D
                 double w = logit[t] / denom;
                 int32_t blk = block_tables[(size_t)b * max_blocks + t / BS];
                 size_t vr = ((size_t)blk * Hkv + kvh) * BS + t % BS;
-                float sv = fmt == ORC_INT8 ? v_scales[vr] : scale;
+                float sv = row_scaled(fmt) ? v_scales[vr] : scale;
                 for (int d = 0; d < D; ++d)
-                    o[d] += w * (double)dequant_value(fmt, v_codes[vr * D + d], sv);
+                    o[d] += w * (double)cached_value(fmt, v_codes + vr * rb, d, sv);
             }
         }
         free(logit);

@@ -54,7 +54,14 @@ def make_case(rng, B, Hq, Hkv, D, BS, fmt, ctx, scale=None, outliers=False):
 
 
 def torch_dequant(cache, scale):
-    if cache.fmt == oracle.INT8:
+    if cache.fmt == oracle.INT4:
+        def nibbles(codes):   # channel 2i = low nibble; (n ^ 8) - 8 sign-extends 4 bits
+            t = torch.from_numpy(codes.astype(np.int32))
+            both = torch.stack([t & 15, t >> 4], dim=-1).flatten(-2)
+            return ((both ^ 8) - 8).to(torch.float32)
+        kk = nibbles(cache.k_codes) * torch.from_numpy(cache.k_scales)[..., None]
+        vv = nibbles(cache.v_codes) * torch.from_numpy(cache.v_scales)[..., None]
+    elif cache.fmt == oracle.INT8:
         kk = torch.from_numpy(cache.k_codes.view(np.int8)).to(torch.float32) * torch.from_numpy(cache.k_scales)[..., None]
         vv = torch.from_numpy(cache.v_codes.view(np.int8)).to(torch.float32) * torch.from_numpy(cache.v_scales)[..., None]
     else:
@@ -86,7 +93,7 @@ def torch_reference(q, cache, bt, ctx, scale, sm_scale=None):
     return out.numpy()
 
 
-@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2, oracle.INT8])
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2, oracle.INT8, oracle.INT4])
 @pytest.mark.parametrize("BS", [16, 64])
 def test_append_layout(fmt, BS):
     rng = np.random.default_rng(fmt * 10 + BS)
@@ -102,6 +109,10 @@ def test_append_layout(fmt, BS):
                 if fmt == oracle.INT8:
                     qq, s = oracle.int8_quant_row(x)
                     assert np.array_equal(codes[blk, h, off].view(np.int8), qq)
+                    assert sc[blk, h, off] == s
+                elif fmt == oracle.INT4:
+                    qq, s = oracle.int4_quant_row(x)
+                    assert np.array_equal(codes[blk, h, off], qq)
                     assert sc[blk, h, off] == s
                 else:
                     s = np.float32(1.0 if scale is None else scale)
@@ -124,7 +135,7 @@ def test_append_skips_minus_one_and_default_scale():
         oracle.append(k, v, np.array([0, 1, 2, 32], np.int64), a, None)
 
 
-@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2, oracle.INT8])
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2, oracle.INT8, oracle.INT4])
 def test_dequant_matches_torch(fmt):
     rng = np.random.default_rng(11 + fmt)
     q, cache, bt, ctx, scale, k, v, slots = make_case(rng, 2, 4, 2, 64, 16, fmt, [20, 9], scale=0.75)
@@ -135,7 +146,7 @@ def test_dequant_matches_torch(fmt):
     assert np.array_equal(ov, vv[blk, :, off, :].float().numpy())
 
 
-@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2, oracle.INT8])
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2, oracle.INT8, oracle.INT4])
 @pytest.mark.parametrize("shape", [(2, 4, 4, 64, 16), (3, 8, 2, 128, 16), (2, 8, 1, 64, 32), (1, 16, 2, 128, 64)])
 def test_attention_matches_torch_sdpa(fmt, shape):
     B, Hq, Hkv, D, BS = shape
@@ -170,7 +181,7 @@ def test_hand_two_token_case():
     assert abs(out[0, 0, 0] - g["out0"]) < 1e-15 and abs(out[0, 0, 1] - g["out1"]) < 1e-15
 
 
-@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.INT8])
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.INT8, oracle.INT4])
 def test_invariants(fmt):
     rng = np.random.default_rng(99 + fmt)
     B, Hq, Hkv, D, BS = 4, 8, 2, 64, 16

@@ -53,7 +53,7 @@ def chunked_case(rng, Hq, Hkv, D, BS, fmt, ctx, chunk, scale=None, outliers=Fals
     return q, cache, bt, ctx, qs, scale
 
 
-@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2, oracle.INT8])
+@pytest.mark.parametrize("fmt", [oracle.E4M3, oracle.E5M2, oracle.INT8, oracle.INT4])
 @pytest.mark.parametrize("Hq,Hkv,D,BS", [(4, 4, 64, 16), (8, 2, 64, 32), (8, 1, 128, 64)])
 def test_matches_masked_sdpa(fmt, Hq, Hkv, D, BS):
     rng = np.random.default_rng(100 * fmt + Hq + D + BS)
