@@ -16,8 +16,8 @@ import threading
 
 import torch
 
-E4M3, E5M2, INT8 = 1, 2, 3
-FORMATS = {"e4m3": E4M3, "fp8": E4M3, "e5m2": E5M2, "fp8_e5m2": E5M2, "int8": INT8}
+E4M3, E5M2, INT8, INT4 = 1, 2, 3, 4
+FORMATS = {"e4m3": E4M3, "fp8": E4M3, "e5m2": E5M2, "fp8_e5m2": E5M2, "int8": INT8, "int4": INT4}
 STATUS = {0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED", 3: "KVQ_ERR_WORKSPACE",
           4: "KVQ_ERR_OUT_OF_RANGE", 5: "KVQ_ERR_TIMEOUT", 6: "KVQ_ERR_CUDA",
           7: "KVQ_ERR_SCRATCH_LIMIT"}
@@ -133,18 +133,20 @@ def _scale_ptr(scale) -> int | None:
 
 class KVCache:
     """A paged quantized cache in device memory:
-    codes uint8 [num_blocks][num_kv_heads][block_size][head_dim] for K and V, and
-    for INT8 the fp32 row scales [num_blocks][num_kv_heads][block_size]."""
+    codes uint8 [num_blocks][num_kv_heads][block_size][head_dim] for K and V
+    ([..][head_dim / 2] packed codes for INT4), and for INT8 / INT4 the fp32 row
+    scales [num_blocks][num_kv_heads][block_size]."""
 
     def __init__(self, num_blocks, num_kv_heads, block_size, head_dim, fmt, device="cuda", fill=None):
         self.fmt = FORMATS[fmt] if isinstance(fmt, str) else int(fmt)
         self.num_blocks, self.num_kv_heads = int(num_blocks), int(num_kv_heads)
         self.block_size, self.head_dim = int(block_size), int(head_dim)
-        shape = (self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim)
+        shape = (self.num_blocks, self.num_kv_heads, self.block_size,
+                 self.head_dim // 2 if self.fmt == INT4 else self.head_dim)
         mk = (lambda: torch.full(shape, fill, dtype=torch.uint8, device=device)) if fill is not None else \
             (lambda: torch.empty(shape, dtype=torch.uint8, device=device))
         self.k_codes, self.v_codes = mk(), mk()
-        if self.fmt == INT8:
+        if self.fmt in (INT8, INT4):
             sshape = shape[:3]
             self.k_scales = torch.zeros(sshape, dtype=torch.float32, device=device)
             self.v_scales = torch.zeros(sshape, dtype=torch.float32, device=device)

@@ -57,14 +57,14 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 kvq_status check_cache(const kvq_cache* c, int32_t fmt) {
     if (!c) return KVQ_ERR_INVALID_ARG;
-    if (fmt != KVQ_E4M3 && fmt != KVQ_E5M2 && fmt != KVQ_INT8) return KVQ_ERR_INVALID_ARG;
+    if (fmt != KVQ_E4M3 && fmt != KVQ_E5M2 && fmt != KVQ_INT8 && fmt != KVQ_INT4) return KVQ_ERR_INVALID_ARG;
     if (c->fmt != fmt) return KVQ_ERR_INVALID_ARG;
     if (!c->k_codes || !c->v_codes || !aligned(c->k_codes, 16) || !aligned(c->v_codes, 16))
         return KVQ_ERR_INVALID_ARG;
     if (c->num_blocks <= 0 || c->num_kv_heads <= 0) return KVQ_ERR_INVALID_ARG;
     if (c->head_dim != 64 && c->head_dim != 128) return KVQ_ERR_UNSUPPORTED;
     if (c->block_size != 16 && c->block_size != 32 && c->block_size != 64) return KVQ_ERR_UNSUPPORTED;
-    if (fmt == KVQ_INT8) {
+    if (fmt == KVQ_INT8 || fmt == KVQ_INT4) {
         if (!c->k_scales || !c->v_scales || !aligned(c->k_scales, 16) || !aligned(c->v_scales, 16))
             return KVQ_ERR_INVALID_ARG;
     }
@@ -110,6 +110,7 @@ kvq_status decode_impl(const void* q, const void* k_new, const void* v_new, cons
     if (num_q_heads % cache->num_kv_heads) return KVQ_ERR_INVALID_ARG;
     const int G = num_q_heads / cache->num_kv_heads;
     if (G > 8) return KVQ_ERR_UNSUPPORTED;
+    if (fmt == KVQ_INT4) return KVQ_ERR_UNSUPPORTED;   // decode of INT4 caches is not built
     if ((int64_t)max_blocks_per_seq * cache->block_size < max_context_len) return KVQ_ERR_INVALID_ARG;
     if (batch > 65535 || cache->num_kv_heads > 65535 || num_q_heads > 65535) return KVQ_ERR_UNSUPPORTED;
     if (batch == 0) return KVQ_OK;
@@ -143,7 +144,7 @@ kvq_status decode_impl(const void* q, const void* k_new, const void* v_new, cons
     a.batch = batch;
     a.num_q_heads = num_q_heads;
     a.max_context_len = max_context_len;
-    a.scale = fmt == KVQ_INT8 ? nullptr : scale;
+    a.scale = (fmt == KVQ_INT8 || fmt == KVQ_INT4) ? nullptr : scale;
     a.sm_scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt((float)cache->head_dim);
     a.out = static_cast<uint16_t*>(out);
     a.ws = static_cast<float*>(workspace);
@@ -207,7 +208,7 @@ kvq_status kvq_append(const void* k, const void* v, const kvq_cache* cache, cons
     unsigned long long* err = err_word(dev);
     if (!err) return KVQ_ERR_CUDA;
     kvq::AppendArgs a{static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), view(cache), slot_mapping,
-                      num_tokens, fmt == KVQ_INT8 ? nullptr : scale, err};
+                      num_tokens, (fmt == KVQ_INT8 || fmt == KVQ_INT4) ? nullptr : scale, err};
     return kvq::launch_append(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
@@ -277,7 +278,7 @@ kvq_status kvq_prefill_attention(const void* q, const kvq_cache* cache, const in
     a.num_q_tokens = num_q_tokens;
     a.num_q_heads = num_q_heads;
     a.max_query_len = max_query_len;
-    a.scale = fmt == KVQ_INT8 ? nullptr : scale;
+    a.scale = (fmt == KVQ_INT8 || fmt == KVQ_INT4) ? nullptr : scale;
     a.sm_scale = sm_scale > 0.f ? sm_scale : 1.0f / std::sqrt((float)cache->head_dim);
     a.out = static_cast<uint16_t*>(out);
     a.err = err;
@@ -298,7 +299,7 @@ kvq_status kvq_dequant(const kvq_cache* cache, const int64_t* slots, int64_t num
     if (!current_device(&dev)) return KVQ_ERR_CUDA;
     unsigned long long* err = err_word(dev);
     if (!err) return KVQ_ERR_CUDA;
-    kvq::DequantArgs a{view(cache), slots, num_slots, fmt == KVQ_INT8 ? nullptr : scale, out_k, out_v, err};
+    kvq::DequantArgs a{view(cache), slots, num_slots, (fmt == KVQ_INT8 || fmt == KVQ_INT4) ? nullptr : scale, out_k, out_v, err};
     return kvq::launch_dequant(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 

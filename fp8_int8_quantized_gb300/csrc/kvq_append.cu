@@ -4,7 +4,9 @@
 // E5M2"; "FP8 E4M3 KV Cache"): the cache holds FP8 codes of x / scale with one
 // fp32 per-tensor scale (1.0 when none is given).  "[Feature] TurboMind support
 // W8A8 or FP8 KV Cache" (lmdeploy issue 1463): online INT8, here symmetric with
-// one fp32 scale amax / 127 per (token, kv-head) row.
+// one fp32 scale amax / 127 per (token, kv-head) row; INT4 (named beside it)
+// the same with amax / 7, codes in [-7, 7] packed two per byte (channel 2i in
+// the low nibble).
 //
 // HBM-bound: per element 2 bytes read, 1 byte written.  One thread handles 16
 // consecutive elements of one (token, kv-head) row: two 16-byte loads of fp16,
@@ -51,6 +53,30 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
         x[2 * i + 1] = f.y;
     }
     const int64_t dst_row = ((slot / BS) * Hkv + h) * BS + slot % BS;
+    if (FMT == INT4) {
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+        const unsigned lane = threadIdx.x & 31u;
+        const unsigned gmask = (CPR == 32 ? 0xFFFFFFFFu : ((1u << CPR) - 1u) << (lane & ~(unsigned)(CPR - 1)));
+#pragma unroll
+        for (int off = CPR / 2; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, off));
+        const float s = __fdiv_rn(amax, 7.0f);
+        uint32_t o4[2] = {0u, 0u};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            int v = 0;
+            if (s != 0.f) {
+                v = __float2int_rn(__fdiv_rn(x[i], s));
+                v = max(-7, min(7, v));
+            }
+            o4[i >> 3] |= (uint32_t)(v & 0xF) << (4 * (i & 7));   // channel 2j low nibble of byte j
+        }
+        uint8_t* dst4 = (which ? a.cache.v_codes : a.cache.k_codes) + dst_row * (D / 2) + c * 8;
+        *reinterpret_cast<uint2*>(dst4) = make_uint2(o4[0], o4[1]);
+        if (c == 0) (which ? a.cache.v_scales : a.cache.k_scales)[dst_row] = s;
+        return;
+    }
     uint8_t* dst = (which ? a.cache.v_codes : a.cache.k_codes) + dst_row * D + c * 16;
     uint32_t o[4];
     if (FMT == INT8) {
@@ -215,7 +241,7 @@ template <int FMT>
 cudaError_t launch_fmt(const AppendArgs& a, cudaStream_t s) {
     const int D = a.cache.head_dim;
     const int64_t per = a.num_tokens * a.cache.num_kv_heads * (D / 16);
-    if constexpr (FMT != INT8) {
+    if constexpr (FMT == E4M3 || FMT == E5M2) {
         if (per * 32 >= kLutMinValues && per < ((int64_t)1 << 31)) {
             int dev = 0, sms = 0;
             cudaError_t e;
@@ -243,6 +269,7 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
     switch (a.cache.fmt) {
         case E4M3: return launch_fmt<E4M3>(a, s);
         case E5M2: return launch_fmt<E5M2>(a, s);
+        case INT4: return launch_fmt<INT4>(a, s);
         default: return launch_fmt<INT8>(a, s);
     }
 }

@@ -1,6 +1,6 @@
 // Debug gather + dequantize-on-read: the fp32 values the decode kernels see.
 // FP8: fl32(decode(code) * scale) with the per-tensor scale ("Accelerating
-// Inference with FP8 KV Cache", "FP8 Formats: E4M3 and E5M2"); INT8:
+// Inference with FP8 KV Cache", "FP8 Formats: E4M3 and E5M2"); INT8 and INT4:
 // fl32(code * row_scale).  One thread per 16 values of one (slot, kv-head) row.
 #include "kvq_device.cuh"
 #include "kvq_launch.h"
@@ -30,10 +30,23 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(DequantArgs a) {
         return;
     }
     const int64_t src_row = ((slot / BS) * Hkv + h) * BS + slot % BS;
+    const float s = (FMT == INT8 || FMT == INT4) ? (which ? a.cache.v_scales : a.cache.k_scales)[src_row]
+                                                 : (a.scale ? __ldg(a.scale) : 1.0f);
+    if (FMT == INT4) {
+        const uint2 r4 = *reinterpret_cast<const uint2*>((which ? a.cache.v_codes : a.cache.k_codes) +
+                                                         src_row * (D / 2) + c * 8);
+        uint32_t h[8];
+        int4x8_to_f16(r4.x, *reinterpret_cast<uint32_t(*)[4]>(&h[0]));
+        int4x8_to_f16(r4.y, *reinterpret_cast<uint32_t(*)[4]>(&h[4]));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 p0 = f16x2_to_f32x2(h[2 * j]), p1 = f16x2_to_f32x2(h[2 * j + 1]);
+            reinterpret_cast<float4*>(out)[j] = make_float4(p0.x * s, p0.y * s, p1.x * s, p1.y * s);
+        }
+        return;
+    }
     const uint4 r = *reinterpret_cast<const uint4*>((which ? a.cache.v_codes : a.cache.k_codes) +
                                                     src_row * D + c * 16);
-    const float s = FMT == INT8 ? (which ? a.cache.v_scales : a.cache.k_scales)[src_row]
-                                : (a.scale ? __ldg(a.scale) : 1.0f);
     const uint32_t w[4] = {r.x, r.y, r.z, r.w};
     float y[16];
 #pragma unroll
@@ -69,6 +82,7 @@ cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t s) {
     switch (a.cache.fmt) {
         case E4M3: return launch_fmt<E4M3>(a, s);
         case E5M2: return launch_fmt<E5M2>(a, s);
+        case INT4: return launch_fmt<INT4>(a, s);
         default: return launch_fmt<INT8>(a, s);
     }
 }

@@ -13,7 +13,10 @@
 
 namespace kvq {
 
-enum Fmt : int { E4M3 = 1, E5M2 = 2, INT8 = 3 };
+enum Fmt : int { E4M3 = 1, E5M2 = 2, INT8 = 3, INT4 = 4 };
+
+// Bytes of one cached (token, kv-head) row of head_dim values.
+__host__ __device__ constexpr int row_bytes(int fmt, int D) { return fmt == INT4 ? D / 2 : D; }
 
 // Error word codes (top byte of the 64-bit device error word).
 enum DevErr : unsigned long long { DEV_ERR_RANGE = 1, DEV_ERR_TIMEOUT = 2 };
@@ -80,6 +83,34 @@ __device__ __forceinline__ uint32_t int8_biased_pair_to_f16x2(uint32_t biased_pa
     __half2 v = *reinterpret_cast<__half2*>(&h);
     v = __hsub2(v, off);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Eight packed INT4 codes (one 32-bit word; byte i holds channel 2i in its low
+// nibble and 2i+1 in its high nibble, 4-bit two's complement) -> four f16x2
+// words of 1032 + code (exact: XOR 0x8 turns each nibble into code + 8, which
+// becomes the low mantissa bits of 1024).  Word i holds channels 2i, 2i+1.
+__device__ __forceinline__ void int4x8_biased(uint32_t w, uint32_t (&h)[4]) {
+    const uint32_t x = w ^ 0x88888888u;
+    const uint32_t lo = x & 0x0F0F0F0Fu;          // channels 0, 2, 4, 6 (bytes 0..3)
+    const uint32_t hi = (x >> 4) & 0x0F0F0F0Fu;   // channels 1, 3, 5, 7
+    const uint32_t a = prmt(lo, hi, 0x5410u);     // [c0, c2, c1, c3]
+    const uint32_t b = prmt(lo, hi, 0x7632u);     // [c4, c6, c5, c7]
+    h[0] = prmt(a, 0x64646464u, 0x4240u);         // fp16 0x64.. | c0, 0x64.. | c1
+    h[1] = prmt(a, 0x64646464u, 0x4341u);         // c2, c3
+    h[2] = prmt(b, 0x64646464u, 0x4240u);         // c4, c5
+    h[3] = prmt(b, 0x64646464u, 0x4341u);         // c6, c7
+}
+
+// The same with the bias removed: four f16x2 words of the exact codes.
+__device__ __forceinline__ void int4x8_to_f16(uint32_t w, uint32_t (&h)[4]) {
+    int4x8_biased(w, h);
+    const __half2 off = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));  // 1032
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __half2 v = *reinterpret_cast<__half2*>(&h[i]);
+        v = __hsub2(v, off);
+        h[i] = *reinterpret_cast<uint32_t*>(&v);
+    }
 }
 
 // Codes in bytes (lo, hi) of a 16-bit value -> f16x2, for any format.

@@ -3,12 +3,13 @@
 //
 // "Accelerating Inference with FP8 KV Cache" (intro): the cache is stored in
 // FP8 and computation runs in FP16.  Here the cached codes are dequantized
-// exactly to fp16 operands (every FP8 value and every INT8 code is an fp16
-// value), products are fp16 x fp16 and sums fp32.  The FP8 per-tensor scale
-// ("FP8 Formats: E4M3 and E5M2") and the INT8 row scales ("[Feature]
-// TurboMind support W8A8 or FP8 KV Cache", online INT8) are folded out of the
-// contractions: logits take s_K (per token for INT8), the softmax weights take
-// the INT8 s_V of their token, the output takes the FP8 s.
+// exactly to fp16 operands (every FP8 value and every INT8 / INT4 code is an
+// fp16 value), products are fp16 x fp16 and sums fp32.  The FP8 per-tensor
+// scale ("FP8 Formats: E4M3 and E5M2") and the INT8 / INT4 row scales
+// ("[Feature] TurboMind support W8A8 or FP8 KV Cache", online INT8 and the INT4
+// named beside it) are folded out of the contractions: logits take s_K (per
+// token for INT8 / INT4), the softmax weights take the s_V of their token, the
+// output takes the FP8 s.
 //
 // Query i of an n-query chunk of a sequence with ctx cached tokens (the
 // chunk's own K/V included) sits at position ctx - n + i and attends to every
@@ -22,8 +23,8 @@
 //     through the block table (L2 serves the other M tiles of the same
 //     sequence), exact conversion to fp16, stores into the 128-byte-swizzled
 //     K-major layout the tensor core reads; positions past the tile's last
-//     query are written as zeros.  They also stage the query tile and the INT8
-//     row scales;
+//     query are written as zeros.  They also stage the query tile and the INT8 /
+//     INT4 row scales;
 //   * thread 0 (also a softmax thread) issues S = Q K^T (M 128, N 128, K
 //     head_dim) into tensor memory and O += P V (M 128, N head_dim, K 128)
 //     with P read from tensor memory, V from shared memory as an MN-major
@@ -235,7 +236,7 @@ enum Bar : int {
     B_VFREE0, B_VFREE1,    // MMA -> dequant, softmax: O += P V done (commit)
     B_SFULL0, B_SFULL1,    // MMA -> softmax: S in its tensor-memory buffer (commit)
     B_PFULL0, B_PFULL1,    // softmax -> MMA: P written over S (128)
-    B_SC0, B_SC1, B_SC2, B_SC3,  // dequant -> softmax: INT8 scales of the tile (128)
+    B_SC0, B_SC1, B_SC2, B_SC3,  // dequant -> softmax: INT8 / INT4 row scales of the tile
     B_OFINAL,              // every MMA done (commit)
     kNumBars
 };
@@ -254,8 +255,8 @@ struct SmemLayout {
     static constexpr uint32_t kQ = 0;
     static constexpr uint32_t kK = kQ + kTileQ;            // two K buffers
     static constexpr uint32_t kV = kK + 2 * kTileKV;       // two V buffers
-    static constexpr uint32_t kKsc = kV + 2 * kTileKV;     // fp32 [4][64] INT8 logit multipliers
-    static constexpr uint32_t kVsc = kKsc + 4 * kKvTile * 4;  // fp32 [4][64] INT8 V row scales
+    static constexpr uint32_t kKsc = kV + 2 * kTileKV;     // fp32 [4][64] INT8 / INT4 logit multipliers
+    static constexpr uint32_t kVsc = kKsc + 4 * kKvTile * 4;  // fp32 [4][64] INT8 / INT4 V row scales
     static constexpr uint32_t kBar = kVsc + 4 * kKvTile * 4;
     static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
     static constexpr uint32_t kAbort = kTmemSlot + 4;
@@ -300,8 +301,11 @@ template <int FMT, int D>
 __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParams a) {
     using L = SmemLayout<D>;
     constexpr int kChunks = D / 8;       // 16-byte fp16 chunks per row
-    constexpr int kCodeVecs = D / 16;    // 16-byte code vectors per token row
-    constexpr int kTileVecs = kKvTile * kCodeVecs;  // 16-code vectors per K or V tile
+    constexpr bool kRowScaled = FMT == INT8 || FMT == INT4;   // one scale per (token, kv-head) row
+    constexpr int kRowBytes = row_bytes(FMT, D);
+    constexpr int kCodeVecs = kRowBytes / 16;              // 16-byte code vectors per token row
+    constexpr int kChunksPerVec = FMT == INT4 ? 4 : 2;     // 8-value fp16 chunks per code vector
+    constexpr int kTileVecs = kKvTile * kCodeVecs;         // code vectors per K or V tile
     constexpr int kVecsPerThread = (kTileVecs + kDqThreads - 1) / kDqThreads;
     constexpr uint32_t kIdescQK = idesc_f16(kRows, kKvTile, 0);
     constexpr uint32_t kIdescPV = idesc_f16(kRows, D, 1);
@@ -341,8 +345,8 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
     // instead of all requesting the same lines at once.
     const int rot = (int)(((unsigned)qt * 37u) % (unsigned)nkv);
     auto tile_of = [&](int j) { const int x = j + rot; return x >= nkv ? x - nkv : x; };
-    const float s_fp8 = (FMT != INT8 && a.scale) ? *a.scale : 1.0f;
-    // logits in log2 units: S * c_k (FP8; K carries the scale's sign) or S * c_k * s_K[t] (INT8)
+    const float s_fp8 = (!kRowScaled && a.scale) ? *a.scale : 1.0f;
+    // logits in log2 units: S * c_k (FP8; K carries the scale's sign) or S * c_k * s_K[t] (INT8 / INT4)
     const float c_k = a.sm_scale * kLog2e * fabsf(s_fp8);
 
     if (tid == 0) {
@@ -421,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
     } else if (warp >= 5) {
         // ------------------------------------------------------ dequant ----
         const int dt = tid - 160;
-        const size_t head_stride = (size_t)a.block_size * D;
+        const size_t head_stride = (size_t)a.block_size * kRowBytes;
         const int32_t* bt = a.block_tables + (size_t)b * a.max_blocks_per_seq;
         // query tile: row r = (query qt*TQ + r / G, head kvh*G + r % G)
         for (int e = dt; e < kRows * kChunks; e += kDqThreads) {
@@ -473,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
                 cv[it] = make_uint4(0, 0, 0, 0);
                 if (blk[it] >= 0)
                     cv[it] = ld_global_nc_v4(codes + ((size_t)blk[it] * Hkv + kvh) * head_stride +
-                                             (size_t)(t & (a.block_size - 1)) * D + vec_of(it) * 16);
+                                             (size_t)(t & (a.block_size - 1)) * kRowBytes + vec_of(it) * 16);
             }
         };
         auto load_scales = [&](int j, float& ks, float& vs) {
@@ -490,12 +494,23 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
         };
         // A negative FP8 scale is folded into K's fp16 signs, so the logit
         // multiplier is never negative.
-        const uint32_t kflip = (FMT != INT8 && s_fp8 < 0.f) ? 0x80008000u : 0u;
+        const uint32_t kflip = (!kRowScaled && s_fp8 < 0.f) ? 0x80008000u : 0u;
         auto store_tile = [&](uint32_t tile, const uint4 (&cv)[kVecsPerThread], uint32_t flip) {
 #pragma unroll
             for (int it = 0; it < kVecsPerThread; ++it) {
                 if (!has(it)) continue;
                 const int u = row_of(it), c16 = vec_of(it);
+                if (FMT == INT4) {   // 32 codes -> four 8-value chunks
+                    uint32_t hw[4];
+                    const uint32_t cw[4] = {cv[it].x, cv[it].y, cv[it].z, cv[it].w};
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        int4x8_to_f16(cw[w], hw);
+                        st_shared_v4(tile + tile_off(L::kBlkKV, u, kChunksPerVec * c16 + w),
+                                     make_uint4(hw[0], hw[1], hw[2], hw[3]));
+                    }
+                    continue;
+                }
                 uint4 h0, h1;
                 dec16<FMT>(cv[it], h0, h1);
                 if (flip) {
@@ -516,23 +531,23 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
             const int sl = t & 1;
             if (t >= 2 && !wait_or_abort(&bars[B_KFREE0 + sl], ((t >> 1) - 1) & 1, abort, a.err)) return false;
             store_tile(sbase + L::kK + sl * L::kTileKV, kc, kflip);
-            if (FMT == INT8 && dt < kKvTile) {
+            if (kRowScaled && dt < kKvTile) {
                 ksc[(t & 3) * kKvTile + dt] = ks * c_k;   // the logit multiplier of token t
                 vsc[(t & 3) * kKvTile + dt] = vs;
             }
             fence_proxy_async();
             mbar_arrive(&bars[B_KFULL0 + sl]);
-            if (FMT == INT8) mbar_arrive(&bars[B_SC0 + (t & 3)]);
+            if (kRowScaled) mbar_arrive(&bars[B_SC0 + (t & 3)]);
             return true;
         };
         fetch_ids(0, blk_k);
         load_codes(a.k_codes, 0, kc, blk_k);
         load_codes(a.v_codes, 0, vc, blk_k);
-        if (FMT == INT8) load_scales(0, ks, vs);
+        if (kRowScaled) load_scales(0, ks, vs);
         put_k(0);
         fetch_ids(1, blk_k);
         load_codes(a.k_codes, 1, kc, blk_k);
-        if (FMT == INT8) load_scales(1, ks, vs);
+        if (kRowScaled) load_scales(1, ks, vs);
         for (int j = 0; j < nkv; ++j) {
             const int sl = j & 1;
             const bool more = j + 1 < nkv;
@@ -542,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
                 for (int it = 0; it < kVecsPerThread; ++it) blk_v[it] = blk_k[it];   // tile j+1
                 fetch_ids(j + 2, blk_k);
                 load_codes(a.k_codes, j + 2, kc, blk_k);
-                if (FMT == INT8) load_scales(j + 2, ks, vs);
+                if (kRowScaled) load_scales(j + 2, ks, vs);
             }
             if (j >= 2 && !wait_or_abort(&bars[B_VFREE0 + sl], ((j >> 1) - 1) & 1, abort, a.err)) break;
             store_tile(sbase + L::kV + sl * L::kTileKV, vc, 0u);
@@ -562,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
             const int sl = j & 1;
             if (!wait_or_abort(&bars[B_SFULL0 + sl], (j >> 1) & 1, abort, a.err)) { ok = false; break; }
             tc_fence_after();
-            if (FMT == INT8 && !wait_or_abort(&bars[B_SC0 + (j & 3)], (j >> 2) & 1, abort, a.err)) {
+            if (kRowScaled && !wait_or_abort(&bars[B_SC0 + (j & 3)], (j >> 2) & 1, abort, a.err)) {
                 ok = false;
                 break;
             }
@@ -578,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
 #pragma unroll
                 for (int q = 0; q < 32; ++q) {
                     const int u = ch * 32 + q;
-                    const float x = FMT == INT8 ? __uint_as_float(sv[q]) * ks[u] : __uint_as_float(sv[q]);
+                    const float x = kRowScaled ? __uint_as_float(sv[q]) * ks[u] : __uint_as_float(sv[q]);
                     if (full || u <= lim) mx = fmaxf(mx, x);
                 }
             };
@@ -593,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
                 reg_fence32(sb);
                 chunk_max(sb, 1);
             }
-            if (FMT != INT8) mx *= c_k;
+            if (!kRowScaled) mx *= c_k;
             const float m_new = fmaxf(m_used, mx);
             float alpha = 1.f;
             bool resc = false;
@@ -630,10 +645,10 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
 #pragma unroll
                     for (int z = 0; z < 2; ++z) {
                         const int u = ch * 16 + 2 * q + z;
-                        float e = fast_exp2(fmaf(__uint_as_float(sv[2 * q + z]), FMT == INT8 ? ks[u] : c_k, neg_m));
+                        float e = fast_exp2(fmaf(__uint_as_float(sv[2 * q + z]), kRowScaled ? ks[u] : c_k, neg_m));
                         if (!full && u > lim) e = 0.f;
                         if (z) l2 += e; else l += e;
-                        pv[z] = FMT == INT8 ? e * vs[u] : e;
+                        pv[z] = kRowScaled ? e * vs[u] : e;
                     }
                     hi[q] = pack_f16x2(pv[0], pv[1]);
                     lo[q] = residual_f16x2(hi[q], pv[0], pv[1]);
@@ -745,6 +760,7 @@ cudaError_t launch_prefill(const PrefillArgs& x, cudaStream_t s) {
     switch (x.cache.fmt) {
         case E4M3: return D == 64 ? launch_t<E4M3, 64>(x, s) : launch_t<E4M3, 128>(x, s);
         case E5M2: return D == 64 ? launch_t<E5M2, 64>(x, s) : launch_t<E5M2, 128>(x, s);
+        case INT4: return D == 64 ? launch_t<INT4, 64>(x, s) : launch_t<INT4, 128>(x, s);
         default: return D == 64 ? launch_t<INT8, 64>(x, s) : launch_t<INT8, 128>(x, s);
     }
 }

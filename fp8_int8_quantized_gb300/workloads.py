@@ -33,9 +33,9 @@ class Workload:
     num_kv_heads: int
     head_dim: int
     block_size: int
-    fmt: str                       # "e4m3" | "e5m2" | "int8"
+    fmt: str                       # "e4m3" | "e5m2" | "int8" | "int4"
     ctx: int | tuple[int, int]     # fixed length, or inclusive uniform range
-    scale_rule: str                # "amax" | "one" | "row" (INT8: per (token, kv-head))
+    scale_rule: str                # "amax" | "one" | "row" (INT8 / INT4: per (token, kv-head))
     outliers: bool = False
     append_chunk: int = 0          # prefill chunk appended per sequence inside a step
     seed: int = 0
@@ -60,6 +60,10 @@ WORKLOADS = {
                                 seed=1003,
                                 description="Llama-2-13B INT8 decode: 40x128, batch 128, ctx 4096, "
                                             "block 64, online INT8 per (token, kv-head)"),
+    "llama2-13b-int4": Workload("llama2-13b-int4", 128, 40, 40, 128, 64, "int4", 4096, "row",
+                                seed=1005,
+                                description="Llama-2-13B INT4 shapes: 40x128, batch 128, ctx 4096, "
+                                            "block 64, online INT4 per (token, kv-head)"),
     "llama3-70b": Workload("llama3-70b", 256, 64, 8, 128, 16, "e4m3", 32768, "amax",
                            outliers=True, append_chunk=2048, seed=1004,
                            description="Llama-3-70B long context: 64/8 heads x128, batch 256, "
@@ -184,10 +188,11 @@ def chunk_positions(wl: Workload, max_tokens: int):
 
 def decode_bytes(wl: Workload, ctx: torch.Tensor) -> dict:
     """Algorithmic HBM bytes of one decode call: every cached K/V byte of every
-    (sequence, kv-head) once, the INT8 row scales, q, out, block tables and lengths."""
+    (sequence, kv-head) once, the INT8 / INT4 row scales, q, out, block tables and
+    lengths."""
     tok = int(ctx.to(torch.int64).sum())
-    kv = 2 * tok * wl.num_kv_heads * wl.head_dim
-    scales = 2 * tok * wl.num_kv_heads * 4 if wl.fmt == "int8" else 0
+    kv = 2 * tok * wl.num_kv_heads * (wl.head_dim // 2 if wl.fmt == "int4" else wl.head_dim)
+    scales = 2 * tok * wl.num_kv_heads * 4 if wl.fmt in ("int8", "int4") else 0
     qo = 2 * wl.batch * wl.num_q_heads * wl.head_dim * 2
     bt = sum(math.ceil(int(c) / wl.block_size) for c in ctx) * 4 + wl.batch * 4
     return {"kv": kv, "scales": scales, "q_out": qo, "tables": bt,
@@ -196,10 +201,10 @@ def decode_bytes(wl: Workload, ctx: torch.Tensor) -> dict:
 
 def append_bytes(wl: Workload, num_tokens: int) -> int:
     """Algorithmic HBM bytes of appending ``num_tokens`` tokens: fp16 K+V read,
-    codes written, slots read, INT8 row scales written."""
+    codes written, slots read, INT8 / INT4 row scales written."""
     e = num_tokens * wl.num_kv_heads * wl.head_dim
-    b = 2 * e * 2 + 2 * e + num_tokens * 8
-    if wl.fmt == "int8":
+    b = 2 * e * 2 + (e if wl.fmt == "int4" else 2 * e) + num_tokens * 8
+    if wl.fmt in ("int8", "int4"):
         b += 2 * num_tokens * wl.num_kv_heads * 4
     return b
 

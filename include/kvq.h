@@ -60,11 +60,14 @@ typedef struct CUstream_st* kvq_stream_t;
 
 /* Cache formats.  [TGI] "Current Hardware Support": "fp8" = E4M3 (OCP
  * E4M3FN: no infinities, S.1111.111 = NaN, max 448) and "fp8_e5m2" = E5M2
- * (max 57344); [LMD]: online INT8. */
+ * (max 57344); [LMD]: online INT8, and the INT4 implementation the same
+ * thread names beside it (read here as INT8 with 4 bits: codes in [-7, 7],
+ * scale amax / 7 per row, two codes per byte, channel 2i in the low nibble). */
 typedef enum {
     KVQ_E4M3 = 1,
     KVQ_E5M2 = 2,
-    KVQ_INT8 = 3
+    KVQ_INT8 = 3,
+    KVQ_INT4 = 4
 } kvq_fmt;
 
 typedef enum {
@@ -80,8 +83,9 @@ typedef enum {
 
 /* The paged cache: caller-owned device memory.
  *   k_codes, v_codes: [num_blocks][num_kv_heads][block_size][head_dim] bytes,
- *                     FP8 codes (u8) or INT8 codes (i8); 16-byte aligned.
- *   k_scales, v_scales: INT8 only, fp32 [num_blocks][num_kv_heads][block_size]
+ *                     FP8 codes (u8) or INT8 codes (i8); for INT4
+ *                     [..][head_dim / 2] bytes of packed codes; 16-byte aligned.
+ *   k_scales, v_scales: INT8 and INT4, fp32 [num_blocks][num_kv_heads][block_size]
  *                     (one scale per (token, kv-head) row); NULL for FP8.
  *   head_dim in {64, 128}; block_size in {16, 32, 64}; fmt a kvq_fmt. */
 typedef struct {
@@ -104,7 +108,8 @@ typedef struct {
  *     and V, or NULL for the default 1.0 ([TGI] "FP8 E4M3 KV Cache").  Each
  *     element is stored as code = RNE-satfinite(fl32(x / scale)).  Ignored for
  *     INT8, where each (token, kv-head) row gets s = fl32(amax / 127) and codes
- *     clamp(rint(fl32(x / s)), -127, 127) (s = 0 and zero codes for a zero row).
+ *     clamp(rint(fl32(x / s)), -127, 127) (s = 0 and zero codes for a zero row);
+ *     INT4 the same with s = fl32(amax / 7) and codes in [-7, 7].
  *   fmt must equal cache->fmt.  num_tokens == 0 is a no-op. */
 KVQ_API kvq_status kvq_append(const void* k, const void* v, const kvq_cache* cache,
                       const int64_t* slot_mapping, int64_t num_tokens,
@@ -126,6 +131,8 @@ KVQ_API size_t kvq_decode_workspace_size(int32_t batch, int32_t num_q_heads, int
  *     with context 0 gets a zero output.
  *   q-head h reads kv-head h / (num_q_heads / num_kv_heads); num_q_heads must be
  *     a multiple of num_kv_heads and the group size at most 8.
+ *   INT4 caches return KVQ_ERR_UNSUPPORTED (decode of INT4 is not built; append,
+ *   dequant and prefill attention take them).
  *   batch at most 4096, and batch * num_kv_heads * ceil(max_context_len / 16)
  *     below 2^31 (KVQ_ERR_UNSUPPORTED otherwise).
  *   scale: FP8 per-tensor scale as in kvq_append (NULL = 1.0); ignored for INT8.

@@ -10,7 +10,7 @@ import fp8_int8_quantized_gb300 as kvq
 import oracle
 from fp8_int8_quantized_gb300 import workloads as W
 
-ORACLE_FMT = {"e4m3": oracle.E4M3, "e5m2": oracle.E5M2, "int8": oracle.INT8}
+ORACLE_FMT = {"e4m3": oracle.E4M3, "e5m2": oracle.E5M2, "int8": oracle.INT8, "int4": oracle.INT4}
 
 # Attention tolerance: |o_gpu - o_ref| <= 2e-3 * max(1, |o_ref|) per element,
 # o_ref the fp64 oracle on the same dequantized cache.  fp16 output rounding
@@ -83,7 +83,7 @@ class DeviceWorkload:
         kc = self.cache.k_codes.index_select(0, idx).cpu().numpy()
         vc = self.cache.v_codes.index_select(0, idx).cpu().numpy()
         ks = vs = None
-        if wl.fmt == "int8":
+        if wl.fmt in ("int8", "int4"):
             ks = self.cache.k_scales.index_select(0, idx).cpu().numpy()
             vs = self.cache.v_scales.index_select(0, idx).cpu().numpy()
         oc = oracle.Cache(len(blocks), wl.num_kv_heads, bs, wl.head_dim, ORACLE_FMT[wl.fmt],

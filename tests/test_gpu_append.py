@@ -1,5 +1,5 @@
 """GPU parity of quantize-on-write (kvq_append) and dequant (kvq_dequant) against
-the CPU oracle: bit-exact for every cache byte and every INT8 row scale."""
+the CPU oracle: bit-exact for every cache byte and every INT8 / INT4 row scale."""
 import numpy as np
 import pytest
 import torch
@@ -105,7 +105,7 @@ def test_large_append_bit_exact_heads_and_blocks(fmt, Hkv, D, BS):
     assert kvq.device_error_check()[0] == 0
 
 
-@pytest.mark.parametrize("fmt", ["e4m3", "e5m2", "int8"])
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2", "int8", "int4"])
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("BS", [16, 32, 64])
 def test_append_bit_exact(fmt, D, BS):
@@ -121,7 +121,7 @@ def test_append_bit_exact(fmt, D, BS):
     c, ref = run_both(k, v, slots, NB, Hkv, BS, D, fmt, scale)
     assert np.array_equal(c.k_codes.cpu().numpy(), ref.k_codes)
     assert np.array_equal(c.v_codes.cpu().numpy(), ref.v_codes)
-    if fmt == "int8":
+    if fmt in ("int8", "int4"):
         assert np.array_equal(c.k_scales.cpu().numpy().view(np.uint32), ref.k_scales.view(np.uint32))
         assert np.array_equal(c.v_scales.cpu().numpy().view(np.uint32), ref.v_scales.view(np.uint32))
     st, _ = kvq.device_error_check()
@@ -156,7 +156,7 @@ def test_append_empty_and_validation():
     assert ei.value.status == 1
 
 
-@pytest.mark.parametrize("name", ["llama2-7b", "llama3-8b", "llama2-13b-int8", "llama3-70b"])
+@pytest.mark.parametrize("name", ["llama2-7b", "llama3-8b", "llama2-13b-int8", "llama2-13b-int4", "llama3-70b"])
 def test_append_full_size_sampled(name):
     """The workloads' own append launches (their full windows), checked on a
     seeded sample of tokens against the oracle."""
@@ -188,12 +188,12 @@ def test_append_full_size_sampled(name):
     i = np.arange(len(pick))
     assert np.array_equal(gk, ref.k_codes[i // bs, :, i % bs])
     assert np.array_equal(gv, ref.v_codes[i // bs, :, i % bs])
-    if wl.fmt == "int8":
+    if wl.fmt in ("int8", "int4"):
         assert np.array_equal(c.k_scales[blk, :, off].cpu().numpy(), ref.k_scales[i // bs, :, i % bs])
         assert np.array_equal(c.v_scales[blk, :, off].cpu().numpy(), ref.v_scales[i // bs, :, i % bs])
 
 
-@pytest.mark.parametrize("fmt", ["e4m3", "e5m2", "int8"])
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2", "int8", "int4"])
 @pytest.mark.parametrize("D", [64, 128])
 def test_dequant_bit_exact(fmt, D):
     g = torch.Generator().manual_seed(3 + D)
@@ -201,7 +201,7 @@ def test_dequant_bit_exact(fmt, D):
     k = (torch.randn((T, Hkv, D), generator=g) * 5).to(torch.float16)
     v = (torch.randn((T, Hkv, D), generator=g) * 5).to(torch.float16)
     slots = torch.randperm(NB * BS, generator=g)[:T].to(torch.int64)
-    scale = 0.05 if fmt != "int8" else None
+    scale = 0.05 if fmt not in ("int8", "int4") else None
     c, ref = run_both(k, v, slots, NB, Hkv, BS, D, fmt, scale)
     st = None if scale is None else torch.tensor([scale], dtype=torch.float32, device="cuda")
     ok, ov = kvq.dequant(c, slots.cuda(), st)

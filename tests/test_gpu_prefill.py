@@ -27,7 +27,7 @@ def _lib():
 
 def small(fmt, B, Hq, Hkv, D, BS, ctx, seed=0):
     wl = W.Workload(f"p-{fmt}", B, Hq, Hkv, D, BS, fmt, max(ctx),
-                    "amax" if fmt == "e4m3" else ("row" if fmt == "int8" else "one"),
+                    "amax" if fmt == "e4m3" else ("row" if fmt in ("int8", "int4") else "one"),
                     outliers=True, seed=seed)
     return DeviceWorkload(wl, chunk_tokens=1 << 16, ctx=torch.tensor(ctx, dtype=torch.int32))
 
@@ -51,6 +51,9 @@ PCASES = [
     ("int8", 3, 8, 2, 64, 64, [129, 1, 256], [129, 1, 17]),
     ("e4m3", 1, 48, 16, 128, 32, [390], [390]),
     ("e4m3", 2, 16, 1, 128, 16, [260, 50], [40, 50]),
+    ("int4", 2, 4, 4, 128, 64, [640, 65], [300, 65]),
+    ("int4", 3, 8, 2, 64, 16, [129, 1, 256], [129, 1, 17]),
+    ("int4", 1, 32, 8, 128, 32, [500], [200]),
 ]
 
 
@@ -101,6 +104,13 @@ def test_empty_and_validation():
         kvq._check(st, "kvq_prefill_attention")
 
 
+def test_int4_decode_is_not_built():
+    dw = small("int4", 1, 4, 4, 64, 16, [20], seed=2)
+    with pytest.raises(kvq.KvqError) as ei:
+        dw.decode()
+    assert ei.value.status == 2
+
+
 def test_chunk_longer_than_context_is_reported_and_others_computed():
     dw = small("e5m2", 2, 4, 4, 64, 16, [40, 30], seed=13)
     n = torch.tensor([41, 30], dtype=torch.int32)            # sequence 0 claims more queries than tokens
@@ -135,6 +145,7 @@ def test_bad_block_id_is_reported_without_fault():
 @pytest.mark.parametrize("name,chunk,seqs", [("llama3-70b", 2048, [0, 255]),
                                              ("llama3-8b", 1024, [0, 33]),
                                              ("llama2-13b-int8", 512, [5]),
+                                             ("llama2-13b-int4", 512, [7]),
                                              ("llama2-7b", 2048, [31])])
 def test_prefill_workload_sampled(name, chunk, seqs):
     wl = W.WORKLOADS[name]
