@@ -110,7 +110,6 @@ kvq_status decode_impl(const void* q, const void* k_new, const void* v_new, cons
     if (num_q_heads % cache->num_kv_heads) return KVQ_ERR_INVALID_ARG;
     const int G = num_q_heads / cache->num_kv_heads;
     if (G > 8) return KVQ_ERR_UNSUPPORTED;
-    if (fmt == KVQ_INT4) return KVQ_ERR_UNSUPPORTED;   // decode of INT4 caches is not built
     if ((int64_t)max_blocks_per_seq * cache->block_size < max_context_len) return KVQ_ERR_INVALID_ARG;
     if (batch > 65535 || cache->num_kv_heads > 65535 || num_q_heads > 65535) return KVQ_ERR_UNSUPPORTED;
     if (batch == 0) return KVQ_OK;
@@ -130,7 +129,7 @@ kvq_status decode_impl(const void* q, const void* k_new, const void* v_new, cons
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return KVQ_ERR_WORKSPACE;
     int kind = g_decode_kernel.load();
     if (kind == 0) kind = 2;
-    if (kind == 1 && G > 4) return KVQ_ERR_UNSUPPORTED;
+    if (kind == 1 && (G > 4 || fmt == KVQ_INT4)) return KVQ_ERR_UNSUPPORTED;   // CUDA-core kernel: 8-bit codes, G <= 4
     int dev;
     if (!current_device(&dev)) return KVQ_ERR_CUDA;
     unsigned long long* err = err_word(dev);

@@ -3,8 +3,10 @@
 // "Accelerating Inference with FP8 KV Cache" (intro): the KV cache is stored in
 // FP8 and computation runs in FP16; here every product is fp16 x fp16 and every
 // sum fp32.  The FP8 per-tensor scale ("FP8 Formats: E4M3 and E5M2") and the
-// INT8 row scales ("[Feature] TurboMind support W8A8 or FP8 KV Cache", online
-// INT8) are folded out of the dot products: logits take s_K, outputs take s_V.
+// INT8 / INT4 row scales ("[Feature] TurboMind support W8A8 or FP8 KV Cache",
+// online INT8 and the INT4 named beside it) are folded out of the dot products:
+// logits take s_K, outputs take s_V.  INT4 rows are head_dim / 2 bytes (two
+// codes per byte) and use the tensor-core consumer only.
 //
 // Work decomposition.  Every (sequence, kv-head) pair owns ceil(ctx / 16)
 // tiles of 16 tokens; all pairs' tiles, in (sequence, kv-head, tile) order,
@@ -77,8 +79,10 @@ enum { kKindSimt = 1, kKindMma = 2 };
 // lengths.
 struct Layout {
     int tile_bytes, q_bytes, scales, full, qbuf, newkv, patch, scan, total;
-    __host__ __device__ Layout(int D, int G, int B, bool int8, bool append) {
-        tile_bytes = kTile * D;
+    // rb: bytes of one cached row (head_dim, or head_dim / 2 for INT4); int8:
+    // the format carries row scales (INT8 or INT4)
+    __host__ __device__ Layout(int rb, int D, int G, int B, bool int8, bool append) {
+        tile_bytes = kTile * rb;
         q_bytes = (G * D * 2 + 127) / 128 * 128;
         scales = kConsumers * kSpw * 2 * tile_bytes;            // [warp][stage][K,V][tile] before this
         full = scales + (int8 ? kConsumers * kSpw * 2 * kTile * 4 : 0);  // INT8: f32 [warp][stage][K,V][32]
@@ -145,6 +149,19 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
 __device__ __forceinline__ uint2 lds64(uint32_t a) {
     uint2 r;
     asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(a));
+    return r;
+}
+// f16x2 of 1032 + code (code + 8 in the low mantissa bits of 1024) -> the exact codes
+__device__ __forceinline__ uint32_t hsub1032(uint32_t h) {
+    const __half2 off = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+    __half2 v = *reinterpret_cast<__half2*>(&h);
+    v = __hsub2(v, off);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t r;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(r) : "r"(a));
     return r;
 }
 __device__ __forceinline__ float2 __uint_as_float2(uint2 v) { return make_float2(__uint_as_float(v.x), __uint_as_float(v.y)); }
@@ -334,16 +351,22 @@ struct SimtConsumer {
 
 template <int FMT, int D>
 struct MmaConsumer {
+    static constexpr bool I4 = FMT == INT4;
+    static constexpr bool kRowScaled = FMT == INT8 || FMT == INT4;
+    static constexpr int RB = row_bytes(FMT, D);  // bytes of one cached row
     static constexpr int KS = D / 16;   // k-steps of QK^T
-    static constexpr int DC = D / 4;    // K bytes per thread per token row
-    static constexpr int KW = DC / 4;   // ... as 32-bit words (== KS)
-    static constexpr int DV = D / 8;    // V bytes per thread per token row
-    static constexpr int VW = DV / 4;
+    static constexpr int DC = D / 4;    // K codes per thread per token row
+    static constexpr int KW = I4 ? DC / 8 : DC / 4;   // ... as 32-bit words (== KS for 8-bit codes)
+    static constexpr int DV = D / 8;    // V codes per thread per token row
+    static constexpr int VW = I4 ? DV / 8 : DV / 4;
     static constexpr int MT = D / 16;   // m-tiles of PV (head_dim / 16)
     static constexpr int kMinCtas = kMinBlocks;
     // INT8 codes enter the tensor cores as fp16 1152 + code (exact); the
-    // constant is taken out again: 1152 * sum(q) from each logit, 1152 * sum(P')
-    // from each output.
+    // constant is taken out again: 1152 * sum(q) from each logit, 1152 *
+    // sum(P') from each output.  INT4 codes are converted to their exact fp16
+    // values first (their row scales are 18x larger, so the rounding of the
+    // biased sums would show in the logits).
+    static constexpr bool kBiased = FMT == INT8;
     static constexpr float kBias = 1152.f;
     uint32_t qa[2 * KS];
     float acc[MT][4];
@@ -354,7 +377,8 @@ struct MmaConsumer {
     float qk_scale;
     // this lane's byte offsets inside a stage tile (the 128-byte swizzle folded
     // in): K row g at chunks 2c, 2c+1 (row 8+g is 8 rows further), V rows 2c
-    // and 2c+1 at chunk g (rows 8+2c, 9+2c are 8 rows further)
+    // and 2c+1 at chunk g (rows 8+2c, 9+2c are 8 rows further); INT4 rows are
+    // unswizzled, the same codes at half the bytes
     uint32_t k_off0, k_off1, v_off0, v_off1;
 
     __device__ void init(int G_, float qks) {
@@ -363,7 +387,12 @@ struct MmaConsumer {
         c = lane & 3;
         G = G_;
         qk_scale = qks;
-        if (D == 128) {
+        if (I4) {
+            k_off0 = g * RB + c * (DC / 2);
+            k_off1 = 0;
+            v_off0 = (2 * c) * RB + (DV / 2) * g;
+            v_off1 = (2 * c + 1) * RB + (DV / 2) * g;
+        } else if (D == 128) {
             k_off0 = g * 128 + (((2 * c) ^ g) << 4);
             k_off1 = g * 128 + (((2 * c + 1) ^ g) << 4);
             v_off0 = (2 * c) * 128 + ((g ^ (2 * c)) << 4);
@@ -390,7 +419,7 @@ struct MmaConsumer {
 #pragma unroll
             for (int i = 0; i < 2 * KS; ++i) qa[i] = 0u;
         }
-        if (FMT == INT8) {
+        if (kBiased) {
             float sq = 0.f;
 #pragma unroll
             for (int i = 0; i < 2 * KS; ++i) {
@@ -416,10 +445,18 @@ struct MmaConsumer {
         for (int i = 0; i < MT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     }
 
-    // K words of rows g (half 0) or 8 + g (half 1): the DC contiguous bytes at DC*c.
+    // K words of rows g (half 0) or 8 + g (half 1): the DC contiguous codes at DC*c.
     __device__ __forceinline__ void load_k(uint32_t kt, int half, uint32_t (&w)[KW]) {
-        const uint32_t rb = kt + half * 8 * D;
-        if (D == 128) {
+        const uint32_t rb = kt + half * 8 * RB;
+        if (I4) {
+            if (D == 128) {
+                const uint4 x0 = lds128(rb + k_off0);
+                w[0] = x0.x; w[1] = x0.y; w[KW > 2 ? 2 : 0] = x0.z; w[KW > 3 ? 3 : 1] = x0.w;
+            } else {
+                const uint2 x0 = lds64(rb + k_off0);
+                w[0] = x0.x; w[KW > 1 ? 1 : 0] = x0.y;
+            }
+        } else if (D == 128) {
             const uint4 x0 = lds128(rb + k_off0), x1 = lds128(rb + k_off1);
             w[0] = x0.x; w[1] = x0.y; w[2] = x0.z; w[3] = x0.w;
             w[4] = x1.x; w[5] = x1.y; w[6] = x1.z; w[7] = x1.w;
@@ -429,9 +466,16 @@ struct MmaConsumer {
         }
     }
 
-    // V words of a row: the thread's DV contiguous bytes at DV*g.
+    // V words of a row: the thread's DV contiguous codes at DV*g.
     __device__ __forceinline__ void load_v(uint32_t a, uint32_t (&w)[VW]) {
-        if (D == 128) {
+        if (I4) {
+            if (D == 128) {
+                const uint2 x = lds64(a);
+                w[0] = x.x; w[VW > 1 ? 1 : 0] = x.y;
+            } else {
+                w[0] = lds32(a);
+            }
+        } else if (D == 128) {
             const uint4 x = lds128(a);
             w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
         } else {
@@ -450,6 +494,21 @@ struct MmaConsumer {
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
             load_k(kt, hb, kw);
+            if (I4) {  // word w: codes 8w .. 8w+7 = k-steps 2w and 2w+1
+#pragma unroll
+                for (int w = 0; w < KW; ++w) {
+                    uint32_t h[4];
+                    int4x8_to_f16(kw[w], h);
+                    if (hb == 0) {
+                        mma_16816(sA, qa[4 * w], 0u, qa[4 * w + 1], 0u, h[0], h[1]);
+                        mma_16816(sA, qa[4 * w + 2], 0u, qa[4 * w + 3], 0u, h[2], h[3]);
+                    } else {
+                        mma_16816(sB, qa[4 * w], 0u, qa[4 * w + 1], 0u, h[0], h[1]);
+                        mma_16816(sB, qa[4 * w + 2], 0u, qa[4 * w + 3], 0u, h[2], h[3]);
+                    }
+                }
+                continue;
+            }
 #pragma unroll
             for (int j = 0; j < KS; ++j) {
                 uint32_t b0, b1;
@@ -459,8 +518,8 @@ struct MmaConsumer {
                 else mma_16816(sB, qa[2 * j], 0u, qa[2 * j + 1], 0u, b0, b1);
             }
         }
-        if (FMT == INT8) {  // remove the operand bias, then apply the K row scales
-            const float corr = kBias * qsum;
+        if (kRowScaled) {  // remove the operand bias (INT8), then apply the K row scales
+            const float corr = kBiased ? kBias * qsum : 0.f;
             const float2 k01 = __uint_as_float2(lds64(sk + 8 * c)), k23 = __uint_as_float2(lds64(sk + 32 + 8 * c));
             z[0] = (sA[0] - corr) * (qk_scale * k01.x);
             z[1] = (sA[1] - corr) * (qk_scale * k01.y);
@@ -484,8 +543,8 @@ struct MmaConsumer {
         uint32_t v0[VW], v1[VW], v2[VW], v3[VW];
         load_v(vt + v_off0, v0);
         load_v(vt + v_off1, v1);
-        load_v(vt + v_off0 + 8 * D, v2);
-        load_v(vt + v_off1 + 8 * D, v3);
+        load_v(vt + v_off0 + 8 * RB, v2);
+        load_v(vt + v_off1 + 8 * RB, v3);
         if (valid < kBox) {  // rows past the context may hold NaN codes: zero them
 #pragma unroll
             for (int e = 0; e < VW; ++e) {
@@ -494,6 +553,34 @@ struct MmaConsumer {
                 if (8 + 2 * c >= valid) v2[e] = 0u;
                 if (9 + 2 * c >= valid) v3[e] = 0u;
             }
+        }
+        if (I4) {  // word w of each row: codes 8w .. 8w+7 = m-tiles 4w .. 4w+3 (dims 2i | 2i+1 = low | high nibble)
+#pragma unroll
+            for (int w = 0; w < VW; ++w) {
+                const uint32_t x0 = v0[w] ^ 0x88888888u, x1 = v1[w] ^ 0x88888888u;  // code + 8 per nibble
+                const uint32_t x2 = v2[w] ^ 0x88888888u, x3 = v3[w] ^ 0x88888888u;
+                const uint32_t m4 = 0x0F0F0F0Fu;
+                // [row 2c, row 2c+1] low (dim 2i) / high (dim 2i+1) nibbles of bytes 0,1 and 2,3
+                const uint32_t l01a = prmt(x0 & m4, x1 & m4, 0x5140u), l01b = prmt(x0 & m4, x1 & m4, 0x7362u);
+                const uint32_t h01a = prmt((x0 >> 4) & m4, (x1 >> 4) & m4, 0x5140u);
+                const uint32_t h01b = prmt((x0 >> 4) & m4, (x1 >> 4) & m4, 0x7362u);
+                const uint32_t l23a = prmt(x2 & m4, x3 & m4, 0x5140u), l23b = prmt(x2 & m4, x3 & m4, 0x7362u);
+                const uint32_t h23a = prmt((x2 >> 4) & m4, (x3 >> 4) & m4, 0x5140u);
+                const uint32_t h23b = prmt((x2 >> 4) & m4, (x3 >> 4) & m4, 0x7362u);
+#pragma unroll
+                for (int bb = 0; bb < 4; ++bb) {
+                    const int i = 4 * w + bb;
+                    const uint32_t sel = (bb & 1) ? 0x4342u : 0x4140u;
+                    // fp16 1032 + code, then the exact code
+                    const uint32_t a0 = hsub1032(prmt(bb < 2 ? l01a : l01b, 0x64646464u, sel));
+                    const uint32_t a1 = hsub1032(prmt(bb < 2 ? h01a : h01b, 0x64646464u, sel));
+                    const uint32_t a2 = hsub1032(prmt(bb < 2 ? l23a : l23b, 0x64646464u, sel));
+                    const uint32_t a3 = hsub1032(prmt(bb < 2 ? h23a : h23b, 0x64646464u, sel));
+                    mma_16816(acc[i], a0, a1, a2, a3, pb0, pb1);
+                    mma_16816(acc[i], a0, a1, a2, a3, pl0, pl1);
+                }
+            }
+            return;
         }
         if (FMT == INT8) {  // code + 128 as unsigned bytes, once per word
 #pragma unroll
@@ -533,7 +620,7 @@ struct MmaConsumer {
         const float2 h01 = f16x2_to_f32x2(pb0), h23 = f16x2_to_f32x2(pb1);
         pl0 = pack_f16x2(p[0] - h01.x, p[1] - h01.y);
         pl1 = pack_f16x2(p[2] - h23.x, p[3] - h23.y);
-        if (FMT == INT8) {  // the weights exactly as the tensor cores see them
+        if (kBiased) {  // the weights exactly as the tensor cores see them
             const float2 l01 = f16x2_to_f32x2(pl0), l23 = f16x2_to_f32x2(pl1);
             sum_fed += ((h01.x + l01.x) + (h01.y + l01.y)) + ((h23.x + l23.x) + (h23.y + l23.y));
         }
@@ -543,7 +630,7 @@ struct MmaConsumer {
         const bool two = cx.valid > kBox;  // warp-uniform: the second box holds context rows
         float z0[4], z1[4];
         qk_box(cx.k, cx.s, cx.valid, z0);
-        if (two) qk_box(cx.k + kBox * D, cx.s + 4 * kBox, cx.valid - kBox, z1);
+        if (two) qk_box(cx.k + kBox * RB, cx.s + 4 * kBox, cx.valid - kBox, z1);
         else z1[0] = z1[1] = z1[2] = z1[3] = -INFINITY;
         float mx = fmaxf(fmaxf(fmaxf(z0[0], z0[1]), fmaxf(z0[2], z0[3])), fmaxf(fmaxf(z1[0], z1[1]), fmaxf(z1[2], z1[3])));
         mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
@@ -560,7 +647,7 @@ struct MmaConsumer {
         }
         m = mn;
         l = l * alpha + (((p0[0] + p0[1]) + (p0[2] + p0[3])) + ((p1[0] + p1[1]) + (p1[2] + p1[3])));
-        if (FMT == INT8) {  // fold the V row scales into P (masked tokens keep p = 0)
+        if (kRowScaled) {  // fold the V row scales into P (masked tokens keep p = 0)
             const uint32_t sv = cx.s + 4 * kTile;
             const float2 a01 = __uint_as_float2(lds64(sv + 8 * c)), a23 = __uint_as_float2(lds64(sv + 32 + 8 * c));
             p0[0] *= a01.x; p0[1] *= a01.y; p0[2] *= a23.x; p0[3] *= a23.y;
@@ -584,7 +671,7 @@ struct MmaConsumer {
         pv_box(cx.v, cx.valid, pb0, pb1, pl0, pl1);
         if (two) {
             p_frags(p1, pb0, pb1, pl0, pl1, psum);
-            pv_box(cx.v + kBox * D, cx.valid - kBox, pb0, pb1, pl0, pl1);
+            pv_box(cx.v + kBox * RB, cx.valid - kBox, pb0, pb1, pl0, pl1);
         }
     }
 
@@ -594,7 +681,7 @@ struct MmaConsumer {
         lq += __shfl_xor_sync(0xFFFFFFFFu, lq, 2);
         if (c == 0 && g < G) f.ml[slot_index(f.hq0 + g, f.nch, f.ch, f.half)] = make_float2(m, lq);
         float bias[2] = {0.f, 0.f};
-        if (FMT == INT8) {  // 1152 * sum(P') of heads 2c and 2c+1
+        if (kBiased) {  // 1152 * sum(P') of heads 2c and 2c+1
             float ps = psum;
             ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 1);
             ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 2);
@@ -628,13 +715,16 @@ __device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
 __device__ __forceinline__ void sts16(uint32_t addr, uint16_t v) {
     asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
 }
+__device__ __forceinline__ void sts8(uint32_t addr, uint8_t v) {
+    asm volatile("st.shared.u8 [%0], %1;" ::"r"(addr), "h"((uint16_t)v) : "memory");
+}
 __device__ __forceinline__ void stsf(uint32_t addr, float v) {
     asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
 // One warp quantizes the newest token's K and V rows (fp16, in shared memory
-// at nkv) exactly as the append kernels do, writes the codes (and INT8 row
-// scales) to the cache row of position `pos`, and patches them into the
+// at nkv) exactly as the append kernels do, writes the codes (and INT8 / INT4
+// row scales) to the cache row of position `pos`, and patches them into the
 // landed stage tile (first token tok0) so this tile's attention sees them.
 // blk < 0: the block id was outside the cache (already recorded); nothing is
 // written.  Lane l handles values D/32 * l ...
@@ -661,19 +751,21 @@ __device__ __noinline__ void append_newest(const uint16_t* nkv, int blk, int pos
 #pragma unroll
     for (int w = 0; w < 2; ++w) {
         uint32_t c = 0;
-        if (FMT == INT8) {
+        if (FMT == INT8 || FMT == INT4) {
+            constexpr float kQmax = FMT == INT4 ? 7.0f : 127.0f;
+            constexpr int kQi = FMT == INT4 ? 7 : 127, kBits = FMT == INT4 ? 4 : 8;
             float amax = 0.f;
 #pragma unroll
             for (int i = 0; i < VPL; ++i) amax = fmaxf(amax, fabsf(x[w][i]));
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-            const float s = __fdiv_rn(amax, 127.0f);
+            const float s = __fdiv_rn(amax, kQmax);
             rs[w] = s;
 #pragma unroll
             for (int i = 0; i < VPL; ++i) {
                 int q = 0;
-                if (s != 0.f) q = max(-127, min(127, __float2int_rn(__fdiv_rn(x[w][i], s))));
-                c |= (uint32_t)(q & 0xFF) << (8 * i);
+                if (s != 0.f) q = max(-kQi, min(kQi, __float2int_rn(__fdiv_rn(x[w][i], s))));
+                c |= (uint32_t)(q & ((1 << kBits) - 1)) << (kBits * i);
             }
         } else {
             float y[VPL];
@@ -684,7 +776,31 @@ __device__ __noinline__ void append_newest(const uint16_t* nkv, int blk, int pos
         }
         code[w] = c;
     }
-    if (blk >= 0) {
+    if (blk >= 0 && FMT == INT4) {  // VPL codes = VPL / 2 bytes per lane, rows unswizzled
+        constexpr int RB = D / 2;
+        const int r = pos - tok0;
+        const uint32_t kb = kt + (r / kBox) * kBox * RB + (r % kBox) * RB;
+        const int BS = a.cache.block_size;
+        const int64_t row = ((int64_t)blk * a.cache.num_kv_heads + kvh) * BS + (pos & (BS - 1));
+        if (D == 128) {
+            sts16(kb + 2 * lane, (uint16_t)code[0]);
+            sts16(kb + tile_bytes + 2 * lane, (uint16_t)code[1]);
+            reinterpret_cast<uint16_t*>(a.cache.k_codes + row * RB)[lane] = (uint16_t)code[0];
+            reinterpret_cast<uint16_t*>(a.cache.v_codes + row * RB)[lane] = (uint16_t)code[1];
+        } else {
+            sts8(kb + lane, (uint8_t)code[0]);
+            sts8(kb + tile_bytes + lane, (uint8_t)code[1]);
+            a.cache.k_codes[row * RB + lane] = (uint8_t)code[0];
+            a.cache.v_codes[row * RB + lane] = (uint8_t)code[1];
+        }
+        if (lane == 0) {
+            stsf(st + 4 * r, rs[0]);
+            stsf(st + 4 * kTile + 4 * r, rs[1]);
+            a.cache.k_scales[row] = rs[0];
+            a.cache.v_scales[row] = rs[1];
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    } else if (blk >= 0) {
         const int r = pos - tok0;  // row in the tile: box r / 16, row r % 16
         const uint32_t kb = kt + (r / kBox) * kBox * D;
         if (D == 128) {
@@ -729,7 +845,9 @@ __global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
     const int B = a.batch, Hkv = a.cache.num_kv_heads, BS = a.cache.block_size;
     const int G = a.num_q_heads / Hkv;
     const bool append = a.k_new != nullptr;
-    const Layout L(D, G, B, FMT == INT8, append);
+    constexpr bool kRowScaled = FMT == INT8 || FMT == INT4;
+    constexpr int RB = row_bytes(FMT, D);
+    const Layout L(RB, D, G, B, kRowScaled, append);
     int* S = reinterpret_cast<int*>(smem + L.scan);
     int* ctx_s = S + B + 1;
     griddep_wait();    // inputs may come from the previous kernel (an append)
@@ -806,11 +924,11 @@ __global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
         prefetch_tmap(&tmv);
     }
     const uint64_t pol = policy_evict_first();
-    const uint32_t box_tx = 2 * kBox * D + (FMT == INT8 ? 2 * kBox * 4 : 0);
+    const uint32_t box_tx = 2 * kBox * RB + (kRowScaled ? 2 * kBox * 4 : 0);
     const uint32_t q_tx = G * D * 2;
 
-    const float s_fp8 = (FMT != INT8 && a.scale) ? __ldg(a.scale) : 1.0f;
-    const float s_out = FMT == INT8 ? 1.0f : s_fp8;
+    const float s_fp8 = (!kRowScaled && a.scale) ? __ldg(a.scale) : 1.0f;
+    const float s_out = kRowScaled ? 1.0f : s_fp8;
     float* ws_acc = a.ws;
     float2* ws_ml = reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(a.ws) +
                                               ws_acc_bytes(B, a.num_q_heads, a.num_chunks, D));
@@ -867,9 +985,9 @@ __global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
                         blk = 0;  // keep the pipeline going on a block that exists
                     }
                     const int row = (blk * Hkv + iw.kvh) * BS + ((tok0 + bx * kBox) & (BS - 1));
-                    tma_load_2d_u32(kt + bx * kBox * D, &tmk, 0, row, fb, pol);
-                    tma_load_2d_u32(kt + L.tile_bytes + bx * kBox * D, &tmv, 0, row, fb, pol);
-                    if (FMT == INT8) {
+                    tma_load_2d_u32(kt + bx * kBox * RB, &tmk, 0, row, fb, pol);
+                    tma_load_2d_u32(kt + L.tile_bytes + bx * kBox * RB, &tmv, 0, row, fb, pol);
+                    if (kRowScaled) {
                         bulk_load_u32(st + bx * kBox * 4, a.cache.k_scales + row, kBox * 4, fb, pol);
                         bulk_load_u32(st + 4 * kTile + bx * kBox * 4, a.cache.v_scales + row, kBox * 4, fb, pol);
                     }
@@ -1027,16 +1145,18 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 
 // 2-D view [rows = blocks * kv-heads * block][head_dim] of one code array;
 // box = 16 rows (one 16-token slice of a paged block).
-bool make_tmap(CUtensorMap* m, void* base, int64_t rows, int D) {
+// rb: bytes per row (head_dim, or head_dim / 2 for INT4); 128-byte rows are
+// loaded with the 128-byte swizzle, narrower ones plain.
+bool make_tmap(CUtensorMap* m, void* base, int64_t rows, int rb) {
     auto enc = get_encode();
     if (!enc) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)D};
-    cuuint32_t box[2] = {(cuuint32_t)D, (cuuint32_t)kBox};
+    cuuint64_t dims[2] = {(cuuint64_t)rb, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)rb};
+    cuuint32_t box[2] = {(cuuint32_t)rb, (cuuint32_t)kBox};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     rb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -1044,8 +1164,8 @@ bool make_tmap(CUtensorMap* m, void* base, int64_t rows, int D) {
 template <int FMT, int D, class Consumer>
 cudaError_t launch_stream(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, cudaStream_t s) {
     auto kern = decode_stream_kernel<FMT, D, Consumer>;
-    const int smem =
-        Layout(D, a.num_q_heads / a.cache.num_kv_heads, a.batch, FMT == INT8, a.k_new != nullptr).total + 1024;
+    const int smem = Layout(row_bytes(FMT, D), D, a.num_q_heads / a.cache.num_kv_heads, a.batch,
+                            FMT == INT8 || FMT == INT4, a.k_new != nullptr).total + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
@@ -1069,13 +1189,16 @@ cudaError_t launch_fmt_d(const CUtensorMap& tk, const CUtensorMap& tv, const Dec
     const int G = a.num_q_heads / a.cache.num_kv_heads;
     cudaError_t e;
     if (a.ev_begin && (e = cudaEventRecord(a.ev_begin, s)) != cudaSuccess) return e;
-    if (a.kernel == kKindSimt) {
-        if (G == 1) e = launch_stream<FMT, D, SimtConsumer<FMT, D, 1>>(tk, tv, a, s);
-        else if (G == 2) e = launch_stream<FMT, D, SimtConsumer<FMT, D, 2>>(tk, tv, a, s);
-        else e = launch_stream<FMT, D, SimtConsumer<FMT, D, 4>>(tk, tv, a, s);
-    } else {
-        e = launch_stream<FMT, D, MmaConsumer<FMT, D>>(tk, tv, a, s);
+    bool simt = false;
+    if constexpr (FMT != INT4) {  // INT4 has the tensor-core consumer only
+        if (a.kernel == kKindSimt) {
+            simt = true;
+            if (G == 1) e = launch_stream<FMT, D, SimtConsumer<FMT, D, 1>>(tk, tv, a, s);
+            else if (G == 2) e = launch_stream<FMT, D, SimtConsumer<FMT, D, 2>>(tk, tv, a, s);
+            else e = launch_stream<FMT, D, SimtConsumer<FMT, D, 4>>(tk, tv, a, s);
+        }
     }
+    if (!simt) e = launch_stream<FMT, D, MmaConsumer<FMT, D>>(tk, tv, a, s);
     if (e != cudaSuccess) return e;
     if (a.ev_end && (e = cudaEventRecord(a.ev_end, s)) != cudaSuccess) return e;
     const int64_t heads = (int64_t)a.batch * a.num_q_heads;
@@ -1094,12 +1217,13 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
     if (a.batch == 0) return cudaSuccess;
     const int64_t rows = (int64_t)a.cache.num_blocks * a.cache.num_kv_heads * a.cache.block_size;
     CUtensorMap tk, tv;
-    if (!make_tmap(&tk, a.cache.k_codes, rows, a.cache.head_dim) ||
-        !make_tmap(&tv, a.cache.v_codes, rows, a.cache.head_dim))
+    const int rb = row_bytes(a.cache.fmt, a.cache.head_dim);
+    if (!make_tmap(&tk, a.cache.k_codes, rows, rb) || !make_tmap(&tv, a.cache.v_codes, rows, rb))
         return cudaErrorInvalidValue;
     switch (a.cache.fmt) {
         case E4M3: return launch_fmt<E4M3>(tk, tv, a, s);
         case E5M2: return launch_fmt<E5M2>(tk, tv, a, s);
+        case INT4: return launch_fmt<INT4>(tk, tv, a, s);
         default: return launch_fmt<INT8>(tk, tv, a, s);
     }
 }

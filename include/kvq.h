@@ -131,8 +131,8 @@ KVQ_API size_t kvq_decode_workspace_size(int32_t batch, int32_t num_q_heads, int
  *     with context 0 gets a zero output.
  *   q-head h reads kv-head h / (num_q_heads / num_kv_heads); num_q_heads must be
  *     a multiple of num_kv_heads and the group size at most 8.
- *   INT4 caches return KVQ_ERR_UNSUPPORTED (decode of INT4 is not built; append,
- *   dequant and prefill attention take them).
+ *   INT4 caches are decoded by the tensor-core kernel (kvq_set_decode_kernel(1)
+ *   with INT4 returns KVQ_ERR_UNSUPPORTED).
  *   batch at most 4096, and batch * num_kv_heads * ceil(max_context_len / 16)
  *     below 2^31 (KVQ_ERR_UNSUPPORTED otherwise).
  *   scale: FP8 per-tensor scale as in kvq_append (NULL = 1.0); ignored for INT8.
@@ -238,7 +238,8 @@ KVQ_API kvq_status kvq_dequant(const kvq_cache* cache, const int64_t* slots, int
                        kvq_stream_t stream);
 
 /* Decode kernel family used by kvq_decode_attention in this process:
- * 0 = automatic (tensor-core kernel), 1 = CUDA-core kernel (group size <= 4),
+ * 0 = automatic (tensor-core kernel), 1 = CUDA-core kernel (group size <= 4,
+ * FP8 and INT8 only),
  * 2 = tensor-core kernel.  A tuning and cross-checking knob; returns the
  * previous value, or -1 for an unknown kind (nothing changes). */
 KVQ_API int32_t kvq_set_decode_kernel(int32_t kind);

@@ -25,7 +25,7 @@ def _lib():
 
 def small(fmt, B, Hq, Hkv, D, BS, ctx, seed=0, outliers=True, scale_rule=None):
     wl = W.Workload(f"t-{fmt}", B, Hq, Hkv, D, BS, fmt, max(ctx), scale_rule or
-                    ("amax" if fmt == "e4m3" else ("row" if fmt == "int8" else "one")),
+                    ("amax" if fmt == "e4m3" else ("row" if fmt in ("int8", "int4") else "one")),
                     outliers=outliers, seed=seed)
     return DeviceWorkload(wl, chunk_tokens=1 << 16, ctx=torch.tensor(ctx, dtype=torch.int32))
 
@@ -40,6 +40,9 @@ CASES = [
     ("int8", 3, 8, 2, 64, 64, [129, 1, 256]),
     ("e4m3", 2, 16, 2, 128, 32, [2050, 700]),
     ("e5m2", 1, 7, 7, 128, 16, [16]),
+    ("int4", 2, 4, 4, 128, 64, [640, 65]),
+    ("int4", 3, 8, 2, 64, 16, [129, 1, 256]),
+    ("int4", 2, 32, 8, 128, 32, [1000, 33]),
 ]
 
 
@@ -48,8 +51,8 @@ CASES = [
 @pytest.mark.parametrize("partition", [0, 64, 256])
 def test_decode_small(case, kernel, partition):
     fmt, B, Hq, Hkv, D, BS, ctx = case
-    if kernel == kvq.KERNEL_SIMT and Hq // Hkv > 4:
-        pytest.skip("CUDA-core kernel covers group size <= 4")
+    if kernel == kvq.KERNEL_SIMT and (Hq // Hkv > 4 or fmt == "int4"):
+        pytest.skip("CUDA-core kernel covers 8-bit codes and group size <= 4")
     dw = small(fmt, B, Hq, Hkv, D, BS, ctx, seed=len(ctx) + D)
     kvq.set_decode_kernel(kernel)
     out = dw.decode(partition_size=partition)
@@ -135,6 +138,7 @@ def test_workspace_too_small_and_empty_batch():
 @pytest.mark.parametrize("name,seqs", [("tiny", [0]), ("llama2-7b", [0, 13, 31]),
                                        ("llama3-8b", [0, 21, 40, 63]),
                                        ("llama2-13b-int8", [0, 77, 127]),
+                                       ("llama2-13b-int4", [0, 64, 127]),
                                        ("llama3-70b", [0, 255])])
 def test_decode_workload_sampled(name, seqs):
     wl = W.WORKLOADS[name]

@@ -1,6 +1,6 @@
 """GPU parity of the decode step that quantizes each sequence's newest K/V row
 into the cache in the same launch (kvq_decode_attention_append): cache bytes,
-INT8 row scales and outputs bit-identical to kvq_append followed by
+INT8 / INT4 row scales and outputs bit-identical to kvq_append followed by
 kvq_decode_attention, and the output within the oracle tolerance on the cache
 the fused call left behind."""
 import numpy as np
@@ -24,7 +24,8 @@ def _lib():
 
 def small(fmt, B, Hq, Hkv, D, BS, ctx, seed):
     wl = W.Workload(f"f-{fmt}", B, Hq, Hkv, D, BS, fmt, max(max(ctx), 1),
-                    "amax" if fmt == "e4m3" else ("row" if fmt == "int8" else "one"), outliers=True, seed=seed)
+                    "amax" if fmt == "e4m3" else ("row" if fmt in ("int8", "int4") else "one"), outliers=True,
+                    seed=seed)
     return DeviceWorkload(wl, chunk_tokens=1 << 16, ctx=torch.tensor(ctx, dtype=torch.int32))
 
 
@@ -79,6 +80,8 @@ CASES = [
     ("int8", 4, 4, 4, 128, 64, [640, 65, 1, 48]),
     ("int8", 3, 8, 2, 64, 64, [129, 0, 256]),
     ("e4m3", 2, 16, 2, 128, 32, [2050, 700]),
+    ("int4", 4, 4, 4, 128, 64, [640, 65, 1, 48]),
+    ("int4", 3, 8, 2, 64, 16, [129, 0, 256]),
 ]
 
 
@@ -87,14 +90,14 @@ CASES = [
 @pytest.mark.parametrize("partition", [0, 64])
 def test_fused_equals_append_then_decode(case, kernel, partition):
     fmt, B, Hq, Hkv, D, BS, ctx = case
-    if kernel == kvq.KERNEL_SIMT and Hq // Hkv > 4:
-        pytest.skip("CUDA-core kernel covers group size <= 4")
+    if kernel == kvq.KERNEL_SIMT and (Hq // Hkv > 4 or fmt == "int4"):
+        pytest.skip("CUDA-core kernel covers 8-bit codes and group size <= 4")
     dw = small(fmt, B, Hq, Hkv, D, BS, ctx, seed=len(ctx) * 31 + D)
     kvq.set_decode_kernel(kernel)
     g = torch.Generator(device="cpu").manual_seed(B * 100 + D)
     k_new = (torch.randn((B, Hkv, D), generator=g) * 2).to(torch.float16).to(dw.device)
     v_new = (torch.randn((B, Hkv, D), generator=g) * 2).to(torch.float16).to(dw.device)
-    if fmt == "int8":
+    if fmt in ("int8", "int4"):
         k_new[0, 0] = 0  # an all-zero row: scale 0, codes 0
     (c1, o1, st1), (c2, o2, st2) = both_paths(dw, k_new, v_new, dw.block_tables, partition)
     assert st1[0] == 0 and st2[0] == 0
@@ -118,12 +121,13 @@ def test_fused_bad_block_id_is_reported_and_not_written():
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
 
 
-@pytest.mark.parametrize("name", ["llama2-7b", "llama3-8b", "llama2-13b-int8"])
+@pytest.mark.parametrize("name", ["llama2-7b", "llama3-8b", "llama2-13b-int8", "llama2-13b-int4"])
 def test_fused_full_size_sampled(name):
     """The benchmark's fused step on a full decode workload: the cache it leaves
     equals kvq_append of the same rows, and sampled sequences' outputs match
     the oracle on that cache."""
     wl = W.WORKLOADS[name]
+    kvq.set_decode_kernel(kvq.KERNEL_AUTO)
     dw = DeviceWorkload(wl)
     cl = dw.lay.context_lens
     k_new, v_new = [], []

@@ -104,13 +104,6 @@ def test_empty_and_validation():
         kvq._check(st, "kvq_prefill_attention")
 
 
-def test_int4_decode_is_not_built():
-    dw = small("int4", 1, 4, 4, 64, 16, [20], seed=2)
-    with pytest.raises(kvq.KvqError) as ei:
-        dw.decode()
-    assert ei.value.status == 2
-
-
 def test_chunk_longer_than_context_is_reported_and_others_computed():
     dw = small("e5m2", 2, 4, 4, 64, 16, [40, 30], seed=13)
     n = torch.tensor([41, 30], dtype=torch.int32)            # sequence 0 claims more queries than tokens
