@@ -37,6 +37,7 @@ METRIC = "quantized-KV decode attention: KV-read GB/s and % of GB300 HBM peak; t
 DEFAULT_WORKLOAD = "llama2-7b"
 L2_BYTES = 129 * 1024 * 1024
 DEFAULT_STEPS = {"tiny": 2000, "llama2-7b": 10000, "llama3-8b": 10000, "llama2-13b-int8": 1000,
+                 "llama2-13b-int4": 2000,
                  "llama3-70b": 300}
 
 
@@ -293,7 +294,8 @@ def cpu_baseline(wl, target_s: float):
     import oracle
     from fp8_int8_quantized_gb300 import workloads as W
     lay = W.Layout(wl)
-    fmt = {"e4m3": oracle.E4M3, "e5m2": oracle.E5M2, "int8": oracle.INT8}[wl.fmt]
+    fmt = {"e4m3": oracle.E4M3, "e5m2": oracle.E5M2, "int8": oracle.INT8,
+           "int4": oracle.INT4}[wl.fmt]
     order = list(range(wl.batch))
 
     def run(seqs):
@@ -528,7 +530,8 @@ def run_kvq(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": {"e4m3": "fp8-e4m3 storage, f16xf16->f32 compute", "e5m2": "fp8-e5m2 storage, f16xf16->f32 compute",
-                  "int8": "int8 storage, f16xf16->f32 compute"}[wl.fmt],
+                  "int8": "int8 storage, f16xf16->f32 compute",
+                  "int4": "int4 storage (two codes per byte), f16xf16->f32 compute"}[wl.fmt],
         "data": "synthetic (seeded N(0,1) fp16 K/V/Q, shuffled block tables)",
         "config": {"workload": wl.name, "description": wl.description, "batch": wl.batch,
                    "num_q_heads": wl.num_q_heads, "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
@@ -635,7 +638,8 @@ def prefill_cpu_baseline(wl, n_chunk: int, target_s: float):
     import oracle
     from fp8_int8_quantized_gb300 import workloads as W
     lay = W.Layout(wl)
-    fmt = {"e4m3": oracle.E4M3, "e5m2": oracle.E5M2, "int8": oracle.INT8}[wl.fmt]
+    fmt = {"e4m3": oracle.E4M3, "e5m2": oracle.E5M2, "int8": oracle.INT8,
+           "int4": oracle.INT4}[wl.fmt]
     bs, c = wl.block_size, int(lay.context_lens[0])
     nb = (c + bs - 1) // bs
     cache = oracle.Cache(nb, wl.num_kv_heads, bs, wl.head_dim, fmt)
@@ -773,7 +777,8 @@ def run_prefill_bench(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": {"e4m3": "fp8-e4m3 storage, f16xf16->f32 compute", "e5m2": "fp8-e5m2 storage, f16xf16->f32 compute",
-                  "int8": "int8 storage, f16xf16->f32 compute"}[wl.fmt],
+                  "int8": "int8 storage, f16xf16->f32 compute",
+                  "int4": "int4 storage (two codes per byte), f16xf16->f32 compute"}[wl.fmt],
         "data": "synthetic (seeded N(0,1) fp16 K/V/Q, shuffled block tables)",
         "config": {"workload": wl.name + "-prefill", "description": wl.description, "batch": wl.batch,
                    "num_q_heads": wl.num_q_heads, "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
@@ -820,7 +825,8 @@ def run_reference(args):
     from fp8_int8_quantized_gb300 import workloads as W
     wl = W.WORKLOADS[args.workload]
     lay = W.Layout(wl)
-    fmt = {"e4m3": oracle.E4M3, "e5m2": oracle.E5M2, "int8": oracle.INT8}[wl.fmt]
+    fmt = {"e4m3": oracle.E4M3, "e5m2": oracle.E5M2, "int8": oracle.INT8,
+           "int4": oracle.INT4}[wl.fmt]
     bs = wl.block_size
     step_tok = wl.append_chunk if wl.append_chunk else 1
     K = args.steps or 5

@@ -9,7 +9,7 @@ per sequence and q-head, computed here with plain fp32 torch operations.
 What this measures is the error the cache format itself introduces -- the
 accuracy question of "Accelerating Inference with FP8 KV Cache" ("FP8 E4M3 KV
 Cache": with a calibrated scale or the 1.0 default) and of "[Feature] TurboMind
-support W8A8 or FP8 KV Cache" (online INT8) -- not the kernels' rounding, which
+support W8A8 or FP8 KV Cache" (online INT8, and INT4) -- not the kernels' rounding, which
 the parity tests bound far below it.
 
     python -m fp8_int8_quantized_gb300.quant_error [--workload NAME] [--batch B] [--json]
@@ -27,8 +27,9 @@ import fp8_int8_quantized_gb300 as kvq
 from fp8_int8_quantized_gb300 import workloads as W
 
 # (format, scale rule): E4M3 / E5M2 with the amax/max calibration scale or
-# the 1.0 default, INT8 with its own scale per (token, kv-head) row
-VARIANTS = [("e4m3", "amax"), ("e4m3", "one"), ("e5m2", "amax"), ("e5m2", "one"), ("int8", "row")]
+# the 1.0 default, INT8 and INT4 with their own scale per (token, kv-head) row
+VARIANTS = [("e4m3", "amax"), ("e4m3", "one"), ("e5m2", "amax"), ("e5m2", "one"), ("int8", "row"),
+            ("int4", "row")]
 WINDOW_TOKENS = 1 << 19  # generation windows (values depend on the window start)
 
 
