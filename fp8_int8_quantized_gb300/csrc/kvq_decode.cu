@@ -151,12 +151,20 @@ __device__ __forceinline__ uint2 lds64(uint32_t a) {
     asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(a));
     return r;
 }
-// f16x2 of 1032 + code (code + 8 in the low mantissa bits of 1024) -> the exact codes
-__device__ __forceinline__ uint32_t hsub1032(uint32_t h) {
-    const __half2 off = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
-    __half2 v = *reinterpret_cast<__half2*>(&h);
-    v = __hsub2(v, off);
-    return *reinterpret_cast<uint32_t*>(&v);
+// Eight packed INT4 codes (one 32-bit word; byte i holds channel 2i in its low
+// nibble and 2i+1 in its high nibble) -> four f16x2 words of the fp16
+// subnormals (code + 8) * 2^-24 (exact: XOR 0x8 turns each nibble into code +
+// 8, which becomes the mantissa of a subnormal).  Word i holds channels 2i, 2i+1.
+__device__ __forceinline__ void int4x8_subnormal(uint32_t w, uint32_t (&h)[4]) {
+    const uint32_t x = w ^ 0x88888888u;
+    const uint32_t lo = x & 0x0F0F0F0Fu;          // channels 0, 2, 4, 6
+    const uint32_t hi = (x >> 4) & 0x0F0F0F0Fu;   // channels 1, 3, 5, 7
+    const uint32_t a = prmt(lo, hi, 0x5410u);     // [c0, c2, c1, c3]
+    const uint32_t b = prmt(lo, hi, 0x7632u);     // [c4, c6, c5, c7]
+    h[0] = prmt(a, 0u, 0x4240u);                  // c0, c1
+    h[1] = prmt(a, 0u, 0x4341u);                  // c2, c3
+    h[2] = prmt(b, 0u, 0x4240u);                  // c4, c5
+    h[3] = prmt(b, 0u, 0x4341u);                  // c6, c7
 }
 
 __device__ __forceinline__ uint32_t lds32(uint32_t a) {
@@ -361,14 +369,16 @@ struct MmaConsumer {
     static constexpr int VW = I4 ? DV / 8 : DV / 4;
     static constexpr int MT = D / 16;   // m-tiles of PV (head_dim / 16)
     static constexpr int kMinCtas = kMinBlocks;
-    // INT8 codes enter the tensor cores as fp16 1152 + code (exact); the
-    // constant is taken out again: 1152 * sum(q) from each logit, 1152 *
-    // sum(P') from each output.  INT4 codes are converted to their exact fp16
-    // values first: their row scales are 18x larger than INT8's, and the
-    // accumulation error of biased sums (both the logits and the outputs; a
-    // measured 2.2e-3 relative with a biased V alone) would reach the tolerance.
-    static constexpr bool kBiased = FMT == INT8;
-    static constexpr float kBias = 1152.f;
+    // INT8 codes enter the tensor cores as fp16 1152 + code (exact); INT4 codes
+    // as the fp16 subnormal (code + 8) * 2^-24 (exact, built by placing the
+    // offset nibble in the low mantissa bits).  The constant is taken out
+    // again: bias * sum(q) from each logit, bias * sum(P') from each output,
+    // and INT4 results are multiplied back by 2^24.  The INT4 bias is small
+    // (8 against codes up to 7): INT4 row scales are 18x INT8's, and a bias of
+    // 1032 left accumulation errors near the tolerance.
+    static constexpr bool kBiased = kRowScaled;
+    static constexpr float kUnit = I4 ? 5.9604644775390625e-08f : 1.f;   // operand value of one code step
+    static constexpr float kBias = I4 ? 8.f * kUnit : 1152.f;            // operand - code * kUnit
     uint32_t qa[2 * KS];
     float acc[MT][4];
     float m, l;
@@ -499,7 +509,7 @@ struct MmaConsumer {
 #pragma unroll
                 for (int w = 0; w < KW; ++w) {
                     uint32_t h[4];
-                    int4x8_to_f16(kw[w], h);
+                    int4x8_subnormal(kw[w], h);
                     if (hb == 0) {
                         mma_16816(sA, qa[4 * w], 0u, qa[4 * w + 1], 0u, h[0], h[1]);
                         mma_16816(sA, qa[4 * w + 2], 0u, qa[4 * w + 3], 0u, h[2], h[3]);
@@ -519,13 +529,14 @@ struct MmaConsumer {
                 else mma_16816(sB, qa[2 * j], 0u, qa[2 * j + 1], 0u, b0, b1);
             }
         }
-        if (kRowScaled) {  // remove the operand bias (INT8), then apply the K row scales
-            const float corr = kBiased ? kBias * qsum : 0.f;
+        if (kRowScaled) {  // remove the operand bias, then apply the K row scales
+            const float corr = kBias * qsum;
+            const float ks = qk_scale / kUnit;
             const float2 k01 = __uint_as_float2(lds64(sk + 8 * c)), k23 = __uint_as_float2(lds64(sk + 32 + 8 * c));
-            z[0] = (sA[0] - corr) * (qk_scale * k01.x);
-            z[1] = (sA[1] - corr) * (qk_scale * k01.y);
-            z[2] = (sB[0] - corr) * (qk_scale * k23.x);
-            z[3] = (sB[1] - corr) * (qk_scale * k23.y);
+            z[0] = (sA[0] - corr) * (ks * k01.x);
+            z[1] = (sA[1] - corr) * (ks * k01.y);
+            z[2] = (sB[0] - corr) * (ks * k23.x);
+            z[3] = (sB[1] - corr) * (ks * k23.y);
         } else {
             z[0] = sA[0] * qk_scale; z[1] = sA[1] * qk_scale; z[2] = sB[0] * qk_scale; z[3] = sB[1] * qk_scale;
         }
@@ -572,11 +583,11 @@ struct MmaConsumer {
                 for (int bb = 0; bb < 4; ++bb) {
                     const int i = 4 * w + bb;
                     const uint32_t sel = (bb & 1) ? 0x4342u : 0x4140u;
-                    // fp16 1032 + code, then the exact code
-                    const uint32_t a0 = hsub1032(prmt(bb < 2 ? l01a : l01b, 0x64646464u, sel));
-                    const uint32_t a1 = hsub1032(prmt(bb < 2 ? h01a : h01b, 0x64646464u, sel));
-                    const uint32_t a2 = hsub1032(prmt(bb < 2 ? l23a : l23b, 0x64646464u, sel));
-                    const uint32_t a3 = hsub1032(prmt(bb < 2 ? h23a : h23b, 0x64646464u, sel));
+                    // fp16 subnormals (code + 8) * 2^-24; the bias leaves with psum at the flush
+                    const uint32_t a0 = prmt(bb < 2 ? l01a : l01b, 0u, sel);
+                    const uint32_t a1 = prmt(bb < 2 ? h01a : h01b, 0u, sel);
+                    const uint32_t a2 = prmt(bb < 2 ? l23a : l23b, 0u, sel);
+                    const uint32_t a3 = prmt(bb < 2 ? h23a : h23b, 0u, sel);
                     mma_16816(acc[i], a0, a1, a2, a3, pb0, pb1);
                     mma_16816(acc[i], a0, a1, a2, a3, pl0, pl1);
                 }
@@ -682,7 +693,7 @@ struct MmaConsumer {
         lq += __shfl_xor_sync(0xFFFFFFFFu, lq, 2);
         if (c == 0 && g < G) f.ml[slot_index(f.hq0 + g, f.nch, f.ch, f.half)] = make_float2(m, lq);
         float bias[2] = {0.f, 0.f};
-        if (kBiased) {  // 1152 * sum(P') of heads 2c and 2c+1
+        if (kBiased) {  // bias * sum(P') of heads 2c and 2c+1
             float ps = psum;
             ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 1);
             ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 2);
@@ -696,11 +707,12 @@ struct MmaConsumer {
             if (h >= G) continue;
             float* dst = f.acc + slot_index(f.hq0 + h, f.nch, f.ch, f.half) * D + DV * g;
             const float bs = bias[e];
+            const float so = f.s_out / kUnit;
 #pragma unroll
             for (int i = 0; i < MT; i += 2)
                 *reinterpret_cast<float4*>(dst + 2 * i) =
-                    make_float4((acc[i][e] - bs) * f.s_out, (acc[i][2 + e] - bs) * f.s_out,
-                                (acc[i + 1][e] - bs) * f.s_out, (acc[i + 1][2 + e] - bs) * f.s_out);
+                    make_float4((acc[i][e] - bs) * so, (acc[i][2 + e] - bs) * so,
+                                (acc[i + 1][e] - bs) * so, (acc[i + 1][2 + e] - bs) * so);
         }
     }
     __device__ void flush_empty(const Flush& f) {
