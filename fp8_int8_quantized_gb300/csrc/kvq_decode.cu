@@ -151,22 +151,6 @@ __device__ __forceinline__ uint2 lds64(uint32_t a) {
     asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(a));
     return r;
 }
-// Eight packed INT4 codes (one 32-bit word; byte i holds channel 2i in its low
-// nibble and 2i+1 in its high nibble) -> four f16x2 words of the fp16
-// subnormals (code + 8) * 2^-24 (exact: XOR 0x8 turns each nibble into code +
-// 8, which becomes the mantissa of a subnormal).  Word i holds channels 2i, 2i+1.
-__device__ __forceinline__ void int4x8_subnormal(uint32_t w, uint32_t (&h)[4]) {
-    const uint32_t x = w ^ 0x88888888u;
-    const uint32_t lo = x & 0x0F0F0F0Fu;          // channels 0, 2, 4, 6
-    const uint32_t hi = (x >> 4) & 0x0F0F0F0Fu;   // channels 1, 3, 5, 7
-    const uint32_t a = prmt(lo, hi, 0x5410u);     // [c0, c2, c1, c3]
-    const uint32_t b = prmt(lo, hi, 0x7632u);     // [c4, c6, c5, c7]
-    h[0] = prmt(a, 0u, 0x4240u);                  // c0, c1
-    h[1] = prmt(a, 0u, 0x4341u);                  // c2, c3
-    h[2] = prmt(b, 0u, 0x4240u);                  // c4, c5
-    h[3] = prmt(b, 0u, 0x4341u);                  // c6, c7
-}
-
 __device__ __forceinline__ uint32_t lds32(uint32_t a) {
     uint32_t r;
     asm volatile("ld.shared.b32 %0, [%1];" : "=r"(r) : "r"(a));
@@ -370,12 +354,16 @@ struct MmaConsumer {
     static constexpr int MT = D / 16;   // m-tiles of PV (head_dim / 16)
     static constexpr int kMinCtas = kMinBlocks;
     // INT8 codes enter the tensor cores as fp16 1152 + code (exact); INT4 codes
-    // as the fp16 subnormal (code + 8) * 2^-24 (exact, built by placing the
-    // offset nibble in the low mantissa bits).  The constant is taken out
-    // again: bias * sum(q) from each logit, bias * sum(P') from each output,
-    // and INT4 results are multiplied back by 2^24.  The INT4 bias is small
-    // (8 against codes up to 7): INT4 row scales are 18x INT8's, and a bias of
-    // 1032 left accumulation errors near the tolerance.
+    // as the fp16 subnormal (code + 8) * 2^-24 (exact: the offset nibble is the
+    // mantissa), or 16x that where the nibble is left in mantissa bits 4..7 --
+    // the high nibble of a byte is masked in place, which saves the shifts and
+    // byte moves of a full expansion.  The matching query values are fed
+    // divided by 16 (QK), and the output rows of such head dims are divided by
+    // 16 at the flush (PV).  The constant is taken out again: bias * sum(q)
+    // from each logit, bias * sum(P') from each output, and INT4 results are
+    // multiplied back by 2^24.  The INT4 bias is small (8 against codes up to
+    // 7): INT4 row scales are 18x INT8's, and a bias of 1032 left accumulation
+    // errors near the tolerance.
     static constexpr bool kBiased = kRowScaled;
     static constexpr float kUnit = I4 ? 5.9604644775390625e-08f : 1.f;   // operand value of one code step
     static constexpr float kBias = I4 ? 8.f * kUnit : 1152.f;            // operand - code * kUnit
@@ -430,12 +418,23 @@ struct MmaConsumer {
 #pragma unroll
             for (int i = 0; i < 2 * KS; ++i) qa[i] = 0u;
         }
-        if (kBiased) {
+        if (I4) {  // per 8 dims: [q0, q5/16] [q1/16, q4] [q2, q7/16] [q3/16, q6], the K operand order
+#pragma unroll
+            for (int w = 0; w < KW; ++w) {
+                const float2 q01 = f16x2_to_f32x2(qa[4 * w]), q23 = f16x2_to_f32x2(qa[4 * w + 1]);
+                const float2 q45 = f16x2_to_f32x2(qa[4 * w + 2]), q67 = f16x2_to_f32x2(qa[4 * w + 3]);
+                qa[4 * w] = pack_f16x2(q01.x, q45.y * 0.0625f);
+                qa[4 * w + 1] = pack_f16x2(q01.y * 0.0625f, q45.x);
+                qa[4 * w + 2] = pack_f16x2(q23.x, q67.y * 0.0625f);
+                qa[4 * w + 3] = pack_f16x2(q23.y * 0.0625f, q67.x);
+            }
+        }
+        if (kBiased) {  // sum of q as fed times each operand's step (16 for the divided values)
             float sq = 0.f;
 #pragma unroll
             for (int i = 0; i < 2 * KS; ++i) {
                 const float2 v = f16x2_to_f32x2(qa[i]);
-                sq += v.x + v.y;
+                sq += I4 ? ((i & 1) ? 16.f * v.x + v.y : v.x + 16.f * v.y) : v.x + v.y;
             }
             sq += __shfl_xor_sync(0xFFFFFFFFu, sq, 1);
             sq += __shfl_xor_sync(0xFFFFFFFFu, sq, 2);
@@ -508,25 +507,28 @@ struct MmaConsumer {
             if (I4) {  // word w: codes 8w .. 8w+7 = k-steps 2w and 2w+1
 #pragma unroll
                 for (int w = 0; w < KW; ++w) {
-                    uint32_t h[4];
-                    int4x8_subnormal(kw[w], h);
+                    // byte i holds dims 2i (low nibble) and 2i+1 (high); masked in place:
+                    // h0 = [d0, 16 d5], h1 = [16 d1, d4], h2 = [d2, 16 d7], h3 = [16 d3, d6]
+                    const uint32_t x = kw[w], y = kw[w] >> 8;
+                    const uint32_t h0 = (x & 0x00F0000Fu) ^ 0x00800008u, h1 = (x & 0x000F00F0u) ^ 0x00080080u;
+                    const uint32_t h2 = (y & 0x00F0000Fu) ^ 0x00800008u, h3 = (y & 0x000F00F0u) ^ 0x00080080u;
                     if (hb == 0) {
-                        mma_16816(sA, qa[4 * w], 0u, qa[4 * w + 1], 0u, h[0], h[1]);
-                        mma_16816(sA, qa[4 * w + 2], 0u, qa[4 * w + 3], 0u, h[2], h[3]);
+                        mma_16816(sA, qa[4 * w], 0u, qa[4 * w + 1], 0u, h0, h1);
+                        mma_16816(sA, qa[4 * w + 2], 0u, qa[4 * w + 3], 0u, h2, h3);
                     } else {
-                        mma_16816(sB, qa[4 * w], 0u, qa[4 * w + 1], 0u, h[0], h[1]);
-                        mma_16816(sB, qa[4 * w + 2], 0u, qa[4 * w + 3], 0u, h[2], h[3]);
+                        mma_16816(sB, qa[4 * w], 0u, qa[4 * w + 1], 0u, h0, h1);
+                        mma_16816(sB, qa[4 * w + 2], 0u, qa[4 * w + 3], 0u, h2, h3);
                     }
                 }
-                continue;
-            }
+            } else {
 #pragma unroll
-            for (int j = 0; j < KS; ++j) {
-                uint32_t b0, b1;
-                if (FMT == INT8) int8_biased(kw[j], b0, b1);
-                else dec_fp8x4<FMT>(kw[j], b0, b1);
-                if (hb == 0) mma_16816(sA, qa[2 * j], 0u, qa[2 * j + 1], 0u, b0, b1);
-                else mma_16816(sB, qa[2 * j], 0u, qa[2 * j + 1], 0u, b0, b1);
+                for (int j = 0; j < KS; ++j) {
+                    uint32_t b0, b1;
+                    if (FMT == INT8) int8_biased(kw[j < KW ? j : 0], b0, b1);
+                    else dec_fp8x4<FMT>(kw[j < KW ? j : 0], b0, b1);
+                    if (hb == 0) mma_16816(sA, qa[2 * j], 0u, qa[2 * j + 1], 0u, b0, b1);
+                    else mma_16816(sB, qa[2 * j], 0u, qa[2 * j + 1], 0u, b0, b1);
+                }
             }
         }
         if (kRowScaled) {  // remove the operand bias, then apply the K row scales
@@ -569,25 +571,16 @@ struct MmaConsumer {
         if (I4) {  // word w of each row: codes 8w .. 8w+7 = m-tiles 4w .. 4w+3 (dims 2i | 2i+1 = low | high nibble)
 #pragma unroll
             for (int w = 0; w < VW; ++w) {
-                const uint32_t x0 = v0[w] ^ 0x88888888u, x1 = v1[w] ^ 0x88888888u;  // code + 8 per nibble
-                const uint32_t x2 = v2[w] ^ 0x88888888u, x3 = v3[w] ^ 0x88888888u;
-                const uint32_t m4 = 0x0F0F0F0Fu;
-                // [row 2c, row 2c+1] low (dim 2i) / high (dim 2i+1) nibbles of bytes 0,1 and 2,3
-                const uint32_t l01a = prmt(x0 & m4, x1 & m4, 0x5140u), l01b = prmt(x0 & m4, x1 & m4, 0x7362u);
-                const uint32_t h01a = prmt((x0 >> 4) & m4, (x1 >> 4) & m4, 0x5140u);
-                const uint32_t h01b = prmt((x0 >> 4) & m4, (x1 >> 4) & m4, 0x7362u);
-                const uint32_t l23a = prmt(x2 & m4, x3 & m4, 0x5140u), l23b = prmt(x2 & m4, x3 & m4, 0x7362u);
-                const uint32_t h23a = prmt((x2 >> 4) & m4, (x3 >> 4) & m4, 0x5140u);
-                const uint32_t h23b = prmt((x2 >> 4) & m4, (x3 >> 4) & m4, 0x7362u);
 #pragma unroll
                 for (int bb = 0; bb < 4; ++bb) {
+                    // byte bb of rows (2c, 2c+1) and (8+2c, 9+2c) in bytes 0 and 2, then the
+                    // nibbles masked in place: dim 2i as the subnormal (code + 8) * 2^-24,
+                    // dim 2i+1 as 16x that (rows g+8 of the m-tile, divided out at the flush)
+                    const uint32_t sel = 0x4400u + 0x1111u * bb;  // bytes [r.bb, r.bb, r'.bb, r'.bb]
+                    const uint32_t u01 = prmt(v0[w], v1[w], sel), u23 = prmt(v2[w], v3[w], sel);
+                    const uint32_t a0 = (u01 & 0x000F000Fu) ^ 0x00080008u, a1 = (u01 & 0x00F000F0u) ^ 0x00800080u;
+                    const uint32_t a2 = (u23 & 0x000F000Fu) ^ 0x00080008u, a3 = (u23 & 0x00F000F0u) ^ 0x00800080u;
                     const int i = 4 * w + bb;
-                    const uint32_t sel = (bb & 1) ? 0x4342u : 0x4140u;
-                    // fp16 subnormals (code + 8) * 2^-24; the bias leaves with psum at the flush
-                    const uint32_t a0 = prmt(bb < 2 ? l01a : l01b, 0u, sel);
-                    const uint32_t a1 = prmt(bb < 2 ? h01a : h01b, 0u, sel);
-                    const uint32_t a2 = prmt(bb < 2 ? l23a : l23b, 0u, sel);
-                    const uint32_t a3 = prmt(bb < 2 ? h23a : h23b, 0u, sel);
                     mma_16816(acc[i], a0, a1, a2, a3, pb0, pb1);
                     mma_16816(acc[i], a0, a1, a2, a3, pl0, pl1);
                 }
@@ -708,11 +701,13 @@ struct MmaConsumer {
             float* dst = f.acc + slot_index(f.hq0 + h, f.nch, f.ch, f.half) * D + DV * g;
             const float bs = bias[e];
             const float so = f.s_out / kUnit;
+            // INT4: the odd dims (rows g+8) were fed as 16x operands, bias included
+            const float bs1 = I4 ? 16.f * bs : bs, so1 = I4 ? so * 0.0625f : so;
 #pragma unroll
             for (int i = 0; i < MT; i += 2)
                 *reinterpret_cast<float4*>(dst + 2 * i) =
-                    make_float4((acc[i][e] - bs) * so, (acc[i][2 + e] - bs) * so,
-                                (acc[i + 1][e] - bs) * so, (acc[i + 1][2 + e] - bs) * so);
+                    make_float4((acc[i][e] - bs) * so, (acc[i][2 + e] - bs1) * so1,
+                                (acc[i + 1][e] - bs) * so, (acc[i + 1][2 + e] - bs1) * so1);
         }
     }
     __device__ void flush_empty(const Flush& f) {
