@@ -15,6 +15,9 @@ Sources, by page title and section:
     ("FP8 E4M3 KV Cache").
   * "[Feature] TurboMind support W8A8 or FP8 KV Cache" (lmdeploy issue 1463):
     online KV-cache INT8 (and the INT4 implementation named beside it).
+  * "[QST] Scale factors and benchmarks" (QQQ issue page): group quantization
+    named for a 4-bit KV cache; read here as INT8 / INT4 with one scale per
+    group of ``group`` consecutive channels of a row.
 
 Parity pins for every function here live in ``tests/test_oracle_*.py``.
 """
@@ -72,19 +75,20 @@ def _load():
         lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
         lib.oracle_append.restype = ctypes.c_int
         lib.oracle_append.argtypes = [P, P, i64, ctypes.c_int, ctypes.c_int, P, P, P, P, P,
-                                      i64, ctypes.c_int, ctypes.c_int, f32]
+                                      i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, f32]
         lib.oracle_dequant.restype = ctypes.c_int
         lib.oracle_dequant.argtypes = [P, P, P, P, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                       ctypes.c_int, P, i64, f32, P, P]
+                                       ctypes.c_int, ctypes.c_int, P, i64, f32, P, P]
         lib.oracle_decode_attention.restype = ctypes.c_int
         lib.oracle_decode_attention.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                 P, P, P, P, i64, ctypes.c_int, ctypes.c_int,
-                                                ctypes.c_int, P, ctypes.c_int, P, f32, f64,
-                                                P, P, i64]
+                                                ctypes.c_int, ctypes.c_int, P, ctypes.c_int, P, f32,
+                                                f64, P, P, i64]
         lib.oracle_prefill_attention.restype = ctypes.c_int
         lib.oracle_prefill_attention.argtypes = [P, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                  P, P, P, P, i64, ctypes.c_int, ctypes.c_int,
-                                                 ctypes.c_int, P, ctypes.c_int, P, P, f32, f64, P]
+                                                 ctypes.c_int, ctypes.c_int, P, ctypes.c_int, P, P, f32,
+                                                 f64, P]
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_init()
         _lib = lib
@@ -154,17 +158,24 @@ def int8_quant_row(x) -> tuple[np.ndarray, np.float32]:
 
 class Cache:
     """Host copy of a paged cache: codes [NB][Hkv][BS][D] ([D / 2] packed bytes for
-    INT4), INT8 / INT4 row scales [NB][Hkv][BS]."""
+    INT4); INT8 / INT4 scales [NB][Hkv][BS] (one per row, group 0) or
+    [NB][Hkv][BS][D / group] (one per group of ``group`` channels)."""
 
     def __init__(self, num_blocks, num_kv_heads, block_size, head_dim, fmt, fill=0xA5,
-                 k_codes=None, v_codes=None, k_scales=None, v_scales=None):
+                 k_codes=None, v_codes=None, k_scales=None, v_scales=None, group=0):
         self.num_blocks, self.num_kv_heads = num_blocks, num_kv_heads
         self.block_size, self.head_dim, self.fmt = block_size, head_dim, fmt
+        self.group = int(group)
+        if self.group and (fmt not in ROW_SCALED or head_dim % self.group
+                           or (fmt == INT4 and self.group % 2)):
+            raise ValueError(f"group {group} not allowed for format {fmt}, head_dim {head_dim}")
         shape = (num_blocks, num_kv_heads, block_size, head_dim // 2 if fmt == INT4 else head_dim)
         self.k_codes = k_codes if k_codes is not None else np.full(shape, fill, np.uint8)
         self.v_codes = v_codes if v_codes is not None else np.full(shape, fill, np.uint8)
         if fmt in ROW_SCALED:
             sshape = (num_blocks, num_kv_heads, block_size)
+            if self.group:
+                sshape += (head_dim // self.group,)
             self.k_scales = k_scales if k_scales is not None else np.full(sshape, np.nan, np.float32)
             self.v_scales = v_scales if v_scales is not None else np.full(sshape, np.nan, np.float32)
         else:
@@ -173,6 +184,11 @@ class Cache:
             _need(a, np.uint8, n)
             if a.shape != shape:
                 raise ValueError(f"{n}: shape {a.shape} != {shape}")
+        if fmt in ROW_SCALED:
+            for a, n in ((self.k_scales, "k_scales"), (self.v_scales, "v_scales")):
+                _need(a, np.float32, n)
+                if a.size != int(np.prod(sshape)):
+                    raise ValueError(f"{n}: {a.size} scales, expected shape {sshape}")
 
 
 def append(k, v, slot_mapping, cache: Cache, scale: float | None = None) -> None:
@@ -186,7 +202,7 @@ def append(k, v, slot_mapping, cache: Cache, scale: float | None = None) -> None
                                cache.num_kv_heads, cache.head_dim, _ptr(slots),
                                _ptr(cache.k_codes), _ptr(cache.v_codes),
                                _ptr(cache.k_scales), _ptr(cache.v_scales),
-                               cache.num_blocks, cache.block_size, cache.fmt, s)
+                               cache.num_blocks, cache.block_size, cache.fmt, cache.group, s)
     if rc != 0:
         raise IndexError("slot_mapping holds a slot outside the cache")
 
@@ -200,7 +216,7 @@ def dequant(cache: Cache, slots, scale: float | None = None):
     s = np.float32(1.0 if scale is None else scale)
     rc = _load().oracle_dequant(_ptr(cache.k_codes), _ptr(cache.v_codes), _ptr(cache.k_scales),
                                 _ptr(cache.v_scales), cache.num_blocks, cache.block_size,
-                                cache.num_kv_heads, cache.head_dim, cache.fmt, _ptr(slots), n, s,
+                                cache.num_kv_heads, cache.head_dim, cache.fmt, cache.group, _ptr(slots), n, s,
                                 _ptr(ok), _ptr(ov))
     if rc != 0:
         raise IndexError("slot outside the cache")
@@ -228,8 +244,8 @@ def decode_attention(q, cache: Cache, block_tables, context_lens, scale: float |
     rc = _load().oracle_decode_attention(_ptr(q.view(np.uint16)), B, Hq, D, _ptr(cache.k_codes),
                                          _ptr(cache.v_codes), _ptr(cache.k_scales),
                                          _ptr(cache.v_scales), cache.num_blocks, cache.block_size,
-                                         cache.num_kv_heads, cache.fmt, _ptr(bt), bt.shape[1],
-                                         _ptr(cl), s, sm, _ptr(out), _ptr(w), wstride)
+                                         cache.num_kv_heads, cache.fmt, cache.group, _ptr(bt),
+                                         bt.shape[1], _ptr(cl), s, sm, _ptr(out), _ptr(w), wstride)
     if rc != 0:
         raise IndexError("block table / context length outside the cache")
     return (out, w) if return_weights else out
@@ -259,8 +275,8 @@ def prefill_attention(q, cache: Cache, block_tables, context_lens, query_start,
     rc = _load().oracle_prefill_attention(_ptr(q.view(np.uint16)), Tq, B, Hq, D, _ptr(cache.k_codes),
                                           _ptr(cache.v_codes), _ptr(cache.k_scales),
                                           _ptr(cache.v_scales), cache.num_blocks, cache.block_size,
-                                          cache.num_kv_heads, cache.fmt, _ptr(bt), bt.shape[1],
-                                          _ptr(cl), _ptr(qs), s, sm, _ptr(out))
+                                          cache.num_kv_heads, cache.fmt, cache.group, _ptr(bt),
+                                          bt.shape[1], _ptr(cl), _ptr(qs), s, sm, _ptr(out))
     if rc != 0:
         raise IndexError("chunk longer than its context, or block table / context outside the cache")
     return out

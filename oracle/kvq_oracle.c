@@ -29,6 +29,11 @@
  *  - INT4 is the same with 4 bits: s = fl32(amax / 7), q in [-7, 7], two codes
  *    per byte (channel 2i in the low nibble, 2i+1 in the high nibble, 4-bit
  *    two's complement), so a cached row is D / 2 bytes;
+ *  - per-group INT8 / INT4 (group quantization, named on the QQQ page "Scale
+ *    factors and benchmarks" for a 4-bit KV cache): the row is cut into D / g
+ *    groups of g consecutive channels, and each group is quantized exactly as a
+ *    row is above (its own amax and fp32 scale); g = 0 or D is the per-row
+ *    format.  Scales are stored [NB][Hkv][BS][D / g];
  *  - attention: logits l_t = sm_scale * <q, k_t> over all t < context_len,
  *    softmax, out = sum_t w_t v_t; q-head h reads kv-head h / (Hq / Hkv);
  *    context_len 0 gives zeros;
@@ -223,22 +228,44 @@ static int int4_code(const uint8_t* row, int d) {
 /* Bytes of one cached (token, kv-head) row. */
 static int row_bytes(int fmt, int D) { return fmt == ORC_INT4 ? D / 2 : D; }
 
-/* Formats that carry one scale per (token, kv-head) row. */
+/* Formats that carry fp32 scales per (token, kv-head) row (one, or one per group). */
 static int row_scaled(int fmt) { return fmt == ORC_INT8 || fmt == ORC_INT4; }
+
+/* Channels per scale of a row-scaled format: group (0 = the whole row). */
+static int group_channels(int D, int group) { return group > 0 ? group : D; }
+
+/* A valid group for the format and head_dim: 0, or a divisor of D (even for INT4). */
+static int group_ok(int fmt, int D, int group) {
+    if (group == 0) return 1;
+    if (!row_scaled(fmt) || group < 0 || D % group != 0) return 0;
+    return fmt != ORC_INT4 || group % 2 == 0;
+}
+
+/* The scale of channel d of cached row `row`: the per-tensor scale for FP8,
+ * else the row's scale of the group holding d. */
+static float scale_of(int fmt, const float* scales, size_t row, int D, int group, int d, float scale) {
+    if (!row_scaled(fmt)) return scale;
+    const int gc = group_channels(D, group);
+    return scales[row * (size_t)(D / gc) + (size_t)(d / gc)];
+}
 
 /* -------------------------------------------------------------- append ---- */
 
 /* Quantize-on-write.  k, v: fp16 bits [T][Hkv][D].  The paged cache holds codes
  * [NB][Hkv][BS][D] (u8 FP8 / i8 INT8; [D / 2] packed bytes for INT4) and, for
- * INT8 and INT4, scales [NB][Hkv][BS].
+ * INT8 and INT4, scales [NB][Hkv][BS][D / g] (g = group channels, the whole
+ * row when group is 0).
  * Token t goes to block slot[t] / BS, row slot[t] % BS; slot -1 is skipped.
  * scale: per-tensor fp32 scale (FP8 only; [TGI] default 1.0 applies when the
- * caller passes none).  Returns 0, or -1 on a slot outside the cache. */
+ * caller passes none).  Returns 0, -1 on a slot outside the cache, -2 on a
+ * group the format and D do not allow. */
 int oracle_append(const uint16_t* k, const uint16_t* v, int64_t T, int Hkv, int D,
                   const int64_t* slot_mapping, uint8_t* k_codes, uint8_t* v_codes,
-                  float* k_scales, float* v_scales, int64_t NB, int BS, int fmt,
+                  float* k_scales, float* v_scales, int64_t NB, int BS, int fmt, int group,
                   float scale) {
     oracle_init();
+    if (!group_ok(fmt, D, group)) return -2;
+    const int gc = group_channels(D, group), ng = D / gc;
     int bad = 0;
     float* x = (float*)malloc(sizeof(float) * (size_t)D);
     for (int64_t t = 0; t < T; ++t) {
@@ -251,12 +278,11 @@ int oracle_append(const uint16_t* k, const uint16_t* v, int64_t T, int Hkv, int 
                 const uint16_t* src = (which ? v : k) + ((size_t)t * Hkv + h) * D;
                 uint8_t* dst = (which ? v_codes : k_codes) + (((size_t)blk * Hkv + h) * BS + off) * row_bytes(fmt, D);
                 for (int d = 0; d < D; ++d) x[d] = (float)half_bits_to_double(src[d]);
+                float* sc = (which ? v_scales : k_scales) + (((size_t)blk * Hkv + h) * BS + off) * ng;
                 if (fmt == ORC_INT8) {
-                    float* sc = which ? v_scales : k_scales;
-                    sc[((size_t)blk * Hkv + h) * BS + off] = int8_quant_row(x, D, (int8_t*)dst);
+                    for (int j = 0; j < ng; ++j) sc[j] = int8_quant_row(x + j * gc, gc, (int8_t*)dst + j * gc);
                 } else if (fmt == ORC_INT4) {
-                    float* sc = which ? v_scales : k_scales;
-                    sc[((size_t)blk * Hkv + h) * BS + off] = int4_quant_row(x, D, dst);
+                    for (int j = 0; j < ng; ++j) sc[j] = int4_quant_row(x + j * gc, gc, dst + j * gc / 2);
                 } else {
                     for (int d = 0; d < D; ++d) dst[d] = oracle_fp8_encode(fmt, x[d] / scale);
                 }
@@ -285,8 +311,9 @@ static float cached_value(int fmt, const uint8_t* row, int d, float s) {
 
 /* Gather + dequantize rows at the given slots: out [n][Hkv][D] fp32 (K and V). */
 int oracle_dequant(const uint8_t* k_codes, const uint8_t* v_codes, const float* k_scales,
-                   const float* v_scales, int64_t NB, int BS, int Hkv, int D, int fmt,
+                   const float* v_scales, int64_t NB, int BS, int Hkv, int D, int fmt, int group,
                    const int64_t* slots, int64_t n, float scale, float* out_k, float* out_v) {
+    if (!group_ok(fmt, D, group)) return -2;
     const size_t rb = (size_t)row_bytes(fmt, D);
     for (int64_t i = 0; i < n; ++i) {
         int64_t slot = slots[i];
@@ -294,9 +321,9 @@ int oracle_dequant(const uint8_t* k_codes, const uint8_t* v_codes, const float* 
         int64_t blk = slot / BS, off = slot % BS;
         for (int h = 0; h < Hkv; ++h) {
             size_t row = ((size_t)blk * Hkv + h) * BS + off;
-            float sk = row_scaled(fmt) ? k_scales[row] : scale;
-            float sv = row_scaled(fmt) ? v_scales[row] : scale;
             for (int d = 0; d < D; ++d) {
+                float sk = scale_of(fmt, k_scales, row, D, group, d, scale);
+                float sv = scale_of(fmt, v_scales, row, D, group, d, scale);
                 out_k[((size_t)i * Hkv + h) * D + d] = cached_value(fmt, k_codes + row * rb, d, sk);
                 out_v[((size_t)i * Hkv + h) * D + d] = cached_value(fmt, v_codes + row * rb, d, sv);
             }
@@ -315,10 +342,11 @@ int oracle_dequant(const uint8_t* k_codes, const uint8_t* v_codes, const float* 
 int oracle_decode_attention(const uint16_t* q, int B, int Hq, int D,
                             const uint8_t* k_codes, const uint8_t* v_codes,
                             const float* k_scales, const float* v_scales,
-                            int64_t NB, int BS, int Hkv, int fmt,
+                            int64_t NB, int BS, int Hkv, int fmt, int group,
                             const int32_t* block_tables, int max_blocks,
                             const int32_t* context_lens, float scale, double sm_scale,
                             double* out, double* weights, int64_t w_stride) {
+    if (!group_ok(fmt, D, group)) return -2;
     int G = Hq / Hkv;
     const size_t rb = (size_t)row_bytes(fmt, D);
     int bad = 0;
@@ -339,10 +367,10 @@ int oracle_decode_attention(const uint16_t* q, int B, int Hq, int D,
                 int32_t blk = block_tables[(size_t)b * max_blocks + t / BS];
                 if (blk < 0 || blk >= NB) { ok = 0; break; }
                 size_t row = ((size_t)blk * Hkv + kvh) * BS + t % BS;
-                float sk = row_scaled(fmt) ? k_scales[row] : scale;
                 double acc = 0.0;
                 for (int d = 0; d < D; ++d)
-                    acc += qv[d] * (double)cached_value(fmt, k_codes + row * rb, d, sk);
+                    acc += qv[d] * (double)cached_value(fmt, k_codes + row * rb, d,
+                                                        scale_of(fmt, k_scales, row, D, group, d, scale));
                 logit[t] = sm_scale * acc;
             }
             if (!ok) { bad = 1; free(logit); continue; }
@@ -355,9 +383,9 @@ int oracle_decode_attention(const uint16_t* q, int B, int Hq, int D,
                 if (weights) weights[((size_t)b * Hq + h) * w_stride + t] = w;
                 int32_t blk = block_tables[(size_t)b * max_blocks + t / BS];
                 size_t row = ((size_t)blk * Hkv + kvh) * BS + t % BS;
-                float sv = row_scaled(fmt) ? v_scales[row] : scale;
                 for (int d = 0; d < D; ++d)
-                    o[d] += w * (double)cached_value(fmt, v_codes + row * rb, d, sv);
+                    o[d] += w * (double)cached_value(fmt, v_codes + row * rb, d,
+                                                     scale_of(fmt, v_scales, row, D, group, d, scale));
             }
             free(logit);
         }
@@ -376,10 +404,11 @@ int oracle_decode_attention(const uint16_t* q, int B, int Hq, int D,
 int oracle_prefill_attention(const uint16_t* q, int64_t Tq, int B, int Hq, int D,
                              const uint8_t* k_codes, const uint8_t* v_codes,
                              const float* k_scales, const float* v_scales,
-                             int64_t NB, int BS, int Hkv, int fmt,
+                             int64_t NB, int BS, int Hkv, int fmt, int group,
                              const int32_t* block_tables, int max_blocks,
                              const int32_t* context_lens, const int32_t* query_start,
                              float scale, double sm_scale, double* out) {
+    if (!group_ok(fmt, D, group)) return -2;
     int G = Hq / Hkv;
     const size_t rb = (size_t)row_bytes(fmt, D);
     int bad = 0;
@@ -409,10 +438,10 @@ int oracle_prefill_attention(const uint16_t* q, int64_t Tq, int B, int Hq, int D
                 int32_t blk = block_tables[(size_t)b * max_blocks + t / BS];
                 if (blk < 0 || blk >= NB) { ok = 0; break; }
                 size_t kr = ((size_t)blk * Hkv + kvh) * BS + t % BS;
-                float sk = row_scaled(fmt) ? k_scales[kr] : scale;
                 double acc = 0.0;
                 for (int d = 0; d < D; ++d)
-                    acc += qv[d] * (double)cached_value(fmt, k_codes + kr * rb, d, sk);
+                    acc += qv[d] * (double)cached_value(fmt, k_codes + kr * rb, d,
+                                                        scale_of(fmt, k_scales, kr, D, group, d, scale));
                 logit[t] = sm_scale * acc;
             }
             if (!ok) { bad = 1; break; }
@@ -424,9 +453,9 @@ int oracle_prefill_attention(const uint16_t* q, int64_t Tq, int B, int Hq, int D
                 double w = logit[t] / denom;
                 int32_t blk = block_tables[(size_t)b * max_blocks + t / BS];
                 size_t vr = ((size_t)blk * Hkv + kvh) * BS + t % BS;
-                float sv = row_scaled(fmt) ? v_scales[vr] : scale;
                 for (int d = 0; d < D; ++d)
-                    o[d] += w * (double)cached_value(fmt, v_codes + vr * rb, d, sv);
+                    o[d] += w * (double)cached_value(fmt, v_codes + vr * rb, d,
+                                                     scale_of(fmt, v_scales, vr, D, group, d, scale));
             }
         }
         free(logit);

@@ -23,7 +23,7 @@ from tests.conftest import golden
 TORCH_DT = {oracle.E4M3: torch.float8_e4m3fn, oracle.E5M2: torch.float8_e5m2}
 
 
-def make_case(rng, B, Hq, Hkv, D, BS, fmt, ctx, scale=None, outliers=False):
+def make_case(rng, B, Hq, Hkv, D, BS, fmt, ctx, scale=None, outliers=False, group=0):
     ctx = np.asarray(ctx, np.int32)
     nblk = [(int(c) + BS - 1) // BS for c in ctx]
     NB = sum(nblk) + 3
@@ -34,7 +34,7 @@ def make_case(rng, B, Hq, Hkv, D, BS, fmt, ctx, scale=None, outliers=False):
     for b, n in enumerate(nblk):
         bt[b, :n] = perm[at:at + n]
         at += n
-    cache = oracle.Cache(NB, Hkv, BS, D, fmt)
+    cache = oracle.Cache(NB, Hkv, BS, D, fmt, group=group)
     slots = []
     for b in range(B):
         for t in range(int(ctx[b])):
@@ -54,16 +54,19 @@ def make_case(rng, B, Hq, Hkv, D, BS, fmt, ctx, scale=None, outliers=False):
 
 
 def torch_dequant(cache, scale):
+    def per_channel(sc):      # row scales broadcast, or group scales repeated over their channels
+        t = torch.from_numpy(sc)
+        return t.repeat_interleave(cache.group, dim=-1) if getattr(cache, "group", 0) else t[..., None]
     if cache.fmt == oracle.INT4:
         def nibbles(codes):   # channel 2i = low nibble; (n ^ 8) - 8 sign-extends 4 bits
             t = torch.from_numpy(codes.astype(np.int32))
             both = torch.stack([t & 15, t >> 4], dim=-1).flatten(-2)
             return ((both ^ 8) - 8).to(torch.float32)
-        kk = nibbles(cache.k_codes) * torch.from_numpy(cache.k_scales)[..., None]
-        vv = nibbles(cache.v_codes) * torch.from_numpy(cache.v_scales)[..., None]
+        kk = nibbles(cache.k_codes) * per_channel(cache.k_scales)
+        vv = nibbles(cache.v_codes) * per_channel(cache.v_scales)
     elif cache.fmt == oracle.INT8:
-        kk = torch.from_numpy(cache.k_codes.view(np.int8)).to(torch.float32) * torch.from_numpy(cache.k_scales)[..., None]
-        vv = torch.from_numpy(cache.v_codes.view(np.int8)).to(torch.float32) * torch.from_numpy(cache.v_scales)[..., None]
+        kk = torch.from_numpy(cache.k_codes.view(np.int8)).to(torch.float32) * per_channel(cache.k_scales)
+        vv = torch.from_numpy(cache.v_codes.view(np.int8)).to(torch.float32) * per_channel(cache.v_scales)
     else:
         s = torch.tensor(1.0 if scale is None else scale, dtype=torch.float32)
         kk = torch.from_numpy(cache.k_codes).view(TORCH_DT[cache.fmt]).to(torch.float32) * s

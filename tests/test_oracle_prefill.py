@@ -44,9 +44,9 @@ def torch_prefill_reference(q, cache, bt, ctx, qs, scale, sm_scale=None):
     return out.numpy()
 
 
-def chunked_case(rng, Hq, Hkv, D, BS, fmt, ctx, chunk, scale=None, outliers=False):
+def chunked_case(rng, Hq, Hkv, D, BS, fmt, ctx, chunk, scale=None, outliers=False, group=0):
     q1, cache, bt, ctx, scale, k, v, slots = make_case(rng, len(ctx), Hq, Hkv, D, BS, fmt, ctx,
-                                                       scale=scale, outliers=outliers)
+                                                       scale=scale, outliers=outliers, group=group)
     qs = np.zeros(len(ctx) + 1, np.int32)
     qs[1:] = np.cumsum(chunk)
     q = rng.standard_normal((int(qs[-1]), Hq, D)).astype(np.float16)
