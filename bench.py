@@ -38,6 +38,7 @@ DEFAULT_WORKLOAD = "llama2-7b"
 L2_BYTES = 129 * 1024 * 1024
 DEFAULT_STEPS = {"tiny": 2000, "llama2-7b": 10000, "llama3-8b": 10000, "llama2-13b-int8": 1000,
                  "llama2-13b-int4": 2000,
+                 "llama2-13b-int4-g32": 2000,
                  "llama3-70b": 300}
 
 
@@ -201,7 +202,8 @@ class Setup:
         self.lay = W.Layout(wl)
         ctx_max = self.lay.max_context_len
         step_tok = wl.append_chunk if wl.append_chunk else 1
-        self.cache = kvq.KVCache(self.lay.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim, wl.fmt, device)
+        self.cache = kvq.KVCache(self.lay.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim, wl.fmt, device,
+                                 group_size=wl.quant_group)
         windows = W.chunk_positions(wl, 1 << 19)
         k0, v0 = W.kv_tokens(wl, *windows[0], device=device)
         sv = W.calibration_scale(wl, k0, v0)
@@ -301,7 +303,7 @@ def cpu_baseline(wl, target_s: float):
     def run(seqs):
         bs = wl.block_size
         nblk = [(int(lay.context_lens[b]) + bs - 1) // bs for b in seqs]
-        cache = oracle.Cache(sum(nblk), wl.num_kv_heads, bs, wl.head_dim, fmt)
+        cache = oracle.Cache(sum(nblk), wl.num_kv_heads, bs, wl.head_dim, fmt, group=wl.quant_group)
         bt = np.zeros((len(seqs), max(nblk)), np.int32)
         at = 0
         for i, n in enumerate(nblk):
@@ -531,7 +533,8 @@ def run_kvq(args):
         "vs_baseline": None,
         "dtype": {"e4m3": "fp8-e4m3 storage, f16xf16->f32 compute", "e5m2": "fp8-e5m2 storage, f16xf16->f32 compute",
                   "int8": "int8 storage, f16xf16->f32 compute",
-                  "int4": "int4 storage (two codes per byte), f16xf16->f32 compute"}[wl.fmt],
+                  "int4": "int4 storage (two codes per byte), f16xf16->f32 compute"}[wl.fmt]
+                 + (f", one scale per {wl.quant_group} channels" if wl.quant_group else ""),
         "data": "synthetic (seeded N(0,1) fp16 K/V/Q, shuffled block tables)",
         "config": {"workload": wl.name, "description": wl.description, "batch": wl.batch,
                    "num_q_heads": wl.num_q_heads, "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
@@ -580,7 +583,8 @@ class PrefillSetup:
         self.lay = W.Layout(wl)
         cl = self.lay.context_lens
         self.n = W.prefill_chunks(wl, cl, chunk)
-        self.cache = kvq.KVCache(self.lay.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim, wl.fmt, device)
+        self.cache = kvq.KVCache(self.lay.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim, wl.fmt, device,
+                                 group_size=wl.quant_group)
         windows = W.chunk_positions(wl, 1 << 19)
         k0, v0 = W.kv_tokens(wl, *windows[0], device=device)
         sv = W.calibration_scale(wl, k0, v0)
@@ -642,7 +646,7 @@ def prefill_cpu_baseline(wl, n_chunk: int, target_s: float):
            "int4": oracle.INT4}[wl.fmt]
     bs, c = wl.block_size, int(lay.context_lens[0])
     nb = (c + bs - 1) // bs
-    cache = oracle.Cache(nb, wl.num_kv_heads, bs, wl.head_dim, fmt)
+    cache = oracle.Cache(nb, wl.num_kv_heads, bs, wl.head_dim, fmt, group=wl.quant_group)
     bt = np.arange(nb, dtype=np.int32)[None]
     k, v = W.kv_tokens(wl, 0, c, "cpu", seqs=[0])
     pos = np.arange(c)
@@ -778,7 +782,8 @@ def run_prefill_bench(args):
         "vs_baseline": None,
         "dtype": {"e4m3": "fp8-e4m3 storage, f16xf16->f32 compute", "e5m2": "fp8-e5m2 storage, f16xf16->f32 compute",
                   "int8": "int8 storage, f16xf16->f32 compute",
-                  "int4": "int4 storage (two codes per byte), f16xf16->f32 compute"}[wl.fmt],
+                  "int4": "int4 storage (two codes per byte), f16xf16->f32 compute"}[wl.fmt]
+                 + (f", one scale per {wl.quant_group} channels" if wl.quant_group else ""),
         "data": "synthetic (seeded N(0,1) fp16 K/V/Q, shuffled block tables)",
         "config": {"workload": wl.name + "-prefill", "description": wl.description, "batch": wl.batch,
                    "num_q_heads": wl.num_q_heads, "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
@@ -836,7 +841,7 @@ def run_reference(args):
     for b in range(nseq):
         n = int(lay.context_lens[b])
         nb = (n + bs - 1) // bs
-        cache = oracle.Cache(nb, wl.num_kv_heads, bs, wl.head_dim, fmt)
+        cache = oracle.Cache(nb, wl.num_kv_heads, bs, wl.head_dim, fmt, group=wl.quant_group)
         bt = np.arange(nb, dtype=np.int32)[None]
         k, v = W.kv_tokens(wl, 0, n, "cpu", seqs=[b])
         pos = np.arange(n)

@@ -45,7 +45,7 @@ class KvqCacheDesc(ctypes.Structure):
                 ("k_scales", ctypes.c_void_p), ("v_scales", ctypes.c_void_p),
                 ("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
-                ("fmt", ctypes.c_int32)]
+                ("fmt", ctypes.c_int32), ("group_size", ctypes.c_int32)]
 
 
 def build(force: bool = False) -> str:
@@ -134,20 +134,24 @@ def _scale_ptr(scale) -> int | None:
 class KVCache:
     """A paged quantized cache in device memory:
     codes uint8 [num_blocks][num_kv_heads][block_size][head_dim] for K and V
-    ([..][head_dim / 2] packed codes for INT4), and for INT8 / INT4 the fp32 row
-    scales [num_blocks][num_kv_heads][block_size]."""
+    ([..][head_dim / 2] packed codes for INT4), and for INT8 / INT4 the fp32
+    scales [num_blocks][num_kv_heads][block_size] (one per row, group_size 0) or
+    [num_blocks][num_kv_heads][block_size][head_dim / group_size] (one per group
+    of channels; group_size head_dim / 2 or head_dim / 4)."""
 
-    def __init__(self, num_blocks, num_kv_heads, block_size, head_dim, fmt, device="cuda", fill=None):
+    def __init__(self, num_blocks, num_kv_heads, block_size, head_dim, fmt, device="cuda", fill=None,
+                 group_size=0):
         self.fmt = FORMATS[fmt] if isinstance(fmt, str) else int(fmt)
         self.num_blocks, self.num_kv_heads = int(num_blocks), int(num_kv_heads)
         self.block_size, self.head_dim = int(block_size), int(head_dim)
+        self.group_size = int(group_size)
         shape = (self.num_blocks, self.num_kv_heads, self.block_size,
                  self.head_dim // 2 if self.fmt == INT4 else self.head_dim)
         mk = (lambda: torch.full(shape, fill, dtype=torch.uint8, device=device)) if fill is not None else \
             (lambda: torch.empty(shape, dtype=torch.uint8, device=device))
         self.k_codes, self.v_codes = mk(), mk()
         if self.fmt in (INT8, INT4):
-            sshape = shape[:3]
+            sshape = shape[:3] + ((self.head_dim // self.group_size,) if self.group_size else ())
             self.k_scales = torch.zeros(sshape, dtype=torch.float32, device=device)
             self.v_scales = torch.zeros(sshape, dtype=torch.float32, device=device)
         else:
@@ -159,7 +163,8 @@ class KVCache:
         return KvqCacheDesc(self.k_codes.data_ptr(), self.v_codes.data_ptr(),
                             self.k_scales.data_ptr() if self.k_scales is not None else None,
                             self.v_scales.data_ptr() if self.v_scales is not None else None,
-                            self.num_blocks, self.block_size, self.num_kv_heads, self.head_dim, self.fmt)
+                            self.num_blocks, self.block_size, self.num_kv_heads, self.head_dim, self.fmt,
+                            self.group_size)
 
     def _cdesc(self) -> KvqCacheDesc:
         # the binding's own descriptor, built once per format (the arrays never move)

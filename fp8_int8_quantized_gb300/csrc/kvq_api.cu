@@ -67,6 +67,10 @@ kvq_status check_cache(const kvq_cache* c, int32_t fmt) {
     if (fmt == KVQ_INT8 || fmt == KVQ_INT4) {
         if (!c->k_scales || !c->v_scales || !aligned(c->k_scales, 16) || !aligned(c->v_scales, 16))
             return KVQ_ERR_INVALID_ARG;
+        const int32_t g = c->group_size;
+        if (g != 0 && g != c->head_dim && g != c->head_dim / 2 && g != c->head_dim / 4) return KVQ_ERR_INVALID_ARG;
+    } else if (c->group_size != 0) {
+        return KVQ_ERR_INVALID_ARG;
     }
     // TMA row coordinates are 32-bit
     if ((int64_t)c->num_blocks * c->num_kv_heads * c->block_size > 0x7FFFFFFFll) return KVQ_ERR_UNSUPPORTED;
@@ -74,8 +78,9 @@ kvq_status check_cache(const kvq_cache* c, int32_t fmt) {
 }
 
 kvq::CacheView view(const kvq_cache* c) {
+    const int32_t ng = c->group_size > 0 ? c->head_dim / c->group_size : 1;
     return kvq::CacheView{static_cast<uint8_t*>(c->k_codes), static_cast<uint8_t*>(c->v_codes), c->k_scales,
-                          c->v_scales, c->num_blocks, c->block_size, c->num_kv_heads, c->head_dim, c->fmt};
+                          c->v_scales, c->num_blocks, c->block_size, c->num_kv_heads, c->head_dim, c->fmt, ng};
 }
 
 // Decode tiles (kDecodeTileTokens tokens) per context chunk.  Every warp of the persistent decode
@@ -110,6 +115,9 @@ kvq_status decode_impl(const void* q, const void* k_new, const void* v_new, cons
     if (num_q_heads % cache->num_kv_heads) return KVQ_ERR_INVALID_ARG;
     const int G = num_q_heads / cache->num_kv_heads;
     if (G > 8) return KVQ_ERR_UNSUPPORTED;
+    // the tensor-core consumer carries one operand row per (q-head, scale group)
+    const int ng = cache->group_size > 0 ? cache->head_dim / cache->group_size : 1;
+    if (G * ng > 8) return KVQ_ERR_UNSUPPORTED;
     if ((int64_t)max_blocks_per_seq * cache->block_size < max_context_len) return KVQ_ERR_INVALID_ARG;
     if (batch > 65535 || cache->num_kv_heads > 65535 || num_q_heads > 65535) return KVQ_ERR_UNSUPPORTED;
     if (batch == 0) return KVQ_OK;
@@ -129,7 +137,8 @@ kvq_status decode_impl(const void* q, const void* k_new, const void* v_new, cons
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return KVQ_ERR_WORKSPACE;
     int kind = g_decode_kernel.load();
     if (kind == 0) kind = 2;
-    if (kind == 1 && (G > 4 || fmt == KVQ_INT4)) return KVQ_ERR_UNSUPPORTED;   // CUDA-core kernel: 8-bit codes, G <= 4
+    // CUDA-core kernel: 8-bit codes, G <= 4, one scale per row
+    if (kind == 1 && (G > 4 || fmt == KVQ_INT4 || ng > 1)) return KVQ_ERR_UNSUPPORTED;
     int dev;
     if (!current_device(&dev)) return KVQ_ERR_CUDA;
     unsigned long long* err = err_word(dev);
@@ -254,6 +263,8 @@ kvq_status kvq_prefill_attention(const void* q, const kvq_cache* cache, const in
         return KVQ_ERR_INVALID_ARG;
     if (num_q_heads % cache->num_kv_heads) return KVQ_ERR_INVALID_ARG;
     if (num_q_heads / cache->num_kv_heads > kvq::prefill_rows_per_tile()) return KVQ_ERR_UNSUPPORTED;
+    // the dequant warps apply one scale per row (to logits and weights)
+    if (cache->group_size > 0 && cache->group_size != cache->head_dim) return KVQ_ERR_UNSUPPORTED;
     if (num_q_tokens > 0x7FFFFFFFll) return KVQ_ERR_UNSUPPORTED;   // query_start entries are int32
     if (batch > 65535 || cache->num_kv_heads > 65535) return KVQ_ERR_UNSUPPORTED;
     if (batch == 0 || max_query_len == 0 || num_q_tokens == 0) return KVQ_OK;

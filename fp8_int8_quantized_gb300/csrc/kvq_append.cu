@@ -6,12 +6,13 @@
 // W8A8 or FP8 KV Cache" (lmdeploy issue 1463): online INT8, here symmetric with
 // one fp32 scale amax / 127 per (token, kv-head) row; INT4 (named beside it)
 // the same with amax / 7, codes in [-7, 7] packed two per byte (channel 2i in
-// the low nibble).
+// the low nibble).  Group quantization ("[QST] Scale factors and benchmarks",
+// the QQQ page) cuts a row into 2 or 4 groups of channels with a scale each.
 //
 // HBM-bound: per element 2 bytes read, 1 byte written.  One thread handles 16
 // consecutive elements of one (token, kv-head) row: two 16-byte loads of fp16,
 // one 16-byte store of codes.  The D/16 threads of a row are adjacent lanes, so
-// the INT8 row maximum is a shuffle reduction among them.
+// the INT8 / INT4 row (or group) maximum is a shuffle reduction among them.
 #include "kvq_device.cuh"
 #include "kvq_launch.h"
 
@@ -19,6 +20,18 @@ namespace kvq {
 namespace {
 
 constexpr int kThreads = 256;
+
+// Maximum of v over the cpg adjacent lanes of this lane's scale group (cpg a
+// power of two dividing CPR; the CPR lanes of a row are aligned and all active).
+template <int CPR>
+__device__ __forceinline__ float group_max(float v, int cpg) {
+    const unsigned lane = threadIdx.x & 31u;
+    const unsigned rmask = (CPR == 32 ? 0xFFFFFFFFu : ((1u << CPR) - 1u) << (lane & ~(unsigned)(CPR - 1)));
+#pragma unroll
+    for (int off = CPR / 2; off > 0; off >>= 1)
+        if (off < cpg) v = fmaxf(v, __shfl_xor_sync(rmask, v, off));
+    return v;
+}
 
 template <int FMT, int D>
 __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
@@ -53,14 +66,12 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
         x[2 * i + 1] = f.y;
     }
     const int64_t dst_row = ((slot / BS) * Hkv + h) * BS + slot % BS;
+    const int ng = a.cache.ngroups, cpg = CPR / ng;  // groups per row, threads per group
     if (FMT == INT4) {
         float amax = 0.f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
-        const unsigned lane = threadIdx.x & 31u;
-        const unsigned gmask = (CPR == 32 ? 0xFFFFFFFFu : ((1u << CPR) - 1u) << (lane & ~(unsigned)(CPR - 1)));
-#pragma unroll
-        for (int off = CPR / 2; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, off));
+        amax = group_max<CPR>(amax, cpg);
         const float s = __fdiv_rn(amax, 7.0f);
         uint32_t o4[2] = {0u, 0u};
 #pragma unroll
@@ -74,7 +85,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
         }
         uint8_t* dst4 = (which ? a.cache.v_codes : a.cache.k_codes) + dst_row * (D / 2) + c * 8;
         *reinterpret_cast<uint2*>(dst4) = make_uint2(o4[0], o4[1]);
-        if (c == 0) (which ? a.cache.v_scales : a.cache.k_scales)[dst_row] = s;
+        if (c % cpg == 0) (which ? a.cache.v_scales : a.cache.k_scales)[dst_row * ng + c / cpg] = s;
         return;
     }
     uint8_t* dst = (which ? a.cache.v_codes : a.cache.k_codes) + dst_row * D + c * 16;
@@ -83,10 +94,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
         float amax = 0.f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
-        const unsigned lane = threadIdx.x & 31u;
-        const unsigned gmask = (CPR == 32 ? 0xFFFFFFFFu : ((1u << CPR) - 1u) << (lane & ~(unsigned)(CPR - 1)));
-#pragma unroll
-        for (int off = CPR / 2; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, off));
+        amax = group_max<CPR>(amax, cpg);
         const float s = __fdiv_rn(amax, 127.0f);
         int q[16];
 #pragma unroll
@@ -102,7 +110,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(AppendArgs a) {
         for (int i = 0; i < 4; ++i)
             o[i] = (uint32_t)q[4 * i] | ((uint32_t)q[4 * i + 1] << 8) | ((uint32_t)q[4 * i + 2] << 16) |
                    ((uint32_t)q[4 * i + 3] << 24);
-        if (c == 0) (which ? a.cache.v_scales : a.cache.k_scales)[dst_row] = s;
+        if (c % cpg == 0) (which ? a.cache.v_scales : a.cache.k_scales)[dst_row * ng + c / cpg] = s;
     } else {
         const float s = a.scale ? __ldg(a.scale) : 1.0f;
         if (s != 1.0f) {

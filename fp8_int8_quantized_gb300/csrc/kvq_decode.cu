@@ -80,12 +80,13 @@ enum { kKindSimt = 1, kKindMma = 2 };
 struct Layout {
     int tile_bytes, q_bytes, scales, full, qbuf, newkv, patch, scan, total;
     // rb: bytes of one cached row (head_dim, or head_dim / 2 for INT4); int8:
-    // the format carries row scales (INT8 or INT4)
-    __host__ __device__ Layout(int rb, int D, int G, int B, bool int8, bool append) {
+    // the format carries row scales (INT8 or INT4), ng of them per row
+    __host__ __device__ Layout(int rb, int D, int G, int B, bool int8, bool append, int ng) {
         tile_bytes = kTile * rb;
         q_bytes = (G * D * 2 + 127) / 128 * 128;
         scales = kConsumers * kSpw * 2 * tile_bytes;            // [warp][stage][K,V][tile] before this
-        full = scales + (int8 ? kConsumers * kSpw * 2 * kTile * 4 : 0);  // INT8: f32 [warp][stage][K,V][32]
+        // INT8 / INT4: f32 [warp][stage][K,V][32 tokens][ng]
+        full = scales + (int8 ? kConsumers * kSpw * 2 * kTile * 4 * ng : 0);
         qbuf = (full + kConsumers * kSpw * 8 + 127) / 128 * 128;  // u64 [warp][stage], then f16 [warp][G][D]
         newkv = qbuf + kConsumers * q_bytes;                    // f16 [warp][K,V][D]
         patch = newkv + (append ? kConsumers * 2 * D * 2 : 0);  // int [warp]
@@ -190,7 +191,7 @@ struct SimtConsumer {
     int lane, j, grp, G;
     float qk_scale;
 
-    __device__ void init(int G_, float qks) {
+    __device__ void init(int G_, float qks, int /*ng: always 1 here*/) {
         lane = threadIdx.x & 31;
         j = lane % LPT;
         grp = lane / LPT;
@@ -367,12 +368,18 @@ struct MmaConsumer {
     static constexpr bool kBiased = kRowScaled;
     static constexpr float kUnit = I4 ? 5.9604644775390625e-08f : 1.f;   // operand value of one code step
     static constexpr float kBias = I4 ? 8.f * kUnit : 1152.f;            // operand - code * kUnit
+    // Operand row / column g (QK rows, PV columns) is (q-head g / ng, scale
+    // group g % ng): with ng groups per row, a row of QK sees only its group's
+    // head dims, its partial logits are scaled by that group's K scales and
+    // summed over the ng rows of the head, and the PV column carries P times
+    // the group's V scales; output dims are taken from the column of their own
+    // group.  ng = 1 is the per-row (or per-tensor) format.
     uint32_t qa[2 * KS];
     float acc[MT][4];
     float m, l;
-    float qsum;  // INT8: sum of this head's query row (head g)
-    float psum;  // INT8: running sum of the fp16 P' weights fed to PV (head g, this thread's tokens)
-    int lane, g, c, G;
+    float qsum;  // INT8 / INT4: sum of this operand row's query values (row g)
+    float psum;  // INT8 / INT4: running sum of the P' weights fed to PV (column g, this thread's tokens)
+    int lane, g, c, G, ng, kg;  // kg = g % ng: this lane's scale group
     float qk_scale;
     // this lane's byte offsets inside a stage tile (the 128-byte swizzle folded
     // in): K row g at chunks 2c, 2c+1 (row 8+g is 8 rows further), V rows 2c
@@ -380,11 +387,13 @@ struct MmaConsumer {
     // unswizzled, the same codes at half the bytes
     uint32_t k_off0, k_off1, v_off0, v_off1;
 
-    __device__ void init(int G_, float qks) {
+    __device__ void init(int G_, float qks, int ng_) {
         lane = threadIdx.x & 31;
         g = lane >> 2;
         c = lane & 3;
         G = G_;
+        ng = ng_;
+        kg = g % ng_;
         qk_scale = qks;
         if (I4) {
             k_off0 = g * RB + c * (DC / 2);
@@ -403,12 +412,14 @@ struct MmaConsumer {
             v_off1 = (2 * c + 1) * D + DV * g;
         }
     }
-    // qa[2j] = Q[g][DC*c + 4j + {0,1}], qa[2j+1] = Q[g][DC*c + 4j + {2,3}]: the
-    // DC halves Q[g][DC*c ...] in order.  q: the group's G query rows
+    // qa[2j] = Q[h][DC*c + 4j + {0,1}], qa[2j+1] = Q[h][DC*c + 4j + {2,3}]: the
+    // DC halves Q[h][DC*c ...] in order, h = g / ng, where this thread's DC dims
+    // lie in row g's scale group (the DC dims of a thread are within one group:
+    // groups are D / ng >= DC wide); else zero.  q: the kv-head's G query rows
     // (shared-memory copy).
     __device__ void set_q(const uint16_t* q) {
-        if (g < G) {
-            const uint4* src = reinterpret_cast<const uint4*>(q + g * D + DC * c);
+        if (g < G * ng && ((c * ng) >> 2) == kg) {
+            const uint4* src = reinterpret_cast<const uint4*>(q + (g / ng) * D + DC * c);
 #pragma unroll
             for (int i = 0; i < (2 * KS) / 4; ++i) {
                 const uint4 x = src[i];
@@ -531,14 +542,27 @@ struct MmaConsumer {
                 }
             }
         }
-        if (kRowScaled) {  // remove the operand bias, then apply the K row scales
+        if (kRowScaled) {  // remove the operand bias, then apply the K row (group) scales
             const float corr = kBias * qsum;
             const float ks = qk_scale / kUnit;
-            const float2 k01 = __uint_as_float2(lds64(sk + 8 * c)), k23 = __uint_as_float2(lds64(sk + 32 + 8 * c));
+            float2 k01, k23;
+            if (ng == 1) {
+                k01 = __uint_as_float2(lds64(sk + 8 * c));
+                k23 = __uint_as_float2(lds64(sk + 32 + 8 * c));
+            } else {  // scales [token][ng]: tokens 2c, 2c+1, 8+2c, 9+2c of group kg
+                const uint32_t a0 = sk + 4 * (2 * c * ng + kg);
+                k01 = make_float2(ldsf(a0), ldsf(a0 + 4 * ng));
+                k23 = make_float2(ldsf(a0 + 32 * ng), ldsf(a0 + 36 * ng));
+            }
             z[0] = (sA[0] - corr) * (ks * k01.x);
             z[1] = (sA[1] - corr) * (ks * k01.y);
             z[2] = (sB[0] - corr) * (ks * k23.x);
             z[3] = (sB[1] - corr) * (ks * k23.y);
+            // the head's logits: sum of its ng group rows (lanes 4 apart per row)
+            for (int off = 1; off < ng; off <<= 1) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) z[e] += __shfl_xor_sync(0xFFFFFFFFu, z[e], 4 * off);
+            }
         } else {
             z[0] = sA[0] * qk_scale; z[1] = sA[1] * qk_scale; z[2] = sB[0] * qk_scale; z[3] = sB[1] * qk_scale;
         }
@@ -635,7 +659,7 @@ struct MmaConsumer {
         const bool two = cx.valid > kBox;  // warp-uniform: the second box holds context rows
         float z0[4], z1[4];
         qk_box(cx.k, cx.s, cx.valid, z0);
-        if (two) qk_box(cx.k + kBox * RB, cx.s + 4 * kBox, cx.valid - kBox, z1);
+        if (two) qk_box(cx.k + kBox * RB, cx.s + 4 * kBox * ng, cx.valid - kBox, z1);
         else z1[0] = z1[1] = z1[2] = z1[3] = -INFINITY;
         float mx = fmaxf(fmaxf(fmaxf(z0[0], z0[1]), fmaxf(z0[2], z0[3])), fmaxf(fmaxf(z1[0], z1[1]), fmaxf(z1[2], z1[3])));
         mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
@@ -652,13 +676,22 @@ struct MmaConsumer {
         }
         m = mn;
         l = l * alpha + (((p0[0] + p0[1]) + (p0[2] + p0[3])) + ((p1[0] + p1[1]) + (p1[2] + p1[3])));
-        if (kRowScaled) {  // fold the V row scales into P (masked tokens keep p = 0)
-            const uint32_t sv = cx.s + 4 * kTile;
-            const float2 a01 = __uint_as_float2(lds64(sv + 8 * c)), a23 = __uint_as_float2(lds64(sv + 32 + 8 * c));
-            p0[0] *= a01.x; p0[1] *= a01.y; p0[2] *= a23.x; p0[3] *= a23.y;
-            if (two) {
-                const float2 b01 = __uint_as_float2(lds64(sv + 64 + 8 * c)), b23 = __uint_as_float2(lds64(sv + 96 + 8 * c));
-                p1[0] *= b01.x; p1[1] *= b01.y; p1[2] *= b23.x; p1[3] *= b23.y;
+        if (kRowScaled) {  // fold the V row (column group) scales into P (masked tokens keep p = 0)
+            const uint32_t sv = cx.s + 4 * kTile * ng;
+            if (ng == 1) {
+                const float2 a01 = __uint_as_float2(lds64(sv + 8 * c)), a23 = __uint_as_float2(lds64(sv + 32 + 8 * c));
+                p0[0] *= a01.x; p0[1] *= a01.y; p0[2] *= a23.x; p0[3] *= a23.y;
+                if (two) {
+                    const float2 b01 = __uint_as_float2(lds64(sv + 64 + 8 * c)), b23 = __uint_as_float2(lds64(sv + 96 + 8 * c));
+                    p1[0] *= b01.x; p1[1] *= b01.y; p1[2] *= b23.x; p1[3] *= b23.y;
+                }
+            } else {  // scales [token][ng]: tokens 2c, 2c+1, 8+2c, 9+2c (+16) of group kg
+                const uint32_t a0 = sv + 4 * (2 * c * ng + kg);
+                p0[0] *= ldsf(a0); p0[1] *= ldsf(a0 + 4 * ng); p0[2] *= ldsf(a0 + 32 * ng); p0[3] *= ldsf(a0 + 36 * ng);
+                if (two) {
+                    const uint32_t b0 = a0 + 64 * ng;
+                    p1[0] *= ldsf(b0); p1[1] *= ldsf(b0 + 4 * ng); p1[2] *= ldsf(b0 + 32 * ng); p1[3] *= ldsf(b0 + 36 * ng);
+                }
             }
             psum *= alpha;
         }
@@ -684,7 +717,7 @@ struct MmaConsumer {
         float lq = l;
         lq += __shfl_xor_sync(0xFFFFFFFFu, lq, 1);
         lq += __shfl_xor_sync(0xFFFFFFFFu, lq, 2);
-        if (c == 0 && g < G) f.ml[slot_index(f.hq0 + g, f.nch, f.ch, f.half)] = make_float2(m, lq);
+        if (c == 0 && kg == 0 && g < G * ng) f.ml[slot_index(f.hq0 + g / ng, f.nch, f.ch, f.half)] = make_float2(m, lq);
         float bias[2] = {0.f, 0.f};
         if (kBiased) {  // bias * sum(P') of heads 2c and 2c+1
             float ps = psum;
@@ -693,11 +726,13 @@ struct MmaConsumer {
             bias[0] = kBias * __shfl_sync(0xFFFFFFFFu, ps, 8 * c);
             bias[1] = kBias * __shfl_sync(0xFFFFFFFFu, ps, 8 * c + 4);
         }
-        // acc[i][0..3] = out[head 2c | 2c+1][d = DV*g + 2i | DV*g + 2i + 1]
+        // acc[i][0..3] = out[column 2c | 2c+1][d = DV*g + 2i | DV*g + 2i + 1]; column n
+        // is head n / ng with the V scales of group n % ng, which must be the group
+        // of this thread's DV dims, (g * ng) / 8
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            const int h = 2 * c + e;
-            if (h >= G) continue;
+            const int n = 2 * c + e, h = n / ng;
+            if (h >= G || n % ng != ((g * ng) >> 3)) continue;
             float* dst = f.acc + slot_index(f.hq0 + h, f.nch, f.ch, f.half) * D + DV * g;
             const float bs = bias[e];
             const float so = f.s_out / kUnit;
@@ -765,8 +800,11 @@ __device__ __noinline__ void append_newest(const uint16_t* nkv, int blk, int pos
             float amax = 0.f;
 #pragma unroll
             for (int i = 0; i < VPL; ++i) amax = fmaxf(amax, fabsf(x[w][i]));
+            // over the 32 / ng lanes of this lane's scale group (all 32 for one per row)
+            const int lpg = 32 / a.cache.ngroups;
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+            for (int off = 16; off > 0; off >>= 1)
+                if (off < lpg) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
             const float s = __fdiv_rn(amax, kQmax);
             rs[w] = s;
 #pragma unroll
@@ -801,11 +839,13 @@ __device__ __noinline__ void append_newest(const uint16_t* nkv, int blk, int pos
             a.cache.k_codes[row * RB + lane] = (uint8_t)code[0];
             a.cache.v_codes[row * RB + lane] = (uint8_t)code[1];
         }
-        if (lane == 0) {
-            stsf(st + 4 * r, rs[0]);
-            stsf(st + 4 * kTile + 4 * r, rs[1]);
-            a.cache.k_scales[row] = rs[0];
-            a.cache.v_scales[row] = rs[1];
+        const int ng = a.cache.ngroups, lpg = 32 / ng;
+        if (lane % lpg == 0) {  // scales [token][ng]: this lane's group lane / lpg
+            const int j = r * ng + lane / lpg;
+            stsf(st + 4 * j, rs[0]);
+            stsf(st + 4 * kTile * ng + 4 * j, rs[1]);
+            a.cache.k_scales[row * ng + lane / lpg] = rs[0];
+            a.cache.v_scales[row * ng + lane / lpg] = rs[1];
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     } else if (blk >= 0) {
@@ -829,11 +869,13 @@ __device__ __noinline__ void append_newest(const uint16_t* nkv, int blk, int pos
             reinterpret_cast<uint16_t*>(a.cache.k_codes + row * D)[lane] = (uint16_t)code[0];
             reinterpret_cast<uint16_t*>(a.cache.v_codes + row * D)[lane] = (uint16_t)code[1];
         }
-        if (FMT == INT8 && lane == 0) {
-            stsf(st + 4 * r, rs[0]);
-            stsf(st + 4 * kTile + 4 * r, rs[1]);
-            a.cache.k_scales[row] = rs[0];
-            a.cache.v_scales[row] = rs[1];
+        const int ng = a.cache.ngroups, lpg = 32 / ng;
+        if (FMT == INT8 && lane % lpg == 0) {  // scales [token][ng]: this lane's group lane / lpg
+            const int j = r * ng + lane / lpg;
+            stsf(st + 4 * j, rs[0]);
+            stsf(st + 4 * kTile * ng + 4 * j, rs[1]);
+            a.cache.k_scales[row * ng + lane / lpg] = rs[0];
+            a.cache.v_scales[row * ng + lane / lpg] = rs[1];
         }
         // the stage is refilled by TMA later: order these generic writes first
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -855,7 +897,9 @@ __global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
     const bool append = a.k_new != nullptr;
     constexpr bool kRowScaled = FMT == INT8 || FMT == INT4;
     constexpr int RB = row_bytes(FMT, D);
-    const Layout L(RB, D, G, B, kRowScaled, append);
+    const int ng = a.cache.ngroups;
+    const Layout L(RB, D, G, B, kRowScaled, append, ng);
+    const uint32_t sc_stage = 2 * kTile * 4 * ng;  // bytes of a stage's K and V scales
     int* S = reinterpret_cast<int*>(smem + L.scan);
     int* ctx_s = S + B + 1;
     griddep_wait();    // inputs may come from the previous kernel (an append)
@@ -907,7 +951,7 @@ __global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
     const int hi = lo + base_len + (gw < extra ? 1 : 0);
 
     uint8_t* tiles = smem + warp * kSpw * 2 * L.tile_bytes;
-    float* scales = reinterpret_cast<float*>(smem + L.scales) + warp * kSpw * 2 * kTile;
+    float* scales = reinterpret_cast<float*>(smem + L.scales) + warp * kSpw * 2 * kTile * ng;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.full) + warp * kSpw;
     uint8_t* qbuf = smem + L.qbuf + warp * L.q_bytes;
     uint16_t* nkv = reinterpret_cast<uint16_t*>(smem + L.newkv) + warp * 2 * D;  // appending launches only
@@ -932,7 +976,7 @@ __global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
         prefetch_tmap(&tmv);
     }
     const uint64_t pol = policy_evict_first();
-    const uint32_t box_tx = 2 * kBox * RB + (kRowScaled ? 2 * kBox * 4 : 0);
+    const uint32_t box_tx = 2 * kBox * RB + (kRowScaled ? 2 * kBox * 4 * ng : 0);
     const uint32_t q_tx = G * D * 2;
 
     const float s_fp8 = (!kRowScaled && a.scale) ? __ldg(a.scale) : 1.0f;
@@ -941,7 +985,7 @@ __global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
     float2* ws_ml = reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(a.ws) +
                                               ws_acc_bytes(B, a.num_q_heads, a.num_chunks, D));
     Consumer cons;
-    cons.init(G, a.sm_scale * s_fp8 * kLog2e);
+    cons.init(G, a.sm_scale * s_fp8 * kLog2e, ng);
 
     // issue side: next flat tile fi, its stage ist, its position iw, the
     // first tile of the last pair whose queries were copied (pend) and the
@@ -983,7 +1027,7 @@ __global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
                 }
                 mbar_arrive_expect_tx(fb, nbox * box_tx + (new_pair ? q_tx : 0u) + (ends ? 4u * D : 0u));
                 const uint32_t kt = tiles_u32 + ist * (2 * L.tile_bytes);
-                const uint32_t st = scales_u32 + ist * (2 * kTile * 4);
+                const uint32_t st = scales_u32 + ist * sc_stage;
 #pragma unroll
                 for (int bx = 0; bx < 2; ++bx) {
                     if (bx >= nbox) break;
@@ -996,8 +1040,9 @@ __global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
                     tma_load_2d_u32(kt + bx * kBox * RB, &tmk, 0, row, fb, pol);
                     tma_load_2d_u32(kt + L.tile_bytes + bx * kBox * RB, &tmv, 0, row, fb, pol);
                     if (kRowScaled) {
-                        bulk_load_u32(st + bx * kBox * 4, a.cache.k_scales + row, kBox * 4, fb, pol);
-                        bulk_load_u32(st + 4 * kTile + bx * kBox * 4, a.cache.v_scales + row, kBox * 4, fb, pol);
+                        const uint32_t sb = kBox * 4 * ng;  // a box's scales: 16 rows of ng
+                        bulk_load_u32(st + bx * sb, a.cache.k_scales + (int64_t)row * ng, sb, fb, pol);
+                        bulk_load_u32(st + 2 * sb + bx * sb, a.cache.v_scales + (int64_t)row * ng, sb, fb, pol);
                     }
                 }
                 if (new_pair)
@@ -1032,9 +1077,9 @@ __global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
         if (append && cw.t == cw.n - 1)
             append_newest<FMT, D>(nkv, *patch_blk, ctx_s[cw.b] - 1, cw.t * kTile, cw.kvh, a, s_fp8,
                                   tiles_u32 + cst * (2 * L.tile_bytes), L.tile_bytes,
-                                  scales_u32 + cst * (2 * kTile * 4), lane);
+                                  scales_u32 + cst * sc_stage, lane);
         const uint32_t kt = tiles_u32 + cst * (2 * L.tile_bytes);
-        const Tile tl{kt, kt + L.tile_bytes, scales_u32 + cst * (2 * kTile * 4), min(kTile, ctx_s[cw.b] - cw.t * kTile)};
+        const Tile tl{kt, kt + L.tile_bytes, scales_u32 + cst * sc_stage, min(kTile, ctx_s[cw.b] - cw.t * kTile)};
         cons.tile(tl);
         __syncwarp();
         const bool pair_end = cw.t == cw.n - 1;
@@ -1173,7 +1218,7 @@ template <int FMT, int D, class Consumer>
 cudaError_t launch_stream(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, cudaStream_t s) {
     auto kern = decode_stream_kernel<FMT, D, Consumer>;
     const int smem = Layout(row_bytes(FMT, D), D, a.num_q_heads / a.cache.num_kv_heads, a.batch,
-                            FMT == INT8 || FMT == INT4, a.k_new != nullptr).total + 1024;
+                            FMT == INT8 || FMT == INT4, a.k_new != nullptr, a.cache.ngroups).total + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);

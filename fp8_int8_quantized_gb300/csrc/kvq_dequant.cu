@@ -1,7 +1,8 @@
 // Debug gather + dequantize-on-read: the fp32 values the decode kernels see.
 // FP8: fl32(decode(code) * scale) with the per-tensor scale ("Accelerating
 // Inference with FP8 KV Cache", "FP8 Formats: E4M3 and E5M2"); INT8 and INT4:
-// fl32(code * row_scale).  One thread per 16 values of one (slot, kv-head) row.
+// fl32(code * scale) with the row's scale, or its group's.  One thread per 16
+// values of one (slot, kv-head) row.
 #include "kvq_device.cuh"
 #include "kvq_launch.h"
 
@@ -30,8 +31,10 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(DequantArgs a) {
         return;
     }
     const int64_t src_row = ((slot / BS) * Hkv + h) * BS + slot % BS;
-    const float s = (FMT == INT8 || FMT == INT4) ? (which ? a.cache.v_scales : a.cache.k_scales)[src_row]
-                                                 : (a.scale ? __ldg(a.scale) : 1.0f);
+    const int ng = a.cache.ngroups;  // the chunk's 16 values lie in group c / (CPR / ng)
+    const float s = (FMT == INT8 || FMT == INT4)
+                        ? (which ? a.cache.v_scales : a.cache.k_scales)[src_row * ng + c / (CPR / ng)]
+                        : (a.scale ? __ldg(a.scale) : 1.0f);
     if (FMT == INT4) {
         const uint2 r4 = *reinterpret_cast<const uint2*>((which ? a.cache.v_codes : a.cache.k_codes) +
                                                          src_row * (D / 2) + c * 8);

@@ -26,6 +26,7 @@ struct CacheView {
     float* k_scales;
     float* v_scales;
     int32_t num_blocks, block_size, num_kv_heads, head_dim, fmt;
+    int32_t ngroups;  // scales per row: 1, or 2 / 4 for group quantization (FP8: 1)
 };
 
 struct AppendArgs {

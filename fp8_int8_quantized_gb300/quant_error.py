@@ -9,8 +9,9 @@ per sequence and q-head, computed here with plain fp32 torch operations.
 What this measures is the error the cache format itself introduces -- the
 accuracy question of "Accelerating Inference with FP8 KV Cache" ("FP8 E4M3 KV
 Cache": with a calibrated scale or the 1.0 default) and of "[Feature] TurboMind
-support W8A8 or FP8 KV Cache" (online INT8, and INT4) -- not the kernels' rounding, which
-the parity tests bound far below it.
+support W8A8 or FP8 KV Cache" (online INT8, and INT4), and of group quantization
+for a 4-bit cache ("[QST] Scale factors and benchmarks", the QQQ page) -- not the
+kernels' rounding, which the parity tests bound far below it.
 
     python -m fp8_int8_quantized_gb300.quant_error [--workload NAME] [--batch B] [--json]
 """
@@ -28,8 +29,24 @@ from fp8_int8_quantized_gb300 import workloads as W
 
 # (format, scale rule): E4M3 / E5M2 with the amax/max calibration scale or
 # the 1.0 default, INT8 and INT4 with their own scale per (token, kv-head) row
+# "gN": INT8 / INT4 with one scale per group of N channels of a row
 VARIANTS = [("e4m3", "amax"), ("e4m3", "one"), ("e5m2", "amax"), ("e5m2", "one"), ("int8", "row"),
-            ("int4", "row")]
+            ("int4", "row"), ("int8", "g32"), ("int4", "g32"), ("int4", "g64")]
+
+
+def variant(base: W.Workload, fmt: str, rule: str) -> W.Workload | None:
+    """The workload of one variant, or None where decode does not take it (q-heads
+    per kv-head times groups per row above 8)."""
+    if rule.startswith("g"):
+        group = int(rule[1:])
+        if base.group * (base.head_dim // group) > 8:
+            return None
+        return dataclasses.replace(base, fmt=fmt, scale_rule="row", quant_group=group)
+    return dataclasses.replace(base, fmt=fmt, scale_rule=rule, quant_group=0)
+
+
+def supported_variants(name: str) -> list[tuple[str, str]]:
+    return [v for v in VARIANTS if variant(W.WORKLOADS[name], *v) is not None]
 WINDOW_TOKENS = 1 << 19  # generation windows (values depend on the window start)
 
 
@@ -60,7 +77,8 @@ def _reference(wl: W.Workload, lay: W.Layout, q: torch.Tensor, device) -> torch.
 
 def _quantized(wl: W.Workload, lay: W.Layout, q: torch.Tensor, device):
     """Output of the quantized path and the per-tensor scale it used."""
-    cache = kvq.KVCache(lay.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim, wl.fmt, device)
+    cache = kvq.KVCache(lay.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim, wl.fmt, device,
+                        group_size=wl.quant_group)
     windows = W.chunk_positions(wl, WINDOW_TOKENS)
     k0, v0 = W.kv_tokens(wl, *windows[0], device=device)
     sv = W.calibration_scale(wl, k0, v0)
@@ -84,7 +102,9 @@ def report(name: str = "llama3-8b", batch: int = 8, device="cuda") -> list[dict]
     ref = _reference(base, lay, q, device)
     rows = []
     for fmt, rule in VARIANTS:
-        wl = dataclasses.replace(base, fmt=fmt, scale_rule=rule)
+        wl = variant(base, fmt, rule)
+        if wl is None:
+            continue
         out, sv = _quantized(wl, lay, q, device)
         d = out - ref
         cos = torch.nn.functional.cosine_similarity(out.flatten(0, 1), ref.flatten(0, 1), dim=-1)

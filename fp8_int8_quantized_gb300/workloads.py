@@ -40,6 +40,11 @@ class Workload:
     append_chunk: int = 0          # prefill chunk appended per sequence inside a step
     seed: int = 0
     description: str = ""
+    quant_group: int = 0           # INT8 / INT4: channels per scale (0 = one scale per row)
+
+    @property
+    def scales_per_row(self) -> int:
+        return self.head_dim // self.quant_group if self.quant_group else 1
 
     @property
     def group(self) -> int:
@@ -64,6 +69,11 @@ WORKLOADS = {
                                 seed=1005,
                                 description="Llama-2-13B INT4 shapes: 40x128, batch 128, ctx 4096, "
                                             "block 64, online INT4 per (token, kv-head)"),
+    "llama2-13b-int4-g32": Workload("llama2-13b-int4-g32", 128, 40, 40, 128, 64, "int4", 4096, "row",
+                                    seed=1006, quant_group=32,
+                                    description="Llama-2-13B INT4 shapes with group quantization: "
+                                                "40x128, batch 128, ctx 4096, block 64, online INT4 "
+                                                "with one scale per 32 channels"),
     "llama3-70b": Workload("llama3-70b", 256, 64, 8, 128, 16, "e4m3", 32768, "amax",
                            outliers=True, append_chunk=2048, seed=1004,
                            description="Llama-3-70B long context: 64/8 heads x128, batch 256, "
@@ -192,7 +202,7 @@ def decode_bytes(wl: Workload, ctx: torch.Tensor) -> dict:
     lengths."""
     tok = int(ctx.to(torch.int64).sum())
     kv = 2 * tok * wl.num_kv_heads * (wl.head_dim // 2 if wl.fmt == "int4" else wl.head_dim)
-    scales = 2 * tok * wl.num_kv_heads * 4 if wl.fmt in ("int8", "int4") else 0
+    scales = 2 * tok * wl.num_kv_heads * 4 * wl.scales_per_row if wl.fmt in ("int8", "int4") else 0
     qo = 2 * wl.batch * wl.num_q_heads * wl.head_dim * 2
     bt = sum(math.ceil(int(c) / wl.block_size) for c in ctx) * 4 + wl.batch * 4
     return {"kv": kv, "scales": scales, "q_out": qo, "tables": bt,
@@ -205,7 +215,7 @@ def append_bytes(wl: Workload, num_tokens: int) -> int:
     e = num_tokens * wl.num_kv_heads * wl.head_dim
     b = 2 * e * 2 + (e if wl.fmt == "int4" else 2 * e) + num_tokens * 8
     if wl.fmt in ("int8", "int4"):
-        b += 2 * num_tokens * wl.num_kv_heads * 4
+        b += 2 * num_tokens * wl.num_kv_heads * 4 * wl.scales_per_row
     return b
 
 

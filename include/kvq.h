@@ -86,8 +86,17 @@ typedef enum {
  *                     FP8 codes (u8) or INT8 codes (i8); for INT4
  *                     [..][head_dim / 2] bytes of packed codes; 16-byte aligned.
  *   k_scales, v_scales: INT8 and INT4, fp32 [num_blocks][num_kv_heads][block_size]
- *                     (one scale per (token, kv-head) row); NULL for FP8.
- *   head_dim in {64, 128}; block_size in {16, 32, 64}; fmt a kvq_fmt. */
+ *                     [head_dim / group_size] (one scale per group of channels of a
+ *                     (token, kv-head) row; one per row when group_size is 0);
+ *                     NULL for FP8.
+ *   head_dim in {64, 128}; block_size in {16, 32, 64}; fmt a kvq_fmt.
+ *   group_size: INT8 / INT4 group quantization (the QQQ page "[QST] Scale
+ *     factors and benchmarks" names group quantization for a 4-bit KV cache):
+ *     0 or head_dim = one scale per row; head_dim / 2 or head_dim / 4 = two or
+ *     four groups of consecutive channels, each quantized as a row is (its own
+ *     amax and scale).  Must be 0 for FP8; any other value is INVALID_ARG.
+ *     Decode takes a group count times the q-heads per kv-head of at most 8
+ *     (UNSUPPORTED otherwise); chunked prefill takes one scale per row only. */
 typedef struct {
     void* k_codes;
     void* v_codes;
@@ -98,6 +107,7 @@ typedef struct {
     int32_t num_kv_heads;
     int32_t head_dim;
     int32_t fmt;
+    int32_t group_size;
 } kvq_cache;
 
 /* Quantize-on-write ([TGI] intro and "FP8 Formats"; [LMD] online INT8).

@@ -33,7 +33,7 @@ class DeviceWorkload:
         self.wl, self.device = wl, device
         self.lay = W.Layout(wl, ctx)
         self.cache = kvq.KVCache(self.lay.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim, wl.fmt,
-                                 device, fill=sentinel)
+                                 device, fill=sentinel, group_size=wl.quant_group)
         self.windows = W.chunk_positions(wl, chunk_tokens)
         k0, v0 = W.kv_tokens(wl, *self.windows[0], device=device)
         self.scale_value = W.calibration_scale(wl, k0, v0)
@@ -88,7 +88,7 @@ class DeviceWorkload:
             vs = self.cache.v_scales.index_select(0, idx).cpu().numpy()
         oc = oracle.Cache(len(blocks), wl.num_kv_heads, bs, wl.head_dim, ORACLE_FMT[wl.fmt],
                           k_codes=np.ascontiguousarray(kc), v_codes=np.ascontiguousarray(vc),
-                          k_scales=ks, v_scales=vs)
+                          k_scales=ks, v_scales=vs, group=wl.quant_group)
         mb = max(1, max(len(t) for t in tables))
         bt = np.zeros((len(seqs), mb), np.int32)
         for i, t in enumerate(tables):

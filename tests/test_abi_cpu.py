@@ -43,6 +43,29 @@ def test_status_codes_match_header():
         assert re.search(rf"\b{name}\s*=\s*{code}\b", src), name
 
 
+def test_cache_struct_matches_header():
+    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    body = re.search(r"typedef struct \{([^}]*)\} kvq_cache;", src).group(1)
+    names = re.findall(r"\b(\w+);", body)
+    assert names == [f[0] for f in kvq.KvqCacheDesc._fields_]
+
+
+def test_group_sizes_checked_before_any_cuda_call(lib):
+    import ctypes
+    d8 = kvq.KvqCacheDesc(16, 16, 16, 16, 8, 16, 2, 128, kvq.INT8, 24)
+    assert lib.kvq_append(16, 16, ctypes.byref(d8), 16, 4, None, kvq.INT8, None) == 1     # 24 does not divide
+    d8.group_size = 16
+    assert lib.kvq_append(16, 16, ctypes.byref(d8), 16, 4, None, kvq.INT8, None) == 1     # 8 groups
+    f8 = kvq.KvqCacheDesc(16, 16, None, None, 8, 16, 2, 128, kvq.E4M3, 32)
+    assert lib.kvq_append(16, 16, ctypes.byref(f8), 16, 4, None, kvq.E4M3, None) == 1     # FP8 has no groups
+    d4 = kvq.KvqCacheDesc(16, 16, 16, 16, 8, 16, 2, 128, kvq.INT4, 32)
+    # 4 groups x 4 q-heads per kv-head = 16 operand rows > 8
+    assert lib.kvq_decode_attention(16, ctypes.byref(d4), 16, 4, 16, 2, 8, 64, None, kvq.INT4, 0.0,
+                                    16, None, 0, 0, None) == 2
+    assert lib.kvq_prefill_attention(16, ctypes.byref(d4), 16, 4, 16, 16, 2, 4, 4, 4, None, kvq.INT4,
+                                     0.0, 16, None) == 2                                   # rows scales only
+
+
 def test_decode_kernel_knob(lib):
     prev = lib.kvq_set_decode_kernel(1)
     assert lib.kvq_set_decode_kernel(prev) == 1

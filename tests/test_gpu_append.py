@@ -22,16 +22,17 @@ def gpu_cache_to_oracle(c: kvq.KVCache) -> oracle.Cache:
     return oracle.Cache(c.num_blocks, c.num_kv_heads, c.block_size, c.head_dim, c.fmt,
                         k_codes=c.k_codes.cpu().numpy(), v_codes=c.v_codes.cpu().numpy(),
                         k_scales=None if c.k_scales is None else c.k_scales.cpu().numpy(),
-                        v_scales=None if c.v_scales is None else c.v_scales.cpu().numpy())
+                        v_scales=None if c.v_scales is None else c.v_scales.cpu().numpy(),
+                        group=c.group_size)
 
 
-def run_both(k, v, slots, NB, Hkv, BS, D, fmt, scale):
+def run_both(k, v, slots, NB, Hkv, BS, D, fmt, scale, group=0):
     dev = torch.device("cuda")
-    c = kvq.KVCache(NB, Hkv, BS, D, fmt, dev, fill=0xA5)
+    c = kvq.KVCache(NB, Hkv, BS, D, fmt, dev, fill=0xA5, group_size=group)
     st = None if scale is None else torch.tensor([scale], dtype=torch.float32, device=dev)
     kvq.append(k.to(dev), v.to(dev), c, slots.to(dev), st)
     torch.cuda.synchronize()
-    ref = oracle.Cache(NB, Hkv, BS, D, ORACLE_FMT[fmt] if isinstance(fmt, str) else fmt)
+    ref = oracle.Cache(NB, Hkv, BS, D, ORACLE_FMT[fmt] if isinstance(fmt, str) else fmt, group=group)
     if c.k_scales is not None:
         ref.k_scales[:] = 0
         ref.v_scales[:] = 0
@@ -156,7 +157,36 @@ def test_append_empty_and_validation():
     assert ei.value.status == 1
 
 
-@pytest.mark.parametrize("name", ["llama2-7b", "llama3-8b", "llama2-13b-int8", "llama2-13b-int4", "llama3-70b"])
+@pytest.mark.parametrize("fmt", ["int8", "int4"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("ng", [2, 4])
+def test_append_groups_bit_exact(fmt, D, ng):
+    """Group quantization: every code and every group scale bit-exact, with an
+    outlier channel, an all-zero group beside non-zero ones and an all-zero row."""
+    g = torch.Generator().manual_seed(D * 3 + ng + len(fmt))
+    Hkv, NB, BS, T = 3, 7, 16, 90
+    k = (torch.randn((T, Hkv, D), generator=g) * 3).to(torch.float16)
+    v = (torch.randn((T, Hkv, D), generator=g) * 3).to(torch.float16)
+    k[:, 1, 5] *= 20
+    v[2, 0, :D // ng] = 0
+    k[6, 2] = 0
+    slots = torch.randperm(NB * BS, generator=g)[:T].to(torch.int64)
+    slots[::11] = -1
+    c, ref = run_both(k, v, slots, NB, Hkv, BS, D, fmt, None, group=D // ng)
+    assert c.k_scales.shape == (NB, Hkv, BS, ng)
+    assert np.array_equal(c.k_codes.cpu().numpy(), ref.k_codes)
+    assert np.array_equal(c.v_codes.cpu().numpy(), ref.v_codes)
+    assert np.array_equal(c.k_scales.cpu().numpy().view(np.uint32), ref.k_scales.view(np.uint32))
+    assert np.array_equal(c.v_scales.cpu().numpy().view(np.uint32), ref.v_scales.view(np.uint32))
+    ok, ov = kvq.dequant(c, slots.clamp(min=0).cuda())
+    rk, rv = oracle.dequant(ref, slots.clamp(min=0).numpy())
+    assert np.array_equal(ok.cpu().numpy().view(np.uint32), rk.view(np.uint32))
+    assert np.array_equal(ov.cpu().numpy().view(np.uint32), rv.view(np.uint32))
+    assert kvq.device_error_check()[0] == 0
+
+
+@pytest.mark.parametrize("name", ["llama2-7b", "llama3-8b", "llama2-13b-int8", "llama2-13b-int4", "llama3-70b",
+                                  "llama2-13b-int4-g32"])
 def test_append_full_size_sampled(name):
     """The workloads' own append launches (their full windows), checked on a
     seeded sample of tokens against the oracle."""
@@ -168,7 +198,8 @@ def test_append_full_size_sampled(name):
     slots = lay.slots(*win).to(dev)
     scale_v = W.calibration_scale(wl, k, v)
     scale = None if scale_v is None else torch.tensor([scale_v], dtype=torch.float32, device=dev)
-    c = kvq.KVCache(lay.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim, wl.fmt, dev, fill=0xA5)
+    c = kvq.KVCache(lay.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim, wl.fmt, dev, fill=0xA5,
+                    group_size=wl.quant_group)
     kvq.append(k, v, c, slots, scale)
     torch.cuda.synchronize()
     assert kvq.device_error_check()[0] == 0
@@ -179,7 +210,7 @@ def test_append_full_size_sampled(name):
     pd = pick.to(dev)
     ks, vs = k[pd].cpu(), v[pd].cpu()
     ref = oracle.Cache(len(pick) // wl.block_size + 1, wl.num_kv_heads, wl.block_size, wl.head_dim,
-                       ORACLE_FMT[wl.fmt])
+                       ORACLE_FMT[wl.fmt], group=wl.quant_group)
     oracle.append(ks.numpy(), vs.numpy(), np.arange(len(pick), dtype=np.int64), ref, scale_v)
     bs = wl.block_size
     blk, off = (s // bs).to(dev), (s % bs).to(dev)

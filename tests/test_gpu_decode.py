@@ -23,10 +23,10 @@ def _lib():
     kvq.set_decode_kernel(kvq.KERNEL_AUTO)
 
 
-def small(fmt, B, Hq, Hkv, D, BS, ctx, seed=0, outliers=True, scale_rule=None):
+def small(fmt, B, Hq, Hkv, D, BS, ctx, seed=0, outliers=True, scale_rule=None, group=0):
     wl = W.Workload(f"t-{fmt}", B, Hq, Hkv, D, BS, fmt, max(ctx), scale_rule or
                     ("amax" if fmt == "e4m3" else ("row" if fmt in ("int8", "int4") else "one")),
-                    outliers=outliers, seed=seed)
+                    outliers=outliers, seed=seed, quant_group=group)
     return DeviceWorkload(wl, chunk_tokens=1 << 16, ctx=torch.tensor(ctx, dtype=torch.int32))
 
 
@@ -43,17 +43,29 @@ CASES = [
     ("int4", 2, 4, 4, 128, 64, [640, 65]),
     ("int4", 3, 8, 2, 64, 16, [129, 1, 256]),
     ("int4", 2, 32, 8, 128, 32, [1000, 33]),
+    # group quantization (last field: channels per scale): q-heads per kv-head x groups <= 8
+    ("int8", 2, 4, 2, 128, 32, [500, 33], 32),
+    ("int4", 2, 4, 4, 128, 64, [640, 65], 32),
+    ("int4", 3, 8, 2, 64, 16, [129, 1, 256], 32),
+    ("int8", 3, 8, 1, 64, 16, [300, 1, 77], 64),
+    ("int8", 2, 3, 3, 64, 16, [200, 45], 16),
+    ("int4", 2, 4, 1, 128, 16, [96, 1000], 64),
 ]
 
 
-@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}-G{c[2] // c[3]}-D{c[4]}-BS{c[5]}")
+def case_id(c):
+    return f"{c[0]}-G{c[2] // c[3]}-D{c[4]}-BS{c[5]}" + (f"-g{c[7]}" if len(c) > 7 else "")
+
+
+@pytest.mark.parametrize("case", CASES, ids=case_id)
 @pytest.mark.parametrize("kernel", [kvq.KERNEL_MMA, kvq.KERNEL_SIMT])
 @pytest.mark.parametrize("partition", [0, 64, 256])
 def test_decode_small(case, kernel, partition):
-    fmt, B, Hq, Hkv, D, BS, ctx = case
-    if kernel == kvq.KERNEL_SIMT and (Hq // Hkv > 4 or fmt == "int4"):
-        pytest.skip("CUDA-core kernel covers 8-bit codes and group size <= 4")
-    dw = small(fmt, B, Hq, Hkv, D, BS, ctx, seed=len(ctx) + D)
+    fmt, B, Hq, Hkv, D, BS, ctx = case[:7]
+    group = case[7] if len(case) > 7 else 0
+    if kernel == kvq.KERNEL_SIMT and (Hq // Hkv > 4 or fmt == "int4" or (group and group != D)):
+        pytest.skip("CUDA-core kernel covers 8-bit codes, one scale per row and group size <= 4")
+    dw = small(fmt, B, Hq, Hkv, D, BS, ctx, seed=len(ctx) + D, group=group)
     kvq.set_decode_kernel(kernel)
     out = dw.decode(partition_size=partition)
     torch.cuda.synchronize()
@@ -139,6 +151,7 @@ def test_workspace_too_small_and_empty_batch():
                                        ("llama3-8b", [0, 21, 40, 63]),
                                        ("llama2-13b-int8", [0, 77, 127]),
                                        ("llama2-13b-int4", [0, 64, 127]),
+                                       ("llama2-13b-int4-g32", [0, 50, 127]),
                                        ("llama3-70b", [0, 255])])
 def test_decode_workload_sampled(name, seqs):
     wl = W.WORKLOADS[name]

@@ -22,15 +22,16 @@ def _lib():
     kvq.set_decode_kernel(kvq.KERNEL_AUTO)
 
 
-def small(fmt, B, Hq, Hkv, D, BS, ctx, seed):
+def small(fmt, B, Hq, Hkv, D, BS, ctx, seed, group=0):
     wl = W.Workload(f"f-{fmt}", B, Hq, Hkv, D, BS, fmt, max(max(ctx), 1),
                     "amax" if fmt == "e4m3" else ("row" if fmt in ("int8", "int4") else "one"), outliers=True,
-                    seed=seed)
+                    seed=seed, quant_group=group)
     return DeviceWorkload(wl, chunk_tokens=1 << 16, ctx=torch.tensor(ctx, dtype=torch.int32))
 
 
 def clone(c: kvq.KVCache) -> kvq.KVCache:
-    n = kvq.KVCache(c.num_blocks, c.num_kv_heads, c.block_size, c.head_dim, c.fmt, c.k_codes.device)
+    n = kvq.KVCache(c.num_blocks, c.num_kv_heads, c.block_size, c.head_dim, c.fmt, c.k_codes.device,
+                    group_size=c.group_size)
     n.k_codes.copy_(c.k_codes)
     n.v_codes.copy_(c.v_codes)
     if c.k_scales is not None:
@@ -82,17 +83,27 @@ CASES = [
     ("e4m3", 2, 16, 2, 128, 32, [2050, 700]),
     ("int4", 4, 4, 4, 128, 64, [640, 65, 1, 48]),
     ("int4", 3, 8, 2, 64, 16, [129, 0, 256]),
+    # group quantization (last field: channels per scale)
+    ("int8", 4, 4, 2, 128, 32, [500, 33, 1, 64], 32),
+    ("int4", 4, 4, 4, 128, 64, [640, 65, 1, 48], 32),
+    ("int4", 3, 8, 2, 64, 16, [129, 0, 256], 32),
+    ("int8", 3, 3, 3, 64, 16, [200, 45, 16], 16),
 ]
 
 
-@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0]}-G{c[2] // c[3]}-D{c[4]}-BS{c[5]}")
+def case_id(c):
+    return f"{c[0]}-G{c[2] // c[3]}-D{c[4]}-BS{c[5]}" + (f"-g{c[7]}" if len(c) > 7 else "")
+
+
+@pytest.mark.parametrize("case", CASES, ids=case_id)
 @pytest.mark.parametrize("kernel", [kvq.KERNEL_MMA, kvq.KERNEL_SIMT])
 @pytest.mark.parametrize("partition", [0, 64])
 def test_fused_equals_append_then_decode(case, kernel, partition):
-    fmt, B, Hq, Hkv, D, BS, ctx = case
-    if kernel == kvq.KERNEL_SIMT and (Hq // Hkv > 4 or fmt == "int4"):
-        pytest.skip("CUDA-core kernel covers 8-bit codes and group size <= 4")
-    dw = small(fmt, B, Hq, Hkv, D, BS, ctx, seed=len(ctx) * 31 + D)
+    fmt, B, Hq, Hkv, D, BS, ctx = case[:7]
+    group = case[7] if len(case) > 7 else 0
+    if kernel == kvq.KERNEL_SIMT and (Hq // Hkv > 4 or fmt == "int4" or group):
+        pytest.skip("CUDA-core kernel covers 8-bit codes, one scale per row and group size <= 4")
+    dw = small(fmt, B, Hq, Hkv, D, BS, ctx, seed=len(ctx) * 31 + D, group=group)
     kvq.set_decode_kernel(kernel)
     g = torch.Generator(device="cpu").manual_seed(B * 100 + D)
     k_new = (torch.randn((B, Hkv, D), generator=g) * 2).to(torch.float16).to(dw.device)
@@ -121,7 +132,8 @@ def test_fused_bad_block_id_is_reported_and_not_written():
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
 
 
-@pytest.mark.parametrize("name", ["llama2-7b", "llama3-8b", "llama2-13b-int8", "llama2-13b-int4"])
+@pytest.mark.parametrize("name", ["llama2-7b", "llama3-8b", "llama2-13b-int8", "llama2-13b-int4",
+                                  "llama2-13b-int4-g32"])
 def test_fused_full_size_sampled(name):
     """The benchmark's fused step on a full decode workload: the cache it leaves
     equals kvq_append of the same rows, and sampled sequences' outputs match
