@@ -19,11 +19,13 @@
 // most two warps and owns two partial slots (max, sum, unnormalised acc) that
 // decode_reduce_kernel merges into the fp16 output.
 //
-// Every warp owns a ring of kSpw stages (a 16-token K tile and V tile of one
-// paged block, 128-byte swizzled for head_dim 128, plus INT8 row scales), each
-// with an mbarrier, and refills a stage with 2-D TMA tile loads
-// (cp.async.bulk.tensor, issued by lane 0) right after consuming it, so its
-// loads run kSpw - 1 tiles ahead across pair boundaries.  Block ids of the
+// Every warp owns a ring of kSpw stages (a stage is a 32-token tile: two
+// 16-row boxes of K and of V from paged blocks, 128-byte swizzled for head_dim
+// 128, plus INT8 / INT4 scales), each with an mbarrier, and refills a stage
+// with 2-D TMA tile loads (cp.async.bulk.tensor, issued by lane 0) right after
+// consuming it, so its loads run the ring's length ahead across pair
+// boundaries.  (More stages for the half-size INT4 tiles measured no faster:
+// INT4 decode is not bound by the bytes in flight.)  Block ids of the
 // next 32 tiles are held one per lane (loaded one window ahead); the first
 // tile of each (sequence, kv-head) pair also carries a bulk copy of the pair's
 // query rows into the warp's query buffer.
@@ -656,11 +658,13 @@ struct MmaConsumer {
     }
 
     __device__ void tile(const Tile& cx) {
-        const bool two = cx.valid > kBox;  // warp-uniform: the second box holds context rows
+        // The second box is always computed, also when it lies past the context
+        // (its logits masked, its V codes zeroed and its weights 0, whatever the
+        // stage holds), so that the two boxes' products can overlap: 1-3% faster
+        // than skipping it on the last tile of a pair.
         float z0[4], z1[4];
         qk_box(cx.k, cx.s, cx.valid, z0);
-        if (two) qk_box(cx.k + kBox * RB, cx.s + 4 * kBox * ng, cx.valid - kBox, z1);
-        else z1[0] = z1[1] = z1[2] = z1[3] = -INFINITY;
+        qk_box(cx.k + kBox * RB, cx.s + 4 * kBox * ng, cx.valid - kBox, z1);
         float mx = fmaxf(fmaxf(fmaxf(z0[0], z0[1]), fmaxf(z0[2], z0[3])), fmaxf(fmaxf(z1[0], z1[1]), fmaxf(z1[2], z1[3])));
         mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
@@ -676,21 +680,30 @@ struct MmaConsumer {
         }
         m = mn;
         l = l * alpha + (((p0[0] + p0[1]) + (p0[2] + p0[3])) + ((p1[0] + p1[1]) + (p1[2] + p1[3])));
-        if (kRowScaled) {  // fold the V row (column group) scales into P (masked tokens keep p = 0)
+        if (kRowScaled) {  // fold the V row (column group) scales into P
             const uint32_t sv = cx.s + 4 * kTile * ng;
+            float a[4], b[4];
             if (ng == 1) {
                 const float2 a01 = __uint_as_float2(lds64(sv + 8 * c)), a23 = __uint_as_float2(lds64(sv + 32 + 8 * c));
-                p0[0] *= a01.x; p0[1] *= a01.y; p0[2] *= a23.x; p0[3] *= a23.y;
-                if (two) {
-                    const float2 b01 = __uint_as_float2(lds64(sv + 64 + 8 * c)), b23 = __uint_as_float2(lds64(sv + 96 + 8 * c));
-                    p1[0] *= b01.x; p1[1] *= b01.y; p1[2] *= b23.x; p1[3] *= b23.y;
-                }
+                const float2 b01 = __uint_as_float2(lds64(sv + 64 + 8 * c)), b23 = __uint_as_float2(lds64(sv + 96 + 8 * c));
+                a[0] = a01.x; a[1] = a01.y; a[2] = a23.x; a[3] = a23.y;
+                b[0] = b01.x; b[1] = b01.y; b[2] = b23.x; b[3] = b23.y;
             } else {  // scales [token][ng]: tokens 2c, 2c+1, 8+2c, 9+2c (+16) of group kg
-                const uint32_t a0 = sv + 4 * (2 * c * ng + kg);
-                p0[0] *= ldsf(a0); p0[1] *= ldsf(a0 + 4 * ng); p0[2] *= ldsf(a0 + 32 * ng); p0[3] *= ldsf(a0 + 36 * ng);
-                if (two) {
-                    const uint32_t b0 = a0 + 64 * ng;
-                    p1[0] *= ldsf(b0); p1[1] *= ldsf(b0 + 4 * ng); p1[2] *= ldsf(b0 + 32 * ng); p1[3] *= ldsf(b0 + 36 * ng);
+                const uint32_t a0 = sv + 4 * (2 * c * ng + kg), b0 = a0 + 64 * ng;
+                a[0] = ldsf(a0); a[1] = ldsf(a0 + 4 * ng); a[2] = ldsf(a0 + 32 * ng); a[3] = ldsf(a0 + 36 * ng);
+                b[0] = ldsf(b0); b[1] = ldsf(b0 + 4 * ng); b[2] = ldsf(b0 + 32 * ng); b[3] = ldsf(b0 + 36 * ng);
+            }
+            if (cx.valid >= kTile) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    p0[e] *= a[e];
+                    p1[e] *= b[e];
+                }
+            } else {  // a masked token keeps p = 0 whatever its (never written) scale slot holds
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    p0[e] = p0[e] != 0.f ? p0[e] * a[e] : 0.f;
+                    p1[e] = p1[e] != 0.f ? p1[e] * b[e] : 0.f;
                 }
             }
             psum *= alpha;
@@ -707,10 +720,8 @@ struct MmaConsumer {
         uint32_t pb0, pb1, pl0, pl1;
         p_frags(p0, pb0, pb1, pl0, pl1, psum);
         pv_box(cx.v, cx.valid, pb0, pb1, pl0, pl1);
-        if (two) {
-            p_frags(p1, pb0, pb1, pl0, pl1, psum);
-            pv_box(cx.v + kBox * RB, cx.valid - kBox, pb0, pb1, pl0, pl1);
-        }
+        p_frags(p1, pb0, pb1, pl0, pl1, psum);
+        pv_box(cx.v + kBox * RB, cx.valid - kBox, pb0, pb1, pl0, pl1);
     }
 
     __device__ void flush(const Flush& f) {

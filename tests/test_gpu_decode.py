@@ -121,6 +121,34 @@ def test_nan_codes_past_the_context_do_not_leak():
     assert rel_err(o, ref) <= ATOL_REL
 
 
+@pytest.mark.parametrize("fmt,group", [("int8", 0), ("int4", 0), ("int4", 32)])
+def test_nan_scales_past_the_context_do_not_leak(fmt, group):
+    """Scale slots of rows past the context that were never written hold NaN
+    (the caller's memory is not cleared): the masked tokens' weights stay 0."""
+    wl = W.Workload("nans", 3, 4, 2, 128, 16, fmt, 40, "row", seed=4, quant_group=group)
+    ctx = torch.tensor([37, 40, 17], dtype=torch.int32)
+    lay = W.Layout(wl, ctx)
+    dev = torch.device("cuda")
+    cache = kvq.KVCache(lay.num_blocks, 2, 16, 128, fmt, dev, fill=0x77, group_size=group)
+    cache.k_scales.fill_(float("nan"))
+    cache.v_scales.fill_(float("nan"))
+    k, v = W.kv_tokens(wl, 0, 40, dev)
+    slots = lay.slots(0, 40).to(dev)          # -1 past each sequence's context
+    kvq.append(k, v, cache, slots)
+    q = W.query(wl, dev)
+    for kernel in (kvq.KERNEL_MMA, kvq.KERNEL_SIMT) if not group and fmt == "int8" else (kvq.KERNEL_MMA,):
+        kvq.set_decode_kernel(kernel)
+        out = kvq.decode_attention(q, cache, lay.block_tables.to(dev), ctx.to(dev), 40)
+        o = out.float().cpu().numpy()
+        assert np.isfinite(o).all(), kernel
+        oc = oracle.Cache(lay.num_blocks, 2, 16, 128, oracle.FORMATS[fmt], k_codes=cache.k_codes.cpu().numpy(),
+                          v_codes=cache.v_codes.cpu().numpy(), k_scales=cache.k_scales.cpu().numpy(),
+                          v_scales=cache.v_scales.cpu().numpy(), group=group)
+        ref = oracle.decode_attention(q.cpu().numpy(), oc, lay.block_tables.numpy(), ctx.numpy(), None)
+        assert rel_err(o, ref) <= ATOL_REL
+    kvq.set_decode_kernel(kvq.KERNEL_AUTO)
+
+
 def test_bad_block_id_is_reported_without_fault():
     dw = small("e4m3", 2, 4, 4, 128, 16, [64, 64], seed=1)
     bt = dw.block_tables.clone()
