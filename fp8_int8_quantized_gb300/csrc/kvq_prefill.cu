@@ -15,31 +15,34 @@
 // chunk's own K/V included) sits at position ctx - n + i and attends to every
 // token t <= that position.
 //
-// Work decomposition.  A CTA owns one M tile of 128 rows: 128 / G consecutive
-// queries of one (sequence, kv-head) times the G q-heads of that kv-head's
-// group, so every K/V tile a CTA dequantizes serves all G heads.  It walks the
-// cache in KV tiles of 128 tokens up to the tile's last position.  Roles:
-//   * warps 4-7 (dequant): plain 16-byte loads of the tile's K and V codes
-//     through the block table (L2 serves the other M tiles of the same
+// Work decomposition.  A query tile is 128 rows: 128 / G consecutive queries
+// of one (sequence, kv-head) times the G q-heads of that kv-head's group, so
+// every K/V tile dequantized serves all G heads.  A CTA owns two consecutive
+// query tiles of the same (sequence, kv-head) and walks the cache in KV tiles
+// of 64 tokens up to the later tile's last position; both query tiles use each
+// dequantized K/V tile, which halves the dequantization per product.  Roles
+// (one CTA per SM: 480 threads, 512 tensor-memory columns, ~131 KB of shared
+// memory):
+//   * warps 9-14 (dequant): plain 16-byte loads of the tile's K and V codes
+//     through the block table (L2 serves the other CTAs of the same
 //     sequence), exact conversion to fp16, stores into the 128-byte-swizzled
-//     K-major layout the tensor core reads; positions past the tile's last
-//     query are written as zeros.  They also stage the query tile and the INT8 /
-//     INT4 row scales;
-//   * thread 0 (also a softmax thread) issues S = Q K^T (M 128, N 128, K
-//     head_dim) into tensor memory and O += P V (M 128, N head_dim, K 128)
-//     with P read from tensor memory, V from shared memory as an MN-major
-//     operand, and commits each group of MMAs to an mbarrier.  With one S
-//     buffer, S of the next tile can only be computed after O += P V of this
-//     one, so a dedicated issuing warp would wait at the same points;
-//   * warps 0-3 (softmax): thread r owns row r (tensor-memory lane r): it reads
-//     its 128 logits with tcgen05.ld, keeps a running maximum (raised only when
-//     the tile's maximum exceeds it by more than 2^8, FA4's lazy rescaling, so
-//     weights stay below 256), rescales its O row in tensor memory when the
-//     maximum moves, and writes the weights back over its logits as fp16 hi +
-//     fp16 residual (two PV MMAs, ~22 bits per weight).  At the end it
-//     normalises its O row and stores it as fp16.
-// Tensor memory per CTA: 128 columns of S / P and 128 of O (256 allocated), so
-// two CTAs share an SM and one's softmax overlaps the other's MMAs.
+//     layout the tensor core reads; positions past the last query are written
+//     as zeros.  K runs one tile ahead of V, and the codes of the next tiles
+//     are held in registers.  They also stage the two query tiles and the
+//     INT8 / INT4 row scales;
+//   * warp 8 (MMA): one elected lane issues, per KV tile j, S = Q K^T for each
+//     query tile (M 128, N 64, K head_dim, into one of two S buffers of that
+//     tile in tensor memory), then O += P V of tile j-1 for each query tile
+//     (M 128, N head_dim, K 64, P read from tensor memory, V an MN-major
+//     shared-memory operand), and commits each group to an mbarrier;
+//   * warps 0-3 and 4-7 (softmax of query tiles 0 and 1): thread r owns row r
+//     (tensor-memory lane r): it reads its 64 logits with tcgen05.ld, keeps a
+//     running maximum (raised only when the tile's maximum exceeds it by more
+//     than 2^8, FA4's lazy rescaling, so weights stay below 256), rescales its
+//     O row in tensor memory when the maximum moves, and writes the weights
+//     back over its logits as fp16 hi + fp16 residual (two PV MMAs, ~22 bits
+//     per weight).  At the end it normalises its O row and stores it as fp16.
+// Tensor memory per query tile: two S / P buffers of 64 columns and 128 of O.
 // Every wait is bounded (2 s); on timeout the CTA records the error, drains
 // the MMAs it issued and exits.
 #include <cuda_fp16.h>
@@ -50,12 +53,14 @@
 namespace kvq {
 namespace {
 
-constexpr int kRows = 128;        // M tile: (query, q-head) rows
+constexpr int kRows = 128;        // query tile: (query, q-head) rows; a CTA holds two
 constexpr int kKvTile = 64;       // tokens per KV tile
-constexpr int kThreads = 256;     // 4 softmax warps, 1 MMA warp, 3 dequant warps
-constexpr int kDqThreads = 96;    // dequantizing threads (warps 5-7)
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColO = 128;   // O accumulator columns start here (two S buffers of 64 before)
+constexpr int kMmaWarp = 8;       // warps 0-7 softmax (4 per query tile), 8 MMA, 9-14 dequant
+constexpr int kDqThreads = 192;   // dequantizing threads (warps 9-14)
+constexpr int kThreads = 32 * (kMmaWarp + 1) + kDqThreads;
+constexpr uint32_t kColsPerTile = 256;   // tensor-memory columns of one query tile
+constexpr uint32_t kTmemCols = 2 * kColsPerTile;
+constexpr uint32_t kColO = 128;   // a tile's O accumulator columns start here (two S buffers of 64 before)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (weights < 2^8)
 
@@ -228,14 +233,16 @@ __device__ __forceinline__ uint4 ld_global_nc_v4(const void* p) {
 // ------------------------------------------------------------- layout -----
 
 // Barriers.  Per-slot barriers serve tiles j with j % slots == slot; their
-// phase for tile j is (j / slots) % 2.
+// phase for tile j is (j / slots) % 2.  S and P barriers exist per query tile.
 enum Bar : int {
-    B_KFULL0, B_KFULL1,    // dequant -> MMA: K tile in its buffer (128 arrivals)
-    B_VFULL0, B_VFULL1,    // dequant -> MMA: V tile (128)
-    B_KFREE0, B_KFREE1,    // MMA -> dequant: S = Q K^T done reading the K buffer (commit)
-    B_VFREE0, B_VFREE1,    // MMA -> dequant, softmax: O += P V done (commit)
-    B_SFULL0, B_SFULL1,    // MMA -> softmax: S in its tensor-memory buffer (commit)
-    B_PFULL0, B_PFULL1,    // softmax -> MMA: P written over S (128)
+    B_KFULL0, B_KFULL1,    // dequant -> MMA: K tile in its buffer (kDqThreads arrivals)
+    B_VFULL0, B_VFULL1,    // dequant -> MMA: V tile (kDqThreads)
+    B_KFREE0, B_KFREE1,    // MMA -> dequant: both S = Q K^T done reading the K buffer (commit)
+    B_VFREE0, B_VFREE1,    // MMA -> dequant, softmax: both O += P V done (commit)
+    B_SFULL00, B_SFULL01,  // MMA -> softmax of query tile 0: S in its buffer 0 / 1 (commit)
+    B_SFULL10, B_SFULL11,  // ... of query tile 1
+    B_PFULL00, B_PFULL01,  // softmax of query tile 0 -> MMA: P written over S (128)
+    B_PFULL10, B_PFULL11,  // ... of query tile 1
     B_SC0, B_SC1, B_SC2, B_SC3,  // dequant -> softmax: INT8 / INT4 row scales of the tile
     B_OFINAL,              // every MMA done (commit)
     kNumBars
@@ -243,17 +250,17 @@ enum Bar : int {
 
 // Shared memory of one CTA (base 1024-byte aligned).  Operand tiles are
 // [rows][D] fp16 stored as D / 64 column blocks of [rows][128 B], each with the
-// 128-byte swizzle: the query tile (128 rows; A of S = Q K^T, K-major), and two
-// buffers each of K (64 rows; B of S, K-major) and V (64 rows; B of O = P V,
-// MN-major).
+// 128-byte swizzle: the two query tiles (128 rows each; A of S = Q K^T,
+// K-major), and two buffers each of K (64 rows; B of S, K-major) and V (64
+// rows; B of O = P V, MN-major).
 template <int D>
 struct SmemLayout {
-    static constexpr uint32_t kBlkQ = kRows * 128;         // one 64-column block of the query tile
+    static constexpr uint32_t kBlkQ = kRows * 128;         // one 64-column block of a query tile
     static constexpr uint32_t kBlkKV = kKvTile * 128;      // one 64-column block of a K / V tile
     static constexpr uint32_t kTileQ = kBlkQ * (D / 64);
     static constexpr uint32_t kTileKV = kBlkKV * (D / 64);
-    static constexpr uint32_t kQ = 0;
-    static constexpr uint32_t kK = kQ + kTileQ;            // two K buffers
+    static constexpr uint32_t kQ = 0;                      // two query tiles
+    static constexpr uint32_t kK = kQ + 2 * kTileQ;        // two K buffers
     static constexpr uint32_t kV = kK + 2 * kTileKV;       // two V buffers
     static constexpr uint32_t kKsc = kV + 2 * kTileKV;     // fp32 [4][64] INT8 / INT4 logit multipliers
     static constexpr uint32_t kVsc = kKsc + 4 * kKvTile * 4;  // fp32 [4][64] INT8 / INT4 V row scales
@@ -298,7 +305,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 // ------------------------------------------------------------- kernel -----
 
 template <int FMT, int D>
-__global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParams a) {
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParams a) {
     using L = SmemLayout<D>;
     constexpr int kChunks = D / 8;       // 16-byte fp16 chunks per row
     constexpr bool kRowScaled = FMT == INT8 || FMT == INT4;   // one scale per (token, kv-head) row
@@ -322,29 +329,34 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int b = blockIdx.z, kvh = blockIdx.y;
     const int Hkv = a.num_kv_heads, Hq = a.num_q_heads, G = Hq / Hkv;
-    const int TQ = kRows / G;                       // queries per M tile
-    const int qt = (int)gridDim.x - 1 - (int)blockIdx.x;  // longest tiles first
+    const int TQ = kRows / G;                       // queries per query tile
+    const int pair = (int)gridDim.x - 1 - (int)blockIdx.x;  // longest pairs first
 
     griddep_wait();
     const int q0 = a.query_start[b];
     const int n = a.query_start[b + 1] - q0;
     const int ctx = a.context_lens[b];
-    if (qt * TQ >= n) return;                       // uniform: this sequence has fewer queries
+    if (2 * pair * TQ >= n) return;                 // uniform: this sequence has fewer queries
     if (n > ctx || n > a.max_query_len || q0 < 0 || (int64_t)q0 + n > a.num_q_tokens ||
         (int64_t)ctx > (int64_t)a.max_blocks_per_seq * a.block_size) {
         if (tid == 0) record_error(a.err, DEV_ERR_RANGE, b);
         return;
     }
-    const int nq = min(TQ, n - qt * TQ);            // valid queries in this tile
-    const int p_first = ctx - n + qt * TQ;          // position of its first query
-    const int p_last = p_first + nq - 1;
-    const int nkv = p_last / kKvTile + 1;           // KV tiles to walk
-    // The M tiles of one (sequence, kv-head) read the same K/V; each walks the
-    // tiles from its own starting point (softmax accumulation is
-    // order-free), so concurrent CTAs spread their reads over the L2 slices
-    // instead of all requesting the same lines at once.
-    const int rot = (int)(((unsigned)qt * 37u) % (unsigned)nkv);
-    auto tile_of = [&](int j) { const int x = j + rot; return x >= nkv ? x - nkv : x; };
+    // Query tiles 2 * pair and 2 * pair + 1 (the second may hold no query).
+    // Tile g covers queries qt_g * TQ .. + nq_g - 1, at positions p_first_g ..
+    // p_last_g, and attends to KV tiles 0 .. nkv_g - 1; the K / V stream walks
+    // the longer range, nkv.
+    int nq[2], p_first[2], p_last[2], nkv_g[2];
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+        const int qt = 2 * pair + g;
+        nq[g] = max(0, min(TQ, n - qt * TQ));
+        p_first[g] = ctx - n + qt * TQ;
+        p_last[g] = p_first[g] + nq[g] - 1;
+        nkv_g[g] = nq[g] > 0 ? p_last[g] / kKvTile + 1 : 0;
+    }
+    const int nkv = max(nkv_g[0], nkv_g[1]);
+    const int p_max = nq[1] > 0 ? p_last[1] : p_last[0];   // last position any query attends to
     const float s_fp8 = (!kRowScaled && a.scale) ? *a.scale : 1.0f;
     // logits in log2 units: S * c_k (FP8; K carries the scale's sign) or S * c_k * s_K[t] (INT8 / INT4)
     const float c_k = a.sm_scale * kLog2e * fabsf(s_fp8);
@@ -352,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i) {
             const bool by_dq = (i >= B_KFULL0 && i <= B_VFULL1) || (i >= B_SC0 && i <= B_SC3);
-            const bool by_sm = i == B_PFULL0 || i == B_PFULL1;
+            const bool by_sm = i >= B_PFULL00 && i <= B_PFULL11;
             mbar_init(&bars[i], by_dq ? (uint32_t)kDqThreads : by_sm ? 128u : 1u);
         }
         *abort = 0;
@@ -369,17 +381,18 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 4) {
+    if (warp == kMmaWarp) {
         // ---------------------------------------------------------- MMA ----
-        // One elected lane issues every MMA, in the order S_0, S_1, O+=P_0 V_0,
-        // S_2, O+=P_1 V_1, ...: S of tile j goes into S buffer j % 2 as soon as
-        // K_j is stored, so it runs while the softmax of tile j-1 works on the
-        // other buffer.  The whole warp runs this code; elect.sync picks the
-        // issuing lane, so descriptors stay warp-uniform.
-        // Descriptors of the first K-step of each operand tile; every other
-        // K-step adds a constant to the 14-bit start-address field (addresses
-        // stay below 2^18 bytes, so the field never carries).
-        const uint64_t dq0 = smem_desc(sbase + L::kQ, 16, 1024);
+        // One elected lane issues every MMA, per KV tile j: S_0,j and S_1,j
+        // (both query tiles against K_j, into S buffer j % 2 of each tile's
+        // tensor-memory columns), then O_0 += P_0,j-1 V_j-1 and O_1 += P_1,j-1
+        // V_j-1: S of tile j runs while the softmax of tile j-1 works on the
+        // other buffers.  A query tile takes no MMA for KV tiles past its last
+        // position.  The whole warp runs this code; elect.sync picks the issuing
+        // lane, so descriptors stay warp-uniform.  Descriptors of the first
+        // K-step of each operand tile; every other K-step adds a constant to the
+        // 14-bit start-address field (addresses stay below 2^18 bytes, so the
+        // field never carries).
         const uint64_t dk0 = smem_desc(sbase + L::kK, 16, 1024);
         const uint64_t dv0 = smem_desc(sbase + L::kV, L::kBlkKV, 1024);
         auto issue_qk = [&](int j) {
@@ -387,30 +400,40 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
             if (!wait_or_abort(&bars[B_KFULL0 + sl], (j >> 1) & 1, abort, a.err)) return false;
             tc_fence_after();
             const uint64_t dk = dk0 + ((sl * L::kTileKV) >> 4);
-            const uint32_t d_tmem = tmem + sl * kKvTile;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk & 3) * 32;
-                mma_ss_warp(d_tmem, dq0 + (((kk >> 2) * L::kBlkQ + off) >> 4), dk + (((kk >> 2) * L::kBlkKV + off) >> 4),
-                            kIdescQK, kk > 0);
+            for (int g = 0; g < 2; ++g) {
+                if (j >= nkv_g[g]) continue;
+                const uint64_t dq0 = smem_desc(sbase + L::kQ + g * L::kTileQ, 16, 1024);
+                const uint32_t d_tmem = tmem + g * kColsPerTile + sl * kKvTile;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk & 3) * 32;
+                    mma_ss_warp(d_tmem, dq0 + (((kk >> 2) * L::kBlkQ + off) >> 4),
+                                dk + (((kk >> 2) * L::kBlkKV + off) >> 4), kIdescQK, kk > 0);
+                }
+                mma_commit_warp(&bars[B_SFULL00 + 2 * g + sl]);
             }
-            mma_commit_warp(&bars[B_SFULL0 + sl]);
             mma_commit_warp(&bars[B_KFREE0 + sl]);
             return true;
         };
         auto issue_pv = [&](int j) {
             const int sl = j & 1;
-            if (!wait_or_abort(&bars[B_PFULL0 + sl], (j >> 1) & 1, abort, a.err)) return false;
             if (!wait_or_abort(&bars[B_VFULL0 + sl], (j >> 1) & 1, abort, a.err)) return false;
-            tc_fence_after();
             const uint64_t dv = dv0 + ((sl * L::kTileKV) >> 4);
-            const uint32_t p_tmem = tmem + sl * kKvTile;
 #pragma unroll
-            for (int kk = 0; kk < kKvTile / 16; ++kk) {
-                const uint32_t a_hi = p_tmem + 16 * kk;   // P of tokens 16kk .. 16kk+15
-                const uint64_t vd = dv + ((kk * 2048) >> 4);
-                mma_ts_warp(tmem + kColO, a_hi, vd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-                mma_ts_warp(tmem + kColO, a_hi + 8, vd, kIdescPV, 1u);
+            for (int g = 0; g < 2; ++g) {
+                if (j >= nkv_g[g]) continue;
+                if (!wait_or_abort(&bars[B_PFULL00 + 2 * g + sl], (j >> 1) & 1, abort, a.err)) return false;
+                tc_fence_after();
+                const uint32_t o_tmem = tmem + g * kColsPerTile + kColO;
+                const uint32_t p_tmem = tmem + g * kColsPerTile + sl * kKvTile;
+#pragma unroll
+                for (int kk = 0; kk < kKvTile / 16; ++kk) {
+                    const uint32_t a_hi = p_tmem + 16 * kk;   // P of tokens 16kk .. 16kk+15
+                    const uint64_t vd = dv + ((kk * 2048) >> 4);
+                    mma_ts_warp(o_tmem, a_hi, vd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_ts_warp(o_tmem, a_hi + 8, vd, kIdescPV, 1u);
+                }
             }
             mma_commit_warp(&bars[B_VFREE0 + sl]);
             return true;
@@ -422,24 +445,24 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
         }
         if (mma_ok && !*abort) issue_pv(nkv - 1);
         mma_commit_warp(&bars[B_OFINAL]);   // after every MMA this CTA issued
-    } else if (warp >= 5) {
+    } else if (warp > kMmaWarp) {
         // ------------------------------------------------------ dequant ----
-        const int dt = tid - 160;
+        const int dt = tid - 32 * (kMmaWarp + 1);   // 0 .. kDqThreads - 1
         const size_t head_stride = (size_t)a.block_size * kRowBytes;
         const int32_t* bt = a.block_tables + (size_t)b * a.max_blocks_per_seq;
-        // query tile: row r = (query qt*TQ + r / G, head kvh*G + r % G)
-        for (int e = dt; e < kRows * kChunks; e += kDqThreads) {
-            const int r = e / kChunks, c = e % kChunks;
+        // query tiles: row r of tile g = (query (2 * pair + g) * TQ + r / G, head kvh * G + r % G)
+        for (int e = dt; e < 2 * kRows * kChunks; e += kDqThreads) {
+            const int g = e / (kRows * kChunks), r = (e / kChunks) % kRows, c = e % kChunks;
             const int qi = r / G;
             uint4 v = make_uint4(0, 0, 0, 0);
-            if (r < TQ * G && qi < nq) {
-                const size_t row = (size_t)(q0 + qt * TQ + qi) * Hq + kvh * G + r % G;
+            if (r < TQ * G && qi < (g ? nq[1] : nq[0])) {
+                const size_t row = (size_t)(q0 + (2 * pair + g) * TQ + qi) * Hq + kvh * G + r % G;
                 v = *reinterpret_cast<const uint4*>(a.q + row * D + c * 8);
             }
-            st_shared_v4(sbase + L::kQ + tile_off(L::kBlkQ, r, c), v);
+            st_shared_v4(sbase + L::kQ + g * L::kTileQ + tile_off(L::kBlkQ, r, c), v);
         }
-        // Thread dt handles vectors e = it * 96 + dt (it = 0 .. kVecsPerThread-1,
-        // e below kTileVecs): the 16 codes c16 of token row u, with rows varying
+        // Thread dt handles vectors e = it * kDqThreads + dt (e below
+        // kTileVecs): the 16 codes c16 of token row u, with rows varying
         // fastest across groups of 8 lanes: each 8-lane group stores one 16-byte
         // column chunk of 8 consecutive rows, which the 128-byte swizzle spreads
         // over all 32 banks, and each warp load reads whole 32-byte sectors of 8
@@ -457,9 +480,9 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
         auto fetch_ids = [&](int j, int (&blk)[kVecsPerThread]) {
 #pragma unroll
             for (int it = 0; it < kVecsPerThread; ++it) {
-                const int t = tile_of(j) * kKvTile + row_of(it);
+                const int t = j * kKvTile + row_of(it);
                 int id = -1;
-                if (has(it) && j < nkv && t <= p_last) {
+                if (has(it) && j < nkv && t <= p_max) {
                     id = bt[t >> lbs];
                     if (id < 0 || id >= a.num_blocks) {
                         record_error(a.err, DEV_ERR_RANGE, id);
@@ -473,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
                               const int (&blk)[kVecsPerThread]) {
 #pragma unroll
             for (int it = 0; it < kVecsPerThread; ++it) {
-                const int t = tile_of(j) * kKvTile + row_of(it);
+                const int t = j * kKvTile + row_of(it);
                 cv[it] = make_uint4(0, 0, 0, 0);
                 if (blk[it] >= 0)
                     cv[it] = ld_global_nc_v4(codes + ((size_t)blk[it] * Hkv + kvh) * head_stride +
@@ -482,8 +505,8 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
         };
         auto load_scales = [&](int j, float& ks, float& vs) {
             ks = vs = 0.f;
-            const int t = tile_of(j) * kKvTile + dt;
-            if (dt < kKvTile && t <= p_last) {
+            const int t = j * kKvTile + dt;
+            if (dt < kKvTile && t <= p_max) {
                 const int id = bt[t >> lbs];
                 if (id >= 0 && id < a.num_blocks) {
                     const size_t srow = ((size_t)id * Hkv + kvh) * a.block_size + (t & (a.block_size - 1));
@@ -567,15 +590,18 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
         }
     } else {
         // ------------------------------------------------------ softmax ----
-        const int r = tid;
-        const bool rv = r < TQ * G && r / G < nq;
-        const int pos = rv ? p_first + r / G : p_last;
-        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+        // Warps 0-3 serve query tile 0, warps 4-7 query tile 1; thread r of a
+        // group owns row r (tensor-memory lane r, reached by warp % 4).
+        const int g = warp >> 2, r = tid & 127;
+        const int nq_g = g ? nq[1] : nq[0], nkv_me = g ? nkv_g[1] : nkv_g[0];
+        const bool rv = r < TQ * G && r / G < nq_g;
+        const int pos = rv ? (g ? p_first[1] : p_first[0]) + r / G : (g ? p_last[1] : p_last[0]);
+        const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16) + g * kColsPerTile;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int j = 0; j < nkv && ok; ++j) {
+        for (int j = 0; j < nkv_me && ok; ++j) {
             const int sl = j & 1;
-            if (!wait_or_abort(&bars[B_SFULL0 + sl], (j >> 1) & 1, abort, a.err)) { ok = false; break; }
+            if (!wait_or_abort(&bars[B_SFULL00 + 2 * g + sl], (j >> 1) & 1, abort, a.err)) { ok = false; break; }
             tc_fence_after();
             if (kRowScaled && !wait_or_abort(&bars[B_SC0 + (j & 3)], (j >> 2) & 1, abort, a.err)) {
                 ok = false;
@@ -584,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
             const float* ks = ksc + (j & 3) * kKvTile;
             const float* vs = vsc + (j & 3) * kKvTile;
             const uint32_t srow = trow + sl * kKvTile;   // this tile's S / P columns
-            const int lim = pos - tile_of(j) * kKvTile;   // columns u <= lim attend
+            const int lim = pos - j * kKvTile;           // columns u <= lim attend
             // lane 0 holds the warp's first position: past it no column is masked
             const bool full = __shfl_sync(0xFFFFFFFFu, lim, 0) >= kKvTile - 1;
             // pass 1: the tile's row maximum; the second TMEM load overlaps the first chunk's work
@@ -680,14 +706,15 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
             l += l2;
             tc_wait_st();
             tc_fence_before();
-            mbar_arrive(&bars[B_PFULL0 + sl]);
+            mbar_arrive(&bars[B_PFULL00 + 2 * g + sl]);
         }
 
-        if (ok && wait_or_abort(&bars[B_OFINAL], 0, abort, a.err)) {
+        if (ok && nq_g > 0 && wait_or_abort(&bars[B_OFINAL], 0, abort, a.err)) {
             tc_fence_after();
             const float inv = s_fp8 / l;
             const int qi = r / G;
-            uint16_t* orow = a.out + ((size_t)(q0 + qt * TQ + (rv ? qi : 0)) * Hq + kvh * G + r % G) * D;
+            uint16_t* orow =
+                a.out + ((size_t)(q0 + (2 * pair + g) * TQ + (rv ? qi : 0)) * Hq + kvh * G + r % G) * D;
 #pragma unroll
             for (int ch = 0; ch < D / 32; ++ch) {
                 uint32_t o[32];
@@ -721,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
 template <int FMT, int D>
 cudaError_t launch_t(const PrefillArgs& x, cudaStream_t s) {
     constexpr uint32_t smem = SmemLayout<D>::kAlloc;
-    static_assert(smem <= 113 * 1024, "two CTAs per SM");
+    static_assert(smem <= 227 * 1024, "shared memory of one CTA");
     auto kern = prefill_kernel<FMT, D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -747,7 +774,8 @@ cudaError_t launch_t(const PrefillArgs& x, cudaStream_t s) {
     p.sm_scale = x.sm_scale;
     const int G = x.num_q_heads / x.cache.num_kv_heads;
     const int TQ = kRows / G;
-    const dim3 grid((unsigned)((x.max_query_len + TQ - 1) / TQ), (unsigned)x.cache.num_kv_heads, (unsigned)x.batch);
+    const int tiles = (x.max_query_len + TQ - 1) / TQ;
+    const dim3 grid((unsigned)((tiles + 1) / 2), (unsigned)x.cache.num_kv_heads, (unsigned)x.batch);
     return launch_pdl(kern, grid, dim3(kThreads), smem, s, p);
 }
 
