@@ -62,10 +62,7 @@ constexpr uint32_t kColsPerTile = 256;   // tensor-memory columns of one query t
 constexpr uint32_t kTmemCols = 2 * kColsPerTile;
 constexpr uint32_t kColO = 128;   // a tile's O accumulator columns start here (two S buffers of 64 before)
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kRescaleLog2 = 8.0f;
-#ifndef KVQ_PF_LTREE
-#define KVQ_PF_LTREE 0
-#endif  // lazy rescale threshold (weights < 2^8)
+constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (weights < 2^8)
 
 // ------------------------------------------------------------- tcgen05 ----
 
@@ -684,9 +681,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
             float l2 = 0.f;                         // second partial sum (shorter add chains)
             auto chunk_p = [&](const uint32_t (&sv)[16], int ch) {
                 uint32_t hi[8], lo[8];
-#if KVQ_PF_LTREE
-                float ps[8];
-#endif
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     float pv[2], ev[2];
@@ -698,18 +692,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
                         ev[z] = e;
                         pv[z] = kRowScaled ? e * vs[u] : e;
                     }
-#if KVQ_PF_LTREE
-                    ps[q] = ev[0] + ev[1];
-#else
                     l += ev[0];
                     l2 += ev[1];
-#endif
                     hi[q] = pack_f16x2(pv[0], pv[1]);
                     lo[q] = residual_f16x2(hi[q], pv[0], pv[1]);
                 }
-#if KVQ_PF_LTREE
-                l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-#endif
                 // tokens 16c .. 16c+15 (read from columns 16c .. 16c+15) -> hi in
                 // columns 16c .. 16c+7, lo in 16c+8 .. 16c+15
                 tmem_st8(srow + ch * 16, hi);
