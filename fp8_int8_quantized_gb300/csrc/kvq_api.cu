@@ -263,8 +263,6 @@ kvq_status kvq_prefill_attention(const void* q, const kvq_cache* cache, const in
         return KVQ_ERR_INVALID_ARG;
     if (num_q_heads % cache->num_kv_heads) return KVQ_ERR_INVALID_ARG;
     if (num_q_heads / cache->num_kv_heads > kvq::prefill_rows_per_tile()) return KVQ_ERR_UNSUPPORTED;
-    // the dequant warps apply one scale per row (to logits and weights)
-    if (cache->group_size > 0 && cache->group_size != cache->head_dim) return KVQ_ERR_UNSUPPORTED;
     if (num_q_tokens > 0x7FFFFFFFll) return KVQ_ERR_UNSUPPORTED;   // query_start entries are int32
     if (batch > 65535 || cache->num_kv_heads > 65535) return KVQ_ERR_UNSUPPORTED;
     if (batch == 0 || max_query_len == 0 || num_q_tokens == 0) return KVQ_OK;

@@ -259,8 +259,9 @@ enum Bar : int {
 // [rows][D] fp16 stored as D / 64 column blocks of [rows][128 B], each with the
 // 128-byte swizzle: the two query tiles (128 rows each; A of S = Q K^T,
 // K-major), and two buffers each of K (64 rows; B of S, K-major) and V (64
-// rows; B of O = P V, MN-major).
-template <int D>
+// rows; B of O = P V, MN-major); with group scales (GRP) also two buffers each
+// of the K and V residuals.
+template <int D, bool GRP>
 struct SmemLayout {
     static constexpr uint32_t kBlkQ = kRows * 128;         // one 64-column block of a query tile
     static constexpr uint32_t kBlkKV = kKvTile * 128;      // one 64-column block of a K / V tile
@@ -269,7 +270,9 @@ struct SmemLayout {
     static constexpr uint32_t kQ = 0;                      // two query tiles
     static constexpr uint32_t kK = kQ + 2 * kTileQ;        // two K buffers
     static constexpr uint32_t kV = kK + 2 * kTileKV;       // two V buffers
-    static constexpr uint32_t kKsc = kV + 2 * kTileKV;     // fp32 [4][64] INT8 / INT4 logit multipliers
+    static constexpr uint32_t kKlo = kV + 2 * kTileKV;     // GRP: two K residual buffers
+    static constexpr uint32_t kVlo = kKlo + (GRP ? 2 * kTileKV : 0);   // GRP: two V residual buffers
+    static constexpr uint32_t kKsc = kVlo + (GRP ? 2 * kTileKV : 0);   // fp32 [4][64] INT8 / INT4 logit multipliers
     static constexpr uint32_t kVsc = kKsc + 4 * kKvTile * 4;  // fp32 [4][64] INT8 / INT4 V row scales
     static constexpr uint32_t kBar = kVsc + 4 * kKvTile * 4;
     static constexpr uint32_t kTmemSlot = kBar + kNumBars * 8;
@@ -298,6 +301,7 @@ struct PrefillParams {
     unsigned long long* err;
     int32_t num_blocks, block_size, num_kv_heads, max_blocks_per_seq;
     int32_t num_q_heads, max_query_len;
+    int32_t ngroups;   // scales per cached row (INT8 / INT4 group quantization), else 1
     int64_t num_q_tokens;
     float sm_scale;
 };
@@ -311,11 +315,18 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 
 // ------------------------------------------------------------- kernel -----
 
-template <int FMT, int D>
+// GRP: INT8 / INT4 with a scale per group of channels.  The group scale varies
+// along the contraction of S = Q K^T (and along the output of P V), so it
+// cannot be taken out per token as a row scale is: the dequantizers store each
+// K and V value x = code * s_group as fp16 hi + fp16 residual (x exactly to
+// ~22 bits), S takes two MMA passes (K hi, K residual) and O three (P hi V hi,
+// P residual V hi, P hi V residual).
+template <int FMT, int D, bool GRP>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParams a) {
-    using L = SmemLayout<D>;
+    using L = SmemLayout<D, GRP>;
     constexpr int kChunks = D / 8;       // 16-byte fp16 chunks per row
-    constexpr bool kRowScaled = FMT == INT8 || FMT == INT4;   // one scale per (token, kv-head) row
+    // one scale per (token, kv-head) row, taken out of the contractions
+    constexpr bool kRowScaled = (FMT == INT8 || FMT == INT4) && !GRP;
     constexpr int kRowBytes = row_bytes(FMT, D);
     constexpr int kCodeVecs = kRowBytes / 16;              // 16-byte code vectors per token row
     constexpr int kChunksPerVec = FMT == INT4 ? 4 : 2;     // 8-value fp16 chunks per code vector
@@ -364,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
     }
     const int nkv = max(nkv_g[0], nkv_g[1]);
     const int p_max = nq[1] > 0 ? p_last[1] : p_last[0];   // last position any query attends to
-    const float s_fp8 = (!kRowScaled && a.scale) ? *a.scale : 1.0f;
+    const float s_fp8 = ((FMT == E4M3 || FMT == E5M2) && a.scale) ? *a.scale : 1.0f;
     // logits in log2 units: S * c_k (FP8; K carries the scale's sign) or S * c_k * s_K[t] (INT8 / INT4)
     const float c_k = a.sm_scale * kLog2e * fabsf(s_fp8);
 
@@ -418,6 +429,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
                     mma_ss_warp(d_tmem, dq0 + (((kk >> 2) * L::kBlkQ + off) >> 4),
                                 dk + (((kk >> 2) * L::kBlkKV + off) >> 4), kIdescQK, kk > 0);
                 }
+                if (GRP) {   // + Q K_residual^T
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk & 3) * 32;
+                        mma_ss_warp(d_tmem, dq0 + (((kk >> 2) * L::kBlkQ + off) >> 4),
+                                    dk + (((L::kKlo - L::kK) + (kk >> 2) * L::kBlkKV + off) >> 4), kIdescQK, 1u);
+                    }
+                }
                 mma_commit_warp(&bars[B_SFULL00 + 2 * g + sl]);
             }
             mma_commit_warp(&bars[B_KFREE0 + sl]);
@@ -440,6 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
                     const uint64_t vd = dv + ((kk * 2048) >> 4);
                     mma_ts_warp(o_tmem, a_hi, vd, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
                     mma_ts_warp(o_tmem, a_hi + 8, vd, kIdescPV, 1u);
+                    if (GRP) mma_ts_warp(o_tmem, a_hi, vd + ((L::kVlo - L::kV) >> 4), kIdescPV, 1u);
                 }
             }
             mma_commit_warp(&bars[B_VFREE0 + sl]);
@@ -455,7 +475,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
     } else if (warp > kMmaWarp) {
         // ------------------------------------------------------ dequant ----
         const int dt = tid - 32 * (kMmaWarp + 1);   // 0 .. kDqThreads - 1
-        const size_t head_stride = (size_t)a.block_size * kRowBytes;
         const int32_t* bt = a.block_tables + (size_t)b * a.max_blocks_per_seq;
         // query tiles: row r of tile g = (query (2 * pair + g) * TQ + r / G, head kvh * G + r % G)
         for (int e = dt; e < 2 * kRows * kChunks; e += kDqThreads) {
@@ -499,15 +518,28 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
                 blk[it] = id;
             }
         };
-        auto load_codes = [&](const uint8_t* codes, int j, uint4 (&cv)[kVecsPerThread],
-                              const int (&blk)[kVecsPerThread]) {
+        // GRP: a code vector's two 16-value halves (one for INT8) each lie in one
+        // scale group (groups are at least 16 channels wide and 16-aligned)
+        constexpr int kSubs = FMT == INT4 ? 2 : 1;
+        constexpr int kVecDims = FMT == INT4 ? 32 : 16;   // head dims of one code vector
+        const int ng = a.ngroups, gdims = D / ng;
+        auto load_codes = [&](const uint8_t* codes, const float* scales, int j, uint4 (&cv)[kVecsPerThread],
+                              float (&gs)[kVecsPerThread][kSubs], const int (&blk)[kVecsPerThread]) {
 #pragma unroll
             for (int it = 0; it < kVecsPerThread; ++it) {
                 const int t = j * kKvTile + row_of(it);
                 cv[it] = make_uint4(0, 0, 0, 0);
-                if (blk[it] >= 0)
-                    cv[it] = ld_global_nc_v4(codes + ((size_t)blk[it] * Hkv + kvh) * head_stride +
-                                             (size_t)(t & (a.block_size - 1)) * kRowBytes + vec_of(it) * 16);
+#pragma unroll
+                for (int z = 0; z < kSubs; ++z) gs[it][z] = 0.f;
+                if (blk[it] >= 0) {
+                    const size_t row = ((size_t)blk[it] * Hkv + kvh) * a.block_size + (t & (a.block_size - 1));
+                    cv[it] = ld_global_nc_v4(codes + row * kRowBytes + vec_of(it) * 16);
+                    if (GRP) {
+#pragma unroll
+                        for (int z = 0; z < kSubs; ++z)
+                            gs[it][z] = __ldg(scales + row * ng + (vec_of(it) * kVecDims + 16 * z) / gdims);
+                    }
+                }
             }
         };
         auto load_scales = [&](int j, float& ks, float& vs) {
@@ -525,11 +557,45 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
         // A negative FP8 scale is folded into K's fp16 signs, so the logit
         // multiplier is never negative.
         const uint32_t kflip = (!kRowScaled && s_fp8 < 0.f) ? 0x80008000u : 0u;
-        auto store_tile = [&](uint32_t tile, const uint4 (&cv)[kVecsPerThread], uint32_t flip) {
+        // GRP: each fp16 code value c becomes x = c * s_group, stored as fp16 hi in
+        // `tile` and the fp16 residual RN(x - hi) in `tile_lo`
+        auto store_scaled = [&](uint32_t tile, uint32_t tile_lo, uint32_t off, const uint32_t (&hw)[4], float sc) {
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const float2 c = f16x2_to_f32x2(hw[w]);
+                const float x0 = c.x * sc, x1 = c.y * sc;
+                hi[w] = pack_f16x2(x0, x1);
+                lo[w] = residual_f16x2(hi[w], x0, x1);
+            }
+            st_shared_v4(tile + off, make_uint4(hi[0], hi[1], hi[2], hi[3]));
+            st_shared_v4(tile_lo + off, make_uint4(lo[0], lo[1], lo[2], lo[3]));
+        };
+        auto store_tile = [&](uint32_t tile, uint32_t tile_lo, const uint4 (&cv)[kVecsPerThread],
+                              const float (&gs)[kVecsPerThread][kSubs], uint32_t flip) {
 #pragma unroll
             for (int it = 0; it < kVecsPerThread; ++it) {
                 if (!has(it)) continue;
                 const int u = row_of(it), c16 = vec_of(it);
+                if (GRP) {
+                    const uint32_t cw[4] = {cv[it].x, cv[it].y, cv[it].z, cv[it].w};
+                    if (FMT == INT4) {   // 32 codes -> four 8-value chunks, two per scale half
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            uint32_t hw[4];
+                            int4x8_to_f16(cw[w], hw);
+                            store_scaled(tile, tile_lo, tile_off(L::kBlkKV, u, kChunksPerVec * c16 + w), hw,
+                                         gs[it][w >> 1]);
+                        }
+                    } else {             // 16 INT8 codes -> two 8-value chunks
+                        uint4 h0, h1;
+                        dec16<FMT>(cv[it], h0, h1);
+                        const uint32_t a0[4] = {h0.x, h0.y, h0.z, h0.w}, a1[4] = {h1.x, h1.y, h1.z, h1.w};
+                        store_scaled(tile, tile_lo, tile_off(L::kBlkKV, u, 2 * c16), a0, gs[it][0]);
+                        store_scaled(tile, tile_lo, tile_off(L::kBlkKV, u, 2 * c16 + 1), a1, gs[it][0]);
+                    }
+                    continue;
+                }
                 if (FMT == INT4) {   // 32 codes -> four 8-value chunks
                     uint32_t hw[4];
                     const uint32_t cw[4] = {cv[it].x, cv[it].y, cv[it].z, cv[it].w};
@@ -556,11 +622,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
         // S never waits on the V side of the pipeline; the codes of the next K
         // and V tiles are loaded into registers meanwhile.
         uint4 kc[kVecsPerThread], vc[kVecsPerThread];
+        float kg[kVecsPerThread][kSubs], vg[kVecsPerThread][kSubs];   // GRP: group scales of the codes
         float ks = 0.f, vs = 0.f;
         auto put_k = [&](int t) {
             const int sl = t & 1;
             if (t >= 2 && !wait_or_abort(&bars[B_KFREE0 + sl], ((t >> 1) - 1) & 1, abort, a.err)) return false;
-            store_tile(sbase + L::kK + sl * L::kTileKV, kc, kflip);
+            store_tile(sbase + L::kK + sl * L::kTileKV, sbase + L::kKlo + sl * L::kTileKV, kc, kg, kflip);
             if (kRowScaled && dt < kKvTile) {
                 ksc[(t & 3) * kKvTile + dt] = ks * c_k;   // the logit multiplier of token t
                 vsc[(t & 3) * kKvTile + dt] = vs;
@@ -571,12 +638,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
             return true;
         };
         fetch_ids(0, blk_k);
-        load_codes(a.k_codes, 0, kc, blk_k);
-        load_codes(a.v_codes, 0, vc, blk_k);
+        load_codes(a.k_codes, a.k_scales, 0, kc, kg, blk_k);
+        load_codes(a.v_codes, a.v_scales, 0, vc, vg, blk_k);
         if (kRowScaled) load_scales(0, ks, vs);
         put_k(0);
         fetch_ids(1, blk_k);
-        load_codes(a.k_codes, 1, kc, blk_k);
+        load_codes(a.k_codes, a.k_scales, 1, kc, kg, blk_k);
         if (kRowScaled) load_scales(1, ks, vs);
         for (int j = 0; j < nkv; ++j) {
             const int sl = j & 1;
@@ -586,14 +653,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
 #pragma unroll
                 for (int it = 0; it < kVecsPerThread; ++it) blk_v[it] = blk_k[it];   // tile j+1
                 fetch_ids(j + 2, blk_k);
-                load_codes(a.k_codes, j + 2, kc, blk_k);
+                load_codes(a.k_codes, a.k_scales, j + 2, kc, kg, blk_k);
                 if (kRowScaled) load_scales(j + 2, ks, vs);
             }
             if (j >= 2 && !wait_or_abort(&bars[B_VFREE0 + sl], ((j >> 1) - 1) & 1, abort, a.err)) break;
-            store_tile(sbase + L::kV + sl * L::kTileKV, vc, 0u);
+            store_tile(sbase + L::kV + sl * L::kTileKV, sbase + L::kVlo + sl * L::kTileKV, vc, vg, 0u);
             fence_proxy_async();
             mbar_arrive(&bars[B_VFULL0 + sl]);
-            if (more) load_codes(a.v_codes, j + 1, vc, blk_v);
+            if (more) load_codes(a.v_codes, a.v_scales, j + 1, vc, vg, blk_v);
         }
     } else {
         // ------------------------------------------------------ softmax ----
@@ -763,11 +830,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
     }
 }
 
-template <int FMT, int D>
+template <int FMT, int D, bool GRP>
 cudaError_t launch_t(const PrefillArgs& x, cudaStream_t s) {
-    constexpr uint32_t smem = SmemLayout<D>::kAlloc;
+    constexpr uint32_t smem = SmemLayout<D, GRP>::kAlloc;
     static_assert(smem <= 227 * 1024, "shared memory of one CTA");
-    auto kern = prefill_kernel<FMT, D>;
+    auto kern = prefill_kernel<FMT, D, GRP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     PrefillParams p;
@@ -790,6 +857,7 @@ cudaError_t launch_t(const PrefillArgs& x, cudaStream_t s) {
     p.max_query_len = x.max_query_len;
     p.num_q_tokens = x.num_q_tokens;
     p.sm_scale = x.sm_scale;
+    p.ngroups = x.cache.ngroups;
     const int G = x.num_q_heads / x.cache.num_kv_heads;
     const int TQ = kRows / G;
     const int tiles = (x.max_query_len + TQ - 1) / TQ;
@@ -804,10 +872,16 @@ int prefill_rows_per_tile() { return kRows; }
 cudaError_t launch_prefill(const PrefillArgs& x, cudaStream_t s) {
     const int D = x.cache.head_dim;
     switch (x.cache.fmt) {
-        case E4M3: return D == 64 ? launch_t<E4M3, 64>(x, s) : launch_t<E4M3, 128>(x, s);
-        case E5M2: return D == 64 ? launch_t<E5M2, 64>(x, s) : launch_t<E5M2, 128>(x, s);
-        case INT4: return D == 64 ? launch_t<INT4, 64>(x, s) : launch_t<INT4, 128>(x, s);
-        default: return D == 64 ? launch_t<INT8, 64>(x, s) : launch_t<INT8, 128>(x, s);
+        case E4M3: return D == 64 ? launch_t<E4M3, 64, false>(x, s) : launch_t<E4M3, 128, false>(x, s);
+        case E5M2: return D == 64 ? launch_t<E5M2, 64, false>(x, s) : launch_t<E5M2, 128, false>(x, s);
+        case INT4:
+            if (x.cache.ngroups > 1)
+                return D == 64 ? launch_t<INT4, 64, true>(x, s) : launch_t<INT4, 128, true>(x, s);
+            return D == 64 ? launch_t<INT4, 64, false>(x, s) : launch_t<INT4, 128, false>(x, s);
+        default:
+            if (x.cache.ngroups > 1)
+                return D == 64 ? launch_t<INT8, 64, true>(x, s) : launch_t<INT8, 128, true>(x, s);
+            return D == 64 ? launch_t<INT8, 64, false>(x, s) : launch_t<INT8, 128, false>(x, s);
     }
 }
 

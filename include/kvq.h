@@ -96,7 +96,7 @@ typedef enum {
  *     four groups of consecutive channels, each quantized as a row is (its own
  *     amax and scale).  Must be 0 for FP8; any other value is INVALID_ARG.
  *     Decode takes a group count times the q-heads per kv-head of at most 8
- *     (UNSUPPORTED otherwise); chunked prefill takes one scale per row only. */
+ *     (UNSUPPORTED otherwise); chunked prefill takes every group size. */
 typedef struct {
     void* k_codes;
     void* v_codes;

@@ -62,8 +62,9 @@ def test_group_sizes_checked_before_any_cuda_call(lib):
     # 4 groups x 4 q-heads per kv-head = 16 operand rows > 8
     assert lib.kvq_decode_attention(16, ctypes.byref(d4), 16, 4, 16, 2, 8, 64, None, kvq.INT4, 0.0,
                                     16, None, 0, 0, None) == 2
+    d4.group_size = 48
     assert lib.kvq_prefill_attention(16, ctypes.byref(d4), 16, 4, 16, 16, 2, 4, 4, 4, None, kvq.INT4,
-                                     0.0, 16, None) == 2                                   # rows scales only
+                                     0.0, 16, None) == 1                                   # 48 does not divide
 
 
 def test_decode_kernel_knob(lib):

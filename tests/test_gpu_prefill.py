@@ -1,8 +1,9 @@
 """GPU parity of chunked-prefill attention (kvq_prefill_attention) against the
 fp64 CPU oracle on the same cache bytes: |o_gpu - o_ref| <= 2e-3 * max(1,
-|o_ref|) per element.  Small cases span several 128-token KV tiles and 128-row
-query tiles, ragged tails, whole-context chunks, one-query and empty chunks,
-every group size class (1, 2, 3, 4, 8, 16) and both head sizes; the
+|o_ref|) per element.  Small cases span several 64-token KV tiles and 128-row
+query tiles (odd and even counts of them: a CTA takes two), ragged tails,
+whole-context chunks, one-query and empty chunks, every q-head group size class
+(1, 2, 3, 4, 8, 16), both head sizes and INT8 / INT4 scale groups; the
 workload-sized cases run the launch the benchmark times and check sampled
 queries, each against the oracle's decode attention over its own prefix (the
 definition of causal attention for one query)."""
@@ -25,10 +26,10 @@ def _lib():
     yield
 
 
-def small(fmt, B, Hq, Hkv, D, BS, ctx, seed=0):
+def small(fmt, B, Hq, Hkv, D, BS, ctx, seed=0, group=0):
     wl = W.Workload(f"p-{fmt}", B, Hq, Hkv, D, BS, fmt, max(ctx),
                     "amax" if fmt == "e4m3" else ("row" if fmt in ("int8", "int4") else "one"),
-                    outliers=True, seed=seed)
+                    outliers=True, seed=seed, quant_group=group)
     return DeviceWorkload(wl, chunk_tokens=1 << 16, ctx=torch.tensor(ctx, dtype=torch.int32))
 
 
@@ -54,13 +55,24 @@ PCASES = [
     ("int4", 2, 4, 4, 128, 64, [640, 65], [300, 65]),
     ("int4", 3, 8, 2, 64, 16, [129, 1, 256], [129, 1, 17]),
     ("int4", 1, 32, 8, 128, 32, [500], [200]),
+    # scale groups (last field: channels per scale)
+    ("int8", 2, 4, 4, 128, 64, [640, 65], [300, 65], 32),
+    ("int8", 3, 8, 2, 64, 16, [129, 1, 256], [129, 1, 17], 16),
+    ("int4", 2, 16, 2, 128, 16, [700, 64], [260, 64], 64),
+    ("int4", 3, 4, 4, 64, 32, [300, 77, 1], [300, 10, 1], 16),
+    ("int4", 1, 32, 8, 128, 32, [500], [200], 32),
 ]
 
 
-@pytest.mark.parametrize("case", PCASES, ids=lambda c: f"{c[0]}-G{c[2] // c[3]}-D{c[4]}-BS{c[5]}")
+def case_id(c):
+    return f"{c[0]}-G{c[2] // c[3]}-D{c[4]}-BS{c[5]}" + (f"-g{c[8]}" if len(c) > 8 else "")
+
+
+@pytest.mark.parametrize("case", PCASES, ids=case_id)
 def test_prefill_small(case):
-    fmt, B, Hq, Hkv, D, BS, ctx, chunk = case
-    dw = small(fmt, B, Hq, Hkv, D, BS, ctx, seed=sum(ctx) + D)
+    fmt, B, Hq, Hkv, D, BS, ctx, chunk = case[:8]
+    group = case[8] if len(case) > 8 else 0
+    dw = small(fmt, B, Hq, Hkv, D, BS, ctx, seed=sum(ctx) + D, group=group)
     q, qs, out = run_prefill(dw, chunk)
     assert kvq.device_error_check()[0] == 0
     oc, bt, cl = dw.oracle_cache_for(list(range(B)))
@@ -139,6 +151,7 @@ def test_bad_block_id_is_reported_without_fault():
                                              ("llama3-8b", 1024, [0, 33]),
                                              ("llama2-13b-int8", 512, [5]),
                                              ("llama2-13b-int4", 512, [7]),
+                                             ("llama2-13b-int4-g32", 512, [9]),
                                              ("llama2-7b", 2048, [31])])
 def test_prefill_workload_sampled(name, chunk, seqs):
     wl = W.WORKLOADS[name]
