@@ -47,6 +47,8 @@
 // the MMAs it issued and exits.
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "kvq_device.cuh"
 #include "kvq_launch.h"
 
@@ -689,7 +691,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
             const bool full = __shfl_sync(0xFFFFFFFFu, lim, 0) >= kKvTile - 1;
             // pass 1: the tile's row maximum; the second TMEM load overlaps the first chunk's work
             float mx = -INFINITY;
-            auto chunk_max = [&](const uint32_t (&sv)[32], int ch) {
+            // Both passes exist in two copies: tiles past the warp's first
+            // position carry no masking code at all (masked tiles are the last
+            // one or two of a query tile's walk).
+            auto chunk_max = [&](const uint32_t (&sv)[32], int ch, auto masked) {
                 // four independent three-input max chains of 8 values each (a
                 // single chain of 64 two-input maxima was 14% slower on the 70B chunk)
                 float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -698,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
                     const int u = ch * 32 + q;
                     float x0 = kRowScaled ? __uint_as_float(sv[q]) * ks[u] : __uint_as_float(sv[q]);
                     float x1 = kRowScaled ? __uint_as_float(sv[q + 1]) * ks[u + 1] : __uint_as_float(sv[q + 1]);
-                    if (!full) {
+                    if constexpr (decltype(masked)::value) {
                         x0 = u <= lim ? x0 : -INFINITY;
                         x1 = u + 1 <= lim ? x1 : -INFINITY;
                     }
@@ -706,17 +711,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
                 }
                 mx = fmax3(mx, fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             };
-            {
+            auto pass1 = [&](auto masked) {
                 uint32_t sa[32], sb[32];
                 tmem_ld32(srow, sa);
                 tc_wait_ld();
                 reg_fence32(sa);
                 tmem_ld32(srow + 32, sb);
-                chunk_max(sa, 0);
+                chunk_max(sa, 0, masked);
                 tc_wait_ld();
                 reg_fence32(sb);
-                chunk_max(sb, 1);
-            }
+                chunk_max(sb, 1, masked);
+            };
+            if (full) pass1(std::false_type{});
+            else pass1(std::true_type{});
             if (!kRowScaled) mx *= c_k;
             const float m_new = fmaxf(m_used, mx);
             float alpha = 1.f;
@@ -746,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
             // pass 2: weights, written over their logits as fp16 hi + residual
             const float neg_m = -m_used;
             float l2 = 0.f;                         // second partial sum (shorter add chains)
-            auto chunk_p = [&](const uint32_t (&sv)[16], int ch) {
+            auto chunk_p = [&](const uint32_t (&sv)[16], int ch, auto masked) {
                 uint32_t hi[8], lo[8];
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
@@ -755,7 +762,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
                     for (int z = 0; z < 2; ++z) {
                         const int u = ch * 16 + 2 * q + z;
                         float e = fast_exp2(fmaf(__uint_as_float(sv[2 * q + z]), kRowScaled ? ks[u] : c_k, neg_m));
-                        if (!full && u > lim) e = 0.f;
+                        if constexpr (decltype(masked)::value) {
+                            if (u > lim) e = 0.f;
+                        }
                         ev[z] = e;
                         pv[z] = kRowScaled ? e * vs[u] : e;
                     }
@@ -769,25 +778,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
                 tmem_st8(srow + ch * 16, hi);
                 tmem_st8(srow + ch * 16 + 8, lo);
             };
-            {
+            auto pass2 = [&](auto masked) {
                 uint32_t sa[16], sb[16];
                 tmem_ld16(srow, sa);
                 tc_wait_ld();
                 reg_fence16(sa);
                 tmem_ld16(srow + 16, sb);
-                chunk_p(sa, 0);
+                chunk_p(sa, 0, masked);
                 tc_wait_ld();
                 reg_fence16(sb);
                 tmem_ld16(srow + 32, sa);
-                chunk_p(sb, 1);
+                chunk_p(sb, 1, masked);
                 tc_wait_ld();
                 reg_fence16(sa);
                 tmem_ld16(srow + 48, sb);
-                chunk_p(sa, 2);
+                chunk_p(sa, 2, masked);
                 tc_wait_ld();
                 reg_fence16(sb);
-                chunk_p(sb, 3);
-            }
+                chunk_p(sb, 3, masked);
+            };
+            if (full) pass2(std::false_type{});
+            else pass2(std::true_type{});
             l += l2;
             tc_wait_st();
             tc_fence_before();
