@@ -34,7 +34,10 @@
 //     query tile (M 128, N 64, K head_dim, into one of two S buffers of that
 //     tile in tensor memory), then O += P V of tile j-1 for each query tile
 //     (M 128, N head_dim, K 64, P read from tensor memory, V an MN-major
-//     shared-memory operand), and commits each group to an mbarrier;
+//     shared-memory operand), and commits each group to an mbarrier.  With
+//     group scales (2.5x the MMAs) warps 8 and 15 issue for one query tile
+//     each: the issue cost of tcgen05.mma is then the critical path, and two
+//     issuing warps overlap it (+28% on the grouped INT4 shape);
 //   * warps 0-3 and 4-7 (softmax of query tiles 0 and 1): thread r owns row r
 //     (tensor-memory lane r): it reads its 64 logits with tcgen05.ld, keeps a
 //     running maximum (raised only when the tile's maximum exceeds it by more
@@ -59,7 +62,9 @@ constexpr int kRows = 128;        // query tile: (query, q-head) rows; a CTA hol
 constexpr int kKvTile = 64;       // tokens per KV tile
 constexpr int kMmaWarp = 8;       // warps 0-7 softmax (4 per query tile), 8 MMA, 9-14 dequant
 constexpr int kDqThreads = 192;   // dequantizing threads (warps 9-14)
-constexpr int kThreads = 32 * (kMmaWarp + 1) + kDqThreads;
+constexpr int kMmaWarp2 = kMmaWarp + 1 + kDqThreads / 32;   // with group scales: query tile 1's MMA warp (15)
+constexpr int kThreads = 32 * (kMmaWarp2 + 1);   // launched with one warp fewer without group scales
+__host__ __device__ constexpr int threads_for(bool grp) { return grp ? kThreads : kThreads - 32; }
 constexpr uint32_t kColsPerTile = 256;   // tensor-memory columns of one query tile
 constexpr uint32_t kTmemCols = 2 * kColsPerTile;
 constexpr uint32_t kColO = 128;   // a tile's O accumulator columns start here (two S buffers of 64 before)
@@ -336,6 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
     constexpr int kVecsPerThread = (kTileVecs + kDqThreads - 1) / kDqThreads;
     constexpr uint32_t kIdescQK = idesc_f16(kRows, kKvTile, 0);
     constexpr uint32_t kIdescPV = idesc_f16(kRows, D, 1);
+    constexpr int kMmaWarps = GRP ? 2 : 1;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -385,7 +391,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
         for (int i = 0; i < kNumBars; ++i) {
             const bool by_dq = (i >= B_KFULL0 && i <= B_VFULL1) || (i >= B_SC0 && i <= B_SC3);
             const bool by_sm = i >= B_PFULL00 && i <= B_PFULL11;
-            mbar_init(&bars[i], by_dq ? (uint32_t)kDqThreads : by_sm ? 128u : 1u);
+            const bool by_mma = (i >= B_KFREE0 && i <= B_VFREE1) || i == B_OFINAL;   // every MMA warp commits
+            mbar_init(&bars[i], by_dq ? (uint32_t)kDqThreads : by_sm ? 128u : by_mma ? (uint32_t)kMmaWarps : 1u);
         }
         *abort = 0;
         fence_barrier_init();
@@ -401,7 +408,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == kMmaWarp) {
+    if (warp == kMmaWarp || (kMmaWarps == 2 && warp == kMmaWarp2)) {
+        // query tiles g0 .. g1 - 1: both, or with group scales (2.5x the MMAs;
+        // their issue is then the critical path) one per MMA warp
+        const int g0 = kMmaWarps == 2 && warp == kMmaWarp2 ? 1 : 0, g1 = kMmaWarps == 2 ? g0 + 1 : 2;
         // ---------------------------------------------------------- MMA ----
         // One elected lane issues every MMA, per KV tile j: S_0,j and S_1,j
         // (both query tiles against K_j, into S buffer j % 2 of each tile's
@@ -420,9 +430,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
             if (!wait_or_abort(&bars[B_KFULL0 + sl], (j >> 1) & 1, abort, a.err)) return false;
             tc_fence_after();
             const uint64_t dk = dk0 + ((sl * L::kTileKV) >> 4);
-#pragma unroll
-            for (int g = 0; g < 2; ++g) {
-                if (j >= nkv_g[g]) continue;
+            for (int g = g0; g < g1; ++g) {
+                if (j >= (g ? nkv_g[1] : nkv_g[0])) continue;
                 const uint64_t dq0 = smem_desc(sbase + L::kQ + g * L::kTileQ, 16, 1024);
                 const uint32_t d_tmem = tmem + g * kColsPerTile + sl * kKvTile;
 #pragma unroll
@@ -448,9 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
             const int sl = j & 1;
             if (!wait_or_abort(&bars[B_VFULL0 + sl], (j >> 1) & 1, abort, a.err)) return false;
             const uint64_t dv = dv0 + ((sl * L::kTileKV) >> 4);
-#pragma unroll
-            for (int g = 0; g < 2; ++g) {
-                if (j >= nkv_g[g]) continue;
+            for (int g = g0; g < g1; ++g) {
+                if (j >= (g ? nkv_g[1] : nkv_g[0])) continue;
                 if (!wait_or_abort(&bars[B_PFULL00 + 2 * g + sl], (j >> 1) & 1, abort, a.err)) return false;
                 tc_fence_after();
                 const uint32_t o_tmem = tmem + g * kColsPerTile + kColO;
@@ -873,7 +881,7 @@ cudaError_t launch_t(const PrefillArgs& x, cudaStream_t s) {
     const int TQ = kRows / G;
     const int tiles = (x.max_query_len + TQ - 1) / TQ;
     const dim3 grid((unsigned)((tiles + 1) / 2), (unsigned)x.cache.num_kv_heads, (unsigned)x.batch);
-    return launch_pdl(kern, grid, dim3(kThreads), smem, s, p);
+    return launch_pdl(kern, grid, dim3(threads_for(GRP)), smem, s, p);
 }
 
 }  // namespace
