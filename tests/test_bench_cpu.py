@@ -52,3 +52,14 @@ def test_reference_arm_other_ranks_exit_quietly():
                         "--steps", "1", "--warmup", "3"], capture_output=True, text=True, timeout=300, cwd=ROOT,
                        env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_tensor_peak_choice():
+    """The prefill roofline divides by the measured burst bf16 rate for a short
+    timed region and by the measured sustained rate for a long one."""
+    sys.path.insert(0, ROOT)
+    import bench
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+        p = json.load(f)
+    assert bench.measured_tensor_peak() == (p["bf16_tflops"], "measured burst")
+    assert bench.measured_tensor_peak(sustained=True) == (p["bf16_tflops_sustained"], "measured sustained")
