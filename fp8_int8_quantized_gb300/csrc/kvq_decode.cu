@@ -1144,13 +1144,19 @@ __global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
 // slots with independent vector loads.
 constexpr int kReduceWarps = 4;
 
+// One CTA per (sequence, q-head): every thread takes part in the maximum over
+// the partial slots, warp w merges slots w, w + 4, ... (four loads in flight
+// per lane), and the four warps' partial sums are combined in shared memory.
+// A single warp per head walking its slots one at a time was latency-bound at
+// small batches with long contexts (hundreds of slots per head).
 template <int D>
 __global__ void __launch_bounds__(kReduceWarps * 32) decode_reduce_kernel(const DecodeArgs a) {
     constexpr int V = D / 32;  // outputs per lane: 4 (D = 128) or 2 (D = 64)
+    __shared__ float red_m[kReduceWarps], red_l[kReduceWarps];
+    __shared__ __align__(16) float red_o[kReduceWarps][D];
     griddep_wait();
-    const int lane = threadIdx.x & 31;
-    const int64_t hq = (int64_t)blockIdx.x * kReduceWarps + (threadIdx.x >> 5);
-    if (hq >= (int64_t)a.batch * a.num_q_heads) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t hq = blockIdx.x;
     const int b = (int)(hq / a.num_q_heads);
     int ctx = a.context_lens[b];
     const int cap = min(a.max_context_len, a.max_blocks_per_seq * a.cache.block_size);
@@ -1161,14 +1167,19 @@ __global__ void __launch_bounds__(kReduceWarps * 32) decode_reduce_kernel(const 
                                                        ws_acc_bytes(a.batch, a.num_q_heads, a.num_chunks, D));
     const int64_t s0 = hq * a.num_chunks * 2;
     float M = -INFINITY;
-    for (int i = lane; i < nslots; i += 32) M = fmaxf(M, ml[s0 + i].x);
+    for (int i = threadIdx.x; i < nslots; i += kReduceWarps * 32) M = fmaxf(M, ml[s0 + i].x);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
+    if (lane == 0) red_m[warp] = M;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < kReduceWarps; ++w) M = fmaxf(M, red_m[w]);
     float Lsum = 0.f, O[V];
 #pragma unroll
     for (int k = 0; k < V; ++k) O[k] = 0.f;
     if (M != -INFINITY) {
-        for (int i = 0; i < nslots; ++i) {
+#pragma unroll 4
+        for (int i = warp; i < nslots; i += kReduceWarps) {
             const float2 v = ml[s0 + i];
             if (v.x == -INFINITY) continue;  // empty slot: its accumulator was never written
             const float e = fast_exp2(v.x - M);
@@ -1182,6 +1193,20 @@ __global__ void __launch_bounds__(kReduceWarps * 32) decode_reduce_kernel(const 
                 O[0] += e * x.x; O[1] += e * x.y;
             }
         }
+    }
+    if (lane == 0) red_l[warp] = Lsum;
+#pragma unroll
+    for (int k = 0; k < V; ++k) red_o[warp][V * lane + k] = O[k];
+    __syncthreads();
+    if (warp != 0) return;
+#pragma unroll
+    for (int k = 0; k < V; ++k) O[k] = 0.f;
+    Lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kReduceWarps; ++w) {
+        Lsum += red_l[w];
+#pragma unroll
+        for (int k = 0; k < V; ++k) O[k] += red_o[w][V * lane + k];
     }
     const float inv = Lsum > 0.f ? 1.0f / Lsum : 0.f;
     uint32_t* dst = reinterpret_cast<uint32_t*>(a.out + hq * D + V * lane);
@@ -1266,8 +1291,7 @@ cudaError_t launch_fmt_d(const CUtensorMap& tk, const CUtensorMap& tv, const Dec
     if (e != cudaSuccess) return e;
     if (a.ev_end && (e = cudaEventRecord(a.ev_end, s)) != cudaSuccess) return e;
     const int64_t heads = (int64_t)a.batch * a.num_q_heads;
-    return launch_pdl(decode_reduce_kernel<D>, dim3((unsigned)((heads + kReduceWarps - 1) / kReduceWarps)),
-                      dim3(kReduceWarps * 32), 0, s, a);
+    return launch_pdl(decode_reduce_kernel<D>, dim3((unsigned)heads), dim3(kReduceWarps * 32), 0, s, a);
 }
 
 template <int FMT>
