@@ -145,8 +145,8 @@ kvq_status decode_impl(const void* q, const void* k_new, const void* v_new, cons
     if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return KVQ_ERR_WORKSPACE;
     int kind = g_decode_kernel.load();
     if (kind == 0) kind = 2;
-    // CUDA-core kernel: 8-bit codes, G <= 4, one scale per row
-    if (kind == 1 && (G > 4 || fmt == KVQ_INT4 || ng > 1)) return KVQ_ERR_UNSUPPORTED;
+    // CUDA-core kernel: 8-bit codes, G <= 4
+    if (kind == 1 && (G > 4 || fmt == KVQ_INT4)) return KVQ_ERR_UNSUPPORTED;
     int dev;
     if (!current_device(&dev)) return KVQ_ERR_CUDA;
     unsigned long long* err = err_word(dev);

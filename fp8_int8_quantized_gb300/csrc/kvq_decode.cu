@@ -190,14 +190,16 @@ struct SimtConsumer {
     static constexpr int kMinCtas = GM == 4 ? 3 : kMinBlocks;  // 4 query rows need more registers
     uint32_t qh[GM][8];
     float m[GM], l[GM], acc[GM][16];
-    int lane, j, grp, G;
+    int lane, j, grp, G, ng, gi;   // INT8: ng scales per row; this lane's 16 dims lie in group gi
     float qk_scale;
 
-    __device__ void init(int G_, float qks, int /*ng: always 1 here*/) {
+    __device__ void init(int G_, float qks, int ng_) {
         lane = threadIdx.x & 31;
         j = lane % LPT;
         grp = lane / LPT;
         G = G_;
+        ng = ng_;
+        gi = (16 * j) / (D / ng_);
         qk_scale = qks;
     }
     // q: the group's G query rows (shared-memory copy)
@@ -225,7 +227,9 @@ struct SimtConsumer {
         }
     }
 
-    // One 16-row half of a tile: K rows at k, V rows at v, row scales at sk / sv.
+    // One 16-row half of a tile: K rows at k, V rows at v, INT8 scales at sk / sv
+    // ([token][ng]: a lane's partial dot product and its weights take the
+    // scale of the group its 16 dims lie in).
     __device__ void half(uint32_t k, uint32_t v, uint32_t sk, uint32_t sv, int valid) {
         float z[PASSES][GM];
 #pragma unroll
@@ -239,7 +243,7 @@ struct SimtConsumer {
                 kh[2 * e] = dec_x2<FMT>((uint16_t)(w[e] & 0xFFFFu));
                 kh[2 * e + 1] = dec_x2<FMT>((uint16_t)(w[e] >> 16));
             }
-            const float ts = (FMT == INT8 ? ldsf(sk + 4 * t) : 1.0f) * qk_scale;
+            const float ks = FMT == INT8 ? ldsf(sk + 4 * (t * ng + gi)) : 1.0f;
 #pragma unroll
             for (int h = 0; h < GM; ++h) {
                 float d0 = 0.f, d1 = 0.f;
@@ -248,10 +252,10 @@ struct SimtConsumer {
                     d0 = fma_f16x2_f32(qh[h][e], kh[e], d0);
                     d1 = fma_f16x2_f32(qh[h][e + 1], kh[e + 1], d1);
                 }
-                float d = d0 + d1;
+                float d = (d0 + d1) * ks;
 #pragma unroll
                 for (int off = LPT / 2; off > 0; off >>= 1) d += __shfl_xor_sync(0xFFFFFFFFu, d, off);
-                z[ps][h] = t < valid ? d * ts : -INFINITY;
+                z[ps][h] = t < valid ? d * qk_scale : -INFINITY;
             }
         }
         float p[PASSES][GM];
@@ -289,7 +293,7 @@ struct SimtConsumer {
             // rows past the context may hold any bytes (NaN codes too): zero them
             if (t >= valid) vw = make_uint4(0u, 0u, 0u, 0u);
             const uint32_t w[4] = {vw.x, vw.y, vw.z, vw.w};
-            const float vs = (FMT == INT8 && t < valid) ? ldsf(sv + 4 * t) : 1.0f;
+            const float vs = (FMT == INT8 && t < valid) ? ldsf(sv + 4 * (t * ng + gi)) : 1.0f;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const float2 lo = f16x2_to_f32x2(dec_x2<FMT>((uint16_t)(w[e] & 0xFFFFu)));
@@ -307,9 +311,10 @@ struct SimtConsumer {
     }
 
     __device__ void tile(const Tile& c) {
-        half(c.k, c.v, c.s, c.s + 4 * kTile, c.valid);
+        const uint32_t sv = c.s + 4 * kTile * ng;
+        half(c.k, c.v, c.s, sv, c.valid);
         if (c.valid > kBox)
-            half(c.k + kBox * D, c.v + kBox * D, c.s + 4 * kBox, c.s + 4 * kTile + 4 * kBox, c.valid - kBox);
+            half(c.k + kBox * D, c.v + kBox * D, c.s + 4 * kBox * ng, sv + 4 * kBox * ng, c.valid - kBox);
     }
 
     // Sum the per-group partials and write this segment's partial slot.

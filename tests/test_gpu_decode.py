@@ -63,8 +63,8 @@ def case_id(c):
 def test_decode_small(case, kernel, partition):
     fmt, B, Hq, Hkv, D, BS, ctx = case[:7]
     group = case[7] if len(case) > 7 else 0
-    if kernel == kvq.KERNEL_SIMT and (Hq // Hkv > 4 or fmt == "int4" or (group and group != D)):
-        pytest.skip("CUDA-core kernel covers 8-bit codes, one scale per row and group size <= 4")
+    if kernel == kvq.KERNEL_SIMT and (Hq // Hkv > 4 or fmt == "int4"):
+        pytest.skip("CUDA-core kernel covers 8-bit codes and group size <= 4")
     dw = small(fmt, B, Hq, Hkv, D, BS, ctx, seed=len(ctx) + D, group=group)
     kvq.set_decode_kernel(kernel)
     out = dw.decode(partition_size=partition)
@@ -136,7 +136,7 @@ def test_nan_scales_past_the_context_do_not_leak(fmt, group):
     slots = lay.slots(0, 40).to(dev)          # -1 past each sequence's context
     kvq.append(k, v, cache, slots)
     q = W.query(wl, dev)
-    for kernel in (kvq.KERNEL_MMA, kvq.KERNEL_SIMT) if not group and fmt == "int8" else (kvq.KERNEL_MMA,):
+    for kernel in (kvq.KERNEL_MMA, kvq.KERNEL_SIMT) if fmt == "int8" else (kvq.KERNEL_MMA,):
         kvq.set_decode_kernel(kernel)
         out = kvq.decode_attention(q, cache, lay.block_tables.to(dev), ctx.to(dev), 40)
         o = out.float().cpu().numpy()

@@ -101,8 +101,8 @@ def case_id(c):
 def test_fused_equals_append_then_decode(case, kernel, partition):
     fmt, B, Hq, Hkv, D, BS, ctx = case[:7]
     group = case[7] if len(case) > 7 else 0
-    if kernel == kvq.KERNEL_SIMT and (Hq // Hkv > 4 or fmt == "int4" or group):
-        pytest.skip("CUDA-core kernel covers 8-bit codes, one scale per row and group size <= 4")
+    if kernel == kvq.KERNEL_SIMT and (Hq // Hkv > 4 or fmt == "int4"):
+        pytest.skip("CUDA-core kernel covers 8-bit codes and group size <= 4")
     dw = small(fmt, B, Hq, Hkv, D, BS, ctx, seed=len(ctx) * 31 + D, group=group)
     kvq.set_decode_kernel(kernel)
     g = torch.Generator(device="cpu").manual_seed(B * 100 + D)
