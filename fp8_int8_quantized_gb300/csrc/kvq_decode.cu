@@ -909,7 +909,8 @@ __global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int B = a.batch, Hkv = a.cache.num_kv_heads, BS = a.cache.block_size;
-    const int G = a.num_q_heads / Hkv;
+    const int Gall = a.num_q_heads / Hkv;   // q-heads per kv-head
+    const int G = a.heads, h0 = a.head_off;   // the ones this launch serves
     const bool append = a.k_new != nullptr;
     constexpr bool kRowScaled = FMT == INT8 || FMT == INT4;
     constexpr int RB = row_bytes(FMT, D);
@@ -1062,7 +1063,8 @@ __global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
                     }
                 }
                 if (new_pair)
-                    bulk_load(qbuf, a.q + ((int64_t)iw.b * a.num_q_heads + (int64_t)iw.kvh * G) * D, q_tx, fb, pol);
+                    bulk_load(qbuf, a.q + ((int64_t)iw.b * a.num_q_heads + (int64_t)iw.kvh * Gall + h0) * D, q_tx, fb,
+                              pol);
                 if (ends) {
                     const int64_t row = ((int64_t)iw.b * Hkv + iw.kvh) * D;
                     bulk_load(nkv, a.k_new + row, 2 * D, fb, pol);
@@ -1101,7 +1103,7 @@ __global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
         const bool pair_end = cw.t == cw.n - 1;
         const bool chunk_end = ctc == C - 1 || pair_end;
         if (chunk_end || fc == hi - 1) {
-            Flush fl{ws_acc, ws_ml, (int64_t)cw.b * a.num_q_heads + (int64_t)cw.kvh * G, cch, seg_half,
+            Flush fl{ws_acc, ws_ml, (int64_t)cw.b * a.num_q_heads + (int64_t)cw.kvh * Gall + h0, cch, seg_half,
                      a.num_chunks, s_out};
             cons.flush(fl);
             if (seg_half == 0 && chunk_end) {  // the whole chunk was this warp's: its second slot is empty
@@ -1258,7 +1260,7 @@ bool make_tmap(CUtensorMap* m, void* base, int64_t rows, int rb) {
 template <int FMT, int D, class Consumer>
 cudaError_t launch_stream(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, cudaStream_t s) {
     auto kern = decode_stream_kernel<FMT, D, Consumer>;
-    const int smem = Layout(row_bytes(FMT, D), D, a.num_q_heads / a.cache.num_kv_heads, a.batch,
+    const int smem = Layout(row_bytes(FMT, D), D, a.heads, a.batch,
                             FMT == INT8 || FMT == INT4, a.k_new != nullptr, a.cache.ngroups).total + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -1284,15 +1286,31 @@ cudaError_t launch_fmt_d(const CUtensorMap& tk, const CUtensorMap& tv, const Dec
     cudaError_t e;
     if (a.ev_begin && (e = cudaEventRecord(a.ev_begin, s)) != cudaSuccess) return e;
     bool simt = false;
+    DecodeArgs p = a;
+    p.head_off = 0;
+    p.heads = G;
     if constexpr (FMT != INT4) {  // INT4 has the tensor-core consumer only
         if (a.kernel == kKindSimt) {
             simt = true;
-            if (G == 1) e = launch_stream<FMT, D, SimtConsumer<FMT, D, 1>>(tk, tv, a, s);
-            else if (G == 2) e = launch_stream<FMT, D, SimtConsumer<FMT, D, 2>>(tk, tv, a, s);
-            else e = launch_stream<FMT, D, SimtConsumer<FMT, D, 4>>(tk, tv, a, s);
+            if (G == 1) e = launch_stream<FMT, D, SimtConsumer<FMT, D, 1>>(tk, tv, p, s);
+            else if (G == 2) e = launch_stream<FMT, D, SimtConsumer<FMT, D, 2>>(tk, tv, p, s);
+            else e = launch_stream<FMT, D, SimtConsumer<FMT, D, 4>>(tk, tv, p, s);
         }
     }
-    if (!simt) e = launch_stream<FMT, D, MmaConsumer<FMT, D>>(tk, tv, a, s);
+    if (!simt) {
+        // The tensor-core consumer's operand rows are (q-head, scale group)
+        // pairs, eight per launch: a group of G q-heads with ng scale groups per
+        // row takes ceil(G * ng / 8) launches over the same tiles, each serving
+        // 8 / ng of the heads; only the first appends the newest rows (the later
+        // ones read them from the cache).
+        const int per = 8 / a.cache.ngroups;
+        for (int h = 0; h < G && e == cudaSuccess; h += per) {
+            p.head_off = h;
+            p.heads = G - h < per ? G - h : per;
+            if (h > 0) p.k_new = p.v_new = nullptr;
+            e = launch_stream<FMT, D, MmaConsumer<FMT, D>>(tk, tv, p, s);
+        }
+    }
     if (e != cudaSuccess) return e;
     if (a.ev_end && (e = cudaEventRecord(a.ev_end, s)) != cudaSuccess) return e;
     const int64_t heads = (int64_t)a.batch * a.num_q_heads;

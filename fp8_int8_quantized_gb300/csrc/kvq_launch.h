@@ -67,6 +67,10 @@ struct DecodeArgs {
     cudaEvent_t ev_begin, ev_end;  // optional: recorded around the main kernel
     const uint16_t* k_new;  // optional fp16 [B][Hkv][D]: newest token's K/V, appended in the launch
     const uint16_t* v_new;
+    // q-heads of each kv-head's group served by one stream launch: heads
+    // head_off .. head_off + heads - 1 (all of them unless the tensor-core
+    // consumer needs more than one pass; set by launch_decode)
+    int32_t head_off, heads;
 };
 
 struct PrefillArgs {

@@ -95,8 +95,9 @@ typedef enum {
  *     0 or head_dim = one scale per row; head_dim / 2 or head_dim / 4 = two or
  *     four groups of consecutive channels, each quantized as a row is (its own
  *     amax and scale).  Must be 0 for FP8; any other value is INVALID_ARG.
- *     Decode takes a group count times the q-heads per kv-head of at most 8
- *     (UNSUPPORTED otherwise); chunked prefill takes every group size. */
+ *     Every entry point takes every group size; decode with more than 8
+ *     (q-head, scale group) pairs per kv-head streams the cache in
+ *     ceil(G * groups / 8) passes. */
 typedef struct {
     void* k_codes;
     void* v_codes;

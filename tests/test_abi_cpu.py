@@ -58,10 +58,9 @@ def test_group_sizes_checked_before_any_cuda_call(lib):
     assert lib.kvq_append(16, 16, ctypes.byref(d8), 16, 4, None, kvq.INT8, None) == 1     # 8 groups
     f8 = kvq.KvqCacheDesc(16, 16, None, None, 8, 16, 2, 128, kvq.E4M3, 32)
     assert lib.kvq_append(16, 16, ctypes.byref(f8), 16, 4, None, kvq.E4M3, None) == 1     # FP8 has no groups
-    d4 = kvq.KvqCacheDesc(16, 16, 16, 16, 8, 16, 2, 128, kvq.INT4, 32)
-    # 4 groups x 4 q-heads per kv-head = 16 operand rows > 8
+    d4 = kvq.KvqCacheDesc(16, 16, 16, 16, 8, 16, 2, 128, kvq.INT4, 40)
     assert lib.kvq_decode_attention(16, ctypes.byref(d4), 16, 4, 16, 2, 8, 64, None, kvq.INT4, 0.0,
-                                    16, None, 0, 0, None) == 2
+                                    16, None, 0, 0, None) == 1                             # 40 does not divide
     d4.group_size = 48
     assert lib.kvq_prefill_attention(16, ctypes.byref(d4), 16, 4, 16, 16, 2, 4, 4, 4, None, kvq.INT4,
                                      0.0, 16, None) == 1                                   # 48 does not divide

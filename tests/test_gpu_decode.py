@@ -50,6 +50,10 @@ CASES = [
     ("int8", 3, 8, 1, 64, 16, [300, 1, 77], 64),
     ("int8", 2, 3, 3, 64, 16, [200, 45], 16),
     ("int4", 2, 4, 1, 128, 16, [96, 1000], 64),
+    # more than 8 (q-head, group) operand rows: several launches over the same tiles
+    ("int8", 2, 16, 2, 128, 32, [500, 64], 32),
+    ("int4", 2, 8, 1, 128, 16, [300, 33], 64),
+    ("int8", 3, 8, 2, 64, 16, [200, 17, 1], 16),
 ]
 
 
