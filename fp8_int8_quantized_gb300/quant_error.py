@@ -35,11 +35,10 @@ VARIANTS = [("e4m3", "amax"), ("e4m3", "one"), ("e5m2", "amax"), ("e5m2", "one")
 
 
 def variant(base: W.Workload, fmt: str, rule: str) -> W.Workload | None:
-    """The workload of one variant, or None where decode does not take it (q-heads
-    per kv-head times groups per row above 8)."""
+    """The workload of one variant (None where it does not apply)."""
     if rule.startswith("g"):
         group = int(rule[1:])
-        if base.group * (base.head_dim // group) > 8:
+        if base.head_dim % group:
             return None
         return dataclasses.replace(base, fmt=fmt, scale_rule="row", quant_group=group)
     return dataclasses.replace(base, fmt=fmt, scale_rule=rule, quant_group=0)
