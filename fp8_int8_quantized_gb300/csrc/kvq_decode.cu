@@ -8,11 +8,11 @@
 // logits take s_K, outputs take s_V.  INT4 rows are head_dim / 2 bytes (two
 // codes per byte) and use the tensor-core consumer only.
 //
-// Work decomposition.  Every (sequence, kv-head) pair owns ceil(ctx / 16)
-// tiles of 16 tokens; all pairs' tiles, in (sequence, kv-head, tile) order,
-// form one flat list.  A persistent grid (a few CTAs per SM, four independent
-// warps each) splits that list into equal contiguous ranges, one per warp, so
-// every warp streams the same number of bytes whatever the context lengths.
+// Work decomposition.  Every (sequence, kv-head) pair owns ceil(ctx / 32)
+// tiles of 32 tokens; all pairs' tiles, in (sequence, kv-head, tile) order,
+// form one flat list.  A persistent grid (two CTAs per SM of six independent
+// warps, eight for INT4) splits that list into equal contiguous ranges, one
+// per warp, so every warp streams the same number of bytes whatever the context lengths.
 // All q-heads of a kv-head's group are served by the warp that reads its tile,
 // so each cached byte is read from HBM once.  Contexts are cut into chunks of
 // C tiles; a warp range is never shorter than C, so a chunk is streamed by at
@@ -55,9 +55,6 @@
 #ifndef KVQ_MIN_BLOCKS
 #define KVQ_MIN_BLOCKS 2
 #endif
-#ifndef KVQ_WARPS
-#define KVQ_WARPS 6
-#endif
 
 namespace kvq {
 namespace {
@@ -65,8 +62,6 @@ namespace {
 constexpr int kTile = kDecodeTileTokens;       // tokens per stage: two boxes
 constexpr int kBox = 16;                       // rows per TMA box (a 16-token slice of one paged block)
 constexpr int kSpw = KVQ_SPW;                  // stages per warp
-constexpr int kConsumers = KVQ_WARPS;          // warps per CTA, each streaming its own range
-constexpr int kThreads = kConsumers * 32;
 constexpr int kMinBlocks = KVQ_MIN_BLOCKS;     // CTAs per SM the registers are sized for
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -83,16 +78,17 @@ struct Layout {
     int tile_bytes, q_bytes, scales, full, qbuf, newkv, patch, scan, total;
     // rb: bytes of one cached row (head_dim, or head_dim / 2 for INT4); int8:
     // the format carries row scales (INT8 or INT4), ng of them per row
-    __host__ __device__ Layout(int rb, int D, int G, int B, bool int8, bool append, int ng) {
+    // W: warps of the CTA
+    __host__ __device__ Layout(int W, int rb, int D, int G, int B, bool int8, bool append, int ng) {
         tile_bytes = kTile * rb;
         q_bytes = (G * D * 2 + 127) / 128 * 128;
-        scales = kConsumers * kSpw * 2 * tile_bytes;            // [warp][stage][K,V][tile] before this
+        scales = W * kSpw * 2 * tile_bytes;            // [warp][stage][K,V][tile] before this
         // INT8 / INT4: f32 [warp][stage][K,V][32 tokens][ng]
-        full = scales + (int8 ? kConsumers * kSpw * 2 * kTile * 4 * ng : 0);
-        qbuf = (full + kConsumers * kSpw * 8 + 127) / 128 * 128;  // u64 [warp][stage], then f16 [warp][G][D]
-        newkv = qbuf + kConsumers * q_bytes;                    // f16 [warp][K,V][D]
-        patch = newkv + (append ? kConsumers * 2 * D * 2 : 0);  // int [warp]
-        scan = patch + (append ? kConsumers * 4 : 0);           // int S[B + 1], ctx[B]
+        full = scales + (int8 ? W * kSpw * 2 * kTile * 4 * ng : 0);
+        qbuf = (full + W * kSpw * 8 + 127) / 128 * 128;  // u64 [warp][stage], then f16 [warp][G][D]
+        newkv = qbuf + W * q_bytes;                    // f16 [warp][K,V][D]
+        patch = newkv + (append ? W * 2 * D * 2 : 0);  // int [warp]
+        scan = patch + (append ? W * 4 : 0);           // int S[B + 1], ctx[B]
         total = scan + (2 * B + 1) * 4;
     }
 };
@@ -188,6 +184,7 @@ struct SimtConsumer {
     static constexpr int TPP = 32 / LPT;   // tokens per pass
     static constexpr int PASSES = kBox / TPP;
     static constexpr int kMinCtas = GM == 4 ? 3 : kMinBlocks;  // 4 query rows need more registers
+    static constexpr int kWarps = 6;
     uint32_t qh[GM][8];
     float m[GM], l[GM], acc[GM][16];
     int lane, j, grp, G, ng, gi;   // INT8: ng scales per row; this lane's 16 dims lie in group gi
@@ -361,6 +358,12 @@ struct MmaConsumer {
     static constexpr int VW = I4 ? DV / 8 : DV / 4;
     static constexpr int MT = D / 16;   // m-tiles of PV (head_dim / 16)
     static constexpr int kMinCtas = kMinBlocks;
+    // Warps per CTA, each streaming its own range.  INT4 tiles are half the
+    // bytes of the others, and the kernel is bound by the latency of the
+    // per-warp register work rather than by HBM: 8 warps (registers capped at
+    // 128, two CTAs per SM) are 11% faster than 6.  The 8-bit formats stay at
+    // 6: at 8 their stages no longer fit two CTAs into shared memory.
+    static constexpr int kWarps = I4 ? 8 : 6;
     // INT8 codes enter the tensor cores as fp16 1152 + code (exact); INT4 codes
     // as the fp16 subnormal (code + 8) * 2^-24 (exact: the offset nibble is the
     // mantissa), or 16x that where the nibble is left in mantissa bits 4..7 --
@@ -902,7 +905,7 @@ __device__ __noinline__ void append_newest(const uint16_t* nkv, int blk, int pos
 // -------------------------------------------------------------- kernel --
 
 template <int FMT, int D, class Consumer>
-__global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
+__global__ void __launch_bounds__(Consumer::kWarps * 32, Consumer::kMinCtas)
     decode_stream_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                          const DecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -915,7 +918,8 @@ __global__ void __launch_bounds__(kThreads, Consumer::kMinCtas)
     constexpr bool kRowScaled = FMT == INT8 || FMT == INT4;
     constexpr int RB = row_bytes(FMT, D);
     const int ng = a.cache.ngroups;
-    const Layout L(RB, D, G, B, kRowScaled, append, ng);
+    constexpr int kConsumers = Consumer::kWarps, kThreads = kConsumers * 32;
+    const Layout L(kConsumers, RB, D, G, B, kRowScaled, append, ng);
     const uint32_t sc_stage = 2 * kTile * 4 * ng;  // bytes of a stage's K and V scales
     int* S = reinterpret_cast<int*>(smem + L.scan);
     int* ctx_s = S + B + 1;
@@ -1260,7 +1264,8 @@ bool make_tmap(CUtensorMap* m, void* base, int64_t rows, int rb) {
 template <int FMT, int D, class Consumer>
 cudaError_t launch_stream(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, cudaStream_t s) {
     auto kern = decode_stream_kernel<FMT, D, Consumer>;
-    const int smem = Layout(row_bytes(FMT, D), D, a.heads, a.batch,
+    constexpr int kConsumers = Consumer::kWarps, kThreads = kConsumers * 32;
+    const int smem = Layout(kConsumers, row_bytes(FMT, D), D, a.heads, a.batch,
                             FMT == INT8 || FMT == INT4, a.k_new != nullptr, a.cache.ngroups).total + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
