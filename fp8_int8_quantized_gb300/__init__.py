@@ -1,6 +1,8 @@
 """Python binding of the kvq C ABI (``include/kvq.h``): a GB300 quantized paged
-KV cache -- FP8 (E4M3 / E5M2, per-tensor scale) or online INT8 quantize-on-write,
-and single-token decode attention that dequantizes on read.
+KV cache -- FP8 (E4M3 / E5M2, per-tensor scale) or online INT8 / INT4
+(one scale per row or per channel group) quantize-on-write -- with single-token
+decode attention (optionally fused with the step's append) and chunked causal
+prefill attention that dequantize on read.
 
 This module only marshals arguments: it checks tensor dtypes, devices and
 layouts, passes raw device pointers and the current CUDA stream to
