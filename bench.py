@@ -28,6 +28,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -98,7 +99,9 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        # the raw samples: $KVQ_CLOCKS_DIR if set, else the system temporary directory
+        self.path = os.path.join(os.environ.get("KVQ_CLOCKS_DIR") or tempfile.gettempdir(),
+                                 f"kvq_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
