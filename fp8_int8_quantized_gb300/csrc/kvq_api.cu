@@ -87,7 +87,7 @@ kvq::CacheView view(const kvq_cache* c) {
 // kernel streams a contiguous range of the flat tile list that is at least one
 // chunk long; chunks of about half a range keep every warp busy while the
 // partial slots stay few (two per chunk).  Counts 16 warps per SM (the kernel
-// runs 12), so chunks come out at about 0.4 of a range.
+// runs 12, and 16 for INT4), so chunks come out at 0.4-0.5 of a range.
 int32_t choose_chunk_tiles(int32_t batch, int32_t num_kv_heads, int32_t group, int32_t max_ctx, int sms) {
     constexpr int TT = kvq::kDecodeTileTokens;
     const int64_t tiles = (int64_t)batch * num_kv_heads * ((max_ctx + TT - 1) / TT);
