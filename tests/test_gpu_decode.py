@@ -43,6 +43,9 @@ CASES = [
     ("int4", 2, 4, 4, 128, 64, [640, 65]),
     ("int4", 3, 8, 2, 64, 16, [129, 1, 256]),
     ("int4", 2, 32, 8, 128, 32, [1000, 33]),
+    ("int4", 2, 16, 2, 128, 16, [700, 40]),
+    ("int4", 2, 8, 1, 64, 32, [333, 64]),
+    ("int8", 2, 10, 2, 128, 16, [257, 96]),
     # group quantization (last field: channels per scale): q-heads per kv-head x groups <= 8
     ("int8", 2, 4, 2, 128, 32, [500, 33], 32),
     ("int4", 2, 4, 4, 128, 64, [640, 65], 32),
