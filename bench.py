@@ -352,6 +352,48 @@ def cpu_baseline(wl, target_s: float):
                       f"{dt:.2f} s"}
 
 
+def e2e_latency(S, K, flush):
+    """End-to-end steps for inputs smaller than L2, one at a time: before each
+    step an untimed write of ``flush`` (twice the L2 size) evicts the cache from
+    L2; the step -- the packed pinned upload, append and decode, the download of
+    the output to pinned memory -- runs on one stream between two events.
+    Returns (ms per step, H2D bytes per step, D2H bytes per step, steps)."""
+    import torch
+
+    import fp8_int8_quantized_gb300 as kvq
+    parts = [S.q, S.k_step, S.v_step, S.slots_step, S.bt, S.cl]
+    offs, at = [], 0
+    for t in parts:
+        offs.append(at)
+        at += (t.numel() * t.element_size() + 255) // 256 * 256
+    h_in = torch.empty(at, dtype=torch.uint8).pin_memory()
+    for t, o in zip(parts, offs):
+        n = t.numel() * t.element_size()
+        h_in[o:o + n].copy_(t.reshape(-1).view(torch.uint8).cpu())
+    d_in = torch.empty(at, dtype=torch.uint8, device=S.q.device)
+    q, k, v, slots, bt, cl = [d_in[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                              for t, o in zip(parts, offs)]
+    out = torch.empty_like(S.q)
+    h_out = torch.empty(S.q.shape, dtype=S.q.dtype).pin_memory()
+    stream = torch.cuda.current_stream()
+    Ke = max(3, min(K, 2000))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ke + 3)]
+    for i, (a, b) in enumerate(ev):
+        flush.fill_(i)
+        a.record(stream)
+        d_in.copy_(h_in, non_blocking=True)
+        if slots.numel() and not S.fused:
+            kvq.append(k, v, S.cache, slots, S.scale)
+        S.decode_step(q, k, v, bt, cl, out)
+        h_out.copy_(out, non_blocking=True)
+        b.record(stream)
+    torch.cuda.synchronize()
+    if not torch.equal(h_out.to(S.out.device), S.out):
+        raise RuntimeError("end-to-end output differs from the device-resident step's")
+    ms = sum(a.elapsed_time(b) for a, b in ev[3:]) / Ke
+    return ms, at, h_out.numel() * h_out.element_size(), Ke
+
+
 def e2e_pipeline(S, K):
     """End-to-end steps as a serving loop issues them, through the public API.
 
@@ -458,16 +500,31 @@ def run_kvq(args):
     if st != 0:
         raise RuntimeError(f"device error {st} ({detail})")
 
+    # Inputs that fit in L2 (small batches) would be read from L2 by every step
+    # after the first: such runs write a buffer of twice the L2 size before
+    # each step and time each step alone between two events.
+    flush = None
+    if S.dec_bytes["total"] <= L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    steps_ev = ([(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+                if flush is not None else None)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        # the timed region: exactly K steps, events only at its two ends
-        start.record(stream)
-        for _ in range(K):
-            S.step()
-        end.record(stream)
+        if flush is None:
+            # the timed region: exactly K steps, events only at its two ends
+            start.record(stream)
+            for _ in range(K):
+                S.step()
+            end.record(stream)
+        else:
+            for i, (a, b) in enumerate(steps_ev):
+                flush.fill_(i)
+                a.record(stream)
+                S.step()
+                b.record(stream)
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -484,6 +541,8 @@ def run_kvq(args):
     torch.cuda.synchronize()
     for i in range(Ki):
         e = ev[i]
+        if flush is not None:
+            flush.fill_(i)
         e[0].record(stream)
         if not S.fused:
             S.append()
@@ -493,7 +552,7 @@ def run_kvq(args):
         e[2].record(stream)
     torch.cuda.synchronize()
     kvq.set_decode_timing_events()
-    total_ms = start.elapsed_time(end)
+    total_ms = (start.elapsed_time(end) if flush is None else sum(a.elapsed_time(b) for a, b in steps_ev))
     app_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / Ki
     dec_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / Ki
     kern_ms = sum(e[3].elapsed_time(e[4]) for e in ev) / Ki
@@ -506,12 +565,15 @@ def run_kvq(args):
     # end to end through the public API: pinned host inputs in, result out
     e2e = None
     if not args.no_e2e:
-        e_ms, h2d, d2h, Ke = e2e_pipeline(S, K)
+        e_ms, h2d, d2h, Ke = e2e_pipeline(S, K) if flush is None else e2e_latency(S, K, flush)
         e_max, e_units = aggregate(e_ms, float(S.dec_bytes["total"]), world)
         e2e = {"value": round(e_units / (e_max * 1e-3) / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": round(e_max, 4), "steps": Ke,
-               "pipeline": "one packed pinned upload per step on a copy stream, double-buffered device "
-                           "inputs and outputs, output read back to pinned memory every step"}
+               "pipeline": ("one packed pinned upload per step on a copy stream, double-buffered device "
+                            "inputs and outputs, output read back to pinned memory every step"
+                            if flush is None else
+                            "one step at a time after an L2 flush: packed pinned upload, kernels and the "
+                            "output's read back to pinned memory on one stream between two events")}
 
     if rank != 0:
         if world > 1:
@@ -550,7 +612,9 @@ def run_kvq(args):
                    "step": f"append {S.slots_step.numel()} tokens + decode {wl.batch} sequences"
                            + (" (the append fused into the decode launch)" if S.fused else ""),
                    "l2": f"inputs larger than L2 ({S.dec_bytes['total'] / 1e6:.0f} MB read per decode > 129 MB)"
-                   if S.dec_bytes["total"] > L2_BYTES else "inputs smaller than L2 (latency case)",
+                   if flush is None else
+                   f"inputs smaller than L2: a {2 * L2_BYTES / 1e6:.0f} MB buffer written before every step, "
+                   "each step timed alone between two events",
                    "kernel": args.kernel, "partition": args.partition or "auto",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "tokens_per_s": round(seqs / (max_ms * 1e-3), 1),
