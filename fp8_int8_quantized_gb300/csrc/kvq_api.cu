@@ -123,9 +123,8 @@ kvq_status decode_impl(const void* q, const void* k_new, const void* v_new, cons
     if (num_q_heads % cache->num_kv_heads) return KVQ_ERR_INVALID_ARG;
     const int G = num_q_heads / cache->num_kv_heads;
     if (G > 8) return KVQ_ERR_UNSUPPORTED;
-    // the tensor-core consumer carries one operand row per (q-head, scale group),
-    // eight per launch: more take several launches over the same tiles
-    const int ng = cache->group_size > 0 ? cache->head_dim / cache->group_size : 1;
+    // (the tensor-core consumer carries one operand row per (q-head, scale
+    // group), eight per launch: more take several launches over the same tiles)
     if ((int64_t)max_blocks_per_seq * cache->block_size < max_context_len) return KVQ_ERR_INVALID_ARG;
     if (batch > 65535 || cache->num_kv_heads > 65535 || num_q_heads > 65535) return KVQ_ERR_UNSUPPORTED;
     if (batch == 0) return KVQ_OK;
