@@ -95,3 +95,45 @@ def test_invalid_args_rejected_before_any_cuda_call(lib):
                                            0.0, 16, None, 0, 0, None) == 1                  # no k_new
     assert lib.kvq_decode_attention_append(16, 24, 16, ctypes.byref(d), 16, 4, 16, 2, 4, 64, None, kvq.E4M3,
                                            0.0, 16, None, 0, 0, None) == 1                  # misaligned k_new
+
+
+def test_more_decode_checks_before_any_cuda_call(lib):
+    import ctypes
+    d = kvq.KvqCacheDesc(16, 16, None, None, 8, 16, 2, 128, kvq.E4M3)
+
+    def dec(q=16, cache=d, ctx=64, batch=2, nq=4, sm=0.0, out=16, ws=256, ws_bytes=1 << 30, part=64, fmt=kvq.E4M3):
+        return lib.kvq_decode_attention(q, ctypes.byref(cache), 16, 4, 16, batch, nq, ctx, None, fmt, sm,
+                                        out, ws, ws_bytes, part, None)
+
+    assert dec(q=8) == 1                                   # q not 16-byte aligned
+    assert dec(out=24) == 1                                # out not 16-byte aligned
+    assert dec(sm=float("nan")) == 1
+    assert dec(sm=float("inf")) == 1
+    assert dec(sm=-1.0) == 1
+    assert dec(batch=-1) == 1
+    assert dec(ctx=-5) == 1
+    assert dec(batch=5000) == 2                            # the context-length scan holds 4096
+    assert dec(batch=0) == 0                               # nothing to do, nothing launched
+    assert dec(ws=None) == 3                               # no workspace
+    assert dec(ws=128) == 3                                # workspace not 256-byte aligned
+    assert dec(ws_bytes=64) == 3                           # workspace too small
+    bs8 = kvq.KvqCacheDesc(16, 16, None, None, 8, 8, 2, 128, kvq.E4M3)
+    assert dec(cache=bs8) == 2                             # block size 8
+    huge = kvq.KvqCacheDesc(16, 16, None, None, 1 << 27, 16, 2, 128, kvq.E4M3)
+    assert dec(cache=huge) == 2                            # TMA row coordinates are 32-bit
+    i4 = kvq.KvqCacheDesc(16, 16, 16, 16, 8, 16, 2, 128, kvq.INT4)
+    prev = lib.kvq_set_decode_kernel(kvq.KERNEL_SIMT)
+    try:
+        assert dec(cache=i4, fmt=kvq.INT4) == 2            # the CUDA-core kernel takes 8-bit codes only
+        assert dec(nq=10) == 2                             # ... and at most 4 q-heads per kv-head
+    finally:
+        lib.kvq_set_decode_kernel(prev)
+
+
+def test_workspace_size_rejects_bad_shapes(lib):
+    assert lib.kvq_decode_workspace_size(0, 4, 2, 128, 64, 64) == 0
+    assert lib.kvq_decode_workspace_size(2, 3, 2, 128, 64, 64) == 0       # 3 % 2 != 0
+    assert lib.kvq_decode_workspace_size(2, 4, 2, 128, -1, 64) == 0
+    assert lib.kvq_decode_workspace_size(2, 4, 2, 128, 64, 64) > 0
+    # more context, more chunks: never smaller
+    assert lib.kvq_decode_workspace_size(2, 4, 2, 128, 4096, 64) >= lib.kvq_decode_workspace_size(2, 4, 2, 128, 64, 64)
