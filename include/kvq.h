@@ -243,7 +243,10 @@ KVQ_API kvq_status kvq_prefill_attention(const void* q, const kvq_cache* cache,
 
 /* Debug gather + dequantize-on-read: for each of num_slots slots, fp32
  * [num_slots][num_kv_heads][head_dim] rows of K and V, each value
- * fl32(decode(code) * scale) (FP8) or fl32(code * row_scale) (INT8). */
+ * fl32(decode(code) * scale) (FP8) or fl32(code * s) (INT8, INT4), s the
+ * scale of the value's row, or of its channel group when group_size > 0.
+ * A slot outside the cache leaves its rows unwritten and is recorded for
+ * kvq_device_error_check (KVQ_ERR_OUT_OF_RANGE). */
 KVQ_API kvq_status kvq_dequant(const kvq_cache* cache, const int64_t* slots, int64_t num_slots,
                        const float* scale, int32_t fmt, float* out_k, float* out_v,
                        kvq_stream_t stream);

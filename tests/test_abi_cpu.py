@@ -137,3 +137,31 @@ def test_workspace_size_rejects_bad_shapes(lib):
     assert lib.kvq_decode_workspace_size(2, 4, 2, 128, 64, 64) > 0
     # more context, more chunks: never smaller
     assert lib.kvq_decode_workspace_size(2, 4, 2, 128, 4096, 64) >= lib.kvq_decode_workspace_size(2, 4, 2, 128, 64, 64)
+
+
+def test_prefill_append_dequant_checks_before_any_cuda_call(lib):
+    import ctypes
+    d = kvq.KvqCacheDesc(16, 16, None, None, 8, 16, 2, 128, kvq.E4M3)
+    one = kvq.KvqCacheDesc(16, 16, None, None, 8, 16, 1, 128, kvq.E4M3)
+
+    def pre(q=16, cache=d, batch=2, ntok=8, nq=4, maxq=4, sm=0.0, out=16, qs=16):
+        return lib.kvq_prefill_attention(q, ctypes.byref(cache), 16, 4, 16, qs, batch, ntok, nq, maxq, None,
+                                         kvq.E4M3, sm, out, None)
+
+    assert pre(q=8) == 1                                   # q not 16-byte aligned
+    assert pre(qs=None) == 1                               # no query_start
+    assert pre(qs=18) == 1                                 # query_start not 4-byte aligned
+    assert pre(sm=float("nan")) == 1
+    assert pre(nq=3) == 1                                  # 3 q-heads over 2 kv-heads
+    assert pre(ntok=-1) == 1
+    assert pre(cache=one, nq=256) == 2                     # 256 q-heads per kv-head: above the 128-row tile
+    assert pre(ntok=1 << 31) == 2                          # query_start entries are int32
+    assert pre(batch=0) == 0 and pre(maxq=0) == 0 and pre(ntok=0) == 0   # nothing to do
+    # append: negative or zero token counts, misaligned slot mapping
+    assert lib.kvq_append(16, 16, ctypes.byref(d), 16, -1, None, kvq.E4M3, None) == 1
+    assert lib.kvq_append(16, 16, ctypes.byref(d), 16, 0, None, kvq.E4M3, None) == 0
+    assert lib.kvq_append(16, 16, ctypes.byref(d), 12, 4, None, kvq.E4M3, None) == 1
+    assert lib.kvq_append(16, 16, ctypes.byref(d), 16, 4, 2, kvq.E4M3, None) == 1      # scale not 4-byte aligned
+    # dequant: negative count, missing outputs
+    assert lib.kvq_dequant(ctypes.byref(d), 16, -1, None, kvq.E4M3, 16, 16, None) == 1
+    assert lib.kvq_dequant(ctypes.byref(d), 16, 0, None, kvq.E4M3, 16, 16, None) == 0
