@@ -175,11 +175,40 @@ def measured_tensor_peak(sustained: bool = False):
         return (1700.0, "fallback sustained") if sustained else (1900.0, "fallback burst")
 
 
+def strip_comments(src: str) -> str:
+    """C/C++/CUDA source without its comments, trailing blanks and empty lines
+    (string and character literals kept as written)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        ch = src[i]
+        if ch in "\"'":
+            j = i + 1
+            while j < n and src[j] != ch:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(ch)
+            i += 1
+    lines = (line.rstrip() for line in "".join(out).splitlines())
+    return "\n".join(line for line in lines if line)
+
+
 def kernel_source_hash() -> str:
+    """Hash of the decode kernel's sources with comments and blank lines
+    removed: a change to the code (not to its comments) invalidates the
+    recorded traffic."""
     h = hashlib.sha256()
     for name in ("kvq_decode.cu", "kvq_device.cuh", "kvq_launch.h"):
-        with open(os.path.join(ROOT, "fp8_int8_quantized_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "fp8_int8_quantized_gb300", "csrc", name), encoding="utf-8") as f:
+            h.update(strip_comments(f.read()).encode())
+            h.update(b"\0")
     return h.hexdigest()[:16]
 
 

@@ -25,10 +25,10 @@
 // with 2-D TMA tile loads (cp.async.bulk.tensor, issued by lane 0) right after
 // consuming it, so its loads run the ring's length ahead across pair
 // boundaries.  (More stages for the half-size INT4 tiles measured no faster:
-// INT4 decode is not bound by the bytes in flight.)  Block ids of the
-// next 32 tiles are held one per lane (loaded one window ahead); the first
-// tile of each (sequence, kv-head) pair also carries a bulk copy of the pair's
-// query rows into the warp's query buffer.
+// INT4 decode is not bound by the bytes in flight.)  Block ids of the 32
+// boxes of the next 16 tiles are held one per lane (loaded one window ahead);
+// the first tile of each (sequence, kv-head) pair also carries a bulk copy of
+// the pair's query rows into the warp's query buffer.
 //
 // Two consumer families:
 //   * kKindSimt: CUDA cores; 16 head-dim values per lane, mixed-precision
@@ -658,7 +658,7 @@ struct MmaConsumer {
         }
     }
 
-    // P of one box as the B operand of PV (k = token, n = head g), carried as
+    // P of one box as the B operand of PV (k = token, n = operand row g), as
     // an fp16 pair hi + lo (lo = the fp16 residual of p - hi): the PV product
     // keeps about 22 bits of each weight instead of 11.  With outlier channels
     // the weighted mean of large V values can cancel, and a single fp16

@@ -63,3 +63,15 @@ def test_tensor_peak_choice():
         p = json.load(f)
     assert bench.measured_tensor_peak() == (p["bf16_tflops"], "measured burst")
     assert bench.measured_tensor_peak(sustained=True) == (p["bf16_tflops_sustained"], "measured sustained")
+
+
+def test_source_hash_ignores_comments_only():
+    import bench
+    code = 'int f(int x) {\n  return x + 1;  // one\n}\n/* a note */\nconst char* s = "a // b /* c */";\n'
+    same = '// header\nint f(int x) {\n\n  return x + 1;\n}\nconst char* s = "a // b /* c */";  /* x */\n'
+    other = 'int f(int x) {\n  return x + 2;\n}\nconst char* s = "a // b /* c */";\n'
+    assert bench.strip_comments(code) == bench.strip_comments(same)
+    assert bench.strip_comments(code) != bench.strip_comments(other)
+    assert '"a // b /* c */"' in bench.strip_comments(code)
+    # the committed traffic figures are keyed by the current decode sources
+    assert bench.recorded_traffic("llama2-7b") is not None
