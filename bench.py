@@ -14,9 +14,12 @@ kvq_decode_attention.
 
 Prints ONE JSON line (rank 0).  ``value`` is decode KV-read GB/s: the
 algorithmic bytes of the decode calls (every cached K/V byte of every context
-once, INT8 row scales, q, out, block tables) over the step time, summed over
+once, INT8 / INT4 scales, q, out, block tables) over the step time, summed over
 ranks (each rank runs its own copy of the workload: weak scaling, no
-collective on the data path).
+collective on the data path).  Workloads whose decode reads more than the L2
+size run K steps back to back between two events; smaller ones (a small
+--batch, or the tiny workload) write a buffer of twice the L2 size before
+every step and time each step alone.
 """
 from __future__ import annotations
 
