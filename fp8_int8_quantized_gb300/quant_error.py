@@ -46,6 +46,8 @@ def variant(base: W.Workload, fmt: str, rule: str) -> W.Workload | None:
 
 def supported_variants(name: str) -> list[tuple[str, str]]:
     return [v for v in VARIANTS if variant(W.WORKLOADS[name], *v) is not None]
+
+
 WINDOW_TOKENS = 1 << 19  # generation windows (values depend on the window start)
 
 

@@ -2,6 +2,7 @@
 shapes and byte counts of the workloads, the paged layout (block tables are a
 permutation of the cache's blocks, slots follow the tables), reproducible
 generation, and the outlier channels."""
+import dataclasses
 import math
 
 import numpy as np
@@ -88,3 +89,14 @@ def test_chunk_windows_cover_the_context():
         assert win[0][0] == 0 and win[-1][1] == (wl.ctx if isinstance(wl.ctx, int) else wl.ctx[1])
         assert all(a[1] == b[0] for a, b in zip(win, win[1:]))
         assert all((p1 - p0) * wl.batch <= max(1 << 19, wl.block_size * wl.batch) for p0, p1 in win)
+
+
+def test_quant_error_variants():
+    from fp8_int8_quantized_gb300 import quant_error as Q
+    base = W.WORKLOADS["llama2-7b"]
+    v = Q.variant(base, "int4", "g32")
+    assert (v.fmt, v.scale_rule, v.quant_group, v.scales_per_row) == ("int4", "row", 32, 4)
+    v = Q.variant(base, "e5m2", "one")
+    assert (v.fmt, v.scale_rule, v.quant_group) == ("e5m2", "one", 0)
+    assert Q.variant(dataclasses.replace(base, head_dim=64), "int4", "g48") is None   # 48 does not divide 64
+    assert set(Q.supported_variants("llama2-7b")) == set(Q.VARIANTS)
