@@ -6,11 +6,14 @@
  *   kvq_append            quantize-on-write of fp16 K/V into the paged cache;
  *   kvq_decode_attention  single-token decode attention that dequantizes the
  *                         cache on read and computes in fp16/fp32.
- *   kvq_decode_attention_append  the same decode with each sequence's newest
- *                         K/V row quantized into the cache in the same launch.
  *
- * plus kvq_dequant, a debugging gather that returns the fp32 values a kernel
- * sees.  The operations follow these pages (cited by title and section):
+ * Around them: kvq_decode_attention_append (the same decode with each
+ * sequence's newest K/V row quantized into the cache in the same launch),
+ * kvq_decode_attention_static_scratch (decode without a caller workspace),
+ * kvq_prefill_attention (causal attention of a chunk of new queries per
+ * sequence over the same cache) and kvq_dequant (a debugging gather of the
+ * fp32 values a kernel sees).  The operations follow these pages (cited by
+ * title and section):
  *
  *   [TGI] "Accelerating Inference with FP8 KV Cache" (text-generation-inference
  *         docs).  Intro: the KV cache is stored in FP8 while computation runs in
@@ -22,7 +25,10 @@
  *         shared by K and V.  "Current Hardware Support": NVIDIA GPUs take
  *         E4M3 ("fp8") and E5M2 ("fp8_e5m2").
  *   [LMD] "[Feature] TurboMind support W8A8 or FP8 KV Cache" (lmdeploy issue
- *         1463): online KV-cache INT8 (quant-policy 8) as the alternative.
+ *         1463): online KV-cache INT8 (quant-policy 8) as the alternative, and
+ *         an INT4 implementation named beside it.
+ *   [QQQ] "[QST] Scale factors and benchmarks" (QQQ issue 2): group
+ *         quantization named for a 4-bit KV cache.
  *
  * Conventions for every call:
  *   - Every pointer argument is a DEVICE pointer owned by the caller, except the
