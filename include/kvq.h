@@ -150,9 +150,10 @@ KVQ_API size_t kvq_decode_workspace_size(int32_t batch, int32_t num_q_heads, int
  *     a multiple of num_kv_heads and the group size at most 8.
  *   INT4 caches are decoded by the tensor-core kernel (kvq_set_decode_kernel(1)
  *   with INT4 returns KVQ_ERR_UNSUPPORTED).
- *   batch at most 4096, and batch * num_kv_heads * ceil(max_context_len / 16)
+ *   batch at most 4096, and batch * num_kv_heads * ceil(max_context_len / 32)
  *     below 2^31 (KVQ_ERR_UNSUPPORTED otherwise).
- *   scale: FP8 per-tensor scale as in kvq_append (NULL = 1.0); ignored for INT8.
+ *   scale: FP8 per-tensor scale as in kvq_append (NULL = 1.0); ignored for INT8
+ *     and INT4.
  *   sm_scale: softmax scale; 0 selects 1 / sqrt(head_dim).
  *   out: fp16 [batch][num_q_heads][head_dim] = softmax(sm_scale * q K^T) V.
  *   workspace: device scratch of kvq_decode_workspace_size() bytes, 256-byte
@@ -171,7 +172,7 @@ KVQ_API kvq_status kvq_decode_attention(const void* q, const kvq_cache* cache,
                                 int32_t partition_size, kvq_stream_t stream);
 
 /* Decode step with the newest token's K/V appended inside the same launch:
- * the result -- cache bytes, INT8 row scales and out -- is bit-identical to
+ * the result -- cache bytes, INT8 / INT4 scales and out -- is bit-identical to
  * kvq_append of k_new / v_new followed by kvq_decode_attention with the same
  * arguments.  It follows the same passages as those two calls; fusing them is
  * a scheduling choice (one launch instead of two) that no page prescribes.
@@ -180,7 +181,7 @@ KVQ_API kvq_status kvq_decode_attention(const void* q, const kvq_cache* cache,
  *     the cache slot block_tables[b][(ctx - 1) / block_size] * block_size +
  *     (ctx - 1) % block_size.  A sequence with context 0 appends nothing.
  *     The row is quantized exactly as kvq_append does (FP8 with `scale`, INT8
- *     with its own row scale).
+ *     and INT4 with the row's own scale, or its groups').
  *   Every other argument, the workspace and the errors are those of
  *   kvq_decode_attention; a block id outside the cache is recorded and its row
  *   is not written. */
