@@ -14,8 +14,13 @@
 // up once per device (cudaGetSymbolAddress, with that device current) by the
 // first call on the device.  All calls share it and it keeps what the last call
 // wrote; the decode kernels write every partial they later read, so nothing in
-// it needs to start at zero.  Two calls whose kernels overlap on the GPU (on
-// different streams, or from different host threads) race on the array.
+// it needs to start at zero.  (A call whose kernels record a device error -- a
+// context length or block id out of range, a bounded wait that ran out -- may
+// leave partials unwritten; its output is then undefined, as with a caller
+// workspace.)  Two calls whose kernels overlap on the GPU (on different
+// streams, or from different host threads) race on the array.  The arguments
+// are checked before the size limit, so a bad argument gets the status
+// kvq_decode_attention would give it.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -55,20 +60,26 @@ kvq_status kvq_decode_attention_static_scratch(const void* q, const kvq_cache* c
                                                int32_t max_context_len, const float* scale, int32_t fmt,
                                                float sm_scale, void* out, int32_t partition_size,
                                                kvq_stream_t stream) {
-    if (!cache) return KVQ_ERR_INVALID_ARG;
+    // The arguments are checked first, exactly as kvq_decode_attention checks
+    // them: called without a workspace it validates everything, launches
+    // nothing, and answers KVQ_ERR_WORKSPACE only when the arguments are good
+    // and a workspace is needed.  Any other answer (an argument error, or OK
+    // for an empty batch) is this call's answer too.
+    const kvq_status st = kvq_decode_attention(q, cache, block_tables, max_blocks_per_seq, context_lens, batch,
+                                               num_q_heads, max_context_len, scale, fmt, sm_scale, out, nullptr, 0,
+                                               partition_size, stream);
+    if (st != KVQ_ERR_WORKSPACE) return st;
     const size_t need = kvq_decode_workspace_size(batch, num_q_heads, cache->num_kv_heads, cache->head_dim,
                                                   max_context_len, partition_size);
+    if (need == 0) return KVQ_ERR_INVALID_ARG;
     if (need > kScratchBytes) return KVQ_ERR_SCRATCH_LIMIT;
-    void* ws = nullptr;
-    if (need > 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVQ_ERR_CUDA;
-        ws = scratch_ptr(dev);
-        if (!ws) return KVQ_ERR_CUDA;
-    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVQ_ERR_CUDA;
+    void* ws = scratch_ptr(dev);
+    if (!ws) return KVQ_ERR_CUDA;
     return kvq_decode_attention(q, cache, block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads,
-                                max_context_len, scale, fmt, sm_scale, out, ws, need > 0 ? kScratchBytes : 0,
-                                partition_size, stream);
+                                max_context_len, scale, fmt, sm_scale, out, ws, kScratchBytes, partition_size,
+                                stream);
 }
 
 }  // extern "C"

@@ -162,7 +162,12 @@ KVQ_API size_t kvq_decode_workspace_size(int32_t batch, int32_t num_q_heads, int
  *   partition_size: tokens per context chunk whose partial result is kept
  *     (a multiple of 64, at most 65536), or 0 to let the library choose from
  *     the sizes and the device's SM count.  Results agree across choices up to
- *     fp32 summation order. */
+ *     fp32 summation order.
+ *   When kvq_device_error_check reports an error recorded by this call (a
+ *   context length or block id out of range, or a bounded wait that ran out),
+ *   `out` is undefined for the whole call: a warp that stopped early may have
+ *   left partial results unwritten, and the merge then reads whatever the
+ *   workspace held. */
 KVQ_API kvq_status kvq_decode_attention(const void* q, const kvq_cache* cache,
                                 const int32_t* block_tables, int32_t max_blocks_per_seq,
                                 const int32_t* context_lens, int32_t batch,
@@ -200,9 +205,10 @@ KVQ_API kvq_status kvq_decode_attention_append(const void* q, const void* k_new,
  * no workspace to pass.  Same arguments and result as kvq_decode_attention
  * without workspace / workspace_bytes: the workspace is a fixed array of
  * kvq_static_scratch_bytes() (64 MiB) in the library's device memory, held by
- * every GPU that loads the library until the process exits.  Sizes whose
- * kvq_decode_workspace_size() exceeds it return KVQ_ERR_SCRATCH_LIMIT with
- * nothing launched.  The first call on a device looks up the array's device
+ * every GPU that loads the library until the process exits.  The arguments
+ * are checked first and give the statuses kvq_decode_attention gives; then
+ * sizes whose kvq_decode_workspace_size() exceeds the array return
+ * KVQ_ERR_SCRATCH_LIMIT with nothing launched.  The first call on a device looks up the array's device
  * address (cudaGetSymbolAddress); make that first call before any stream
  * capture.  Calls share the array and it keeps the last call's contents;
  * nothing in it needs to start at zero.  Calls whose kernels overlap on the GPU

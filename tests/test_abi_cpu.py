@@ -165,3 +165,25 @@ def test_prefill_append_dequant_checks_before_any_cuda_call(lib):
     # dequant: negative count, missing outputs
     assert lib.kvq_dequant(ctypes.byref(d), 16, -1, None, kvq.E4M3, 16, 16, None) == 1
     assert lib.kvq_dequant(ctypes.byref(d), 16, 0, None, kvq.E4M3, 16, 16, None) == 0
+
+
+def test_static_scratch_checks_arguments_before_its_size_limit(lib):
+    """The no-workspace decode gives the statuses kvq_decode_attention gives for
+    bad arguments (even where the sizes would also overflow its fixed array), and
+    KVQ_ERR_SCRATCH_LIMIT only for good arguments that need more than the array;
+    all of these before any CUDA call."""
+    import ctypes
+    d = kvq.KvqCacheDesc(16, 16, None, None, 1 << 16, 16, 4, 128, kvq.E4M3)
+    d256 = kvq.KvqCacheDesc(16, 16, None, None, 1 << 16, 16, 4, 256, kvq.E4M3)
+
+    def st(cache=d, batch=64, nq=32, ctx=8192, part=64, q=16):
+        return lib.kvq_decode_attention_static_scratch(q, ctypes.byref(cache), 16, 1 << 12, 16, batch, nq, ctx,
+                                                       None, kvq.E4M3, 0.0, 16, part, None)
+
+    assert lib.kvq_decode_workspace_size(64, 32, 4, 128, 8192, 64) > lib.kvq_static_scratch_bytes()
+    assert st() == 7                                       # good arguments, more than the array holds
+    assert st(part=32) == 1                                # partition not a multiple of 64
+    assert st(batch=5000) == 2                             # above the context-length scan's 4096
+    assert st(cache=d256) == 2                             # head_dim 256
+    assert st(q=8) == 1                                    # misaligned q
+    assert st(batch=0) == 0                                # nothing to do, nothing launched
