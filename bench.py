@@ -12,6 +12,14 @@ kvq_decode_attention.
   python bench.py --impl reference ...     # the CPU oracle, timed on host cores
   python bench.py --prefill [--workload llama3-70b] [--chunk N]   # chunked prefill
 
+The default workload is the Llama-3-70B decode batch (256 sequences of 32768
+tokens, 64/8 heads, E4M3, plus a 2048-token chunk appended per sequence), the
+largest single-GPU batch of the target list.  In the same run (N=1) the other
+target decode batches -- Llama-2-7B E4M3, Llama-3-8B E5M2 and Llama-2-13B
+INT8 -- are measured each in its own timed region and reported under
+``per_config`` (step and stream-kernel GB/s, roofline fractions, bulk append
+GB/s, tokens/s, clocks).
+
 Prints ONE JSON line (rank 0).  ``value`` is decode KV-read GB/s: the
 algorithmic bytes of the decode calls (every cached K/V byte of every context
 once, INT8 / INT4 scales, q, out, block tables) over the step time, summed over
@@ -38,12 +46,16 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "quantized-KV decode attention: KV-read GB/s and % of GB300 HBM peak; tokens/s"
-DEFAULT_WORKLOAD = "llama2-7b"
+# The largest single-GPU decode batch of the target list is the headline; the
+# other decode batches of that list are measured in the same run (per_config).
+DEFAULT_WORKLOAD = "llama3-70b"
+PER_CONFIG = ("llama2-7b", "llama3-8b", "llama2-13b-int8")
+PER_CONFIG_STEPS = {"llama2-7b": 3000, "llama3-8b": 3000, "llama2-13b-int8": 400}
 L2_BYTES = 129 * 1024 * 1024
 DEFAULT_STEPS = {"tiny": 2000, "llama2-7b": 10000, "llama3-8b": 10000, "llama2-13b-int8": 1000,
                  "llama2-13b-int4": 2000,
                  "llama2-13b-int4-g32": 2000,
-                 "llama3-70b": 300}
+                 "llama3-70b": 300, "llama3-70b-int8-g32": 200}
 
 
 def parse():
@@ -60,6 +72,8 @@ def parse():
     ap.add_argument("--unfused", action="store_true",
                     help="append one-token steps with a separate kvq_append launch")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the other target decode batches (measured after the headline at N=1)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU-baseline sample time")
     ap.add_argument("--prefill", action="store_true",
                     help="time a chunked-prefill step (append of the chunk + causal attention of its queries)")
@@ -325,10 +339,12 @@ class Setup:
 
 # ---------------------------------------------------------------- kvq arm --
 
-def cpu_baseline(wl, target_s: float):
+def cpu_baseline(wl, target_s: float, scale_value):
     """The oracle, as it stands, on a bounded sample of the same workload: the
     decode of a few whole sequences (all their q-heads, full context) plus the
-    append of their step tokens, on a cache the oracle itself filled."""
+    append of their step tokens, on a cache the oracle itself filled (untimed)
+    with the GPU arm's per-tensor scale.  The sample size is chosen so that the
+    untimed fill and the timed work together take about ``target_s``."""
     import numpy as np
     import torch
 
@@ -349,13 +365,14 @@ def cpu_baseline(wl, target_s: float):
             bt[i, :n] = np.arange(at, at + n)
             at += n
         cl = lay.context_lens[seqs].numpy().astype(np.int32)
+        t_fill = time.perf_counter()
         # fill (untimed): the oracle's own append of every position
         for i, b in enumerate(seqs):
             n = int(cl[i])
             k, v = W.kv_tokens(wl, 0, n, "cpu", seqs=[b])
             pos = np.arange(n)
             slots = (bt[i][pos // bs].astype(np.int64) * bs + pos % bs)
-            oracle.append(k.numpy(), v.numpy(), slots, cache, 1.0 if wl.fmt == "e4m3" else None)
+            oracle.append(k.numpy(), v.numpy(), slots, cache, scale_value)
         q = W.query(wl, "cpu")[seqs].numpy()
         step_tok = wl.append_chunk if wl.append_chunk else 1
         ks, vs, ss = [], [], []
@@ -368,20 +385,22 @@ def cpu_baseline(wl, target_s: float):
             vs.append(v.numpy())
             ss.append(bt[i][pos // bs].astype(np.int64) * bs + pos % bs)
         k, v, s = np.concatenate(ks), np.concatenate(vs), np.concatenate(ss)
+        t_fill = time.perf_counter() - t_fill
         t0 = time.perf_counter()
-        oracle.append(k, v, s, cache, 1.0 if wl.fmt == "e4m3" else None)
-        oracle.decode_attention(q, cache, bt, cl, 1.0 if wl.fmt == "e4m3" else None)
+        oracle.append(k, v, s, cache, scale_value)
+        oracle.decode_attention(q, cache, bt, cl, scale_value)
         dt = time.perf_counter() - t0
-        return dt, W.decode_bytes(wl, torch.from_numpy(cl))
+        return dt, t_fill, W.decode_bytes(wl, torch.from_numpy(cl))
 
-    dt, by = run(order[:1])
-    n = max(1, min(wl.batch, int(target_s / max(dt, 1e-3))))
+    dt, fill, by = run(order[:1])
+    n = max(1, min(wl.batch, int(target_s / max(dt + fill, 1e-3))))
     if n > 1:
-        dt, by = run(order[:n])
+        dt, fill, by = run(order[:n])
     return {"value": by["total"] / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{n} of {wl.batch} sequences (all {wl.num_q_heads} q-heads, full context, "
                       f"{by['tokens']} cached tokens) decoded plus their step tokens appended, "
-                      f"{dt:.2f} s"}
+                      f"{dt:.2f} s timed (cache filled by the oracle beforehand, {fill:.1f} s untimed), "
+                      f"per-tensor scale {scale_value if scale_value is not None else 'none (1.0 / row scales)'}"}
 
 
 def e2e_latency(S, K, flush):
@@ -502,6 +521,137 @@ def e2e_pipeline(S, K):
     return a.elapsed_time(b) / Ke, at, h_out[0].numel() * h_out[0].element_size(), Ke
 
 
+def time_steps(S, K, stream, flush, gpu_index):
+    """K decode steps of a resident workload.
+
+    The timed region is exactly K steps with events only at its two ends (or,
+    when the step's inputs fit in L2, each step timed alone after an L2 flush).
+    A second, instrumented pass over min(K, 2000) steps times each part of the
+    step: append start / decode start / decode end, and -- recorded by the
+    library on the same stream -- the decode stream kernel's own start and end.
+    Events between kernels serialise them, so that pass feeds only the
+    per-kernel figures and the roofline, never the step value."""
+    import torch
+
+    import fp8_int8_quantized_gb300 as kvq
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    steps_ev = ([(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+                if flush is not None else None)
+    torch.cuda.synchronize()
+    with ClockSampler(gpu_index) as clk:
+        if flush is None:
+            start.record(stream)
+            for _ in range(K):
+                S.step()
+            end.record(stream)
+        else:
+            for i, (a, b) in enumerate(steps_ev):
+                flush.fill_(i)
+                a.record(stream)
+                S.step()
+                b.record(stream)
+        torch.cuda.synchronize()
+    Ki = min(K, 2000)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(Ki)]
+    for e in ev:  # materialise the event handles
+        for x in e:
+            x.record(stream)
+    torch.cuda.synchronize()
+    for i in range(Ki):
+        e = ev[i]
+        if flush is not None:
+            flush.fill_(i)
+        e[0].record(stream)
+        if not S.fused:
+            S.append()
+        e[1].record(stream)
+        kvq.set_decode_timing_events(e[3], e[4])
+        S.decode_step()
+        e[2].record(stream)
+    torch.cuda.synchronize()
+    kvq.set_decode_timing_events()
+    total_ms = (start.elapsed_time(end) if flush is None else sum(a.elapsed_time(b) for a, b in steps_ev))
+    return {"ms_step": total_ms / K, "instrumented": Ki,
+            "app_ms": sum(e[0].elapsed_time(e[1]) for e in ev) / Ki,
+            "dec_ms": sum(e[1].elapsed_time(e[2]) for e in ev) / Ki,
+            "kern_ms": sum(e[3].elapsed_time(e[4]) for e in ev) / Ki,
+            "clocks": clk.summary()}
+
+
+def bulk_append_gbs(S, stream, reps=5):
+    """Quantize-on-write throughput of the workload's format on a bulk append:
+    kvq_append of the rows of the first fill window again (the same values
+    into the same slots, so the cache is unchanged), CUDA events around each of
+    ``reps`` calls.  Returns (GB/s, rows per call, ms per call)."""
+    import torch
+
+    import fp8_int8_quantized_gb300 as kvq
+    from fp8_int8_quantized_gb300 import workloads as W
+    wl = S.wl
+    p0, p1 = W.chunk_positions(wl, 1 << 19)[0]
+    k, v = W.kv_tokens(wl, p0, p1, S.device)
+    slots = S.lay.slots(p0, p1).to(S.device)
+    cl = S.lay.context_lens.to(S.device)
+    step_tok = wl.append_chunk if wl.append_chunk else 1
+    pos = torch.arange(p0, p1, device=S.device).repeat(wl.batch)
+    keep = pos < (cl.repeat_interleave(p1 - p0) - step_tok)  # the rows the fill wrote
+    k, v, slots = k[keep].contiguous(), v[keep].contiguous(), slots[keep].contiguous()
+    kvq.append(k, v, S.cache, slots, S.scale)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in ev:
+        a.record(stream)
+        kvq.append(k, v, S.cache, slots, S.scale)
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / reps
+    return W.append_bytes(wl, slots.numel()) / (ms * 1e-3) / 1e9, slots.numel(), ms
+
+
+def per_config_entry(name, dev, args, local, peak):
+    """One target decode batch measured in the headline's run: step GB/s, the
+    decode stream kernel's GB/s and roofline fractions, the bulk append rate,
+    tokens/s and the clocks seen during its timed region."""
+    import torch
+
+    import fp8_int8_quantized_gb300 as kvq
+    from fp8_int8_quantized_gb300 import workloads as W
+    wl = W.WORKLOADS[name]
+    S = Setup(wl, dev, 0, args.unfused)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, args.warmup)):
+        S.step()
+    torch.cuda.synchronize()
+    st, detail = kvq.device_error_check()
+    if st != 0:
+        raise RuntimeError(f"{name}: device error {st} ({detail})")
+    K = PER_CONFIG_STEPS.get(name, 200)
+    flush = (torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+             if S.dec_bytes["total"] <= L2_BYTES else None)
+    r = time_steps(S, K, stream, flush, local)
+    kern_bytes = S.dec_bytes["total"] + (S.app_bytes if S.fused else 0)
+    achieved = kern_bytes / (r["kern_ms"] * 1e-3) / 1e9
+    app_gbs, app_rows, app_ms = bulk_append_gbs(S, stream)
+    out = {"workload": name, "description": wl.description, "steps": K, "warmup": max(3, args.warmup),
+           "decode_bytes": S.dec_bytes["total"],
+           "ms_per_step": round(r["ms_step"], 5),
+           "value": round(S.dec_bytes["total"] / (r["ms_step"] * 1e-3) / 1e9, 2), "unit": "GB/s",
+           "tokens_per_s": round(wl.batch / (r["ms_step"] * 1e-3), 1),
+           "step": f"append {S.slots_step.numel()} tokens + decode {wl.batch} sequences"
+                   + (" (the append fused into the decode launch)" if S.fused else ""),
+           "decode_kernel_ms": round(r["kern_ms"], 5),
+           "decode_kernel_gbs": round(achieved, 1),
+           "frac": round(achieved / peak, 4), "frac_of_nominal_8TBps": round(achieved / 8000.0, 4),
+           "traffic": recorded_traffic(name),
+           "append_gbs": round(app_gbs, 2),
+           "append": f"kvq_append of {app_rows} (token, all kv-heads) rows of the workload's first fill "
+                     f"window, {app_ms:.4f} ms per call",
+           "clocks": r["clocks"]}
+    del S
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_kvq(args):
     import torch
 
@@ -538,57 +688,13 @@ def run_kvq(args):
     flush = None
     if S.dec_bytes["total"] <= L2_BYTES:
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    steps_ev = ([(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-                if flush is not None else None)
     if world > 1:
         torch.distributed.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        if flush is None:
-            # the timed region: exactly K steps, events only at its two ends
-            start.record(stream)
-            for _ in range(K):
-                S.step()
-            end.record(stream)
-        else:
-            for i, (a, b) in enumerate(steps_ev):
-                flush.fill_(i)
-                a.record(stream)
-                S.step()
-                b.record(stream)
-        torch.cuda.synchronize()
+    r = time_steps(S, K, stream, flush, local)
     if world > 1:
         torch.distributed.barrier()
-    # A second, instrumented pass over min(K, 2000) steps times each part of
-    # the step: append start / decode start / decode end, and (recorded by the
-    # library on the same stream) the decode stream kernel's own start and
-    # end.  Events between kernels serialise them, so this pass is only used
-    # for the per-kernel figures and the roofline, never for value.
-    Ki = min(K, 2000)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(Ki)]
-    for e in ev:  # materialise the event handles
-        for x in e:
-            x.record(stream)
-    torch.cuda.synchronize()
-    for i in range(Ki):
-        e = ev[i]
-        if flush is not None:
-            flush.fill_(i)
-        e[0].record(stream)
-        if not S.fused:
-            S.append()
-        e[1].record(stream)
-        kvq.set_decode_timing_events(e[3], e[4])
-        S.decode_step()
-        e[2].record(stream)
-    torch.cuda.synchronize()
-    kvq.set_decode_timing_events()
-    total_ms = (start.elapsed_time(end) if flush is None else sum(a.elapsed_time(b) for a, b in steps_ev))
-    app_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / Ki
-    dec_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / Ki
-    kern_ms = sum(e[3].elapsed_time(e[4]) for e in ev) / Ki
-    ms_step = total_ms / K
+    Ki, app_ms, dec_ms, kern_ms = r["instrumented"], r["app_ms"], r["dec_ms"], r["kern_ms"]
+    ms_step = r["ms_step"]
     max_ms, units = aggregate(ms_step, float(S.dec_bytes["total"]), world)
     _, seqs = aggregate(ms_step, float(wl.batch), world)
     value = units / (max_ms * 1e-3) / 1e9
@@ -617,10 +723,23 @@ def run_kvq(args):
     achieved = kern_bytes / (kern_ms * 1e-3) / 1e9
     # the recorded figures are for the workload's own batch
     traffic = recorded_traffic(wl.name) if wl.batch == W.WORKLOADS[wl.name].batch else None
+    scale_value = S.scale_value
+    step_desc = (f"append {S.slots_step.numel()} tokens + decode {wl.batch} sequences"
+                 + (" (the append fused into the decode launch)" if S.fused else ""))
+    in_l2 = flush is not None
+    # the step's own append (the 70B workload's 2048-token chunks), when it is
+    # a separate kvq_append launch
+    append_gbs = round(S.app_bytes / (app_ms * 1e-3) / 1e9, 2) if app_ms > 0 and not S.fused else None
+    del S
+    torch.cuda.empty_cache()
+    # the other target decode batches, each in its own timed region (N=1 only)
+    per_config = None
+    if (world == 1 and not args.no_per_config and args.workload == DEFAULT_WORKLOAD and not args.batch
+            and not args.partition):
+        per_config = {n: per_config_entry(n, dev, args, local, peak) for n in PER_CONFIG}
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        cpu = cpu_baseline(wl, args.cpu_seconds)
-    clocks = clk.summary()
+        cpu = cpu_baseline(wl, args.cpu_seconds, scale_value)
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -641,30 +760,29 @@ def run_kvq(args):
                    "num_q_heads": wl.num_q_heads, "num_kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
                    "block_size": wl.block_size, "format": wl.fmt,
                    "context": wl.ctx if isinstance(wl.ctx, int) else list(wl.ctx),
-                   "step": f"append {S.slots_step.numel()} tokens + decode {wl.batch} sequences"
-                           + (" (the append fused into the decode launch)" if S.fused else ""),
-                   "l2": f"inputs larger than L2 ({S.dec_bytes['total'] / 1e6:.0f} MB read per decode > 129 MB)"
-                   if flush is None else
-                   f"inputs smaller than L2: a {2 * L2_BYTES / 1e6:.0f} MB buffer written before every step, "
-                   "each step timed alone between two events",
+                   "step": step_desc,
+                   "l2": (f"inputs larger than L2 ({units / world / 1e6:.0f} MB read per decode > 129 MB)"
+                          if not in_l2 else
+                          f"inputs smaller than L2: a {2 * L2_BYTES / 1e6:.0f} MB buffer written before every "
+                          "step, each step timed alone between two events"),
                    "kernel": args.kernel, "partition": args.partition or "auto",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "tokens_per_s": round(seqs / (max_ms * 1e-3), 1),
         "instrumented_steps": Ki,
         "decode_ms": round(dec_ms, 5),
         "append_ms": round(app_ms, 5),
-        "append_gbs": (round(S.app_bytes / (app_ms * 1e-3) / 1e9, 2) if app_ms > 0 and not S.fused
-                       else None),
-        "decode_bytes": S.dec_bytes["total"],
+        "append_gbs": append_gbs,
+        "decode_bytes": int(units / world),
         "decode_kernel_ms": round(kern_ms, 5),
         "roofline": {"bound": "hbm", "kernel": "decode_stream_kernel",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "frac_of_nominal_8TBps": round(achieved / 8000.0, 4), "traffic": traffic},
+        "per_config": per_config,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,
-        "clocks": clocks,
+        "clocks": r["clocks"],
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -794,8 +912,7 @@ def run_prefill_bench(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     kvq.lib()
-    name = args.workload if args.workload != DEFAULT_WORKLOAD else "llama3-70b"
-    wl = W.WORKLOADS[name]
+    wl = W.WORKLOADS[args.workload]
     if args.batch:
         import dataclasses
         wl = dataclasses.replace(wl, batch=args.batch)
@@ -948,24 +1065,31 @@ def run_reference(args):
     K = args.steps or 5
     Wm = max(3, args.warmup)
     nseq = min(wl.batch, 4)
+    kv = [W.kv_tokens(wl, 0, int(lay.context_lens[b]), "cpu", seqs=[b]) for b in range(nseq)]
+    # the per-tensor scale by the workloads' calibration rule (amax / format
+    # max), taken over the sampled sequences' K and V
+    scale = None
+    if wl.scale_rule == "amax":
+        scale = W.calibration_scale(wl, torch.cat([k for k, _ in kv]), torch.cat([v for _, v in kv]))
     caches = []
     for b in range(nseq):
         n = int(lay.context_lens[b])
         nb = (n + bs - 1) // bs
         cache = oracle.Cache(nb, wl.num_kv_heads, bs, wl.head_dim, fmt, group=wl.quant_group)
         bt = np.arange(nb, dtype=np.int32)[None]
-        k, v = W.kv_tokens(wl, 0, n, "cpu", seqs=[b])
+        k, v = kv[b]
         pos = np.arange(n)
-        oracle.append(k.numpy(), v.numpy(), (pos // bs) * bs + pos % bs, cache, None)
+        oracle.append(k.numpy(), v.numpy(), (pos // bs) * bs + pos % bs, cache, scale)
         q = W.query(wl, "cpu")[b:b + 1].numpy()
         p0 = max(0, n - step_tok)
         sk, sv = k[p0:].numpy(), v[p0:].numpy()
         caches.append((cache, bt, np.array([n], np.int32), q, sk, sv, np.arange(p0, n, dtype=np.int64)))
+    del kv
 
     def step(i):
         cache, bt, cl, q, sk, sv, slots = caches[i % nseq]
-        oracle.append(sk, sv, slots, cache, None)
-        oracle.decode_attention(q, cache, bt, cl, None)
+        oracle.append(sk, sv, slots, cache, scale)
+        oracle.decode_attention(q, cache, bt, cl, scale)
 
     for i in range(Wm):
         step(i)
