@@ -346,7 +346,7 @@ struct SimtConsumer {
 
 // ----------------------------------------------------------------- MMA --
 
-template <int FMT, int D>
+template <int FMT, int D, bool R16 = false>
 struct MmaConsumer {
     static constexpr bool I4 = FMT == INT4;
     static constexpr bool kRowScaled = FMT == INT8 || FMT == INT4;
@@ -357,38 +357,65 @@ struct MmaConsumer {
     static constexpr int DV = D / 8;    // V codes per thread per token row
     static constexpr int VW = I4 ? DV / 8 : DV / 4;
     static constexpr int MT = D / 16;   // m-tiles of PV (head_dim / 16)
+    // Operand rows (q-head, scale group pairs) per pass: 8, or 16 with R16.
+    // QK^T's m16 tile has 16 rows; the 8-row consumer fills rows 0-7 (this
+    // thread's row g) and leaves rows 8-15 zero, the 16-row one also fills
+    // rows 8-15 (row g + 8) and takes a second n8 tile of PV columns.  The
+    // 16-row consumer serves group-quantized caches whose q-heads x groups per
+    // kv-head exceed 8, so that one pass over the cache serves twice the
+    // pairs; it holds twice the accumulators, so it runs 4 warps per CTA with
+    // up to 255 registers.
+    static constexpr int NR = R16 ? 2 : 1;
+    static constexpr int kRows = 8 * NR;
     static constexpr int kMinCtas = kMinBlocks;
     // Warps per CTA, each streaming its own range.  INT4 tiles are half the
     // bytes of the others, and the kernel is bound by the latency of the
     // per-warp register work rather than by HBM: 8 warps (registers capped at
     // 128, two CTAs per SM) are 11% faster than 6.  The 8-bit formats stay at
     // 6: at 8 their stages no longer fit two CTAs into shared memory.
-    static constexpr int kWarps = I4 ? 8 : 6;
-    // INT8 codes enter the tensor cores as fp16 1152 + code (exact); INT4 codes
-    // as the fp16 subnormal (code + 8) * 2^-24 (exact: the offset nibble is the
-    // mantissa), or 16x that where the nibble is left in mantissa bits 4..7 --
-    // the high nibble of a byte is masked in place, which saves the shifts and
-    // byte moves of a full expansion.  The matching query values are fed
-    // divided by 16 (QK), and the output rows of such head dims are divided by
-    // 16 at the flush (PV).  The constant is taken out again: bias * sum(q)
-    // from each logit, bias * sum(P') from each output, and INT4 results are
-    // multiplied back by 2^24.  The INT4 bias is small (8 against codes up to
-    // 7): INT4 row scales are 18x INT8's, and a bias of 1032 left accumulation
-    // errors near the tolerance.
+    static constexpr int kWarps = R16 ? 4 : (I4 ? 8 : 6);
+    // INT8 codes enter the tensor cores as fp16 subnormals, code * 2^-24, and
+    // INT4 codes the same, or 16x that where the nibble is left in mantissa
+    // bits 4..7 -- the high nibble of a byte is masked in place, which saves
+    // the shifts and byte moves of a full expansion.  The matching query
+    // values are fed divided by 16 (QK), and the output rows of such head dims
+    // are divided by 16 at the flush (PV); results are multiplied back by 2^24.
+    //   K (QK): the offset code + 128 (INT8) or code + 8 (INT4) is the
+    //   mantissa as loaded, and bias * sum(q) is taken out of each logit.  A
+    //   logit depends only on its own token, so this rounding does not depend
+    //   on how a context is split.
+    //   V (PV): one exact fp16 subtraction per operand register removes the
+    //   offset before the product, so the accumulators hold unbiased sums.  An
+    //   offset left in them, drained by bias * sum(P') later, made their fp32
+    //   rounding relative to the biased sums: INT8 rows holding a x20 outlier
+    //   channel (row scales ~19x the Gaussian rows') reached 6.6e-3 relative
+    //   error over 4096-token chunks with 1152 + code operands, and even with
+    //   a small offset drained every four tiles the result still moved by 4e-5
+    //   with the context split (INT4 outlier rows: scales ~8.6).
     static constexpr bool kBiased = kRowScaled;
-    static constexpr float kUnit = I4 ? 5.9604644775390625e-08f : 1.f;   // operand value of one code step
-    static constexpr float kBias = I4 ? 8.f * kUnit : 1152.f;            // operand - code * kUnit
-    // Operand row / column g (QK rows, PV columns) is (q-head g / ng, scale
-    // group g % ng): with ng groups per row, a row of QK sees only its group's
+    static constexpr float kUnit = 5.9604644775390625e-08f;           // operand value of one code step (2^-24)
+    static constexpr float kBias = (I4 ? 8.f : 128.f) * kUnit;        // K operand - code * kUnit
+    // INT8 / INT4 weights enter PV as P' times the token's V scale, in fp16
+    // (hi + residual).  INT8 row scales of Gaussian rows are ~0.025, which
+    // would put most weights below fp16's normal range (6.1e-5), where hi and
+    // residual keep only an absolute 2^-25: 2e-5 relative error over 4096
+    // tokens.  The weights are therefore computed as 2^kLogF * 2^(z - m): the
+    // running sum l and the accumulators carry the same factor, which cancels
+    // when the partials are merged (out = acc / l).
+    // 2^6 (INT8) and 2^2 (INT4) keep every weight of any fp16 row (scale at most
+    // 65504 / 127, or / 7) below fp16's largest value.
+    static constexpr float kLogF = FMT == INT8 ? 6.f : (I4 ? 2.f : 0.f);
+    // Operand row / column r (QK rows, PV columns) is (q-head r / ng, scale
+    // group r % ng): with ng groups per row, a row of QK sees only its group's
     // head dims, its partial logits are scaled by that group's K scales and
     // summed over the ng rows of the head, and the PV column carries P times
     // the group's V scales; output dims are taken from the column of their own
-    // group.  ng = 1 is the per-row (or per-tensor) format.
-    uint32_t qa[2 * KS];
-    float acc[MT][4];
-    float m, l;
-    float qsum;  // INT8 / INT4: sum of this operand row's query values (row g)
-    float psum;  // INT8 / INT4: running sum of the P' weights fed to PV (column g, this thread's tokens)
+    // group.  ng = 1 is the per-row (or per-tensor) format.  A thread holds
+    // rows g and (R16) g + 8, which share their scale group (ng divides 8).
+    uint32_t qa[NR][2 * KS];
+    float acc[NR][MT][4];
+    float m[NR], l[NR];
+    float qsum[NR];  // INT8 / INT4: sum of this operand row's query values (rows g, g + 8)
     int lane, g, c, G, ng, kg;  // kg = g % ng: this lane's scale group
     // INT8 / INT4 with at most 4 operand rows (q-head, group pairs): PV
     // columns 0-3 carry the weights' fp16 high parts and columns 4-7 their
@@ -411,7 +438,7 @@ struct MmaConsumer {
         G = G_;
         ng = ng_;
         kg = g % ng_;
-        lo_cols = kRowScaled && G_ * ng_ <= 4;
+        lo_cols = !R16 && kRowScaled && G_ * ng_ <= 4;
         qk_scale = qks;
         if (I4) {
             k_off0 = g * RB + c * (DC / 2);
@@ -430,58 +457,65 @@ struct MmaConsumer {
             v_off1 = (2 * c + 1) * D + DV * g;
         }
     }
-    // qa[2j] = Q[h][DC*c + 4j + {0,1}], qa[2j+1] = Q[h][DC*c + 4j + {2,3}]: the
-    // DC halves Q[h][DC*c ...] in order, h = g / ng, where this thread's DC dims
-    // lie in row g's scale group (the DC dims of a thread are within one group:
-    // groups are D / ng >= DC wide); else zero.  q: the kv-head's G query rows
+    // qa[r][2j] = Q[h][DC*c + 4j + {0,1}], qa[r][2j+1] = Q[h][DC*c + 4j + {2,3}]:
+    // the DC halves Q[h][DC*c ...] in order, for operand row g (r = 0) or g + 8
+    // (r = 1) with h = row / ng, where this thread's DC dims lie in the row's
+    // scale group (the DC dims of a thread are within one group: groups are
+    // D / ng >= DC wide); else zero.  q: the kv-head's G query rows
     // (shared-memory copy).
     __device__ void set_q(const uint16_t* q) {
-        if (g < G * ng && ((c * ng) >> 2) == kg) {
-            const uint4* src = reinterpret_cast<const uint4*>(q + (g / ng) * D + DC * c);
 #pragma unroll
-            for (int i = 0; i < (2 * KS) / 4; ++i) {
-                const uint4 x = src[i];
-                qa[4 * i] = x.x; qa[4 * i + 1] = x.y; qa[4 * i + 2] = x.z; qa[4 * i + 3] = x.w;
+        for (int r = 0; r < NR; ++r) {
+            const int row = g + 8 * r;
+            if (row < G * ng && ((c * ng) >> 2) == kg) {
+                const uint4* src = reinterpret_cast<const uint4*>(q + (row / ng) * D + DC * c);
+#pragma unroll
+                for (int i = 0; i < (2 * KS) / 4; ++i) {
+                    const uint4 x = src[i];
+                    qa[r][4 * i] = x.x; qa[r][4 * i + 1] = x.y; qa[r][4 * i + 2] = x.z; qa[r][4 * i + 3] = x.w;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 2 * KS; ++i) qa[r][i] = 0u;
             }
-        } else {
+            if (I4) {  // per 8 dims: [q0, q5/16] [q1/16, q4] [q2, q7/16] [q3/16, q6], the K operand order
 #pragma unroll
-            for (int i = 0; i < 2 * KS; ++i) qa[i] = 0u;
-        }
-        if (I4) {  // per 8 dims: [q0, q5/16] [q1/16, q4] [q2, q7/16] [q3/16, q6], the K operand order
-#pragma unroll
-            for (int w = 0; w < KW; ++w) {
-                const float2 q01 = f16x2_to_f32x2(qa[4 * w]), q23 = f16x2_to_f32x2(qa[4 * w + 1]);
-                const float2 q45 = f16x2_to_f32x2(qa[4 * w + 2]), q67 = f16x2_to_f32x2(qa[4 * w + 3]);
-                qa[4 * w] = pack_f16x2(q01.x, q45.y * 0.0625f);
-                qa[4 * w + 1] = pack_f16x2(q01.y * 0.0625f, q45.x);
-                qa[4 * w + 2] = pack_f16x2(q23.x, q67.y * 0.0625f);
-                qa[4 * w + 3] = pack_f16x2(q23.y * 0.0625f, q67.x);
+                for (int w = 0; w < KW; ++w) {
+                    const float2 q01 = f16x2_to_f32x2(qa[r][4 * w]), q23 = f16x2_to_f32x2(qa[r][4 * w + 1]);
+                    const float2 q45 = f16x2_to_f32x2(qa[r][4 * w + 2]), q67 = f16x2_to_f32x2(qa[r][4 * w + 3]);
+                    qa[r][4 * w] = pack_f16x2(q01.x, q45.y * 0.0625f);
+                    qa[r][4 * w + 1] = pack_f16x2(q01.y * 0.0625f, q45.x);
+                    qa[r][4 * w + 2] = pack_f16x2(q23.x, q67.y * 0.0625f);
+                    qa[r][4 * w + 3] = pack_f16x2(q23.y * 0.0625f, q67.x);
+                }
             }
-        }
-        if (kBiased) {  // sum of q as fed times each operand's step (16 for the divided values)
-            float sq = 0.f;
+            if (kBiased) {  // sum of q as fed times each operand's step (16 for the divided values)
+                float sq = 0.f;
 #pragma unroll
-            for (int i = 0; i < 2 * KS; ++i) {
-                const float2 v = f16x2_to_f32x2(qa[i]);
-                sq += I4 ? ((i & 1) ? 16.f * v.x + v.y : v.x + 16.f * v.y) : v.x + v.y;
+                for (int i = 0; i < 2 * KS; ++i) {
+                    const float2 v = f16x2_to_f32x2(qa[r][i]);
+                    sq += I4 ? ((i & 1) ? 16.f * v.x + v.y : v.x + 16.f * v.y) : v.x + v.y;
+                }
+                sq += __shfl_xor_sync(0xFFFFFFFFu, sq, 1);
+                sq += __shfl_xor_sync(0xFFFFFFFFu, sq, 2);
+                qsum[r] = sq;
             }
-            sq += __shfl_xor_sync(0xFFFFFFFFu, sq, 1);
-            sq += __shfl_xor_sync(0xFFFFFFFFu, sq, 2);
-            qsum = sq;
         }
     }
-    // INT8 word (4 codes) -> the two f16x2 operands 1152 + code of bytes (0,1) and (2,3)
+    // INT8 word (4 codes) -> the two f16x2 operands (code + 128) * 2^-24 of bytes (0,1) and (2,3)
     __device__ __forceinline__ static void int8_biased(uint32_t w, uint32_t& lo, uint32_t& hi) {
         const uint32_t x = w ^ 0x80808080u;  // code + 128 as an unsigned byte
-        lo = prmt(x, 0x64646464u, 0x4140u);
-        hi = prmt(x, 0x64646464u, 0x4342u);
+        lo = prmt(x, 0u, 0x4140u);
+        hi = prmt(x, 0u, 0x4342u);
     }
     __device__ void reset() {
-        m = -INFINITY;
-        l = 0.f;
-        psum = 0.f;
 #pragma unroll
-        for (int i = 0; i < MT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+        for (int r = 0; r < NR; ++r) {
+            m[r] = -INFINITY;
+            l[r] = 0.f;
+#pragma unroll
+            for (int i = 0; i < MT; ++i) acc[r][i][0] = acc[r][i][1] = acc[r][i][2] = acc[r][i][3] = 0.f;
+        }
     }
 
     // K words of rows g (half 0) or 8 + g (half 1): the DC contiguous codes at DC*c.
@@ -523,11 +557,18 @@ struct MmaConsumer {
         }
     }
 
-    // QK^T of one 16-row box: this thread's logits, head g, box tokens
-    // 2c, 2c+1, 8+2c, 9+2c (already scaled, masked past `valid`).
-    __device__ __forceinline__ void qk_box(uint32_t kt, uint32_t sk, int valid, float (&z)[4]) {
-        // S^T: rows = q-heads (g), columns = tokens; half A = box tokens 0..7
-        // (this thread's B operand row is token g), half B = tokens 8..15.
+    // One QK^T product of the 16-row operand: rows g (and g + 8 with R16).
+    __device__ __forceinline__ void qk_mma(float (&s)[4], int i0, int i1, uint32_t b0, uint32_t b1) {
+        if (R16) mma_16816(s, qa[0][i0], qa[NR - 1][i0], qa[0][i1], qa[NR - 1][i1], b0, b1);
+        else mma_16816(s, qa[0][i0], 0u, qa[0][i1], 0u, b0, b1);
+    }
+
+    // QK^T of one 16-row box: this thread's logits of operand rows g (z[0]) and
+    // g + 8 (z[1], R16), box tokens 2c, 2c+1, 8+2c, 9+2c (already scaled,
+    // masked past `valid`).
+    __device__ __forceinline__ void qk_box(uint32_t kt, uint32_t sk, int valid, float (&z)[NR][4]) {
+        // S^T: rows = operand rows (g, g + 8), columns = tokens; half A = box
+        // tokens 0..7 (this thread's B operand row is token g), half B = tokens 8..15.
         float sA[4] = {0.f, 0.f, 0.f, 0.f}, sB[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t kw[KW];
 #pragma unroll
@@ -542,11 +583,11 @@ struct MmaConsumer {
                     const uint32_t h0 = (x & 0x00F0000Fu) ^ 0x00800008u, h1 = (x & 0x000F00F0u) ^ 0x00080080u;
                     const uint32_t h2 = (y & 0x00F0000Fu) ^ 0x00800008u, h3 = (y & 0x000F00F0u) ^ 0x00080080u;
                     if (hb == 0) {
-                        mma_16816(sA, qa[4 * w], 0u, qa[4 * w + 1], 0u, h0, h1);
-                        mma_16816(sA, qa[4 * w + 2], 0u, qa[4 * w + 3], 0u, h2, h3);
+                        qk_mma(sA, 4 * w, 4 * w + 1, h0, h1);
+                        qk_mma(sA, 4 * w + 2, 4 * w + 3, h2, h3);
                     } else {
-                        mma_16816(sB, qa[4 * w], 0u, qa[4 * w + 1], 0u, h0, h1);
-                        mma_16816(sB, qa[4 * w + 2], 0u, qa[4 * w + 3], 0u, h2, h3);
+                        qk_mma(sB, 4 * w, 4 * w + 1, h0, h1);
+                        qk_mma(sB, 4 * w + 2, 4 * w + 3, h2, h3);
                     }
                 }
             } else {
@@ -555,13 +596,12 @@ struct MmaConsumer {
                     uint32_t b0, b1;
                     if (FMT == INT8) int8_biased(kw[j < KW ? j : 0], b0, b1);
                     else dec_fp8x4<FMT>(kw[j < KW ? j : 0], b0, b1);
-                    if (hb == 0) mma_16816(sA, qa[2 * j], 0u, qa[2 * j + 1], 0u, b0, b1);
-                    else mma_16816(sB, qa[2 * j], 0u, qa[2 * j + 1], 0u, b0, b1);
+                    if (hb == 0) qk_mma(sA, 2 * j, 2 * j + 1, b0, b1);
+                    else qk_mma(sB, 2 * j, 2 * j + 1, b0, b1);
                 }
             }
         }
         if (kRowScaled) {  // remove the operand bias, then apply the K row (group) scales
-            const float corr = kBias * qsum;
             const float ks = qk_scale / kUnit;
             float2 k01, k23;
             if (ng == 1) {
@@ -572,33 +612,45 @@ struct MmaConsumer {
                 k01 = make_float2(ldsf(a0), ldsf(a0 + 4 * ng));
                 k23 = make_float2(ldsf(a0 + 32 * ng), ldsf(a0 + 36 * ng));
             }
-            z[0] = (sA[0] - corr) * (ks * k01.x);
-            z[1] = (sA[1] - corr) * (ks * k01.y);
-            z[2] = (sB[0] - corr) * (ks * k23.x);
-            z[3] = (sB[1] - corr) * (ks * k23.y);
-            // the head's logits: sum of its ng group rows (lanes 4 apart per row)
-            for (int off = 1; off < ng; off <<= 1) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) z[e] += __shfl_xor_sync(0xFFFFFFFFu, z[e], 4 * off);
+            for (int r = 0; r < NR; ++r) {
+                const float corr = kBias * qsum[r];
+                z[r][0] = (sA[2 * r] - corr) * (ks * k01.x);
+                z[r][1] = (sA[2 * r + 1] - corr) * (ks * k01.y);
+                z[r][2] = (sB[2 * r] - corr) * (ks * k23.x);
+                z[r][3] = (sB[2 * r + 1] - corr) * (ks * k23.y);
+                // the head's logits: sum of its ng group rows (lanes 4 apart per row)
+                for (int off = 1; off < ng; off <<= 1) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) z[r][e] += __shfl_xor_sync(0xFFFFFFFFu, z[r][e], 4 * off);
+                }
             }
         } else {
-            z[0] = sA[0] * qk_scale; z[1] = sA[1] * qk_scale; z[2] = sB[0] * qk_scale; z[3] = sB[1] * qk_scale;
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                z[r][0] = sA[2 * r] * qk_scale; z[r][1] = sA[2 * r + 1] * qk_scale;
+                z[r][2] = sB[2 * r] * qk_scale; z[r][3] = sB[2 * r + 1] * qk_scale;
+            }
         }
         if (valid < kBox) {
-            if (2 * c >= valid) z[0] = -INFINITY;
-            if (2 * c + 1 >= valid) z[1] = -INFINITY;
-            if (8 + 2 * c >= valid) z[2] = -INFINITY;
-            if (9 + 2 * c >= valid) z[3] = -INFINITY;
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                if (2 * c >= valid) z[r][0] = -INFINITY;
+                if (2 * c + 1 >= valid) z[r][1] = -INFINITY;
+                if (8 + 2 * c >= valid) z[r][2] = -INFINITY;
+                if (9 + 2 * c >= valid) z[r][3] = -INFINITY;
+            }
         }
     }
 
     // out^T += V^T P^T for one box.  A operand rows = head_dim DV*g + 2i (+1
     // for rows g+8), columns = box tokens 2c, 2c+1 | 8+2c, 9+2c.
-    // LO: the residual weights ride in columns 4-7 of (pb0, pb1); else they
-    // are (pl0, pl1), a second MMA per m-tile.
+    // LO: the residual weights ride in columns 4-7 of pb[0]; else they are
+    // pl[0], a second MMA per m-tile.  R16: pb[1] / pl[1] are the weights of
+    // operand columns 8-15 (the second accumulator).
     template <bool LO>
-    __device__ __forceinline__ void pv_box(uint32_t vt, int valid, uint32_t pb0, uint32_t pb1, uint32_t pl0,
-                                           uint32_t pl1) {
+    __device__ __forceinline__ void pv_box(uint32_t vt, int valid, const uint32_t (&pb)[NR][2],
+                                           const uint32_t (&pl)[NR][2]) {
         uint32_t v0[VW], v1[VW], v2[VW], v3[VW];
         load_v(vt + v_off0, v0);
         load_v(vt + v_off1, v1);
@@ -623,11 +675,17 @@ struct MmaConsumer {
                     // dim 2i+1 as 16x that (rows g+8 of the m-tile, divided out at the flush)
                     const uint32_t sel = 0x4400u + 0x1111u * bb;  // bytes [r.bb, r.bb, r'.bb, r'.bb]
                     const uint32_t u01 = prmt(v0[w], v1[w], sel), u23 = prmt(v2[w], v3[w], sel);
-                    const uint32_t a0 = (u01 & 0x000F000Fu) ^ 0x00080008u, a1 = (u01 & 0x00F000F0u) ^ 0x00800080u;
-                    const uint32_t a2 = (u23 & 0x000F000Fu) ^ 0x00080008u, a3 = (u23 & 0x00F000F0u) ^ 0x00800080u;
+                    // then the offsets (8 and 16 * 8 steps) subtracted exactly
+                    const uint32_t a0 = hsub2_exact((u01 & 0x000F000Fu) ^ 0x00080008u, 0x00080008u);
+                    const uint32_t a1 = hsub2_exact((u01 & 0x00F000F0u) ^ 0x00800080u, 0x00800080u);
+                    const uint32_t a2 = hsub2_exact((u23 & 0x000F000Fu) ^ 0x00080008u, 0x00080008u);
+                    const uint32_t a3 = hsub2_exact((u23 & 0x00F000F0u) ^ 0x00800080u, 0x00800080u);
                     const int i = 4 * w + bb;
-                    mma_16816(acc[i], a0, a1, a2, a3, pb0, pb1);
-                    if (!LO) mma_16816(acc[i], a0, a1, a2, a3, pl0, pl1);
+#pragma unroll
+                    for (int r = 0; r < NR; ++r) {
+                        mma_16816(acc[r][i], a0, a1, a2, a3, pb[r][0], pb[r][1]);
+                        if (!LO) mma_16816(acc[r][i], a0, a1, a2, a3, pl[r][0], pl[r][1]);
+                    }
                 }
             }
             return;
@@ -644,17 +702,20 @@ struct MmaConsumer {
             const uint32_t x01 = prmt(v0[i >> 1], v1[i >> 1], sel);
             const uint32_t x23 = prmt(v2[i >> 1], v3[i >> 1], sel);
             uint32_t a0, a1, a2, a3;
-            if (FMT == INT8) {  // fp16 1152 + code; the bias leaves with psum at the flush
-                a0 = prmt(x01, 0x64646464u, 0x4140u);
-                a1 = prmt(x01, 0x64646464u, 0x4342u);
-                a2 = prmt(x23, 0x64646464u, 0x4140u);
-                a3 = prmt(x23, 0x64646464u, 0x4342u);
+            if (FMT == INT8) {  // fp16 subnormals (code + 128) * 2^-24, less 128 * 2^-24 (exact)
+                a0 = hsub2_exact(prmt(x01, 0u, 0x4140u), 0x00800080u);
+                a1 = hsub2_exact(prmt(x01, 0u, 0x4342u), 0x00800080u);
+                a2 = hsub2_exact(prmt(x23, 0u, 0x4140u), 0x00800080u);
+                a3 = hsub2_exact(prmt(x23, 0u, 0x4342u), 0x00800080u);
             } else {
                 dec_fp8x4<FMT>(x01, a0, a1);
                 dec_fp8x4<FMT>(x23, a2, a3);
             }
-            mma_16816(acc[i], a0, a1, a2, a3, pb0, pb1);
-            if (!LO) mma_16816(acc[i], a0, a1, a2, a3, pl0, pl1);
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                mma_16816(acc[r][i], a0, a1, a2, a3, pb[r][0], pb[r][1]);
+                if (!LO) mma_16816(acc[r][i], a0, a1, a2, a3, pl[r][0], pl[r][1]);
+            }
         }
     }
 
@@ -664,16 +725,12 @@ struct MmaConsumer {
     // the weighted mean of large V values can cancel, and a single fp16
     // rounding of P would then show in the output.
     __device__ __forceinline__ void p_frags(const float (&p)[4], uint32_t& pb0, uint32_t& pb1, uint32_t& pl0,
-                                            uint32_t& pl1, float& sum_fed) {
+                                            uint32_t& pl1) {
         pb0 = pack_f16x2(p[0], p[1]);
         pb1 = pack_f16x2(p[2], p[3]);
         const float2 h01 = f16x2_to_f32x2(pb0), h23 = f16x2_to_f32x2(pb1);
         pl0 = pack_f16x2(p[0] - h01.x, p[1] - h01.y);
         pl1 = pack_f16x2(p[2] - h23.x, p[3] - h23.y);
-        if (kBiased) {  // the weights exactly as the tensor cores see them
-            const float2 l01 = f16x2_to_f32x2(pl0), l23 = f16x2_to_f32x2(pl1);
-            sum_fed += ((h01.x + l01.x) + (h01.y + l01.y)) + ((h23.x + l23.x) + (h23.y + l23.y));
-        }
     }
 
     __device__ void tile(const Tile& cx) {
@@ -681,25 +738,34 @@ struct MmaConsumer {
         // (its logits masked, its V codes zeroed and its weights 0, whatever the
         // stage holds), so that the two boxes' products can overlap: 1-3% faster
         // than skipping it on the last tile of a pair.
-        float z0[4], z1[4];
+        float z0[NR][4], z1[NR][4];
         qk_box(cx.k, cx.s, cx.valid, z0);
         qk_box(cx.k + kBox * RB, cx.s + 4 * kBox * ng, cx.valid - kBox, z1);
-        float mx = fmaxf(fmaxf(fmaxf(z0[0], z0[1]), fmaxf(z0[2], z0[3])), fmaxf(fmaxf(z1[0], z1[1]), fmaxf(z1[2], z1[3])));
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
-        const float mn = fmaxf(m, mx);
-        float alpha = 1.f, p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
-        if (mn != -INFINITY) {
-            alpha = fast_exp2(m - mn);
+        float alpha[NR], p0[NR][4], p1[NR][4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                p0[e] = fast_exp2(z0[e] - mn);
-                p1[e] = fast_exp2(z1[e] - mn);
+        for (int r = 0; r < NR; ++r) {
+            float mx = fmaxf(fmaxf(fmaxf(z0[r][0], z0[r][1]), fmaxf(z0[r][2], z0[r][3])),
+                             fmaxf(fmaxf(z1[r][0], z1[r][1]), fmaxf(z1[r][2], z1[r][3])));
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+            const float mn = fmaxf(m[r], mx);
+            alpha[r] = 1.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) p0[r][e] = p1[r][e] = 0.f;
+            if (mn != -INFINITY) {
+                alpha[r] = fast_exp2(m[r] - mn);
+                const float mb = mn - kLogF;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    p0[r][e] = fast_exp2(z0[r][e] - mb);
+                    p1[r][e] = fast_exp2(z1[r][e] - mb);
+                }
             }
+            m[r] = mn;
+            l[r] = l[r] * alpha[r] + (((p0[r][0] + p0[r][1]) + (p0[r][2] + p0[r][3])) +
+                                      ((p1[r][0] + p1[r][1]) + (p1[r][2] + p1[r][3])));
         }
-        m = mn;
-        l = l * alpha + (((p0[0] + p0[1]) + (p0[2] + p0[3])) + ((p1[0] + p1[1]) + (p1[2] + p1[3])));
-        if (kRowScaled) {  // fold the V row (column group) scales into P
+        if (kRowScaled) {  // fold the V row (column group) scales into P; rows g and g + 8 share a group
             const uint32_t sv = cx.s + 4 * kTile * ng;
             float a[4], b[4];
             if (ng == 1) {
@@ -712,88 +778,98 @@ struct MmaConsumer {
                 a[0] = ldsf(a0); a[1] = ldsf(a0 + 4 * ng); a[2] = ldsf(a0 + 32 * ng); a[3] = ldsf(a0 + 36 * ng);
                 b[0] = ldsf(b0); b[1] = ldsf(b0 + 4 * ng); b[2] = ldsf(b0 + 32 * ng); b[3] = ldsf(b0 + 36 * ng);
             }
-            if (cx.valid >= kTile) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    p0[e] *= a[e];
-                    p1[e] *= b[e];
-                }
-            } else {  // a masked token keeps p = 0 whatever its (never written) scale slot holds
+            for (int r = 0; r < NR; ++r) {
+                if (cx.valid >= kTile) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    p0[e] = p0[e] != 0.f ? p0[e] * a[e] : 0.f;
-                    p1[e] = p1[e] != 0.f ? p1[e] * b[e] : 0.f;
+                    for (int e = 0; e < 4; ++e) {
+                        p0[r][e] *= a[e];
+                        p1[r][e] *= b[e];
+                    }
+                } else {  // a masked token keeps p = 0 whatever its (never written) scale slot holds
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        p0[r][e] = p0[r][e] != 0.f ? p0[r][e] * a[e] : 0.f;
+                        p1[r][e] = p1[r][e] != 0.f ? p1[r][e] * b[e] : 0.f;
+                    }
                 }
             }
-            psum *= alpha;
         }
         // rescale the accumulators: columns 2c and 2c+1 are operand rows 2c and
-        // 2c+1 (rows (2c and 2c+1) mod 4 when the residuals use columns 4-7)
-        if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
+        // 2c+1 (rows (2c and 2c+1) mod 4 when the residuals use columns 4-7);
+        // the second accumulator's columns are rows 8 + 2c and 9 + 2c
+        bool any = alpha[0] != 1.f;
+        if (R16) any = any || alpha[NR - 1] != 1.f;
+        if (__any_sync(0xFFFFFFFFu, any)) {
             const int src = 8 * ((kRowScaled && lo_cols) ? (c & 1) : c);
-            const float a0 = __shfl_sync(0xFFFFFFFFu, alpha, src);
-            const float a1 = __shfl_sync(0xFFFFFFFFu, alpha, src + 4);
 #pragma unroll
-            for (int i = 0; i < MT; ++i) {
-                acc[i][0] *= a0; acc[i][1] *= a1; acc[i][2] *= a0; acc[i][3] *= a1;
+            for (int r = 0; r < NR; ++r) {
+                const float a0 = __shfl_sync(0xFFFFFFFFu, alpha[r], src);
+                const float a1 = __shfl_sync(0xFFFFFFFFu, alpha[r], src + 4);
+#pragma unroll
+                for (int i = 0; i < MT; ++i) {
+                    acc[r][i][0] *= a0; acc[r][i][1] *= a1; acc[r][i][2] *= a0; acc[r][i][3] *= a1;
+                }
             }
         }
-        uint32_t pb0, pb1, pl0, pl1;
+        uint32_t pb[NR][2], pl[NR][2];
         if (kRowScaled && lo_cols) {  // lanes of rows 4-7 feed the residuals of rows 0-3 (16 lanes below)
-            p_frags(p0, pb0, pb1, pl0, pl1, psum);
-            pl0 = __shfl_xor_sync(0xFFFFFFFFu, pl0, 16);
-            pl1 = __shfl_xor_sync(0xFFFFFFFFu, pl1, 16);
-            if (g >= 4) { pb0 = pl0; pb1 = pl1; }
-            pv_box<true>(cx.v, cx.valid, pb0, pb1, pl0, pl1);
-            p_frags(p1, pb0, pb1, pl0, pl1, psum);
-            pl0 = __shfl_xor_sync(0xFFFFFFFFu, pl0, 16);
-            pl1 = __shfl_xor_sync(0xFFFFFFFFu, pl1, 16);
-            if (g >= 4) { pb0 = pl0; pb1 = pl1; }
-            pv_box<true>(cx.v + kBox * RB, cx.valid - kBox, pb0, pb1, pl0, pl1);
+            p_frags(p0[0], pb[0][0], pb[0][1], pl[0][0], pl[0][1]);
+            pl[0][0] = __shfl_xor_sync(0xFFFFFFFFu, pl[0][0], 16);
+            pl[0][1] = __shfl_xor_sync(0xFFFFFFFFu, pl[0][1], 16);
+            if (g >= 4) { pb[0][0] = pl[0][0]; pb[0][1] = pl[0][1]; }
+            pv_box<true>(cx.v, cx.valid, pb, pl);
+            p_frags(p1[0], pb[0][0], pb[0][1], pl[0][0], pl[0][1]);
+            pl[0][0] = __shfl_xor_sync(0xFFFFFFFFu, pl[0][0], 16);
+            pl[0][1] = __shfl_xor_sync(0xFFFFFFFFu, pl[0][1], 16);
+            if (g >= 4) { pb[0][0] = pl[0][0]; pb[0][1] = pl[0][1]; }
+            pv_box<true>(cx.v + kBox * RB, cx.valid - kBox, pb, pl);
         } else {
-            p_frags(p0, pb0, pb1, pl0, pl1, psum);
-            pv_box<false>(cx.v, cx.valid, pb0, pb1, pl0, pl1);
-            p_frags(p1, pb0, pb1, pl0, pl1, psum);
-            pv_box<false>(cx.v + kBox * RB, cx.valid - kBox, pb0, pb1, pl0, pl1);
+#pragma unroll
+            for (int r = 0; r < NR; ++r) p_frags(p0[r], pb[r][0], pb[r][1], pl[r][0], pl[r][1]);
+            pv_box<false>(cx.v, cx.valid, pb, pl);
+#pragma unroll
+            for (int r = 0; r < NR; ++r) p_frags(p1[r], pb[r][0], pb[r][1], pl[r][0], pl[r][1]);
+            pv_box<false>(cx.v + kBox * RB, cx.valid - kBox, pb, pl);
         }
     }
 
     __device__ void flush(const Flush& f) {
-        float lq = l;
-        lq += __shfl_xor_sync(0xFFFFFFFFu, lq, 1);
-        lq += __shfl_xor_sync(0xFFFFFFFFu, lq, 2);
-        if (c == 0 && kg == 0 && g < G * ng) f.ml[slot_index(f.hq0 + g / ng, f.nch, f.ch, f.half)] = make_float2(m, lq);
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            float lq = l[r];
+            lq += __shfl_xor_sync(0xFFFFFFFFu, lq, 1);
+            lq += __shfl_xor_sync(0xFFFFFFFFu, lq, 2);
+            const int row = g + 8 * r;
+            if (c == 0 && kg == 0 && row < G * ng)
+                f.ml[slot_index(f.hq0 + row / ng, f.nch, f.ch, f.half)] = make_float2(m[r], lq);
+        }
         if (kRowScaled && lo_cols) {  // column n += column n + 4 (lanes c and c + 2)
 #pragma unroll
             for (int i = 0; i < MT; ++i)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) acc[i][e] += __shfl_xor_sync(0xFFFFFFFFu, acc[i][e], 2);
+                for (int e = 0; e < 4; ++e) acc[0][i][e] += __shfl_xor_sync(0xFFFFFFFFu, acc[0][i][e], 2);
         }
-        float bias[2] = {0.f, 0.f};
-        if (kBiased) {  // bias * sum(P') of heads 2c and 2c+1
-            float ps = psum;
-            ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 1);
-            ps += __shfl_xor_sync(0xFFFFFFFFu, ps, 2);
-            bias[0] = kBias * __shfl_sync(0xFFFFFFFFu, ps, 8 * c);
-            bias[1] = kBias * __shfl_sync(0xFFFFFFFFu, ps, 8 * c + 4);
-        }
-        // acc[i][0..3] = out[column 2c | 2c+1][d = DV*g + 2i | DV*g + 2i + 1]; column n
-        // is head n / ng with the V scales of group n % ng, which must be the group
-        // of this thread's DV dims, (g * ng) / 8
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int n = 2 * c + e, h = n / ng;
-            if (h >= G || n % ng != ((g * ng) >> 3)) continue;
-            float* dst = f.acc + slot_index(f.hq0 + h, f.nch, f.ch, f.half) * D + DV * g;
-            const float bs = bias[e];
-            const float so = f.s_out / kUnit;
-            // INT4: the odd dims (rows g+8) were fed as 16x operands, bias included
-            const float bs1 = I4 ? 16.f * bs : bs, so1 = I4 ? so * 0.0625f : so;
+        for (int r = 0; r < NR; ++r) {
+            // acc[r][i][0..3] = out[column 8r + 2c | 8r + 2c+1][d = DV*g + 2i | DV*g + 2i + 1];
+            // column n is head n / ng with the V scales of group n % ng, which must
+            // be the group of this thread's DV dims, (g * ng) / 8
 #pragma unroll
-            for (int i = 0; i < MT; i += 2)
-                *reinterpret_cast<float4*>(dst + 2 * i) =
-                    make_float4((acc[i][e] - bs) * so, (acc[i][2 + e] - bs1) * so1,
-                                (acc[i + 1][e] - bs) * so, (acc[i + 1][2 + e] - bs1) * so1);
+            for (int e = 0; e < 2; ++e) {
+                const int n = 8 * r + 2 * c + e, h = n / ng;
+                if (h >= G || n % ng != ((g * ng) >> 3)) continue;
+                float* dst = f.acc + slot_index(f.hq0 + h, f.nch, f.ch, f.half) * D + DV * g;
+                // INT8 / INT4 operands are 2^-24 per code step; INT4's odd dims
+                // (rows g+8) were fed as 16x operands
+                const float so = kRowScaled ? f.s_out / kUnit : f.s_out;
+                const float so1 = I4 ? so * 0.0625f : so;
+#pragma unroll
+                for (int i = 0; i < MT; i += 2)
+                    *reinterpret_cast<float4*>(dst + 2 * i) =
+                        make_float4(acc[r][i][e] * so, acc[r][i][2 + e] * so1,
+                                    acc[r][i + 1][e] * so, acc[r][i + 1][2 + e] * so1);
+            }
         }
     }
     __device__ void flush_empty(const Flush& f) {
@@ -1336,16 +1412,25 @@ cudaError_t launch_fmt_d(const CUtensorMap& tk, const CUtensorMap& tv, const Dec
     }
     if (!simt) {
         // The tensor-core consumer's operand rows are (q-head, scale group)
-        // pairs, eight per launch: a group of G q-heads with ng scale groups per
-        // row takes ceil(G * ng / 8) launches over the same tiles, each serving
-        // 8 / ng of the heads; only the first appends the newest rows (the later
-        // ones read them from the cache).
-        const int per = 8 / a.cache.ngroups;
-        for (int h = 0; h < G && e == cudaSuccess; h += per) {
-            p.head_off = h;
-            p.heads = G - h < per ? G - h : per;
-            if (h > 0) p.k_new = p.v_new = nullptr;
+        // pairs: eight per pass, or sixteen with the 16-row consumer, which
+        // serves kv-heads whose q-heads x groups exceed 8.  Beyond 16 a group
+        // of G q-heads with ng scale groups per row takes ceil(G * ng / 16)
+        // launches over the same tiles, each serving 16 / ng of the heads;
+        // only the first appends the newest rows (the later ones read them
+        // from the cache).
+        const int ng = a.cache.ngroups;
+        if (G * ng <= 8) {
             e = launch_stream<FMT, D, MmaConsumer<FMT, D>>(tk, tv, p, s);
+        } else if constexpr (FMT == INT8 || FMT == INT4) {  // groups: only these formats have them
+            const int per = 16 / ng;
+            for (int h = 0; h < G && e == cudaSuccess; h += per) {
+                p.head_off = h;
+                p.heads = G - h < per ? G - h : per;
+                if (h > 0) p.k_new = p.v_new = nullptr;
+                e = launch_stream<FMT, D, MmaConsumer<FMT, D, true>>(tk, tv, p, s);
+            }
+        } else {
+            e = cudaErrorInvalidValue;  // FP8 has no groups and at most 8 q-heads per kv-head
         }
     }
     if (e != cudaSuccess) return e;

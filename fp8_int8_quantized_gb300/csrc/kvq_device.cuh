@@ -124,6 +124,15 @@ __device__ __forceinline__ uint32_t dec_x2(uint16_t two) {
     }
 }
 
+// a - b on two f16x2 words, round to nearest with subnormals kept (no flush
+// to zero): exact wherever a, b and the difference are all multiples of 2^-24
+// inside fp16's range, as for small integers times 2^-24.
+__device__ __forceinline__ uint32_t hsub2_exact(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 // d = c + a.lo * b.lo + a.hi * b.hi with f16 inputs and fp32 accumulation
 // (a product of two fp16 values is exact in fp32).
 __device__ __forceinline__ float fma_f16x2_f32(uint32_t a, uint32_t b, float c) {

@@ -20,6 +20,9 @@ def test_decode_bytes_of_the_fixed_context_workloads():
         "llama2-13b-int4": 2_684_354_560 + 167_772_160 + 2 * 1_310_720 + 128 * 64 * 4 + 128 * 4,
         "llama2-13b-int4-g32": 2_684_354_560 + 4 * 167_772_160 + 2 * 1_310_720 + 128 * 64 * 4 + 128 * 4,
         "llama3-70b": 17_179_869_184 + 2 * 4_194_304 + 256 * 2048 * 4 + 256 * 4,
+        # four fp32 scales per (token, kv-head) row of K and of V
+        "llama3-70b-int8-g32": 17_179_869_184 + 2 * 256 * 32768 * 8 * 4 * 4 + 2 * 4_194_304 + 256 * 2048 * 4
+                               + 256 * 4,
     }
     for name, total in want.items():
         wl = W.WORKLOADS[name]
