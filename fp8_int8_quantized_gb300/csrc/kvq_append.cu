@@ -241,6 +241,127 @@ __global__ void __launch_bounds__(kLutThreads, 2) append_lut_kernel(AppendArgs a
     }
 }
 
+// rint(fl32(x / s)) for |x| <= amax and s = fl32(amax / qmax) (so |x / s|
+// is at most qmax plus a few ulps), from the quotient by the reciprocal:
+// y = fl32(x * r), r = fl32(1 / s), is within |x / s| * 2^-23 <= 1.6e-5 of
+// x / s, and fl32(x / s) within half an ulp (<= 2^-18) of it, so y and
+// fl32(x / s) round to the same integer unless a half-integer lies between
+// them -- only possible when y is within 1.9e-5 of one.  Those rare values
+// (y within 2^-14 of a half-integer) take the IEEE division instead, so the
+// result is exactly the division's.
+__device__ __forceinline__ int quant_rint(float x, float s, float r) {
+    const float y = x * r;
+    const float q = rintf(y);
+    if (fabsf(y - q) > 0.5f - 6.103515625e-05f) return __float2int_rn(__fdiv_rn(x, s));
+    return (int)q;
+}
+
+// INT8 / INT4 append of any batch: a persistent grid streams (token, kv-head,
+// 16-value chunk) units, K and V together, two units per iteration with all
+// eight 16-byte loads issued before the first row maximum.  The D/16 lanes of
+// a row are adjacent (a unit's lane is its index mod 32, and D/16 divides 32),
+// so the row (or group) maximum is a shuffle reduction among them, as in
+// append_kernel; each value is quantized as quant_rint above (bit-identical to
+// the division).
+template <int FMT, int D>
+__global__ void __launch_bounds__(kLutThreads, 2) append_rows_kernel(AppendArgs a, FastDiv by_heads) {
+    constexpr int CPR = D / 16;  // units per row
+    constexpr int LOG_CPR = D == 128 ? 3 : 2;
+    constexpr float kQmax = FMT == INT4 ? 7.0f : 127.0f;
+    constexpr int kQi = FMT == INT4 ? 7 : 127;
+    griddep_wait();
+    griddep_launch();
+    const int Hkv = a.cache.num_kv_heads;
+    const int BS = a.cache.block_size;  // 16, 32 or 64
+    const int lbs = __ffs(BS) - 1;
+    const int64_t nslots = (int64_t)a.cache.num_blocks * BS;
+    const uint32_t units = (uint32_t)(a.num_tokens * Hkv * CPR);  // < 2^31 (checked by the launcher)
+    const uint32_t stride = gridDim.x * kLutThreads;               // a multiple of 32: lanes keep their rows
+    const int ng = a.cache.ngroups, cpg = CPR / ng;                // groups per row, units per group
+
+    struct Unit {
+        uint4 r[4];
+        int64_t slot;
+        uint32_t row;
+    };
+    auto load = [&](uint32_t u, Unit& x) {
+        const uint4* k = reinterpret_cast<const uint4*>(a.k) + 2 * (int64_t)u;  // 16 fp16 = two uint4
+        const uint4* v = reinterpret_cast<const uint4*>(a.v) + 2 * (int64_t)u;
+        x.r[0] = __ldg(k);
+        x.r[1] = __ldg(k + 1);
+        x.r[2] = __ldg(v);
+        x.r[3] = __ldg(v + 1);
+        x.row = u >> LOG_CPR;
+        x.slot = __ldg(a.slot_mapping + by_heads.div(x.row));
+    };
+    // quantize 16 values (two uint4 of fp16) with the row / group maximum of
+    // their lanes; returns the scale; codes into o (INT8: 4 words, INT4: 2)
+    auto quant16 = [&](const uint4& r0, const uint4& r1, uint32_t (&o)[4]) -> float {
+        const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float2 f = f16x2_to_f32x2(w[i]);
+            x[2 * i] = f.x;
+            x[2 * i + 1] = f.y;
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+        amax = group_max<CPR>(amax, cpg);
+        const float s = __fdiv_rn(amax, kQmax);
+        const float rs = s != 0.f ? __frcp_rn(s) : 0.f;
+        o[0] = o[1] = o[2] = o[3] = 0u;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            int v = 0;
+            if (s != 0.f) v = max(-kQi, min(kQi, quant_rint(x[i], s, rs)));
+            if (FMT == INT4) o[i >> 3] |= (uint32_t)(v & 0xF) << (4 * (i & 7));   // channel 2j: low nibble of byte j
+            else o[i >> 2] |= (uint32_t)(v & 0xFF) << (8 * (i & 3));
+        }
+        return s;
+    };
+    auto store = [&](uint32_t u, const Unit& x) {
+        const int c = (int)(u & (CPR - 1));
+        uint32_t ok[4], ov[4];
+        // every lane of the row quantizes (the maxima are shuffles among them),
+        // also where the slot is skipped or out of range
+        const float sk = quant16(x.r[0], x.r[1], ok);
+        const float sv = quant16(x.r[2], x.r[3], ov);
+        const int h = (int)(x.row - by_heads.div(x.row) * (uint32_t)Hkv);
+        if (x.slot == -1) return;
+        if (x.slot < 0 || x.slot >= nslots) {
+            if (c == 0 && h == 0) record_error(a.err, DEV_ERR_RANGE, x.slot);
+            return;
+        }
+        const int64_t dst_row = (((x.slot >> lbs) * Hkv + h) << lbs) + (x.slot & (BS - 1));
+        if (FMT == INT4) {
+            *reinterpret_cast<uint2*>(a.cache.k_codes + dst_row * (D / 2) + c * 8) = make_uint2(ok[0], ok[1]);
+            *reinterpret_cast<uint2*>(a.cache.v_codes + dst_row * (D / 2) + c * 8) = make_uint2(ov[0], ov[1]);
+        } else {
+            *reinterpret_cast<uint4*>(a.cache.k_codes + dst_row * D + c * 16) = make_uint4(ok[0], ok[1], ok[2], ok[3]);
+            *reinterpret_cast<uint4*>(a.cache.v_codes + dst_row * D + c * 16) = make_uint4(ov[0], ov[1], ov[2], ov[3]);
+        }
+        if (c % cpg == 0) {
+            a.cache.k_scales[dst_row * ng + c / cpg] = sk;
+            a.cache.v_scales[dst_row * ng + c / cpg] = sv;
+        }
+    };
+    // All lanes of a warp run the same number of iterations of both halves:
+    // the shuffles of the row maxima need every lane of a row, so a unit past
+    // the end is loaded as zeros (never stored) instead of skipped.
+    const uint32_t lane0 = blockIdx.x * kLutThreads + (threadIdx.x & ~31u);
+    for (uint32_t base = lane0; base < units; base += 2 * stride) {
+        const uint32_t u0 = base + (threadIdx.x & 31u), u1 = u0 + stride;
+        Unit x0, x1;
+        const bool v0 = u0 < units, v1 = u1 < units;
+        if (v0) load(u0, x0); else x0 = Unit{{}, -1, 0};
+        if (v1) load(u1, x1); else x1 = Unit{{}, -1, 0};
+        store(u0, x0);
+        if (base + stride < units) store(u1, x1);
+    }
+}
+
 // Values per call from which the tabulating kernel pays off (its table costs
 // 32768 divisions per CTA).
 constexpr int64_t kLutMinValues = (int64_t)1 << 22;
@@ -262,6 +383,21 @@ cudaError_t launch_fmt(const AppendArgs& a, cudaStream_t s) {
             const int64_t want = (per + kLutThreads - 1) / kLutThreads;
             const int64_t grid = want < (int64_t)sms * 2 ? want : (int64_t)sms * 2;
             return launch_pdl(kern, dim3((unsigned)grid), dim3(kLutThreads), kLutEntries, s, a,
+                              FastDiv((uint32_t)a.cache.num_kv_heads));
+        }
+    }
+    if constexpr (FMT == INT8 || FMT == INT4) {
+        if (per < ((int64_t)1 << 31)) {
+            int dev = 0, sms = 0;
+            cudaError_t e;
+            if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+            if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+            const int64_t want = (per + kLutThreads - 1) / kLutThreads;
+            const int64_t grid = want < (int64_t)sms * 2 ? want : (int64_t)sms * 2;
+            if (D == 64)
+                return launch_pdl(append_rows_kernel<FMT, 64>, dim3((unsigned)grid), dim3(kLutThreads), 0, s, a,
+                                  FastDiv((uint32_t)a.cache.num_kv_heads));
+            return launch_pdl(append_rows_kernel<FMT, 128>, dim3((unsigned)grid), dim3(kLutThreads), 0, s, a,
                               FastDiv((uint32_t)a.cache.num_kv_heads));
         }
     }

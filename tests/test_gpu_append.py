@@ -185,8 +185,51 @@ def test_append_groups_bit_exact(fmt, D, ng):
     assert kvq.device_error_check()[0] == 0
 
 
+@pytest.mark.parametrize("fmt,group", [("int8", 0), ("int4", 0), ("int8", 32), ("int4", 64)])
+def test_append_rounding_ties_and_bulk_rows_bit_exact(fmt, group):
+    """INT8 / INT4 codes are rint(fl32(x / s)), ties to even.  Rows whose scale
+    is a power of two make x / s exactly k + 0.5 (ties), or one fp16 step off
+    it (near-ties); then a bulk append of 24000 random rows with x20 outlier
+    channels (about 3000 values whose quotient lies within 2^-14 of a
+    half-integer).  Every code and scale bit-exact against the oracle."""
+    qmax = 127 if fmt == "int8" else 7
+    Hkv, D = 2, 128
+    ties = []
+    for e in (-3, 0, 2):                          # s = 2^e exactly: amax = qmax * 2^e
+        s = 2.0 ** e
+        row = torch.zeros(D, dtype=torch.float64)
+        row[0] = qmax * s
+        k = torch.arange(-qmax, qmax)              # k + 0.5 for k in [-qmax, qmax - 1]
+        n = min(D - 1, k.numel())
+        row[1:1 + n] = (k[:n] + 0.5) * s
+        ties.append(row)
+        near = row.clone().to(torch.float16)
+        nb = near.view(torch.int16)
+        nb[1:] += 1                                # the next fp16 value away from zero
+        ties.append(near.double())
+    t = torch.stack(ties).to(torch.float16)        # [rows][D]
+    kt = t[:, None, :].repeat(1, Hkv, 1)
+    assert (kt.double()[:, 0, 1:1 + 10] / 2.0 ** -3).fmod(1).abs().ne(0).any()   # not all integers
+    g = torch.Generator().manual_seed(len(fmt) + group)
+    T = 24000
+    kb = torch.randn((T, Hkv, D), generator=g) * 2
+    vb = torch.randn((T, Hkv, D), generator=g) * 2
+    kb[:, :, 7] *= 20
+    vb[:, 1, 100] *= 20
+    k = torch.cat([kt, kb.to(torch.float16)])
+    v = torch.cat([kt.flip(2), vb.to(torch.float16)])
+    NB, BS = (k.shape[0] + 15) // 16, 16
+    slots = torch.randperm(NB * BS, generator=g)[:k.shape[0]].to(torch.int64)
+    c, ref = run_both(k, v, slots, NB, Hkv, BS, D, fmt, None, group=group)
+    assert np.array_equal(c.k_codes.cpu().numpy(), ref.k_codes)
+    assert np.array_equal(c.v_codes.cpu().numpy(), ref.v_codes)
+    assert np.array_equal(c.k_scales.cpu().numpy().view(np.uint32), ref.k_scales.view(np.uint32))
+    assert np.array_equal(c.v_scales.cpu().numpy().view(np.uint32), ref.v_scales.view(np.uint32))
+    assert kvq.device_error_check()[0] == 0
+
+
 @pytest.mark.parametrize("name", ["llama2-7b", "llama3-8b", "llama2-13b-int8", "llama2-13b-int4", "llama3-70b",
-                                  "llama2-13b-int4-g32"])
+                                  "llama2-13b-int4-g32", "llama3-70b-int8-g32"])
 def test_append_full_size_sampled(name):
     """The workloads' own append launches (their full windows), checked on a
     seeded sample of tokens against the oracle."""
