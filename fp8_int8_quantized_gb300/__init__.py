@@ -28,7 +28,7 @@ EXPORTS = ("kvq_append", "kvq_decode_workspace_size", "kvq_decode_attention", "k
            "kvq_dequant",
            "kvq_set_decode_kernel", "kvq_device_error_check", "kvq_status_string", "kvq_abi_version",
            "kvq_decode_attention_static_scratch", "kvq_static_scratch_bytes", "kvq_set_decode_timing_events",
-           "kvq_prefill_attention")
+           "kvq_prefill_attention", "kvq_encode_fp8")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkvq.so")
@@ -85,6 +85,8 @@ def lib():
         L.kvq_prefill_attention.restype = ctypes.c_int
         L.kvq_prefill_attention.argtypes = [P, P, P, i32, P, P, i32, i64, i32, i32, P, i32, ctypes.c_float, P,
                                             P]
+        L.kvq_encode_fp8.restype = ctypes.c_int
+        L.kvq_encode_fp8.argtypes = [P, P, i64, i32, P]
         L.kvq_dequant.restype = ctypes.c_int
         L.kvq_dequant.argtypes = [P, P, i64, P, i32, P, P, P]
         L.kvq_set_decode_timing_events.restype = None

@@ -13,6 +13,11 @@
 #include "kvq_device.cuh"
 #include "kvq_launch.h"
 
+namespace kvq {
+// The debug FP8 encoder's launcher (kvq_dequant.cu).
+cudaError_t launch_encode_fp8(const float* x, uint8_t* codes, int64_t n, int fmt, cudaStream_t s);
+}  // namespace kvq
+
 namespace {
 
 // First error a kernel met on this device: code << 56 | detail.
@@ -318,6 +323,17 @@ kvq_status kvq_dequant(const kvq_cache* cache, const int64_t* slots, int64_t num
     if (!err) return KVQ_ERR_CUDA;
     kvq::DequantArgs a{view(cache), slots, num_slots, (fmt == KVQ_INT8 || fmt == KVQ_INT4) ? nullptr : scale, out_k, out_v, err};
     return kvq::launch_dequant(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+kvq_status kvq_encode_fp8(const float* x, void* codes, int64_t n, int32_t fmt, kvq_stream_t stream) {
+    if (fmt != KVQ_E4M3 && fmt != KVQ_E5M2) return KVQ_ERR_INVALID_ARG;
+    if (n < 0) return KVQ_ERR_INVALID_ARG;
+    if (n == 0) return KVQ_OK;
+    if (!x || !codes || !aligned(x, 16) || !aligned(codes, 16)) return KVQ_ERR_INVALID_ARG;
+    return kvq::launch_encode_fp8(x, static_cast<uint8_t*>(codes), n, fmt,
+                                  reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? KVQ_OK
+               : KVQ_ERR_CUDA;
 }
 
 kvq_status kvq_device_error_check(kvq_stream_t stream, int64_t* detail) {

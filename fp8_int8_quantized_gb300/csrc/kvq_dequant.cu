@@ -78,7 +78,45 @@ cudaError_t launch_fmt(const DequantArgs& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// Debug: the FP8 encoder of the append kernels (enc_fp8x2, the hardware
+// cvt.rn.satfinite conversion) on raw fp32 values, so that it can be checked
+// on every fp32 input.  One thread per 16 values (four 16-byte loads, one
+// 16-byte store), grid-stride; the last n % 16 values one by one.
+template <int FMT>
+__global__ void __launch_bounds__(kThreads) encode_kernel(const float* x, uint8_t* codes, int64_t n) {
+    const int64_t groups = n / 16;
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t gi = (int64_t)blockIdx.x * kThreads + threadIdx.x; gi < groups; gi += stride) {
+        const float4* src = reinterpret_cast<const float4*>(x) + 4 * gi;
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float4 v = src[j];
+            o[j] = (uint32_t)enc_fp8x2<FMT>(v.x, v.y) | ((uint32_t)enc_fp8x2<FMT>(v.z, v.w) << 16);
+        }
+        reinterpret_cast<uint4*>(codes)[gi] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    const int64_t t = 16 * groups + (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    if (t < n) codes[t] = (uint8_t)(enc_fp8x2<FMT>(x[t], 0.f) & 0xFFu);
+}
+
 }  // namespace
+
+cudaError_t launch_encode_fp8(const float* x, uint8_t* codes, int64_t n, int fmt, cudaStream_t s) {
+    if (n == 0) return cudaSuccess;
+    int dev = 0, sms = 0;
+    cudaError_t e;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const int64_t want = (n / 16 + kThreads - 1) / kThreads;
+    int64_t grid = want < (int64_t)sms * 8 ? want : (int64_t)sms * 8;
+    if (grid < 1) grid = 1;
+    if (fmt == E4M3)
+        encode_kernel<E4M3><<<(unsigned)grid, kThreads, 0, s>>>(x, codes, n);
+    else
+        encode_kernel<E5M2><<<(unsigned)grid, kThreads, 0, s>>>(x, codes, n);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_dequant(const DequantArgs& a, cudaStream_t s) {
     if (a.num_slots == 0) return cudaSuccess;

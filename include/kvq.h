@@ -11,8 +11,9 @@
  * sequence's newest K/V row quantized into the cache in the same launch),
  * kvq_decode_attention_static_scratch (decode without a caller workspace),
  * kvq_prefill_attention (causal attention of a chunk of new queries per
- * sequence over the same cache) and kvq_dequant (a debugging gather of the
- * fp32 values a kernel sees).  The operations follow these pages (cited by
+ * sequence over the same cache), kvq_dequant (a debugging gather of the
+ * fp32 values a kernel sees) and kvq_encode_fp8 (the append kernels' FP8
+ * encoder on raw fp32 values, for checking it).  The operations follow these pages (cited by
  * title and section):
  *
  *   [TGI] "Accelerating Inference with FP8 KV Cache" (text-generation-inference
@@ -263,6 +264,17 @@ KVQ_API kvq_status kvq_prefill_attention(const void* q, const kvq_cache* cache,
 KVQ_API kvq_status kvq_dequant(const kvq_cache* cache, const int64_t* slots, int64_t num_slots,
                        const float* scale, int32_t fmt, float* out_k, float* out_v,
                        kvq_stream_t stream);
+
+/* Debug: the FP8 encoder of the append kernels on raw fp32 values
+ * ([TGI] "FP8 Formats: E4M3 and E5M2"; OCP E4M3FN / E5M2): codes[i] =
+ * RNE-satfinite(x[i]) -- round to nearest, ties to even, |x| beyond the
+ * format's largest finite value (Inf included) to +-that value, NaN to a NaN
+ * code -- which is what kvq_append stores for an fp16 input once it has divided
+ * it by the scale.  It exists so that the hardware conversion can be checked
+ * on every fp32 input.
+ *   x: fp32 [n]; codes: u8 [n]; both 16-byte aligned.  fmt: KVQ_E4M3 or
+ *   KVQ_E5M2 (anything else is KVQ_ERR_INVALID_ARG).  n == 0 is a no-op. */
+KVQ_API kvq_status kvq_encode_fp8(const float* x, void* codes, int64_t n, int32_t fmt, kvq_stream_t stream);
 
 /* Decode kernel family used by kvq_decode_attention in this process:
  * 0 = automatic (tensor-core kernel), 1 = CUDA-core kernel (group size <= 4,

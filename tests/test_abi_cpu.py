@@ -187,3 +187,11 @@ def test_static_scratch_checks_arguments_before_its_size_limit(lib):
     assert st(cache=d256) == 2                             # head_dim 256
     assert st(q=8) == 1                                    # misaligned q
     assert st(batch=0) == 0                                # nothing to do, nothing launched
+
+
+def test_encode_checks_before_any_cuda_call(lib):
+    assert lib.kvq_encode_fp8(16, 16, 32, kvq.INT8, None) == 1        # not an FP8 format
+    assert lib.kvq_encode_fp8(16, 16, -1, kvq.E4M3, None) == 1        # negative count
+    assert lib.kvq_encode_fp8(16, 24, 32, kvq.E5M2, None) == 1        # codes not 16-byte aligned
+    assert lib.kvq_encode_fp8(None, 16, 32, kvq.E4M3, None) == 1
+    assert lib.kvq_encode_fp8(None, None, 0, kvq.E4M3, None) == 0     # nothing to do
