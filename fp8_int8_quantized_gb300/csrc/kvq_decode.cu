@@ -55,6 +55,9 @@
 #ifndef KVQ_MIN_BLOCKS
 #define KVQ_MIN_BLOCKS 2
 #endif
+#ifndef KVQ_INT4_WARPS
+#define KVQ_INT4_WARPS 8
+#endif
 
 namespace kvq {
 namespace {
@@ -373,7 +376,7 @@ struct MmaConsumer {
     // per-warp register work rather than by HBM: 8 warps (registers capped at
     // 128, two CTAs per SM) are 11% faster than 6.  The 8-bit formats stay at
     // 6: at 8 their stages no longer fit two CTAs into shared memory.
-    static constexpr int kWarps = R16 ? 4 : (I4 ? 8 : 6);
+    static constexpr int kWarps = R16 ? 4 : (I4 ? KVQ_INT4_WARPS : 6);
     // INT8 codes enter the tensor cores as fp16 subnormals, code * 2^-24, and
     // INT4 codes the same, or 16x that where the nibble is left in mantissa
     // bits 4..7 -- the high nibble of a byte is masked in place, which saves
@@ -427,8 +430,8 @@ struct MmaConsumer {
     float qk_scale;
     // this lane's byte offsets inside a stage tile (the 128-byte swizzle folded
     // in): K row g at chunks 2c, 2c+1 (row 8+g is 8 rows further), V rows 2c
-    // and 2c+1 at chunk g (rows 8+2c, 9+2c are 8 rows further); INT4 rows are
-    // unswizzled, the same codes at half the bytes
+    // and 2c+1 at chunk g (rows 8+2c, 9+2c are 8 rows further); INT4 rows
+    // hold the same codes at half the bytes (64-byte swizzle at head_dim 128)
     uint32_t k_off0, k_off1, v_off0, v_off1;
 
     __device__ void init(int G_, float qks, int ng_) {
@@ -440,7 +443,12 @@ struct MmaConsumer {
         kg = g % ng_;
         lo_cols = !R16 && kRowScaled && G_ * ng_ <= 4;
         qk_scale = qks;
-        if (I4) {
+        if (I4 && D == 128) {  // 64-byte rows, 64-byte swizzle: 16-byte chunk ^= (row / 2) % 4
+            k_off0 = g * RB + ((c ^ ((g >> 1) & 3)) << 4);
+            k_off1 = 0;
+            v_off0 = (2 * c) * RB + ((((g >> 1) ^ c) & 3) << 4) + 8 * (g & 1);
+            v_off1 = (2 * c + 1) * RB + ((((g >> 1) ^ c) & 3) << 4) + 8 * (g & 1);
+        } else if (I4) {
             k_off0 = g * RB + c * (DC / 2);
             k_off1 = 0;
             v_off0 = (2 * c) * RB + (DV / 2) * g;
@@ -949,15 +957,16 @@ __device__ __noinline__ void append_newest(const uint16_t* nkv, int blk, int pos
         }
         code[w] = c;
     }
-    if (blk >= 0 && FMT == INT4) {  // VPL codes = VPL / 2 bytes per lane, rows unswizzled
+    if (blk >= 0 && FMT == INT4) {  // VPL codes = VPL / 2 bytes per lane
         constexpr int RB = D / 2;
         const int r = pos - tok0;
         const uint32_t kb = kt + (r / kBox) * kBox * RB + (r % kBox) * RB;
         const int BS = a.cache.block_size;
         const int64_t row = ((int64_t)blk * a.cache.num_kv_heads + kvh) * BS + (pos & (BS - 1));
-        if (D == 128) {
-            sts16(kb + 2 * lane, (uint16_t)code[0]);
-            sts16(kb + tile_bytes + 2 * lane, (uint16_t)code[1]);
+        if (D == 128) {  // the stage's 64-byte rows are 64-byte swizzled
+            const uint32_t off = ((((lane >> 3) ^ (r >> 1)) & 3) << 4) | ((2 * lane) & 15);
+            sts16(kb + off, (uint16_t)code[0]);
+            sts16(kb + tile_bytes + off, (uint16_t)code[1]);
             reinterpret_cast<uint16_t*>(a.cache.k_codes + row * RB)[lane] = (uint16_t)code[0];
             reinterpret_cast<uint16_t*>(a.cache.v_codes + row * RB)[lane] = (uint16_t)code[1];
         } else {
@@ -1106,6 +1115,7 @@ __global__ void __launch_bounds__(Consumer::kWarps * 32, Consumer::kMinCtas)
     }
     const uint64_t pol = policy_evict_first();
     const uint32_t box_tx = 2 * kBox * RB + (kRowScaled ? 2 * kBox * 4 * ng : 0);
+    const bool big_box = BS >= kTile;  // a tile lies in one block: one 32-row box per tensor
     const uint32_t q_tx = G * D * 2;
 
     const float s_fp8 = (!kRowScaled && a.scale) ? __ldg(a.scale) : 1.0f;
@@ -1146,42 +1156,48 @@ __global__ void __launch_bounds__(Consumer::kWarps * 32, Consumer::kMinCtas)
             if (ends && lpend >= fc) break;
             const int id0 = __shfl_sync(0xFFFFFFFFu, idc, (2 * rel) & 31);
             const int id1 = __shfl_sync(0xFFFFFFFFu, idc, (2 * rel + 1) & 31);
+            const int tok0 = iw.t * kTile;
+            // a 16-row box past the context is not loaded; a 32-row box (blocks
+            // of 32 or more tokens) always is (the rows past the context are
+            // masked like those of an unwritten second box)
+            const int nbox = big_box ? 2 : (ctx_s[iw.b] - tok0 > kBox ? 2 : 1);
+            uint64_t* fb = &full[ist];
             if (lane == 0) {
-                const int tok0 = iw.t * kTile;
-                const int nbox = ctx_s[iw.b] - tok0 > kBox ? 2 : 1;  // a box past the context is not loaded
-                uint64_t* fb = &full[ist];
                 if (ends) {  // block of the newest row; -1 (not written) if outside the cache
                     const int nb = ctx_s[iw.b] - 1 - tok0 >= kBox ? id1 : id0;
                     *patch_blk = nb < 0 || nb >= a.cache.num_blocks ? -1 : nb;
                 }
                 mbar_arrive_expect_tx(fb, nbox * box_tx + (new_pair ? q_tx : 0u) + (ends ? 4u * D : 0u));
-                const uint32_t kt = tiles_u32 + ist * (2 * L.tile_bytes);
-                const uint32_t st = scales_u32 + ist * sc_stage;
-#pragma unroll
-                for (int bx = 0; bx < 2; ++bx) {
-                    if (bx >= nbox) break;
-                    int blk = bx ? id1 : id0;
-                    if (blk < 0 || blk >= a.cache.num_blocks) {
-                        record_error(a.err, DEV_ERR_RANGE, blk);
-                        blk = 0;  // keep the pipeline going on a block that exists
-                    }
-                    const int row = (blk * Hkv + iw.kvh) * BS + ((tok0 + bx * kBox) & (BS - 1));
-                    tma_load_2d_u32(kt + bx * kBox * RB, &tmk, 0, row, fb, pol);
-                    tma_load_2d_u32(kt + L.tile_bytes + bx * kBox * RB, &tmv, 0, row, fb, pol);
-                    if (kRowScaled) {
-                        const uint32_t sb = kBox * 4 * ng;  // a box's scales: 16 rows of ng
-                        bulk_load_u32(st + bx * sb, a.cache.k_scales + (int64_t)row * ng, sb, fb, pol);
-                        bulk_load_u32(st + 2 * sb + bx * sb, a.cache.v_scales + (int64_t)row * ng, sb, fb, pol);
-                    }
+            }
+            // The copies of a tile are issued by lanes 0-7 at once: lane j moves
+            // box j & 1 of K (j = 0, 1) or V (2, 3) codes, or of their row
+            // scales (4-7); one 32-row copy per tensor (lanes 0, 2, 4, 6) when
+            // the tile lies in one block of 32 or more tokens.  (Lane 0's
+            // expect-tx may land after some of their bytes; the phase cannot
+            // complete before that arrival.)
+            const int bx = lane & 1, which = (lane >> 1) & 1;
+            if (lane < (kRowScaled ? 8 : 4) && bx < (big_box ? 1 : nbox)) {
+                int blk = bx ? id1 : id0;
+                if (blk < 0 || blk >= a.cache.num_blocks) {
+                    record_error(a.err, DEV_ERR_RANGE, blk);
+                    blk = 0;  // keep the pipeline going on a block that exists
                 }
-                if (new_pair)
-                    bulk_load(qbuf, a.q + ((int64_t)iw.b * a.num_q_heads + (int64_t)iw.kvh * Gall + h0) * D, q_tx, fb,
-                              pol);
-                if (ends) {
-                    const int64_t row = ((int64_t)iw.b * Hkv + iw.kvh) * D;
-                    bulk_load(nkv, a.k_new + row, 2 * D, fb, pol);
-                    bulk_load(nkv + D, a.v_new + row, 2 * D, fb, pol);
+                const int row = (blk * Hkv + iw.kvh) * BS + ((tok0 + bx * kBox) & (BS - 1));
+                if (lane < 4) {
+                    const uint32_t dst = tiles_u32 + ist * (2 * L.tile_bytes) + which * L.tile_bytes + bx * kBox * RB;
+                    tma_load_2d_u32(dst, which ? &tmv : &tmk, 0, row, fb, pol);
+                } else {
+                    const uint32_t sb = (big_box ? kTile : kBox) * 4 * ng;  // the copy's rows of ng scales
+                    const uint32_t dst = scales_u32 + ist * sc_stage + which * (kTile * 4 * ng) + bx * (kBox * 4 * ng);
+                    bulk_load_u32(dst, (which ? a.cache.v_scales : a.cache.k_scales) + (int64_t)row * ng, sb, fb, pol);
                 }
+            }
+            if (new_pair && lane == 8)
+                bulk_load(qbuf, a.q + ((int64_t)iw.b * a.num_q_heads + (int64_t)iw.kvh * Gall + h0) * D, q_tx, fb, pol);
+            if (ends && (lane == 9 || lane == 10)) {
+                const int64_t row = ((int64_t)iw.b * Hkv + iw.kvh) * D;
+                if (lane == 9) bulk_load(nkv, a.k_new + row, 2 * D, fb, pol);
+                else bulk_load(nkv + D, a.v_new + row, 2 * D, fb, pol);
             }
             if (new_pair) pend = fi;
             if (ends) lpend = fi;
@@ -1352,19 +1368,24 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 
 // 2-D view [rows = blocks * kv-heads * block][head_dim] of one code array;
-// box = 16 rows (one 16-token slice of a paged block).
+// box = 16 rows (one 16-token slice of a paged block), or 32 rows (a whole
+// 32-token tile) when blocks hold 32 or more tokens.
 // rb: bytes per row (head_dim, or head_dim / 2 for INT4); 128-byte rows are
-// loaded with the 128-byte swizzle, narrower ones plain.
-bool make_tmap(CUtensorMap* m, void* base, int64_t rows, int rb) {
+// loaded with the 128-byte swizzle, INT4 rows of head_dim 128 (64 bytes) with
+// the 64-byte swizzle (16-byte chunk index XOR (row / 2) % 4, so the V rows
+// 2c of the four lane groups no longer share their banks), other rows plain
+// (the 8-bit formats at head_dim 64 also have 64-byte rows, read unswizzled).
+bool make_tmap(CUtensorMap* m, void* base, int64_t rows, int rb, int box_rows, bool int4) {
     auto enc = get_encode();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)rb, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)rb};
-    cuuint32_t box[2] = {(cuuint32_t)rb, (cuuint32_t)kBox};
+    cuuint32_t box[2] = {(cuuint32_t)rb, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     rb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     rb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                               : (int4 && rb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE),
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -1451,7 +1472,10 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
     const int64_t rows = (int64_t)a.cache.num_blocks * a.cache.num_kv_heads * a.cache.block_size;
     CUtensorMap tk, tv;
     const int rb = row_bytes(a.cache.fmt, a.cache.head_dim);
-    if (!make_tmap(&tk, a.cache.k_codes, rows, rb) || !make_tmap(&tv, a.cache.v_codes, rows, rb))
+    const int box_rows = a.cache.block_size >= kTile ? kTile : kBox;
+    const bool int4 = a.cache.fmt == INT4;
+    if (!make_tmap(&tk, a.cache.k_codes, rows, rb, box_rows, int4) ||
+        !make_tmap(&tv, a.cache.v_codes, rows, rb, box_rows, int4))
         return cudaErrorInvalidValue;
     switch (a.cache.fmt) {
         case E4M3: return launch_fmt<E4M3>(tk, tv, a, s);
