@@ -249,11 +249,28 @@ __global__ void __launch_bounds__(kLutThreads, 2) append_lut_kernel(AppendArgs a
 // them -- only possible when y is within 1.9e-5 of one.  Those rare values
 // (y within 2^-14 of a half-integer) take the IEEE division instead, so the
 // result is exactly the division's.
-__device__ __forceinline__ int quant_rint(float x, float s, float r) {
+//
+// The rounding itself is one fp32 addition: t = y + 1.5 * 2^23 lands in the
+// binade where the ulp is 1, so it rounds y to the nearest integer, ties to
+// even, and for |y| < 2^22 the bit pattern of t is 0x4B400000 + rint(y): its
+// low byte is the INT8 code and its low nibble the INT4 code, in two's
+// complement.  (This keeps the conversions off the slow transcendental /
+// conversion pipe, which bounded the append at about half of HBM speed.)
+// quant_t returns that bit pattern and flags a near half-integer.
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
+constexpr float kNearHalf = 0.5f - 6.103515625e-05f;
+
+__device__ __forceinline__ uint32_t quant_t(float x, float r, bool& near) {
     const float y = x * r;
-    const float q = rintf(y);
-    if (fabsf(y - q) > 0.5f - 6.103515625e-05f) return __float2int_rn(__fdiv_rn(x, s));
-    return (int)q;
+    const float t = y + kRoundMagic;
+    near |= !(fabsf(y - (t - kRoundMagic)) <= kNearHalf);   // NaN (an Inf or NaN input) too
+    return __float_as_uint(t);
+}
+
+// The same code by the IEEE division (the rare near-tie values, and
+// non-finite inputs, as the division treats them).
+__device__ __forceinline__ uint32_t quant_div(float x, float s, int qmax) {
+    return (uint32_t)max(-qmax, min(qmax, __float2int_rn(__fdiv_rn(x, s))));
 }
 
 // INT8 / INT4 append of any batch: a persistent grid streams (token, kv-head,
@@ -295,30 +312,54 @@ __global__ void __launch_bounds__(kLutThreads, 2) append_rows_kernel(AppendArgs 
         x.slot = __ldg(a.slot_mapping + by_heads.div(x.row));
     };
     // quantize 16 values (two uint4 of fp16) with the row / group maximum of
-    // their lanes; returns the scale; codes into o (INT8: 4 words, INT4: 2)
+    // their lanes; returns the scale; codes into o (INT8: 4 words, INT4: 2).
+    // The maximum is taken on the fp16 pairs (|x| and max are exact in fp16),
+    // and each output word is quantized and packed straight from its fp16
+    // source words, so that few values are live at once.
     auto quant16 = [&](const uint4& r0, const uint4& r1, uint32_t (&o)[4]) -> float {
         const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-        float x[16];
+        __half2 m2 = __habs2(*reinterpret_cast<const __half2*>(&w[0]));
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float2 f = f16x2_to_f32x2(w[i]);
-            x[2 * i] = f.x;
-            x[2 * i + 1] = f.y;
-        }
-        float amax = 0.f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+        for (int i = 1; i < 8; ++i) m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __half2*>(&w[i])));
+        float amax = fmaxf(__low2float(m2), __high2float(m2));
         amax = group_max<CPR>(amax, cpg);
         const float s = __fdiv_rn(amax, kQmax);
-        const float rs = s != 0.f ? __frcp_rn(s) : 0.f;
-        o[0] = o[1] = o[2] = o[3] = 0u;
+        const float rs = s != 0.f ? __frcp_rn(s) : 0.f;   // s == 0: every t is the zero code
+        constexpr int VPW = FMT == INT4 ? 8 : 4;            // values per output word
+        constexpr int NW = 16 / VPW;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            int v = 0;
-            if (s != 0.f) v = max(-kQi, min(kQi, quant_rint(x[i], s, rs)));
-            if (FMT == INT4) o[i >> 3] |= (uint32_t)(v & 0xF) << (4 * (i & 7));   // channel 2j: low nibble of byte j
-            else o[i >> 2] |= (uint32_t)(v & 0xFF) << (8 * (i & 3));
+        for (int k = 0; k < NW; ++k) {
+            uint32_t t[VPW];
+            bool near = false;
+#pragma unroll
+            for (int j = 0; j < VPW / 2; ++j) {
+                const float2 f = f16x2_to_f32x2(w[k * (VPW / 2) + j]);
+                t[2 * j] = quant_t(f.x, rs, near);
+                t[2 * j + 1] = quant_t(f.y, rs, near);
+            }
+            if (near && s != 0.f) {  // rare: the values within 2^-14 of a half-integer, by division
+#pragma unroll
+                for (int j = 0; j < VPW / 2; ++j) {
+                    const float2 f = f16x2_to_f32x2(w[k * (VPW / 2) + j]);
+                    const float v2[2] = {f.x, f.y};
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float y = v2[e] * rs;
+                        if (!(fabsf(y - (__uint_as_float(t[2 * j + e]) - kRoundMagic)) <= kNearHalf))
+                            t[2 * j + e] = quant_div(v2[e], s, kQi);
+                    }
+                }
+            }
+            if (FMT == INT4) {  // channel 2j: low nibble of byte j
+                uint32_t b[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) b[j] = (t[2 * j] & 0xFu) | ((t[2 * j + 1] & 0xFu) << 4);
+                o[k] = prmt(prmt(b[0], b[1], 0x0040u), prmt(b[2], b[3], 0x0040u), 0x5410u);
+            } else {  // byte j: the low byte of t
+                o[k] = prmt(prmt(t[0], t[1], 0x0040u), prmt(t[2], t[3], 0x0040u), 0x5410u);
+            }
         }
+        if (FMT == INT4) o[2] = o[3] = 0u;
         return s;
     };
     auto store = [&](uint32_t u, const Unit& x) {

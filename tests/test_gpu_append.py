@@ -207,7 +207,10 @@ def test_append_rounding_ties_and_bulk_rows_bit_exact(fmt, group):
         nb = near.view(torch.int16)
         nb[1:] += 1                                # the next fp16 value away from zero
         ties.append(near.double())
+    sub = torch.randn(D, dtype=torch.float64, generator=torch.Generator().manual_seed(5)) * 2e-6
+    ties.append(sub)                               # a row of fp16 subnormals (a tiny scale)
     t = torch.stack(ties).to(torch.float16)        # [rows][D]
+    assert (t[-1].abs() < 6.1e-5).all() and t[-1].any()
     kt = t[:, None, :].repeat(1, Hkv, 1)
     assert (kt.double()[:, 0, 1:1 + 10] / 2.0 ** -3).fmod(1).abs().ne(0).any()   # not all integers
     g = torch.Generator().manual_seed(len(fmt) + group)
