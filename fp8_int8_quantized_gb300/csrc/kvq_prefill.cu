@@ -513,20 +513,34 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
         int blk_k[kVecsPerThread];                  // physical block of each row of the tile whose K codes
                                                     // are loaded next, -1 = zeros
         int blk_v[kVecsPerThread];                  // the same for the tile whose V codes are loaded next
-        auto fetch_ids = [&](int j, int (&blk)[kVecsPerThread]) {
+        // Block ids are loaded one iteration before they are used (fetch_raw),
+        // and checked at that use (check_ids): the loads of a tile's codes then
+        // wait on one global latency, not on the id load and the code load in
+        // series.  kNoRow marks a row past the tile's last position.
+        constexpr int kNoRow = (int)0x80000000;
+        auto fetch_raw = [&](int j, int (&raw)[kVecsPerThread]) {
 #pragma unroll
             for (int it = 0; it < kVecsPerThread; ++it) {
                 const int t = j * kKvTile + row_of(it);
-                int id = -1;
-                if (has(it) && j < nkv && t <= p_max) {
-                    id = bt[t >> lbs];
-                    if (id < 0 || id >= a.num_blocks) {
-                        record_error(a.err, DEV_ERR_RANGE, id);
-                        id = -1;
-                    }
+                raw[it] = (has(it) && j < nkv && t <= p_max) ? __ldg(bt + (t >> lbs)) : kNoRow;
+            }
+        };
+        auto check_ids = [&](int (&blk)[kVecsPerThread]) {
+#pragma unroll
+            for (int it = 0; it < kVecsPerThread; ++it) {
+                int id = blk[it];
+                if (id == kNoRow) {
+                    id = -1;
+                } else if (id < 0 || id >= a.num_blocks) {
+                    record_error(a.err, DEV_ERR_RANGE, id);
+                    id = -1;
                 }
                 blk[it] = id;
             }
+        };
+        auto fetch_ids = [&](int j, int (&blk)[kVecsPerThread]) {
+            fetch_raw(j, blk);
+            check_ids(blk);
         };
         // GRP: a code vector's two 16-value halves (one for INT8) each lie in one
         // scale group (groups are at least 16 channels wide and 16-aligned)
@@ -647,12 +661,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
             if (kRowScaled) mbar_arrive(&bars[B_SC0 + (t & 3)]);
             return true;
         };
+        int blk_n[kVecsPerThread];                  // raw block ids of the tile after blk_k's
         fetch_ids(0, blk_k);
         load_codes(a.k_codes, a.k_scales, 0, kc, kg, blk_k);
         load_codes(a.v_codes, a.v_scales, 0, vc, vg, blk_k);
         if (kRowScaled) load_scales(0, ks, vs);
         put_k(0);
         fetch_ids(1, blk_k);
+        fetch_raw(2, blk_n);
         load_codes(a.k_codes, a.k_scales, 1, kc, kg, blk_k);
         if (kRowScaled) load_scales(1, ks, vs);
         for (int j = 0; j < nkv; ++j) {
@@ -661,8 +677,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
             if (more) {
                 if (!put_k(j + 1)) break;
 #pragma unroll
-                for (int it = 0; it < kVecsPerThread; ++it) blk_v[it] = blk_k[it];   // tile j+1
-                fetch_ids(j + 2, blk_k);
+                for (int it = 0; it < kVecsPerThread; ++it) {
+                    blk_v[it] = blk_k[it];   // tile j+1
+                    blk_k[it] = blk_n[it];   // tile j+2, loaded an iteration ago
+                }
+                check_ids(blk_k);
+                fetch_raw(j + 3, blk_n);
                 load_codes(a.k_codes, a.k_scales, j + 2, kc, kg, blk_k);
                 if (kRowScaled) load_scales(j + 2, ks, vs);
             }
