@@ -313,6 +313,15 @@ def dequant(cache: KVCache, slots: torch.Tensor, scale: torch.Tensor | None = No
     return ok, ov
 
 
+def encode_fp8(x: torch.Tensor, fmt: int, stream=None) -> torch.Tensor:
+    """kvq_encode_fp8: uint8 FP8 codes (``fmt`` E4M3 or E5M2) of a flat fp32 tensor."""
+    n = x.numel()
+    codes = torch.empty(n, dtype=torch.uint8, device=x.device)
+    st = lib().kvq_encode_fp8(_dev(x, torch.float32, "x"), codes.data_ptr(), n, fmt, _stream(stream))
+    _check(st, "kvq_encode_fp8")
+    return codes
+
+
 def set_decode_kernel(kind: int) -> int:
     prev = lib().kvq_set_decode_kernel(int(kind))
     if prev < 0:

@@ -68,4 +68,5 @@ def test_encoder_tail_and_arguments():
     want = oracle.fp8_encode(oracle.E4M3, x.cpu().numpy()[:999])
     assert np.array_equal(codes.cpu().numpy()[:999], want)
     assert (codes.cpu().numpy()[999:] == 0).all()
+    assert np.array_equal(kvq.encode_fp8(x[:999].contiguous(), oracle.E4M3).cpu().numpy(), want)
     assert lib.kvq_encode_fp8(x.data_ptr(), codes.data_ptr(), 16, 3, None) == 1        # INT8 is not FP8
