@@ -258,6 +258,7 @@ enum Bar : int {
     B_PFULL00, B_PFULL01,  // softmax of query tile 0 -> MMA: P written over S (128)
     B_PFULL10, B_PFULL11,  // ... of query tile 1
     B_SC0, B_SC1, B_SC2, B_SC3,  // dequant -> softmax: INT8 / INT4 row scales of the tile
+    B_QREADY,              // softmax -> MMA: both query tiles in shared memory (256)
     B_OFINAL,              // every MMA done (commit)
     kNumBars
 };
@@ -392,7 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
             const bool by_dq = (i >= B_KFULL0 && i <= B_VFULL1) || (i >= B_SC0 && i <= B_SC3);
             const bool by_sm = i >= B_PFULL00 && i <= B_PFULL11;
             const bool by_mma = (i >= B_KFREE0 && i <= B_VFREE1) || i == B_OFINAL;   // every MMA warp commits
-            mbar_init(&bars[i], by_dq ? (uint32_t)kDqThreads : by_sm ? 128u : by_mma ? (uint32_t)kMmaWarps : 1u);
+            mbar_init(&bars[i], by_dq ? (uint32_t)kDqThreads : by_sm ? 128u : by_mma ? (uint32_t)kMmaWarps
+                                 : i == B_QREADY ? 256u : 1u);
         }
         *abort = 0;
         fence_barrier_init();
@@ -427,6 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
         const uint64_t dv0 = smem_desc(sbase + L::kV, L::kBlkKV, 1024);
         auto issue_qk = [&](int j) {
             const int sl = j & 1;
+            if (j == 0 && !wait_or_abort(&bars[B_QREADY], 0, abort, a.err)) return false;
             if (!wait_or_abort(&bars[B_KFULL0 + sl], (j >> 1) & 1, abort, a.err)) return false;
             tc_fence_after();
             const uint64_t dk = dk0 + ((sl * L::kTileKV) >> 4);
@@ -486,17 +489,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
         // ------------------------------------------------------ dequant ----
         const int dt = tid - 32 * (kMmaWarp + 1);   // 0 .. kDqThreads - 1
         const int32_t* bt = a.block_tables + (size_t)b * a.max_blocks_per_seq;
-        // query tiles: row r of tile g = (query (2 * pair + g) * TQ + r / G, head kvh * G + r % G)
-        for (int e = dt; e < 2 * kRows * kChunks; e += kDqThreads) {
-            const int g = e / (kRows * kChunks), r = (e / kChunks) % kRows, c = e % kChunks;
-            const int qi = r / G;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (r < TQ * G && qi < (g ? nq[1] : nq[0])) {
-                const size_t row = (size_t)(q0 + (2 * pair + g) * TQ + qi) * Hq + kvh * G + r % G;
-                v = *reinterpret_cast<const uint4*>(a.q + row * D + c * 8);
-            }
-            st_shared_v4(sbase + L::kQ + g * L::kTileQ + tile_off(L::kBlkQ, r, c), v);
-        }
         // Thread dt handles vectors e = it * kDqThreads + dt (e below
         // kTileVecs): the 16 codes c16 of token row u, with rows varying
         // fastest across groups of 8 lanes: each 8-lane group stores one 16-byte
@@ -701,6 +693,25 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
         const bool rv = r < TQ * G && r / G < nq_g;
         const int pos = rv ? (g ? p_first[1] : p_first[0]) + r / G : (g ? p_last[1] : p_last[0]);
         const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16) + g * kColsPerTile;
+        {
+            // stage query row r of tile g = (query (2 * pair + g) * TQ + r / G,
+            // head kvh * G + r % G) into the 128-byte-swizzled A operand (zeros
+            // for rows without a query), while the dequant warps fetch the first
+            // K / V tiles
+            const uint4* src = reinterpret_cast<const uint4*>(
+                a.q + ((size_t)(q0 + (2 * pair + g) * TQ + (rv ? r / G : 0)) * Hq + kvh * G + r % G) * D);
+#pragma unroll
+            for (int c0 = 0; c0 < kChunks; c0 += 8) {   // eight 16-byte loads in flight at a time
+                uint4 v[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) v[c] = rv ? src[c0 + c] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    st_shared_v4(sbase + L::kQ + g * L::kTileQ + tile_off(L::kBlkQ, r, c0 + c), v[c]);
+            }
+            fence_proxy_async();
+            mbar_arrive(&bars[B_QREADY]);
+        }
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < nkv_me && ok; ++j) {
