@@ -419,8 +419,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const PrefillParam
         // (both query tiles against K_j, into S buffer j % 2 of each tile's
         // tensor-memory columns), then O_0 += P_0,j-1 V_j-1 and O_1 += P_1,j-1
         // V_j-1: S of tile j runs while the softmax of tile j-1 works on the
-        // other buffers.  A query tile takes no MMA for KV tiles past its last
-        // position.  The whole warp runs this code; elect.sync picks the issuing
+        // other buffers.  S_j overwrites the buffer that held P_j-2, which
+        // O += P_j-2 V_j-2 (issued just before, by this thread) reads: the
+        // tensor cores run one thread's products in issue order, so that read
+        // precedes the write (a wait for its completion here would stall the
+        // issue by a commit-to-waiter round trip, ~300-450 cycles, every tile).
+        // A query tile takes no MMA for KV tiles past its last position.  The whole warp runs this code; elect.sync picks the issuing
         // lane, so descriptors stay warp-uniform.  Descriptors of the first
         // K-step of each operand tile; every other K-step adds a constant to the
         // 14-bit start-address field (addresses stay below 2^18 bytes, so the
