@@ -890,6 +890,306 @@ struct MmaConsumer {
     }
 };
 
+// ------------------------------------------------ MMA, grouped INT8 --
+
+// INT8 with one scale per group of GS = D / NG channels (NG = 2 or 4, GS at
+// least 32), for kv-heads whose q-heads x groups exceed 8: one pass over the
+// cache serves all G <= 8 q-heads.  The operand rows are the q-heads (as in the
+// per-row consumer) and the group scales are applied per contraction slice
+// instead of per operand row:
+//   QK: each k16 slice of S^T = Q K^T lies inside one group (slice j covers
+//   group j / (GS / 16)); within group gi lane c holds the GS / 4 contiguous
+//   channels at GS * gi + (GS / 4) * c, so its K codes are one 8- or 16-byte
+//   load per token and group.  Each group's slices accumulate separately; a
+//   logit is sum_g (S_g - 128 * 2^-24 * sum_g(q)) * s_K[t][g] (the per-row
+//   consumer's offset and unit, per group).
+//   PV: each m16 tile of out^T = V^T P^T (16 head dims) lies inside one group;
+//   lane g holds the GS / 8 contiguous dims at GS * gi + (GS / 8) * g of each
+//   group, so the operand building is the per-row consumer's, word for word,
+//   and the m-tiles of group gi take the weights P * s_V[t][gi] (fp16 hi and
+//   residual, two MMAs per m-tile).
+// The 16-row multi-pass alternative read the cache once per 16 (q-head, group)
+// pairs: twice for Llama-3-70B's G = 8 with 32-channel groups.
+template <int D, int NG>
+struct MmaGroupConsumer {
+    static constexpr int GS = D / NG;        // channels per scale group
+    static constexpr int SPG = GS / 16;      // k16 slices (and m16 tiles) per group
+    static constexpr int KS = D / 16;        // k-slices of QK^T
+    static constexpr int MT = D / 16;        // m-tiles of PV
+    static constexpr int KB = GS / 4;        // K bytes of one lane per token and group
+    static constexpr int VB = GS / 8;        // V bytes of one lane per token and group
+    static constexpr int VW = D / 32;        // V words of one lane per token (VB / 4 per group)
+    static_assert(GS >= 32 && GS % 32 == 0, "groups of at least 32 channels");
+    static constexpr int kMinCtas = kMinBlocks;
+    static constexpr int kWarps = 6;
+    static constexpr float kUnit = 5.9604644775390625e-08f;   // operand value of one code step (2^-24)
+    static constexpr float kBias = 128.f * kUnit;             // K operand - code * kUnit
+    static constexpr float kLogF = 6.f;                        // weights carry 2^6 (cancels in acc / l)
+    uint32_t qa[2 * KS];   // slice j: {q at the lane's dims 4s, 4s+1 | 4s+2, 4s+3 of group j / SPG}, s = j % SPG
+    float acc[MT][4];
+    float m, l;
+    float qsum[NG];        // per group: sum of this lane's row's query values over the group
+    int lane, g, c, G;
+    float qk_scale;
+    uint32_t k_off[NG];    // row g's K chunk of each group (the 128-byte swizzle folded in)
+    uint32_t v_off[VW][2]; // word w of rows 2c and 2c+1 (rows 8+2c, 9+2c are 8 rows further)
+
+    // byte offset of byte o of row r inside a stage tile
+    __device__ __forceinline__ static uint32_t off(int r, int o) {
+        if (D == 128) return r * 128 + (o ^ ((r & 7) << 4));
+        return r * D + o;
+    }
+    // byte offset, in a row, of V word w of lane g: group w / (VB / 4), word w % (VB / 4) of its chunk
+    __device__ __forceinline__ static int vword(int g_, int w) {
+        return GS * (w / (VB / 4)) + VB * g_ + 4 * (w % (VB / 4));
+    }
+
+    __device__ void init(int G_, float qks, int) {
+        lane = threadIdx.x & 31;
+        g = lane >> 2;
+        c = lane & 3;
+        G = G_;
+        qk_scale = qks;
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi) k_off[gi] = off(g, GS * gi + KB * c);
+#pragma unroll
+        for (int w = 0; w < VW; ++w) {
+            v_off[w][0] = off(2 * c, vword(g, w));
+            v_off[w][1] = off(2 * c + 1, vword(g, w));
+        }
+    }
+    // q: the kv-head's G query rows (shared-memory copy)
+    __device__ void set_q(const uint16_t* q) {
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi) {
+            uint32_t w[KB / 2];   // this lane's GS / 4 query values of group gi, as f16 pairs
+            if (g < G) {
+                const uint32_t* src = reinterpret_cast<const uint32_t*>(q + g * D + GS * gi + KB * c);
+#pragma unroll
+                for (int i = 0; i < KB / 2; ++i) w[i] = src[i];
+            } else {
+#pragma unroll
+                for (int i = 0; i < KB / 2; ++i) w[i] = 0u;
+            }
+            float sq = 0.f;
+#pragma unroll
+            for (int i = 0; i < KB / 2; ++i) {
+                qa[2 * SPG * gi + i] = w[i];
+                const float2 v = f16x2_to_f32x2(w[i]);
+                sq += v.x + v.y;
+            }
+            sq += __shfl_xor_sync(0xFFFFFFFFu, sq, 1);
+            sq += __shfl_xor_sync(0xFFFFFFFFu, sq, 2);
+            qsum[gi] = sq;
+        }
+    }
+    __device__ void reset() {
+        m = -INFINITY;
+        l = 0.f;
+#pragma unroll
+        for (int i = 0; i < MT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    }
+
+    // QK^T of one 16-row box: this thread's logits of q-head g, box tokens 2c,
+    // 2c+1, 8+2c, 9+2c (already scaled, masked past `valid`).
+    __device__ __forceinline__ void qk_box(uint32_t kt, uint32_t sk, int valid, float (&z)[4]) {
+        const float ks = qk_scale / kUnit;
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+            float sacc[NG][4];
+#pragma unroll
+            for (int gi = 0; gi < NG; ++gi) {
+                sacc[gi][0] = sacc[gi][1] = sacc[gi][2] = sacc[gi][3] = 0.f;
+                uint32_t kw[KB / 4];
+                const uint32_t a = kt + hb * 8 * D + k_off[gi];
+                if (KB == 16) {
+                    const uint4 x = lds128(a);
+                    kw[0] = x.x; kw[KB / 4 > 1 ? 1 : 0] = x.y; kw[KB / 4 > 2 ? 2 : 0] = x.z; kw[KB / 4 > 3 ? 3 : 0] = x.w;
+                } else {
+                    const uint2 x = lds64(a);
+                    kw[0] = x.x; kw[KB / 4 > 1 ? 1 : 0] = x.y;
+                }
+#pragma unroll
+                for (int s = 0; s < SPG; ++s) {
+                    const uint32_t x = kw[s] ^ 0x80808080u;   // code + 128 as an unsigned byte
+                    const uint32_t b0 = prmt(x, 0u, 0x4140u), b1 = prmt(x, 0u, 0x4342u);
+                    mma_16816(sacc[gi], qa[2 * (SPG * gi + s)], 0u, qa[2 * (SPG * gi + s) + 1], 0u, b0, b1);
+                }
+            }
+            // tokens 8 hb + 2c, 8 hb + 2c + 1: scales [token][NG]
+            const uint32_t s0 = sk + 4 * NG * (8 * hb + 2 * c);
+            float k0[NG], k1[NG];
+            if (NG == 4) {
+                const uint4 x0 = lds128(s0), x1 = lds128(s0 + 16);
+                k0[0] = __uint_as_float(x0.x); k0[1 % NG] = __uint_as_float(x0.y);
+                k0[2 % NG] = __uint_as_float(x0.z); k0[3 % NG] = __uint_as_float(x0.w);
+                k1[0] = __uint_as_float(x1.x); k1[1 % NG] = __uint_as_float(x1.y);
+                k1[2 % NG] = __uint_as_float(x1.z); k1[3 % NG] = __uint_as_float(x1.w);
+            } else {
+                const uint4 x = lds128(s0);
+                k0[0] = __uint_as_float(x.x); k0[1 % NG] = __uint_as_float(x.y);
+                k1[0] = __uint_as_float(x.z); k1[1 % NG] = __uint_as_float(x.w);
+            }
+            float z0 = 0.f, z1 = 0.f;
+#pragma unroll
+            for (int gi = 0; gi < NG; ++gi) {
+                const float corr = kBias * qsum[gi];
+                z0 = fmaf(sacc[gi][0] - corr, k0[gi], z0);
+                z1 = fmaf(sacc[gi][1] - corr, k1[gi], z1);
+            }
+            z[2 * hb] = z0 * ks;
+            z[2 * hb + 1] = z1 * ks;
+        }
+        if (valid < kBox) {
+            if (2 * c >= valid) z[0] = -INFINITY;
+            if (2 * c + 1 >= valid) z[1] = -INFINITY;
+            if (8 + 2 * c >= valid) z[2] = -INFINITY;
+            if (9 + 2 * c >= valid) z[3] = -INFINITY;
+        }
+    }
+
+    // P (fp16 hi + residual) of one box as the B operand of PV, k = token,
+    // n = q-head g
+    __device__ __forceinline__ static void p_frags(const float (&p)[4], uint32_t& pb0, uint32_t& pb1, uint32_t& pl0,
+                                                   uint32_t& pl1) {
+        pb0 = pack_f16x2(p[0], p[1]);
+        pb1 = pack_f16x2(p[2], p[3]);
+        const float2 h01 = f16x2_to_f32x2(pb0), h23 = f16x2_to_f32x2(pb1);
+        pl0 = pack_f16x2(p[0] - h01.x, p[1] - h01.y);
+        pl1 = pack_f16x2(p[2] - h23.x, p[3] - h23.y);
+    }
+
+    // out^T += V^T P_g^T for one box: p = weights of box tokens 2c, 2c+1, 8+2c,
+    // 9+2c; sv = their V scales per group
+    __device__ __forceinline__ void pv_box(uint32_t vt, int valid, const float (&p)[4], const float (&sv)[4][NG]) {
+        uint32_t v0[VW], v1[VW], v2[VW], v3[VW];
+#pragma unroll
+        for (int w = 0; w < VW; ++w) {
+            v0[w] = lds32(vt + v_off[w][0]);
+            v1[w] = lds32(vt + v_off[w][1]);
+            v2[w] = lds32(vt + v_off[w][0] + 8 * D);
+            v3[w] = lds32(vt + v_off[w][1] + 8 * D);
+        }
+        if (valid < kBox) {  // rows past the context may hold NaN codes: zero them
+#pragma unroll
+            for (int w = 0; w < VW; ++w) {
+                if (2 * c >= valid) v0[w] = 0u;
+                if (2 * c + 1 >= valid) v1[w] = 0u;
+                if (8 + 2 * c >= valid) v2[w] = 0u;
+                if (9 + 2 * c >= valid) v3[w] = 0u;
+            }
+        }
+#pragma unroll
+        for (int w = 0; w < VW; ++w) {  // code + 128 as unsigned bytes
+            v0[w] ^= 0x80808080u; v1[w] ^= 0x80808080u; v2[w] ^= 0x80808080u; v3[w] ^= 0x80808080u;
+        }
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi) {
+            float pg[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) pg[e] = p[e] != 0.f ? p[e] * sv[e][gi] : 0.f;
+            uint32_t pb0, pb1, pl0, pl1;
+            p_frags(pg, pb0, pb1, pl0, pl1);
+#pragma unroll
+            for (int mm = 0; mm < SPG; ++mm) {
+                const int i = SPG * gi + mm;   // m-tile; its dims are 2 mm, 2 mm + 1 of the lane's group chunk
+                const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
+                const uint32_t x01 = prmt(v0[i >> 1], v1[i >> 1], sel);
+                const uint32_t x23 = prmt(v2[i >> 1], v3[i >> 1], sel);
+                // fp16 subnormals (code + 128) * 2^-24, less 128 * 2^-24 (exact)
+                const uint32_t a0 = hsub2_exact(prmt(x01, 0u, 0x4140u), 0x00800080u);
+                const uint32_t a1 = hsub2_exact(prmt(x01, 0u, 0x4342u), 0x00800080u);
+                const uint32_t a2 = hsub2_exact(prmt(x23, 0u, 0x4140u), 0x00800080u);
+                const uint32_t a3 = hsub2_exact(prmt(x23, 0u, 0x4342u), 0x00800080u);
+                mma_16816(acc[i], a0, a1, a2, a3, pb0, pb1);
+                mma_16816(acc[i], a0, a1, a2, a3, pl0, pl1);
+            }
+        }
+    }
+
+    __device__ __forceinline__ void v_scales(uint32_t sv0, float (&sv)[4][NG]) {
+        // tokens 2c, 2c+1, 8+2c, 9+2c of the box: scales [token][NG]
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const uint32_t a = sv0 + 4 * NG * (2 * c + (e & 1) + 8 * (e >> 1));
+            if (NG == 4) {
+                const uint4 x = lds128(a);
+                sv[e][0] = __uint_as_float(x.x); sv[e][1 % NG] = __uint_as_float(x.y);
+                sv[e][2 % NG] = __uint_as_float(x.z); sv[e][3 % NG] = __uint_as_float(x.w);
+            } else {
+                const uint2 x = lds64(a);
+                sv[e][0] = __uint_as_float(x.x); sv[e][1 % NG] = __uint_as_float(x.y);
+            }
+        }
+    }
+
+    __device__ void tile(const Tile& cx) {
+        float z0[4], z1[4];
+        qk_box(cx.k, cx.s, cx.valid, z0);
+        qk_box(cx.k + kBox * D, cx.s + 4 * kBox * NG, cx.valid - kBox, z1);
+        float mx = fmaxf(fmaxf(fmaxf(z0[0], z0[1]), fmaxf(z0[2], z0[3])), fmaxf(fmaxf(z1[0], z1[1]), fmaxf(z1[2], z1[3])));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+        const float mn = fmaxf(m, mx);
+        float alpha = 1.f, p0[4], p1[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) p0[e] = p1[e] = 0.f;
+        if (mn != -INFINITY) {
+            alpha = fast_exp2(m - mn);
+            const float mb = mn - kLogF;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                p0[e] = fast_exp2(z0[e] - mb);
+                p1[e] = fast_exp2(z1[e] - mb);
+            }
+        }
+        m = mn;
+        l = l * alpha + (((p0[0] + p0[1]) + (p0[2] + p0[3])) + ((p1[0] + p1[1]) + (p1[2] + p1[3])));
+        // rescale the accumulators: columns 2c and 2c+1 are q-heads 2c and 2c+1
+        if (__any_sync(0xFFFFFFFFu, alpha != 1.f)) {
+            const float a0 = __shfl_sync(0xFFFFFFFFu, alpha, 8 * c);
+            const float a1 = __shfl_sync(0xFFFFFFFFu, alpha, 8 * c + 4);
+#pragma unroll
+            for (int i = 0; i < MT; ++i) {
+                acc[i][0] *= a0; acc[i][1] *= a1; acc[i][2] *= a0; acc[i][3] *= a1;
+            }
+        }
+        const uint32_t sv = cx.s + 4 * kTile * NG;
+        float s0[4][NG];
+        v_scales(sv, s0);
+        pv_box(cx.v, cx.valid, p0, s0);
+        v_scales(sv + 4 * kBox * NG, s0);
+        pv_box(cx.v + kBox * D, cx.valid - kBox, p1, s0);
+    }
+
+    __device__ void flush(const Flush& f) {
+        float lq = l;
+        lq += __shfl_xor_sync(0xFFFFFFFFu, lq, 1);
+        lq += __shfl_xor_sync(0xFFFFFFFFu, lq, 2);
+        if (c == 0 && g < G) f.ml[slot_index(f.hq0 + g, f.nch, f.ch, f.half)] = make_float2(m, lq);
+        // acc[i][e] (acc[i][2 + e]) = out[q-head 2c + e][dim 2 mm (+1) of the lane's chunk of group i / SPG]
+        const float so = f.s_out / kUnit;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int h = 2 * c + e;
+            if (h >= G) continue;
+            float* dst = f.acc + slot_index(f.hq0 + h, f.nch, f.ch, f.half) * D + VB * g;
+#pragma unroll
+            for (int gi = 0; gi < NG; ++gi) {
+#pragma unroll
+                for (int mm = 0; mm < SPG; mm += 2) {
+                    const int i = SPG * gi + mm;
+                    *reinterpret_cast<float4*>(dst + GS * gi + 2 * mm) =
+                        make_float4(acc[i][e] * so, acc[i][2 + e] * so, acc[i + 1][e] * so, acc[i + 1][2 + e] * so);
+                }
+            }
+        }
+    }
+    __device__ void flush_empty(const Flush& f) {
+        if (lane < G) f.ml[slot_index(f.hq0 + lane, f.nch, f.ch, f.half)] = make_float2(-INFINITY, 0.f);
+    }
+};
+
 // ------------------------------------------------------ append in decode --
 
 __device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
@@ -1447,6 +1747,12 @@ cudaError_t launch_fmt_d(const CUtensorMap& tk, const CUtensorMap& tv, const Dec
         const int ng = a.cache.ngroups;
         if (G * ng <= 8) {
             e = launch_stream<FMT, D, MmaConsumer<FMT, D>>(tk, tv, p, s);
+        } else if (FMT == INT8 && D / ng >= 32) {  // one pass, a scale group per contraction slice
+            e = cudaErrorInvalidValue;
+            if constexpr (FMT == INT8) {
+                if (ng == 2) e = launch_stream<FMT, D, MmaGroupConsumer<D, 2>>(tk, tv, p, s);
+                else if constexpr (D >= 128) e = launch_stream<FMT, D, MmaGroupConsumer<D, 4>>(tk, tv, p, s);
+            }
         } else if constexpr (FMT == INT8 || FMT == INT4) {  // groups: only these formats have them
             const int per = 16 / ng;
             for (int h = 0; h < G && e == cudaSuccess; h += per) {

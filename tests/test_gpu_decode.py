@@ -53,9 +53,12 @@ CASES = [
     ("int8", 3, 8, 1, 64, 16, [300, 1, 77], 64),
     ("int8", 2, 3, 3, 64, 16, [200, 45], 16),
     ("int4", 2, 4, 1, 128, 16, [96, 1000], 64),
-    # more than 8 (q-head, group) operand rows: the 16-row consumer, one pass up
-    # to 16 rows, several launches over the same tiles beyond
+    # more than 8 (q-head, group) operand rows: INT8 with groups of 32 or more
+    # channels takes the grouped consumer (one pass, a scale group per
+    # contraction slice); INT4 and 16-channel INT8 groups the 16-row consumer,
+    # one pass up to 16 rows, several launches over the same tiles beyond
     ("int8", 2, 16, 2, 128, 32, [500, 64], 32),
+    ("int8", 2, 48, 8, 64, 16, [300, 90], 32),
     ("int4", 2, 8, 1, 128, 16, [300, 33], 64),
     ("int8", 3, 8, 2, 64, 16, [200, 17, 1], 16),
     ("int8", 2, 24, 8, 128, 16, [333, 1000], 32),
@@ -98,6 +101,8 @@ SPLIT_CASES = [
     ("int4", 4, 16, 2, 128, 16, [3000, 1500, 64, 4097], 0),
     ("int8", 4, 8, 4, 128, 16, [3000, 1500, 64, 4097], 32),
     ("int4", 4, 8, 8, 128, 16, [3000, 1500, 64, 4097], 32),
+    ("int8", 4, 32, 4, 128, 16, [3000, 1500, 64, 4097], 32),
+    ("int8", 4, 20, 4, 128, 16, [3000, 1500, 64, 4097], 64),
 ]
 
 

@@ -89,6 +89,7 @@ CASES = [
     ("int4", 3, 8, 2, 64, 16, [129, 0, 256], 32),
     ("int8", 3, 3, 3, 64, 16, [200, 45, 16], 16),
     ("int8", 3, 16, 2, 128, 32, [500, 1, 64], 32),
+    ("int8", 3, 40, 8, 128, 16, [300, 1, 77], 64),
     ("int4", 2, 8, 1, 64, 16, [129, 48], 16),
 ]
 
