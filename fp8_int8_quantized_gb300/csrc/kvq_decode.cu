@@ -55,6 +55,9 @@
 #ifndef KVQ_MIN_BLOCKS
 #define KVQ_MIN_BLOCKS 2
 #endif
+#ifndef KVQ_GA_WARPS
+#define KVQ_GA_WARPS 4
+#endif
 #ifndef KVQ_INT4_WARPS
 #define KVQ_INT4_WARPS 8
 #endif
@@ -157,6 +160,15 @@ __device__ __forceinline__ uint32_t lds32(uint32_t a) {
     uint32_t r;
     asm volatile("ld.shared.b32 %0, [%1];" : "=r"(r) : "r"(a));
     return r;
+}
+// Four 8x8 matrices of 16-bit elements: lane t gives the row address of row
+// t % 8 of matrix t / 8; register m of lane t receives elements 2 (t % 4),
+// 2 (t % 4) + 1 of row t / 4 of matrix m (here: bytes 4 (t % 4) .. + 3 of a
+// 16-byte row segment).
+__device__ __forceinline__ void ldsm_x4(uint32_t a, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(a));
 }
 __device__ __forceinline__ float2 __uint_as_float2(uint2 v) { return make_float2(__uint_as_float(v.x), __uint_as_float(v.y)); }
 __device__ __forceinline__ float ldsf(uint32_t a) {
@@ -897,10 +909,12 @@ struct MmaConsumer {
 // cache serves all G <= 8 q-heads.  The operand rows are the q-heads (as in the
 // per-row consumer) and the group scales are applied per contraction slice
 // instead of per operand row:
-//   QK: each k16 slice of S^T = Q K^T lies inside one group (slice j covers
-//   group j / (GS / 16)); within group gi lane c holds the GS / 4 contiguous
-//   channels at GS * gi + (GS / 4) * c, so its K codes are one 8- or 16-byte
-//   load per token and group.  Each group's slices accumulate separately; a
+//   QK: k16 slice j of S^T = Q K^T is channels 16 j .. 16 j + 15, inside group
+//   j / (GS / 16); lane c holds channels 16 j + 4c .. 16 j + 4c + 3, which an
+//   ldmatrix of the swizzled 16-byte row segments delivers four slices at a
+//   time (8-byte loads of a lane's group chunk met 2-way bank conflicts: rows
+//   g and g ^ 1 share banks under the 128-byte swizzle).  Each group's slices
+//   accumulate separately; a
 //   logit is sum_g (S_g - 128 * 2^-24 * sum_g(q)) * s_K[t][g] (the per-row
 //   consumer's offset and unit, per group).
 //   PV: each m16 tile of out^T = V^T P^T (16 head dims) lies inside one group;
@@ -916,22 +930,22 @@ struct MmaGroupConsumer {
     static constexpr int SPG = GS / 16;      // k16 slices (and m16 tiles) per group
     static constexpr int KS = D / 16;        // k-slices of QK^T
     static constexpr int MT = D / 16;        // m-tiles of PV
-    static constexpr int KB = GS / 4;        // K bytes of one lane per token and group
+    static constexpr int NLD = KS / 4;       // ldmatrix.x4 per half box (four slices each)
     static constexpr int VB = GS / 8;        // V bytes of one lane per token and group
     static constexpr int VW = D / 32;        // V words of one lane per token (VB / 4 per group)
     static_assert(GS >= 32 && GS % 32 == 0, "groups of at least 32 channels");
     static constexpr int kMinCtas = kMinBlocks;
-    static constexpr int kWarps = 6;
+    static constexpr int kWarps = KVQ_GA_WARPS;
     static constexpr float kUnit = 5.9604644775390625e-08f;   // operand value of one code step (2^-24)
     static constexpr float kBias = 128.f * kUnit;             // K operand - code * kUnit
     static constexpr float kLogF = 6.f;                        // weights carry 2^6 (cancels in acc / l)
-    uint32_t qa[2 * KS];   // slice j: {q at the lane's dims 4s, 4s+1 | 4s+2, 4s+3 of group j / SPG}, s = j % SPG
+    uint32_t qa[2 * KS];   // slice j: {q[16j + 4c], q[16j + 4c + 1] | q[16j + 4c + 2], q[16j + 4c + 3]}
     float acc[MT][4];
     float m, l;
     float qsum[NG];        // per group: sum of this lane's row's query values over the group
     int lane, g, c, G;
     float qk_scale;
-    uint32_t k_off[NG];    // row g's K chunk of each group (the 128-byte swizzle folded in)
+    uint32_t k_off[NLD];   // this lane's row address for ldmatrix x (slices 4x .. 4x + 3), swizzle folded in
     uint32_t v_off[VW][2]; // word w of rows 2c and 2c+1 (rows 8+2c, 9+2c are 8 rows further)
 
     // byte offset of byte o of row r inside a stage tile
@@ -950,8 +964,9 @@ struct MmaGroupConsumer {
         c = lane & 3;
         G = G_;
         qk_scale = qks;
+        // ldmatrix: lane t gives row t % 8 of matrix t / 8 (slice 4x + t / 8)
 #pragma unroll
-        for (int gi = 0; gi < NG; ++gi) k_off[gi] = off(g, GS * gi + KB * c);
+        for (int x = 0; x < NLD; ++x) k_off[x] = off(lane & 7, 16 * (4 * x + (lane >> 3)));
 #pragma unroll
         for (int w = 0; w < VW; ++w) {
             v_off[w][0] = off(2 * c, vword(g, w));
@@ -962,21 +977,16 @@ struct MmaGroupConsumer {
     __device__ void set_q(const uint16_t* q) {
 #pragma unroll
         for (int gi = 0; gi < NG; ++gi) {
-            uint32_t w[KB / 2];   // this lane's GS / 4 query values of group gi, as f16 pairs
-            if (g < G) {
-                const uint32_t* src = reinterpret_cast<const uint32_t*>(q + g * D + GS * gi + KB * c);
-#pragma unroll
-                for (int i = 0; i < KB / 2; ++i) w[i] = src[i];
-            } else {
-#pragma unroll
-                for (int i = 0; i < KB / 2; ++i) w[i] = 0u;
-            }
             float sq = 0.f;
 #pragma unroll
-            for (int i = 0; i < KB / 2; ++i) {
-                qa[2 * SPG * gi + i] = w[i];
-                const float2 v = f16x2_to_f32x2(w[i]);
-                sq += v.x + v.y;
+            for (int s = 0; s < SPG; ++s) {
+                const int j = SPG * gi + s;
+                uint2 w = make_uint2(0u, 0u);
+                if (g < G) w = *reinterpret_cast<const uint2*>(q + g * D + 16 * j + 4 * c);
+                qa[2 * j] = w.x;
+                qa[2 * j + 1] = w.y;
+                const float2 v0 = f16x2_to_f32x2(w.x), v1 = f16x2_to_f32x2(w.y);
+                sq += (v0.x + v0.y) + (v1.x + v1.y);
             }
             sq += __shfl_xor_sync(0xFFFFFFFFu, sq, 1);
             sq += __shfl_xor_sync(0xFFFFFFFFu, sq, 2);
@@ -998,22 +1008,17 @@ struct MmaGroupConsumer {
         for (int hb = 0; hb < 2; ++hb) {
             float sacc[NG][4];
 #pragma unroll
-            for (int gi = 0; gi < NG; ++gi) {
-                sacc[gi][0] = sacc[gi][1] = sacc[gi][2] = sacc[gi][3] = 0.f;
-                uint32_t kw[KB / 4];
-                const uint32_t a = kt + hb * 8 * D + k_off[gi];
-                if (KB == 16) {
-                    const uint4 x = lds128(a);
-                    kw[0] = x.x; kw[KB / 4 > 1 ? 1 : 0] = x.y; kw[KB / 4 > 2 ? 2 : 0] = x.z; kw[KB / 4 > 3 ? 3 : 0] = x.w;
-                } else {
-                    const uint2 x = lds64(a);
-                    kw[0] = x.x; kw[KB / 4 > 1 ? 1 : 0] = x.y;
-                }
+            for (int gi = 0; gi < NG; ++gi) sacc[gi][0] = sacc[gi][1] = sacc[gi][2] = sacc[gi][3] = 0.f;
 #pragma unroll
-                for (int s = 0; s < SPG; ++s) {
-                    const uint32_t x = kw[s] ^ 0x80808080u;   // code + 128 as an unsigned byte
-                    const uint32_t b0 = prmt(x, 0u, 0x4140u), b1 = prmt(x, 0u, 0x4342u);
-                    mma_16816(sacc[gi], qa[2 * (SPG * gi + s)], 0u, qa[2 * (SPG * gi + s) + 1], 0u, b0, b1);
+            for (int x = 0; x < NLD; ++x) {
+                uint32_t kw[4];   // slices 4x .. 4x + 3: row g's bytes 16 j + 4c .. + 3
+                ldsm_x4(kt + hb * 8 * D + k_off[x], kw);
+#pragma unroll
+                for (int m4 = 0; m4 < 4; ++m4) {
+                    const int j = 4 * x + m4;
+                    const uint32_t w = kw[m4] ^ 0x80808080u;   // code + 128 as an unsigned byte
+                    const uint32_t b0 = prmt(w, 0u, 0x4140u), b1 = prmt(w, 0u, 0x4342u);
+                    mma_16816(sacc[j / SPG], qa[2 * j], 0u, qa[2 * j + 1], 0u, b0, b1);
                 }
             }
             // tokens 8 hb + 2c, 8 hb + 2c + 1: scales [token][NG]
@@ -1086,8 +1091,13 @@ struct MmaGroupConsumer {
 #pragma unroll
         for (int gi = 0; gi < NG; ++gi) {
             float pg[4];
+            if (valid >= kBox) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) pg[e] = p[e] != 0.f ? p[e] * sv[e][gi] : 0.f;
+                for (int e = 0; e < 4; ++e) pg[e] = p[e] * sv[e][gi];
+            } else {  // a masked token keeps p = 0 whatever its (never written) scale slot holds
+#pragma unroll
+                for (int e = 0; e < 4; ++e) pg[e] = p[e] != 0.f ? p[e] * sv[e][gi] : 0.f;
+            }
             uint32_t pb0, pb1, pl0, pl1;
             p_frags(pg, pb0, pb1, pl0, pl1);
 #pragma unroll
