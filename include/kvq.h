@@ -102,9 +102,10 @@ typedef enum {
  *     0 or head_dim = one scale per row; head_dim / 2 or head_dim / 4 = two or
  *     four groups of consecutive channels, each quantized as a row is (its own
  *     amax and scale).  Must be 0 for FP8; any other value is INVALID_ARG.
- *     Every entry point takes every group size; decode with more than 8
- *     (q-head, scale group) pairs per kv-head streams the cache in
- *     ceil(G * groups / 8) passes. */
+ *     Every entry point takes every group size.  Decode reads the cache once,
+ *     except for kv-heads with more than 8 (q-head, scale group) pairs in INT4
+ *     or in INT8 with 16-channel groups: those stream it ceil(G * groups / 16)
+ *     times. */
 typedef struct {
     void* k_codes;
     void* v_codes;
