@@ -182,11 +182,13 @@ def test_nan_codes_past_the_context_do_not_leak():
     assert rel_err(o, ref) <= ATOL_REL
 
 
-@pytest.mark.parametrize("fmt,group", [("int8", 0), ("int4", 0), ("int4", 32)])
-def test_nan_scales_past_the_context_do_not_leak(fmt, group):
+@pytest.mark.parametrize("fmt,group,hq", [("int8", 0, 4), ("int4", 0, 4), ("int4", 32, 4), ("int8", 32, 16),
+                                          ("int8", 64, 16)])
+def test_nan_scales_past_the_context_do_not_leak(fmt, group, hq):
     """Scale slots of rows past the context that were never written hold NaN
-    (the caller's memory is not cleared): the masked tokens' weights stay 0."""
-    wl = W.Workload("nans", 3, 4, 2, 128, 16, fmt, 40, "row", seed=4, quant_group=group)
+    (the caller's memory is not cleared): the masked tokens' weights stay 0.
+    Sixteen q-heads over two kv-heads with groups take the grouped consumer."""
+    wl = W.Workload("nans", 3, hq, 2, 128, 16, fmt, 40, "row", seed=4, quant_group=group)
     ctx = torch.tensor([37, 40, 17], dtype=torch.int32)
     lay = W.Layout(wl, ctx)
     dev = torch.device("cuda")
@@ -197,7 +199,7 @@ def test_nan_scales_past_the_context_do_not_leak(fmt, group):
     slots = lay.slots(0, 40).to(dev)          # -1 past each sequence's context
     kvq.append(k, v, cache, slots)
     q = W.query(wl, dev)
-    for kernel in (kvq.KERNEL_MMA, kvq.KERNEL_SIMT) if fmt == "int8" else (kvq.KERNEL_MMA,):
+    for kernel in (kvq.KERNEL_MMA, kvq.KERNEL_SIMT) if fmt == "int8" and hq <= 8 else (kvq.KERNEL_MMA,):
         kvq.set_decode_kernel(kernel)
         out = kvq.decode_attention(q, cache, lay.block_tables.to(dev), ctx.to(dev), 40)
         o = out.float().cpu().numpy()
