@@ -64,12 +64,14 @@ def test_encoder_every_fp16_pattern(fmt, scale):
 
 
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
-@pytest.mark.parametrize("scale", [None, 0.0123, 3.7, -0.75])
+@pytest.mark.parametrize("scale", [None, 0.0123, 3.7, -0.75, 1.0 / 448.0, 1e-6, 0.2409319132566452, 3e-33, 0.125])
 def test_encoder_every_fp16_pattern_large_append(fmt, scale):
-    """Appends large enough for the code-table kernel (every CTA tabulates the
-    codes of the non-negative fp16 patterns for the call's scale and takes the
-    sign from the input): 64 copies of every fp16 bit pattern in shuffled
-    slots, bit-exact against the oracle; a negative scale included."""
+    """Appends large enough for the bulk kernel (2^22 values or more; it
+    quantizes from the reciprocal of the scale and takes the IEEE division near
+    the codes' midpoints): 64 copies of every fp16 bit pattern in shuffled
+    slots, bit-exact against the oracle; a negative scale, a power of two, a
+    scale whose reciprocal would lose precision (division for every value) and
+    the 70B workload's calibration scale included."""
     bits = torch.arange(65536, dtype=torch.int32).to(torch.int16).view(torch.float16)
     g = torch.Generator().manual_seed(17)
     k = bits.repeat(64)[torch.randperm(64 * 65536, generator=g)].reshape(-1, 1, 128).clone()
@@ -84,6 +86,36 @@ def test_encoder_every_fp16_pattern_large_append(fmt, scale):
         nan = np.isnan(tab[want]) & (want != 0xA5)
         assert np.array_equal(got[~nan], want[~nan])
         assert np.isnan(tab[got[nan]]).all()
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("scale", [0.0173, 0.2409319132566452, 3.7, 1.0 / 448.0])
+def test_large_append_near_code_midpoints(fmt, scale):
+    """Inputs whose quotients x / s sit on or next to the midpoints between
+    adjacent codes (where the reciprocal's quotient may round the other way):
+    for every midpoint m of the format's positive values, the fp16 values
+    nearest m * s and their fp16 neighbours two steps either way, both signs,
+    repeated past 2^22 values so that the bulk kernel runs; bit-exact against
+    the oracle's division."""
+    tab = oracle.fp8_decode_table(ORACLE_FMT[fmt]).astype(np.float64)
+    pos = np.unique(tab[np.isfinite(tab) & (tab > 0)])
+    mids = (pos[:-1] + pos[1:]) / 2
+    centre = np.minimum(mids * scale, 65504.0).astype(np.float16).view(np.int16).astype(np.int32)
+    cand = np.concatenate([centre + d for d in range(-2, 3)])
+    cand = cand[(cand > 0) & (cand < 0x7C00)].astype(np.int16).view(np.float16)
+    vals = np.concatenate([cand, -cand]).astype(np.float16)
+    reps = (1 << 22) // vals.size + 1
+    g = torch.Generator().manual_seed(23)
+    flat = torch.from_numpy(np.tile(vals, reps))
+    flat = flat[torch.randperm(flat.numel(), generator=g)]
+    n = flat.numel() // 128 * 128
+    k = flat[:n].reshape(-1, 1, 128).clone()
+    v = flat[:n].flip(0).reshape(-1, 1, 128).clone()
+    T = k.shape[0]
+    slots = torch.arange(T, dtype=torch.int64)
+    c, ref = run_both(k, v, slots, (T + 15) // 16, 1, 16, 128, fmt, scale)
+    assert np.array_equal(c.k_codes.cpu().numpy(), ref.k_codes)
+    assert np.array_equal(c.v_codes.cpu().numpy(), ref.v_codes)
 
 
 @pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
