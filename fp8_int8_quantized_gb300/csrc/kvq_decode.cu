@@ -914,9 +914,8 @@ struct MmaConsumer {
 //   ldmatrix of the swizzled 16-byte row segments delivers four slices at a
 //   time (8-byte loads of a lane's group chunk met 2-way bank conflicts: rows
 //   g and g ^ 1 share banks under the 128-byte swizzle).  Each group's slices
-//   accumulate separately; a
-//   logit is sum_g (S_g - 128 * 2^-24 * sum_g(q)) * s_K[t][g] (the per-row
-//   consumer's offset and unit, per group).
+//   accumulate separately; a logit is sum_g (S_g - 128 * 2^-24 * sum_g(q)) *
+//   s_K[t][g] (the per-row consumer's offset and unit, per group).
 //   PV: each m16 tile of out^T = V^T P^T (16 head dims) lies inside one group;
 //   lane g holds the GS / 8 contiguous dims at GS * gi + (GS / 8) * g of each
 //   group, so the operand building is the per-row consumer's, word for word,
@@ -935,6 +934,8 @@ struct MmaGroupConsumer {
     static constexpr int VW = D / 32;        // V words of one lane per token (VB / 4 per group)
     static_assert(GS >= 32 && GS % 32 == 0, "groups of at least 32 channels");
     static constexpr int kMinCtas = kMinBlocks;
+    // 4 warps per CTA, two CTAs per SM: ~231 registers per thread, and the
+    // stages, group scales and 8-head query rows take ~21 KB per warp
     static constexpr int kWarps = KVQ_GA_WARPS;
     static constexpr float kUnit = 5.9604644775390625e-08f;   // operand value of one code step (2^-24)
     static constexpr float kBias = 128.f * kUnit;             // K operand - code * kUnit
