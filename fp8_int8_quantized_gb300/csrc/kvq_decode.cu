@@ -59,7 +59,13 @@
 #define KVQ_GA_WARPS 4
 #endif
 #ifndef KVQ_INT4_WARPS
-#define KVQ_INT4_WARPS 8
+#define KVQ_INT4_WARPS 16
+#endif
+#ifndef KVQ_MMA_WARPS
+#define KVQ_MMA_WARPS 6
+#endif
+#ifndef KVQ_R16_WARPS
+#define KVQ_R16_WARPS 4
 #endif
 
 namespace kvq {
@@ -382,13 +388,17 @@ struct MmaConsumer {
     // up to 255 registers.
     static constexpr int NR = R16 ? 2 : 1;
     static constexpr int kRows = 8 * NR;
-    static constexpr int kMinCtas = kMinBlocks;
     // Warps per CTA, each streaming its own range.  INT4 tiles are half the
     // bytes of the others, and the kernel is bound by the latency of the
-    // per-warp register work rather than by HBM: 8 warps (registers capped at
-    // 128, two CTAs per SM) are 11% faster than 6.  The 8-bit formats stay at
-    // 6: at 8 their stages no longer fit two CTAs into shared memory.
-    static constexpr int kWarps = R16 ? 4 : (I4 ? KVQ_INT4_WARPS : 6);
+    // per-warp register work rather than by HBM: 16 warps per SM (registers
+    // capped at 128) are 11% faster than 12, and as one CTA of 16 warps 2%
+    // faster than as two of 8 (the warp schedulers favour the older of two
+    // CTAs, whose warps then finish their equal ranges ~10% earlier and leave
+    // the SM half occupied).  The 8-bit formats stay at two CTAs of 6: their
+    // stages fill shared memory, and at 12 warps per CTA a large batch of
+    // 8-head groups would not fit.
+    static constexpr int kMinCtas = (I4 && !R16) ? 1 : kMinBlocks;
+    static constexpr int kWarps = R16 ? KVQ_R16_WARPS : (I4 ? KVQ_INT4_WARPS : KVQ_MMA_WARPS);
     // INT8 codes enter the tensor cores as fp16 subnormals, code * 2^-24, and
     // INT4 codes the same, or 16x that where the nibble is left in mantissa
     // bits 4..7 -- the high nibble of a byte is masked in place, which saves
