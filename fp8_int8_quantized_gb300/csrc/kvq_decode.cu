@@ -367,7 +367,7 @@ struct SimtConsumer {
 
 // ----------------------------------------------------------------- MMA --
 
-template <int FMT, int D, bool R16 = false>
+template <int FMT, int D, bool R16 = false, bool WIDE = false>
 struct MmaConsumer {
     static constexpr bool I4 = FMT == INT4;
     static constexpr bool kRowScaled = FMT == INT8 || FMT == INT4;
@@ -397,8 +397,11 @@ struct MmaConsumer {
     // the SM half occupied).  The 8-bit formats stay at two CTAs of 6: their
     // stages fill shared memory, and at 12 warps per CTA a large batch of
     // 8-head groups would not fit.
-    static constexpr int kMinCtas = (I4 && !R16) ? 1 : kMinBlocks;
-    static constexpr int kWarps = R16 ? KVQ_R16_WARPS : (I4 ? KVQ_INT4_WARPS : KVQ_MMA_WARPS);
+    static constexpr int kMinCtas = ((I4 && !R16) || WIDE) ? 1 : kMinBlocks;
+    // WIDE: the 8-bit formats' 12 warps as one CTA per SM (8-head groups, when
+    // the stages fit: +0.7% on the Llama-3-70B batch; neutral to -0.3% for
+    // the smaller groups, which keep two CTAs)
+    static constexpr int kWarps = R16 ? KVQ_R16_WARPS : (I4 ? KVQ_INT4_WARPS : (WIDE ? 2 * KVQ_MMA_WARPS : KVQ_MMA_WARPS));
     // INT8 codes enter the tensor cores as fp16 subnormals, code * 2^-24, and
     // INT4 codes the same, or 16x that where the nibble is left in mantissa
     // bits 4..7 -- the high nibble of a byte is masked in place, which saves
@@ -1767,7 +1770,17 @@ cudaError_t launch_fmt_d(const CUtensorMap& tk, const CUtensorMap& tv, const Dec
         // from the cache).
         const int ng = a.cache.ngroups;
         if (G * ng <= 8) {
-            e = launch_stream<FMT, D, MmaConsumer<FMT, D>>(tk, tv, p, s);
+            if constexpr (FMT != INT4) {
+                // one CTA of 12 warps per SM for 8-head groups when its shared memory fits
+                const int wide_smem = Layout(2 * KVQ_MMA_WARPS, row_bytes(FMT, D), D, G, a.batch, FMT == INT8,
+                                             a.k_new != nullptr, ng).total + 1024;
+                if (G == 8 && wide_smem <= 227 * 1024)
+                    e = launch_stream<FMT, D, MmaConsumer<FMT, D, false, true>>(tk, tv, p, s);
+                else
+                    e = launch_stream<FMT, D, MmaConsumer<FMT, D>>(tk, tv, p, s);
+            } else {
+                e = launch_stream<FMT, D, MmaConsumer<FMT, D>>(tk, tv, p, s);
+            }
         } else if (FMT == INT8 && D / ng >= 32) {  // one pass, a scale group per contraction slice
             e = cudaErrorInvalidValue;
             if constexpr (FMT == INT8) {

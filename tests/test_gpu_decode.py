@@ -46,6 +46,8 @@ CASES = [
     ("int4", 2, 16, 2, 128, 16, [700, 40]),
     ("int4", 2, 8, 1, 64, 32, [333, 64]),
     ("int8", 2, 10, 2, 128, 16, [257, 96]),
+    ("int8", 2, 16, 2, 128, 16, [700, 129]),     # 8-head groups: one CTA of 12 warps per SM
+    ("e5m2", 3, 16, 2, 64, 32, [300, 40, 1]),
     # group quantization (last field: channels per scale): q-heads per kv-head x groups <= 8
     ("int8", 2, 4, 2, 128, 32, [500, 33], 32),
     ("int4", 2, 4, 4, 128, 64, [640, 65], 32),
@@ -96,6 +98,7 @@ SPLIT_CASES = [
     ("e4m3", 4, 8, 2, 128, 16, [3000, 1500, 64, 4097], 0),
     ("e5m2", 4, 32, 8, 128, 16, [3000, 1500, 64, 4097], 0),
     ("int8", 4, 8, 8, 128, 64, [3000, 1500, 64, 4097], 0),
+    ("int8", 4, 16, 2, 128, 16, [3000, 1500, 64, 4097], 0),
     ("int8", 4, 16, 4, 128, 16, [3000, 1500, 64, 4097], 0),
     ("int4", 4, 8, 8, 128, 64, [3000, 1500, 64, 4097], 0),
     ("int4", 4, 16, 2, 128, 16, [3000, 1500, 64, 4097], 0),
