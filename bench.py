@@ -55,7 +55,7 @@ L2_BYTES = 129 * 1024 * 1024
 DEFAULT_STEPS = {"tiny": 2000, "llama2-7b": 10000, "llama3-8b": 10000, "llama2-13b-int8": 1000,
                  "llama2-13b-int4": 2000,
                  "llama2-13b-int4-g32": 2000,
-                 "llama3-70b": 300, "llama3-70b-int8-g32": 200}
+                 "llama3-70b": 300, "llama3-70b-int8-g32": 200, "llama3-70b-int4-g32": 300}
 
 
 def parse():

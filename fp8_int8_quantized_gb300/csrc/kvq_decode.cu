@@ -58,6 +58,12 @@
 #ifndef KVQ_GA_WARPS
 #define KVQ_GA_WARPS 4
 #endif
+#ifndef KVQ_GA4_WARPS
+#define KVQ_GA4_WARPS 16
+#endif
+#ifndef KVQ_GA4_CTAS
+#define KVQ_GA4_CTAS 1
+#endif
 #ifndef KVQ_INT4_WARPS
 #define KVQ_INT4_WARPS 16
 #endif
@@ -173,6 +179,15 @@ __device__ __forceinline__ uint32_t lds32(uint32_t a) {
 // 16-byte row segment).
 __device__ __forceinline__ void ldsm_x4(uint32_t a, uint32_t (&r)[4]) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(a));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t a, uint32_t (&r)[2]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(a));
+}
+// transposed: lane (g, c) gets 16-bit element g of rows 2c (low half) and 2c + 1 (high half)
+__device__ __forceinline__ void ldsm_x4_t(uint32_t a, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(a));
 }
@@ -382,10 +397,11 @@ struct MmaConsumer {
     // QK^T's m16 tile has 16 rows; the 8-row consumer fills rows 0-7 (this
     // thread's row g) and leaves rows 8-15 zero, the 16-row one also fills
     // rows 8-15 (row g + 8) and takes a second n8 tile of PV columns.  The
-    // 16-row consumer serves group-quantized caches whose q-heads x groups per
-    // kv-head exceed 8, so that one pass over the cache serves twice the
-    // pairs; it holds twice the accumulators, so it runs 4 warps per CTA with
-    // up to 255 registers.
+    // 16-row consumer serves INT4 caches with 16-channel groups (head_dim 64)
+    // whose q-heads x groups per kv-head exceed 8, so that one pass over the
+    // cache serves twice the pairs (the grouped consumer below takes the other
+    // grouped caches); it holds twice the accumulators, so it runs 4 warps per
+    // CTA with up to 255 registers.
     static constexpr int NR = R16 ? 2 : 1;
     static constexpr int kRows = 8 * NR;
     // Warps per CTA, each streaming its own range.  INT4 tiles are half the
@@ -468,16 +484,21 @@ struct MmaConsumer {
         kg = g % ng_;
         lo_cols = !R16 && kRowScaled && G_ * ng_ <= 4;
         qk_scale = qks;
-        if (I4 && D == 128) {  // 64-byte rows, 64-byte swizzle: 16-byte chunk ^= (row / 2) % 4
-            k_off0 = g * RB + ((c ^ ((g >> 1) & 3)) << 4);
+        if (I4) {
+            // 64-byte rows (head_dim 128): 64-byte swizzle, 16-byte chunk ^= (row / 2) % 4;
+            // 32-byte rows plain.  V: row addresses of ldmatrix.trans x (v_off0, v_off1):
+            // lane t gives row 8 ((t >> 3) & 1) + t % 8 of chunk 2x + t / 16
+            const int vr = 8 * ((lane >> 3) & 1) + (lane & 7), vc = lane >> 4;
+            if (D == 128) {
+                k_off0 = g * RB + ((c ^ ((g >> 1) & 3)) << 4);
+                v_off0 = vr * RB + ((vc ^ ((vr >> 1) & 3)) << 4);
+                v_off1 = vr * RB + (((2 + vc) ^ ((vr >> 1) & 3)) << 4);
+            } else {
+                k_off0 = g * RB + c * (DC / 2);
+                v_off0 = vr * RB + 16 * vc;
+                v_off1 = 0;
+            }
             k_off1 = 0;
-            v_off0 = (2 * c) * RB + ((((g >> 1) ^ c) & 3) << 4) + 8 * (g & 1);
-            v_off1 = (2 * c + 1) * RB + ((((g >> 1) ^ c) & 3) << 4) + 8 * (g & 1);
-        } else if (I4) {
-            k_off0 = g * RB + c * (DC / 2);
-            k_off1 = 0;
-            v_off0 = (2 * c) * RB + (DV / 2) * g;
-            v_off1 = (2 * c + 1) * RB + (DV / 2) * g;
         } else if (D == 128) {
             k_off0 = g * 128 + (((2 * c) ^ g) << 4);
             k_off1 = g * 128 + (((2 * c + 1) ^ g) << 4);
@@ -687,6 +708,43 @@ struct MmaConsumer {
     template <bool LO>
     __device__ __forceinline__ void pv_box(uint32_t vt, int valid, const uint32_t (&pb)[NR][2],
                                            const uint32_t (&pl)[NR][2]) {
+        if constexpr (I4) {
+            // ldmatrix.trans: r[x][0] / r[x][2] = bytes 2g, 2g + 1 of 16-byte chunk 2x / 2x + 1 of
+            // tokens 2c (bits 0-15) and 2c + 1 (bits 16-31); r[x][1] / r[x][3] tokens 8 + 2c, 9 + 2c
+            constexpr int NCH = RB / 16;
+            uint32_t r[NCH / 2][4];
+            ldsm_x4_t(vt + v_off0, r[0]);
+            if constexpr (NCH == 4) ldsm_x4_t(vt + v_off1, r[NCH / 2 - 1]);
+            if (valid < kBox) {  // rows past the context may hold NaN codes: zero them
+                const uint32_t mlo = (2 * c < valid ? 0x0000FFFFu : 0u) | (2 * c + 1 < valid ? 0xFFFF0000u : 0u);
+                const uint32_t mhi = (8 + 2 * c < valid ? 0x0000FFFFu : 0u) | (9 + 2 * c < valid ? 0xFFFF0000u : 0u);
+#pragma unroll
+                for (int x = 0; x < NCH / 2; ++x) {
+                    r[x][0] &= mlo; r[x][1] &= mhi; r[x][2] &= mlo; r[x][3] &= mhi;
+                }
+            }
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch) {
+                // code + 8 in every nibble (a zeroed token becomes 8 - 8 = 0)
+                const uint32_t lo = r[ch >> 1][2 * (ch & 1)] ^ 0x88888888u, hi = r[ch >> 1][2 * (ch & 1) + 1] ^ 0x88888888u;
+#pragma unroll
+                for (int bb = 0; bb < 2; ++bb) {
+                    // m-tile 2 ch + bb: dim 32 ch + 4g + 2bb (low nibble, rows g) and + 1 (the high
+                    // nibble in place: 16x, rows g + 8), less the offsets (8 and 16 * 8 steps, exact)
+                    const uint32_t u = bb ? lo >> 8 : lo, w = bb ? hi >> 8 : hi;
+                    const uint32_t a0 = hsub2_exact(u & 0x000F000Fu, 0x00080008u);
+                    const uint32_t a1 = hsub2_exact(u & 0x00F000F0u, 0x00800080u);
+                    const uint32_t a2 = hsub2_exact(w & 0x000F000Fu, 0x00080008u);
+                    const uint32_t a3 = hsub2_exact(w & 0x00F000F0u, 0x00800080u);
+#pragma unroll
+                    for (int rr = 0; rr < NR; ++rr) {
+                        mma_16816(acc[rr][2 * ch + bb], a0, a1, a2, a3, pb[rr][0], pb[rr][1]);
+                        if (!LO) mma_16816(acc[rr][2 * ch + bb], a0, a1, a2, a3, pl[rr][0], pl[rr][1]);
+                    }
+                }
+            }
+            return;
+        }
         uint32_t v0[VW], v1[VW], v2[VW], v3[VW];
         load_v(vt + v_off0, v0);
         load_v(vt + v_off1, v1);
@@ -700,33 +758,6 @@ struct MmaConsumer {
                 if (8 + 2 * c >= valid) v2[e] = 0u;
                 if (9 + 2 * c >= valid) v3[e] = 0u;
             }
-        }
-        if (I4) {  // word w of each row: codes 8w .. 8w+7 = m-tiles 4w .. 4w+3 (dims 2i | 2i+1 = low | high nibble)
-#pragma unroll
-            for (int w = 0; w < VW; ++w) {
-                // code + 8 in every nibble (a zeroed row becomes 8 - 8 = 0)
-                v0[w] ^= 0x88888888u; v1[w] ^= 0x88888888u; v2[w] ^= 0x88888888u; v3[w] ^= 0x88888888u;
-#pragma unroll
-                for (int bb = 0; bb < 4; ++bb) {
-                    // byte bb of rows (2c, 2c+1) and (8+2c, 9+2c) in bytes 0 and 2, then the
-                    // flipped nibbles masked in place: dim 2i as the subnormal (code + 8) * 2^-24,
-                    // dim 2i+1 as 16x that (rows g+8 of the m-tile, divided out at the flush)
-                    const uint32_t sel = 0x4400u + 0x1111u * bb;  // bytes [r.bb, r.bb, r'.bb, r'.bb]
-                    const uint32_t u01 = prmt(v0[w], v1[w], sel), u23 = prmt(v2[w], v3[w], sel);
-                    // then the offsets (8 and 16 * 8 steps) subtracted exactly
-                    const uint32_t a0 = hsub2_exact(u01 & 0x000F000Fu, 0x00080008u);
-                    const uint32_t a1 = hsub2_exact(u01 & 0x00F000F0u, 0x00800080u);
-                    const uint32_t a2 = hsub2_exact(u23 & 0x000F000Fu, 0x00080008u);
-                    const uint32_t a3 = hsub2_exact(u23 & 0x00F000F0u, 0x00800080u);
-                    const int i = 4 * w + bb;
-#pragma unroll
-                    for (int r = 0; r < NR; ++r) {
-                        mma_16816(acc[r][i], a0, a1, a2, a3, pb[r][0], pb[r][1]);
-                        if (!LO) mma_16816(acc[r][i], a0, a1, a2, a3, pl[r][0], pl[r][1]);
-                    }
-                }
-            }
-            return;
         }
         if (FMT == INT8) {  // code + 128 as unsigned bytes, once per word
 #pragma unroll
@@ -888,6 +919,31 @@ struct MmaConsumer {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) acc[0][i][e] += __shfl_xor_sync(0xFFFFFFFFu, acc[0][i][e], 2);
         }
+        if constexpr (I4) {
+            // acc[r][2 ch + bb][e | 2 + e] = out[column 8r + 2c + e][d = 32 ch + 4g + 2bb | + 1];
+            // column n is head n / ng with the V scales of group n % ng, which must
+            // be the group of the chunk's dims 32 ch + 4g .. + 3; the odd dims were
+            // fed as 16x operands
+            constexpr int NCH = RB / 16;
+            const float so = f.s_out / kUnit, so1 = so * 0.0625f;
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int n = 8 * r + 2 * c + e, h = n / ng;
+                    if (h >= G) continue;
+                    float* dst = f.acc + slot_index(f.hq0 + h, f.nch, f.ch, f.half) * D + 4 * g;
+#pragma unroll
+                    for (int ch = 0; ch < NCH; ++ch) {
+                        if (n % ng != ((32 * ch + 4 * g) * ng) / D) continue;
+                        *reinterpret_cast<float4*>(dst + 32 * ch) =
+                            make_float4(acc[r][2 * ch][e] * so, acc[r][2 * ch][2 + e] * so1,
+                                        acc[r][2 * ch + 1][e] * so, acc[r][2 * ch + 1][2 + e] * so1);
+                    }
+                }
+            }
+            return;
+        }
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
             // acc[r][i][0..3] = out[column 8r + 2c | 8r + 2c+1][d = DV*g + 2i | DV*g + 2i + 1];
@@ -898,15 +954,13 @@ struct MmaConsumer {
                 const int n = 8 * r + 2 * c + e, h = n / ng;
                 if (h >= G || n % ng != ((g * ng) >> 3)) continue;
                 float* dst = f.acc + slot_index(f.hq0 + h, f.nch, f.ch, f.half) * D + DV * g;
-                // INT8 / INT4 operands are 2^-24 per code step; INT4's odd dims
-                // (rows g+8) were fed as 16x operands
+                // INT8 operands are 2^-24 per code step
                 const float so = kRowScaled ? f.s_out / kUnit : f.s_out;
-                const float so1 = I4 ? so * 0.0625f : so;
 #pragma unroll
                 for (int i = 0; i < MT; i += 2)
                     *reinterpret_cast<float4*>(dst + 2 * i) =
-                        make_float4(acc[r][i][e] * so, acc[r][i][2 + e] * so1,
-                                    acc[r][i + 1][e] * so, acc[r][i + 1][2 + e] * so1);
+                        make_float4(acc[r][i][e] * so, acc[r][i][2 + e] * so,
+                                    acc[r][i + 1][e] * so, acc[r][i + 1][2 + e] * so);
             }
         }
     }
@@ -915,61 +969,71 @@ struct MmaConsumer {
     }
 };
 
-// ------------------------------------------------ MMA, grouped INT8 --
+// ------------------------------------------- MMA, grouped INT8 / INT4 --
 
-// INT8 with one scale per group of GS = D / NG channels (NG = 2 or 4, GS at
-// least 32), for kv-heads whose q-heads x groups exceed 8: one pass over the
-// cache serves all G <= 8 q-heads.  The operand rows are the q-heads (as in the
-// per-row consumer) and the group scales are applied per contraction slice
-// instead of per operand row:
-//   QK: k16 slice j of S^T = Q K^T is channels 16 j .. 16 j + 15, inside group
-//   j / (GS / 16); lane c holds channels 16 j + 4c .. 16 j + 4c + 3, which an
-//   ldmatrix of the swizzled 16-byte row segments delivers four slices at a
-//   time (8-byte loads of a lane's group chunk met 2-way bank conflicts: rows
-//   g and g ^ 1 share banks under the 128-byte swizzle).  Each group's slices
-//   accumulate separately; a logit is sum_g (S_g - 128 * 2^-24 * sum_g(q)) *
-//   s_K[t][g] (the per-row consumer's offset and unit, per group).
-//   PV: each m16 tile of out^T = V^T P^T (16 head dims) lies inside one group;
-//   lane g holds the GS / 8 contiguous dims at GS * gi + (GS / 8) * g of each
-//   group, so the operand building is the per-row consumer's, word for word,
-//   and the m-tiles of group gi take the weights P * s_V[t][gi] (fp16 hi and
-//   residual, two MMAs per m-tile).
+// INT8 or INT4 with one scale per group of GS = D / NG channels, for kv-heads
+// whose q-heads x groups exceed 8: one pass over the cache serves all G <= 8
+// q-heads.  The operand rows are the q-heads (as in the per-row consumer) and
+// the group scales are applied per contraction slice (QK) and per output
+// m-tile (PV) instead of per operand row.  Both products read the stage tile
+// in 16-byte row segments ("chunks": 16 INT8 or 32 INT4 channels) through
+// ldmatrix, so that each tensor-core instruction sees the channels of one
+// chunk, which lies inside one group (groups are whole chunks):
+//   QK: ldmatrix gives lane (g, c) bytes 4c .. 4c + 3 of row g's chunk: one
+//   k16 slice of S^T = Q K^T (INT8), or two (INT4, through the per-row
+//   consumer's in-place nibble masks, the query permuted to match).  Each
+//   group's slices accumulate separately; a logit is
+//   sum_g (S_g - bias * sum_g(q)) * s_K[t][g] (the per-row consumer's offset
+//   and unit, per group).  (8-byte loads of a lane's group chunk met 2-way
+//   bank conflicts: rows g and g ^ 1 share banks under the 128-byte swizzle.)
+//   PV: ldmatrix.trans gives lane (g, c) bytes 2g and 2g + 1 of rows 2c and
+//   2c + 1 (tokens) of a chunk in one register: A-operand values of
+//   out^T = V^T P^T with the token pair already along k.  The m16 tile of INT8
+//   chunk q is dims 16q + 2g (rows g) and 16q + 2g + 1 (rows g + 8); INT4
+//   chunk q holds two m-tiles, dims 32q + 4g + 2bb (rows g) and + 1 (rows
+//   g + 8, fed as 16x operands), bb = 0, 1 -- masked straight out of the
+//   loaded register, with no byte permutes.  The m-tiles of group gi take the
+//   weights P * s_V[t][gi] (fp16 hi and residual, two MMAs per m-tile).
 // The 16-row multi-pass alternative read the cache once per 16 (q-head, group)
 // pairs: twice for Llama-3-70B's G = 8 with 32-channel groups.
-template <int D, int NG>
+template <int FMT, int D, int NG>
 struct MmaGroupConsumer {
-    static constexpr int GS = D / NG;        // channels per scale group
-    static constexpr int SPG = GS / 16;      // k16 slices (and m16 tiles) per group
-    static constexpr int KS = D / 16;        // k-slices of QK^T
-    static constexpr int MT = D / 16;        // m-tiles of PV
-    static constexpr int NLD = KS / 4;       // ldmatrix.x4 per half box (four slices each)
-    static constexpr int VB = GS / 8;        // V bytes of one lane per token and group
-    static constexpr int VW = D / 32;        // V words of one lane per token (VB / 4 per group)
-    static_assert(GS >= 32 && GS % 32 == 0, "groups of at least 32 channels");
-    static constexpr int kMinCtas = kMinBlocks;
-    // 4 warps per CTA, two CTAs per SM: ~231 registers per thread, and the
-    // stages, group scales and 8-head query rows take ~21 KB per warp
-    static constexpr int kWarps = KVQ_GA_WARPS;
-    static constexpr float kUnit = 5.9604644775390625e-08f;   // operand value of one code step (2^-24)
-    static constexpr float kBias = 128.f * kUnit;             // K operand - code * kUnit
-    static constexpr float kLogF = 6.f;                        // weights carry 2^6 (cancels in acc / l)
-    uint32_t qa[2 * KS];   // slice j: {q[16j + 4c], q[16j + 4c + 1] | q[16j + 4c + 2], q[16j + 4c + 3]}
+    static constexpr bool I4 = FMT == INT4;
+    static constexpr int RB = row_bytes(FMT, D);  // bytes of one cached row
+    static constexpr int GS = D / NG;             // channels per scale group
+    static constexpr int NCH = RB / 16;           // 16-byte chunks per row
+    static constexpr int CPG = GS / (I4 ? 32 : 16);  // chunks per group
+    static constexpr int KS = D / 16;             // k-slices of QK^T
+    static constexpr int MT = D / 16;             // m-tiles of PV
+    static constexpr int NLK = I4 ? 1 : NCH / 4;  // K: ldmatrix per half box (.x4; INT4 at head_dim 64: .x2)
+    static constexpr int NLV = NCH / 2;           // V: ldmatrix.x4.trans per box (two chunks each)
+    static_assert(CPG >= 1 && GS % (I4 ? 32 : 16) == 0, "groups of whole 16-byte chunks");
+    // INT8: 4 warps per CTA, two CTAs per SM (the stages, group scales and
+    // 8-head query rows take ~21 KB per warp; 206 registers).  INT4 stages are
+    // half the bytes and the consumer is bound by instruction issue: one CTA of
+    // 16 warps per SM with registers capped at 128 (a few spilled) is 3% faster
+    // than two CTAs of 8 and 7% faster than three of 4 at 168 registers
+    static constexpr int kMinCtas = I4 ? KVQ_GA4_CTAS : kMinBlocks;
+    static constexpr int kWarps = I4 ? KVQ_GA4_WARPS : KVQ_GA_WARPS;
+    static constexpr float kUnit = 5.9604644775390625e-08f;      // operand value of one code step (2^-24)
+    static constexpr float kBias = (I4 ? 8.f : 128.f) * kUnit;   // K operand - code * kUnit
+    static constexpr float kLogF = I4 ? 2.f : 6.f;               // weights carry 2^kLogF (cancels in acc / l)
+    // INT8 slice j: {q[16j + 4c], q[16j + 4c + 1] | q[16j + 4c + 2], q[16j + 4c + 3]};
+    // INT4 chunk q, dims b = 32q + 8c ..: [q_b0, q_b5/16] [q_b1/16, q_b4] [q_b2, q_b7/16] [q_b3/16, q_b6]
+    uint32_t qa[2 * KS];
     float acc[MT][4];
     float m, l;
     float qsum[NG];        // per group: sum of this lane's row's query values over the group
     int lane, g, c, G;
     float qk_scale;
-    uint32_t k_off[NLD];   // this lane's row address for ldmatrix x (slices 4x .. 4x + 3), swizzle folded in
-    uint32_t v_off[VW][2]; // word w of rows 2c and 2c+1 (rows 8+2c, 9+2c are 8 rows further)
+    uint32_t k_off[NLK];   // this lane's row address for K ldmatrix x (chunks 4x .. 4x + 3), swizzle folded in
+    uint32_t v_off[NLV];   // ... for V ldmatrix.trans x: chunks 2x, 2x + 1, rows 0-7 and 8-15 each
 
     // byte offset of byte o of row r inside a stage tile
     __device__ __forceinline__ static uint32_t off(int r, int o) {
-        if (D == 128) return r * 128 + (o ^ ((r & 7) << 4));
-        return r * D + o;
-    }
-    // byte offset, in a row, of V word w of lane g: group w / (VB / 4), word w % (VB / 4) of its chunk
-    __device__ __forceinline__ static int vword(int g_, int w) {
-        return GS * (w / (VB / 4)) + VB * g_ + 4 * (w % (VB / 4));
+        if (I4 && D == 128) return r * 64 + (o ^ (((r >> 1) & 3) << 4));   // 64-byte swizzle
+        if (!I4 && D == 128) return r * 128 + (o ^ ((r & 7) << 4));       // 128-byte swizzle
+        return r * RB + o;
     }
 
     __device__ void init(int G_, float qks, int) {
@@ -978,29 +1042,47 @@ struct MmaGroupConsumer {
         c = lane & 3;
         G = G_;
         qk_scale = qks;
-        // ldmatrix: lane t gives row t % 8 of matrix t / 8 (slice 4x + t / 8)
+        // ldmatrix: lane t gives row t % 8 of matrix t / 8 (chunk 4x + t / 8; .x2 reads lanes 0-15)
 #pragma unroll
-        for (int x = 0; x < NLD; ++x) k_off[x] = off(lane & 7, 16 * (4 * x + (lane >> 3)));
+        for (int x = 0; x < NLK; ++x) k_off[x] = off(lane & 7, 16 * ((4 * x + (lane >> 3)) % NCH));
+        // matrices of V load x: (chunk 2x, rows 0-7), (2x, 8-15), (2x + 1, 0-7), (2x + 1, 8-15)
 #pragma unroll
-        for (int w = 0; w < VW; ++w) {
-            v_off[w][0] = off(2 * c, vword(g, w));
-            v_off[w][1] = off(2 * c + 1, vword(g, w));
-        }
+        for (int x = 0; x < NLV; ++x) v_off[x] = off(8 * ((lane >> 3) & 1) + (lane & 7), 16 * (2 * x + (lane >> 4)));
     }
     // q: the kv-head's G query rows (shared-memory copy)
     __device__ void set_q(const uint16_t* q) {
 #pragma unroll
         for (int gi = 0; gi < NG; ++gi) {
             float sq = 0.f;
+            if constexpr (I4) {
 #pragma unroll
-            for (int s = 0; s < SPG; ++s) {
-                const int j = SPG * gi + s;
-                uint2 w = make_uint2(0u, 0u);
-                if (g < G) w = *reinterpret_cast<const uint2*>(q + g * D + 16 * j + 4 * c);
-                qa[2 * j] = w.x;
-                qa[2 * j + 1] = w.y;
-                const float2 v0 = f16x2_to_f32x2(w.x), v1 = f16x2_to_f32x2(w.y);
-                sq += (v0.x + v0.y) + (v1.x + v1.y);
+                for (int cc = 0; cc < CPG; ++cc) {
+                    const int ch = CPG * gi + cc;
+                    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+                    if (g < G) w = *reinterpret_cast<const uint4*>(q + g * D + 32 * ch + 8 * c);
+                    const float2 q01 = f16x2_to_f32x2(w.x), q23 = f16x2_to_f32x2(w.y);
+                    const float2 q45 = f16x2_to_f32x2(w.z), q67 = f16x2_to_f32x2(w.w);
+                    qa[4 * ch] = pack_f16x2(q01.x, q45.y * 0.0625f);
+                    qa[4 * ch + 1] = pack_f16x2(q01.y * 0.0625f, q45.x);
+                    qa[4 * ch + 2] = pack_f16x2(q23.x, q67.y * 0.0625f);
+                    qa[4 * ch + 3] = pack_f16x2(q23.y * 0.0625f, q67.x);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {  // q as fed times each operand's step (16 for the divided values)
+                        const float2 v = f16x2_to_f32x2(qa[4 * ch + i]);
+                        sq += (i & 1) ? 16.f * v.x + v.y : v.x + 16.f * v.y;
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int s = 0; s < CPG; ++s) {
+                    const int j = CPG * gi + s;
+                    uint2 w = make_uint2(0u, 0u);
+                    if (g < G) w = *reinterpret_cast<const uint2*>(q + g * D + 16 * j + 4 * c);
+                    qa[2 * j] = w.x;
+                    qa[2 * j + 1] = w.y;
+                    const float2 v0 = f16x2_to_f32x2(w.x), v1 = f16x2_to_f32x2(w.y);
+                    sq += (v0.x + v0.y) + (v1.x + v1.y);
+                }
             }
             sq += __shfl_xor_sync(0xFFFFFFFFu, sq, 1);
             sq += __shfl_xor_sync(0xFFFFFFFFu, sq, 2);
@@ -1014,25 +1096,48 @@ struct MmaGroupConsumer {
         for (int i = 0; i < MT; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
     }
 
+    // One QK^T product of a k16 slice into the accumulator rows g (odd = 0)
+    // or g + 8 (odd = 1): the query operand qa[i], qa[i + 1] in that row half
+    __device__ __forceinline__ void qk_mma(float (&s)[4], int odd, int i, uint32_t b0, uint32_t b1) {
+        if (odd) mma_16816(s, 0u, qa[i], 0u, qa[i + 1], b0, b1);
+        else mma_16816(s, qa[i], 0u, qa[i + 1], 0u, b0, b1);
+    }
+
     // QK^T of one 16-row box: this thread's logits of q-head g, box tokens 2c,
     // 2c+1, 8+2c, 9+2c (already scaled, masked past `valid`).
     __device__ __forceinline__ void qk_box(uint32_t kt, uint32_t sk, int valid, float (&z)[4]) {
         const float ks = qk_scale / kUnit;
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
-            float sacc[NG][4];
+            // group 2p accumulates in rows 0-7 of sacc[p] (the A operand's rows g),
+            // group 2p + 1 in rows 8-15 (rows g + 8): half the accumulators
+            float sacc[NG / 2][4];
 #pragma unroll
-            for (int gi = 0; gi < NG; ++gi) sacc[gi][0] = sacc[gi][1] = sacc[gi][2] = sacc[gi][3] = 0.f;
+            for (int gp = 0; gp < NG / 2; ++gp) sacc[gp][0] = sacc[gp][1] = sacc[gp][2] = sacc[gp][3] = 0.f;
+            if constexpr (I4) {
+                uint32_t kw[NCH];   // chunk ch: row g's codes 32 ch + 8c .. + 7 (byte i: dims 2i, 2i + 1)
+                if constexpr (NCH == 4) ldsm_x4(kt + hb * 8 * RB + k_off[0], kw);
+                else ldsm_x2(kt + hb * 8 * RB + k_off[0], kw);
 #pragma unroll
-            for (int x = 0; x < NLD; ++x) {
-                uint32_t kw[4];   // slices 4x .. 4x + 3: row g's bytes 16 j + 4c .. + 3
-                ldsm_x4(kt + hb * 8 * D + k_off[x], kw);
+                for (int ch = 0; ch < NCH; ++ch) {
+                    // bit 3 of every nibble flipped (code + 8), masked in place:
+                    // [d0, 16 d5] [16 d1, d4] and [d2, 16 d7] [16 d3, d6]
+                    const uint32_t x = kw[ch] ^ 0x88888888u, y = x >> 8;
+                    qk_mma(sacc[ch / CPG / 2], (ch / CPG) & 1, 4 * ch, x & 0x00F0000Fu, x & 0x000F00F0u);
+                    qk_mma(sacc[ch / CPG / 2], (ch / CPG) & 1, 4 * ch + 2, y & 0x00F0000Fu, y & 0x000F00F0u);
+                }
+            } else {
 #pragma unroll
-                for (int m4 = 0; m4 < 4; ++m4) {
-                    const int j = 4 * x + m4;
-                    const uint32_t w = kw[m4] ^ 0x80808080u;   // code + 128 as an unsigned byte
-                    const uint32_t b0 = prmt(w, 0u, 0x4140u), b1 = prmt(w, 0u, 0x4342u);
-                    mma_16816(sacc[j / SPG], qa[2 * j], 0u, qa[2 * j + 1], 0u, b0, b1);
+                for (int x = 0; x < NLK; ++x) {
+                    uint32_t kw[4];   // slices 4x .. 4x + 3: row g's bytes 16 j + 4c .. + 3
+                    ldsm_x4(kt + hb * 8 * RB + k_off[x], kw);
+#pragma unroll
+                    for (int m4 = 0; m4 < 4; ++m4) {
+                        const int j = 4 * x + m4;
+                        const uint32_t w = kw[m4] ^ 0x80808080u;   // code + 128 as an unsigned byte
+                        const uint32_t b0 = prmt(w, 0u, 0x4140u), b1 = prmt(w, 0u, 0x4342u);
+                        qk_mma(sacc[j / CPG / 2], (j / CPG) & 1, 2 * j, b0, b1);
+                    }
                 }
             }
             // tokens 8 hb + 2c, 8 hb + 2c + 1: scales [token][NG]
@@ -1053,8 +1158,8 @@ struct MmaGroupConsumer {
 #pragma unroll
             for (int gi = 0; gi < NG; ++gi) {
                 const float corr = kBias * qsum[gi];
-                z0 = fmaf(sacc[gi][0] - corr, k0[gi], z0);
-                z1 = fmaf(sacc[gi][1] - corr, k1[gi], z1);
+                z0 = fmaf(sacc[gi / 2][2 * (gi & 1)] - corr, k0[gi], z0);
+                z1 = fmaf(sacc[gi / 2][2 * (gi & 1) + 1] - corr, k1[gi], z1);
             }
             z[2 * hb] = z0 * ks;
             z[2 * hb + 1] = z1 * ks;
@@ -1081,27 +1186,23 @@ struct MmaGroupConsumer {
     // out^T += V^T P_g^T for one box: p = weights of box tokens 2c, 2c+1, 8+2c,
     // 9+2c; sv = their V scales per group
     __device__ __forceinline__ void pv_box(uint32_t vt, int valid, const float (&p)[4], const float (&sv)[4][NG]) {
-        uint32_t v0[VW], v1[VW], v2[VW], v3[VW];
+        // r[x][0] / r[x][2]: chunk 2x / 2x + 1, tokens 2c (bits 0-15) and 2c + 1 (bits 16-31);
+        // r[x][1] / r[x][3]: the same for tokens 8 + 2c and 9 + 2c
+        uint32_t r[NLV][4];
 #pragma unroll
-        for (int w = 0; w < VW; ++w) {
-            v0[w] = lds32(vt + v_off[w][0]);
-            v1[w] = lds32(vt + v_off[w][1]);
-            v2[w] = lds32(vt + v_off[w][0] + 8 * D);
-            v3[w] = lds32(vt + v_off[w][1] + 8 * D);
-        }
+        for (int x = 0; x < NLV; ++x) ldsm_x4_t(vt + v_off[x], r[x]);
         if (valid < kBox) {  // rows past the context may hold NaN codes: zero them
+            const uint32_t mlo = (2 * c < valid ? 0x0000FFFFu : 0u) | (2 * c + 1 < valid ? 0xFFFF0000u : 0u);
+            const uint32_t mhi = (8 + 2 * c < valid ? 0x0000FFFFu : 0u) | (9 + 2 * c < valid ? 0xFFFF0000u : 0u);
 #pragma unroll
-            for (int w = 0; w < VW; ++w) {
-                if (2 * c >= valid) v0[w] = 0u;
-                if (2 * c + 1 >= valid) v1[w] = 0u;
-                if (8 + 2 * c >= valid) v2[w] = 0u;
-                if (9 + 2 * c >= valid) v3[w] = 0u;
+            for (int x = 0; x < NLV; ++x) {
+                r[x][0] &= mlo; r[x][1] &= mhi; r[x][2] &= mlo; r[x][3] &= mhi;
             }
         }
 #pragma unroll
-        for (int w = 0; w < VW; ++w) {  // code + 128 as unsigned bytes
-            v0[w] ^= 0x80808080u; v1[w] ^= 0x80808080u; v2[w] ^= 0x80808080u; v3[w] ^= 0x80808080u;
-        }
+        for (int x = 0; x < NLV; ++x)   // code + 8 in every nibble, or code + 128 in every byte (zeroed rows give 0 below)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) r[x][e] ^= I4 ? 0x88888888u : 0x80808080u;
 #pragma unroll
         for (int gi = 0; gi < NG; ++gi) {
             float pg[4];
@@ -1115,18 +1216,32 @@ struct MmaGroupConsumer {
             uint32_t pb0, pb1, pl0, pl1;
             p_frags(pg, pb0, pb1, pl0, pl1);
 #pragma unroll
-            for (int mm = 0; mm < SPG; ++mm) {
-                const int i = SPG * gi + mm;   // m-tile; its dims are 2 mm, 2 mm + 1 of the lane's group chunk
-                const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;
-                const uint32_t x01 = prmt(v0[i >> 1], v1[i >> 1], sel);
-                const uint32_t x23 = prmt(v2[i >> 1], v3[i >> 1], sel);
-                // fp16 subnormals (code + 128) * 2^-24, less 128 * 2^-24 (exact)
-                const uint32_t a0 = hsub2_exact(prmt(x01, 0u, 0x4140u), 0x00800080u);
-                const uint32_t a1 = hsub2_exact(prmt(x01, 0u, 0x4342u), 0x00800080u);
-                const uint32_t a2 = hsub2_exact(prmt(x23, 0u, 0x4140u), 0x00800080u);
-                const uint32_t a3 = hsub2_exact(prmt(x23, 0u, 0x4342u), 0x00800080u);
-                mma_16816(acc[i], a0, a1, a2, a3, pb0, pb1);
-                mma_16816(acc[i], a0, a1, a2, a3, pl0, pl1);
+            for (int cc = 0; cc < CPG; ++cc) {
+                const int ch = CPG * gi + cc;
+                const uint32_t lo = r[ch >> 1][2 * (ch & 1)], hi = r[ch >> 1][2 * (ch & 1) + 1];
+                if constexpr (I4) {
+#pragma unroll
+                    for (int bb = 0; bb < 2; ++bb) {
+                        // byte bb of each token's pair: dim 32 ch + 4g + 2bb (low nibble, rows g) and
+                        // + 1 (high nibble in place: 16x, rows g + 8), less the offsets (exact)
+                        const uint32_t u = bb ? lo >> 8 : lo, w = bb ? hi >> 8 : hi;
+                        const uint32_t a0 = hsub2_exact(u & 0x000F000Fu, 0x00080008u);
+                        const uint32_t a1 = hsub2_exact(u & 0x00F000F0u, 0x00800080u);
+                        const uint32_t a2 = hsub2_exact(w & 0x000F000Fu, 0x00080008u);
+                        const uint32_t a3 = hsub2_exact(w & 0x00F000F0u, 0x00800080u);
+                        mma_16816(acc[2 * ch + bb], a0, a1, a2, a3, pb0, pb1);
+                        mma_16816(acc[2 * ch + bb], a0, a1, a2, a3, pl0, pl1);
+                    }
+                } else {
+                    // bytes 0 | 2: dim 16 ch + 2g (rows g); bytes 1 | 3: dim 16 ch + 2g + 1 (rows g + 8),
+                    // as fp16 subnormals (code + 128) * 2^-24, less 128 * 2^-24 (exact)
+                    const uint32_t a0 = hsub2_exact(prmt(lo, 0u, 0x4240u), 0x00800080u);
+                    const uint32_t a1 = hsub2_exact(prmt(lo, 0u, 0x4341u), 0x00800080u);
+                    const uint32_t a2 = hsub2_exact(prmt(hi, 0u, 0x4240u), 0x00800080u);
+                    const uint32_t a3 = hsub2_exact(prmt(hi, 0u, 0x4341u), 0x00800080u);
+                    mma_16816(acc[ch], a0, a1, a2, a3, pb0, pb1);
+                    mma_16816(acc[ch], a0, a1, a2, a3, pl0, pl1);
+                }
             }
         }
     }
@@ -1150,7 +1265,7 @@ struct MmaGroupConsumer {
     __device__ void tile(const Tile& cx) {
         float z0[4], z1[4];
         qk_box(cx.k, cx.s, cx.valid, z0);
-        qk_box(cx.k + kBox * D, cx.s + 4 * kBox * NG, cx.valid - kBox, z1);
+        qk_box(cx.k + kBox * RB, cx.s + 4 * kBox * NG, cx.valid - kBox, z1);
         float mx = fmaxf(fmaxf(fmaxf(z0[0], z0[1]), fmaxf(z0[2], z0[3])), fmaxf(fmaxf(z1[0], z1[1]), fmaxf(z1[2], z1[3])));
         mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
@@ -1183,7 +1298,7 @@ struct MmaGroupConsumer {
         v_scales(sv, s0);
         pv_box(cx.v, cx.valid, p0, s0);
         v_scales(sv + 4 * kBox * NG, s0);
-        pv_box(cx.v + kBox * D, cx.valid - kBox, p1, s0);
+        pv_box(cx.v + kBox * RB, cx.valid - kBox, p1, s0);
     }
 
     __device__ void flush(const Flush& f) {
@@ -1191,21 +1306,24 @@ struct MmaGroupConsumer {
         lq += __shfl_xor_sync(0xFFFFFFFFu, lq, 1);
         lq += __shfl_xor_sync(0xFFFFFFFFu, lq, 2);
         if (c == 0 && g < G) f.ml[slot_index(f.hq0 + g, f.nch, f.ch, f.half)] = make_float2(m, lq);
-        // acc[i][e] (acc[i][2 + e]) = out[q-head 2c + e][dim 2 mm (+1) of the lane's chunk of group i / SPG]
+        // acc[i][e] (acc[i][2 + e]) = out[q-head 2c + e][m-tile i's dim of rows g (g + 8)]
         const float so = f.s_out / kUnit;
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int h = 2 * c + e;
             if (h >= G) continue;
-            float* dst = f.acc + slot_index(f.hq0 + h, f.nch, f.ch, f.half) * D + VB * g;
+            float* dst = f.acc + slot_index(f.hq0 + h, f.nch, f.ch, f.half) * D;
+            if constexpr (I4) {  // chunk ch: dims 32 ch + 4g .. + 3; the odd ones were fed as 16x operands
+                const float so1 = so * 0.0625f;
 #pragma unroll
-            for (int gi = 0; gi < NG; ++gi) {
+                for (int ch = 0; ch < NCH; ++ch)
+                    *reinterpret_cast<float4*>(dst + 32 * ch + 4 * g) =
+                        make_float4(acc[2 * ch][e] * so, acc[2 * ch][2 + e] * so1, acc[2 * ch + 1][e] * so,
+                                    acc[2 * ch + 1][2 + e] * so1);
+            } else {  // chunk ch: dims 16 ch + 2g, + 1
 #pragma unroll
-                for (int mm = 0; mm < SPG; mm += 2) {
-                    const int i = SPG * gi + mm;
-                    *reinterpret_cast<float4*>(dst + GS * gi + 2 * mm) =
-                        make_float4(acc[i][e] * so, acc[i][2 + e] * so, acc[i + 1][e] * so, acc[i + 1][2 + e] * so);
-                }
+                for (int ch = 0; ch < NCH; ++ch)
+                    *reinterpret_cast<float2*>(dst + 16 * ch + 2 * g) = make_float2(acc[ch][e] * so, acc[ch][2 + e] * so);
             }
         }
     }
@@ -1761,13 +1879,14 @@ cudaError_t launch_fmt_d(const CUtensorMap& tk, const CUtensorMap& tv, const Dec
         }
     }
     if (!simt) {
-        // The tensor-core consumer's operand rows are (q-head, scale group)
-        // pairs: eight per pass, or sixteen with the 16-row consumer, which
-        // serves kv-heads whose q-heads x groups exceed 8.  Beyond 16 a group
-        // of G q-heads with ng scale groups per row takes ceil(G * ng / 16)
-        // launches over the same tiles, each serving 16 / ng of the heads;
-        // only the first appends the newest rows (the later ones read them
-        // from the cache).
+        // The per-row tensor-core consumer's operand rows are (q-head, scale
+        // group) pairs, eight per pass.  Kv-heads with more pairs take the
+        // grouped consumer (one pass for all G q-heads), except INT4 with
+        // 16-channel groups (head_dim 64): the 16-row consumer serves sixteen
+        // pairs per pass, and a group of G q-heads with ng scale groups per
+        // row takes ceil(G * ng / 16) launches over the same tiles, each
+        // serving 16 / ng of the heads; only the first appends the newest rows
+        // (the later ones read them from the cache).
         const int ng = a.cache.ngroups;
         if (G * ng <= 8) {
             if constexpr (FMT != INT4) {
@@ -1781,13 +1900,15 @@ cudaError_t launch_fmt_d(const CUtensorMap& tk, const CUtensorMap& tv, const Dec
             } else {
                 e = launch_stream<FMT, D, MmaConsumer<FMT, D>>(tk, tv, p, s);
             }
-        } else if (FMT == INT8 && D / ng >= 32) {  // one pass, a scale group per contraction slice
+        } else if (FMT == INT8 || (FMT == INT4 && D / ng >= 32)) {
+            // one pass, a scale group per contraction slice and output m-tile
+            // (groups are whole 16-byte chunks of a row: 16 INT8 or 32 INT4 channels)
             e = cudaErrorInvalidValue;
-            if constexpr (FMT == INT8) {
-                if (ng == 2) e = launch_stream<FMT, D, MmaGroupConsumer<D, 2>>(tk, tv, p, s);
-                else if constexpr (D >= 128) e = launch_stream<FMT, D, MmaGroupConsumer<D, 4>>(tk, tv, p, s);
+            if constexpr (FMT == INT8 || FMT == INT4) {
+                if (ng == 2) e = launch_stream<FMT, D, MmaGroupConsumer<FMT, D, 2>>(tk, tv, p, s);
+                else if constexpr (FMT == INT8 || D >= 128) e = launch_stream<FMT, D, MmaGroupConsumer<FMT, D, 4>>(tk, tv, p, s);
             }
-        } else if constexpr (FMT == INT8 || FMT == INT4) {  // groups: only these formats have them
+        } else if constexpr (FMT == INT4 && D == 64) {
             const int per = 16 / ng;
             for (int h = 0; h < G && e == cudaSuccess; h += per) {
                 p.head_off = h;

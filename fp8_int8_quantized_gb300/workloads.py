@@ -79,6 +79,11 @@ WORKLOADS = {
                                     description="Llama-3-70B shapes with group-quantized INT8: 64/8 heads "
                                                 "x128, batch 256, ctx 32768, block 16, online INT8 with one "
                                                 "scale per 32 channels, 1% outliers x20"),
+    "llama3-70b-int4-g32": Workload("llama3-70b-int4-g32", 256, 64, 8, 128, 16, "int4", 32768, "row",
+                                    outliers=True, seed=1008, quant_group=32,
+                                    description="Llama-3-70B shapes with group-quantized INT4: 64/8 heads "
+                                                "x128, batch 256, ctx 32768, block 16, online INT4 with one "
+                                                "scale per 32 channels, 1% outliers x20"),
     "llama3-70b": Workload("llama3-70b", 256, 64, 8, 128, 16, "e4m3", 32768, "amax",
                            outliers=True, append_chunk=2048, seed=1004,
                            description="Llama-3-70B long context: 64/8 heads x128, batch 256, "

@@ -103,8 +103,8 @@ typedef enum {
  *     four groups of consecutive channels, each quantized as a row is (its own
  *     amax and scale).  Must be 0 for FP8; any other value is INVALID_ARG.
  *     Every entry point takes every group size.  Decode reads the cache once,
- *     except for kv-heads with more than 8 (q-head, scale group) pairs in INT4
- *     or in INT8 with 16-channel groups: those stream it ceil(G * groups / 16)
+ *     except for INT4 kv-heads of head_dim 64 with 16-channel groups and more
+ *     than 8 (q-head, scale group) pairs: those stream it ceil(G * 4 / 16)
  *     times. */
 typedef struct {
     void* k_codes;

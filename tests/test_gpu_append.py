@@ -264,7 +264,7 @@ def test_append_rounding_ties_and_bulk_rows_bit_exact(fmt, group):
 
 
 @pytest.mark.parametrize("name", ["llama2-7b", "llama3-8b", "llama2-13b-int8", "llama2-13b-int4", "llama3-70b",
-                                  "llama2-13b-int4-g32", "llama3-70b-int8-g32"])
+                                  "llama2-13b-int4-g32", "llama3-70b-int8-g32", "llama3-70b-int4-g32"])
 def test_append_full_size_sampled(name):
     """The workloads' own append launches (their full windows), checked on a
     seeded sample of tokens against the oracle."""

@@ -55,10 +55,10 @@ CASES = [
     ("int8", 3, 8, 1, 64, 16, [300, 1, 77], 64),
     ("int8", 2, 3, 3, 64, 16, [200, 45], 16),
     ("int4", 2, 4, 1, 128, 16, [96, 1000], 64),
-    # more than 8 (q-head, group) operand rows: INT8 with groups of 32 or more
-    # channels takes the grouped consumer (one pass, a scale group per
-    # contraction slice); INT4 and 16-channel INT8 groups the 16-row consumer,
-    # one pass up to 16 rows, several launches over the same tiles beyond
+    # more than 8 (q-head, group) operand rows: INT8, and INT4 with groups of
+    # 32 or more channels, take the grouped consumer (one pass, a scale group
+    # per contraction slice and output m-tile); INT4 with 16-channel groups the
+    # 16-row consumer, one pass up to 16 rows, several launches beyond
     ("int8", 2, 16, 2, 128, 32, [500, 64], 32),
     ("int8", 2, 48, 8, 64, 16, [300, 90], 32),
     ("int4", 2, 8, 1, 128, 16, [300, 33], 64),
@@ -68,6 +68,11 @@ CASES = [
     ("int8", 2, 64, 8, 128, 16, [1500, 40], 32),
     ("int4", 2, 32, 8, 64, 16, [600, 31], 32),
     ("int8", 2, 40, 8, 128, 64, [520, 77], 64),
+    ("int4", 2, 64, 8, 128, 16, [1500, 40], 32),
+    ("int4", 2, 12, 4, 128, 32, [400, 77], 32),
+    ("int4", 2, 16, 2, 64, 16, [400, 77], 32),
+    ("int4", 2, 8, 2, 64, 16, [300, 45], 16),
+    ("int8", 2, 40, 8, 64, 32, [300, 90], 16),
 ]
 
 
@@ -106,6 +111,8 @@ SPLIT_CASES = [
     ("int4", 4, 8, 8, 128, 16, [3000, 1500, 64, 4097], 32),
     ("int8", 4, 32, 4, 128, 16, [3000, 1500, 64, 4097], 32),
     ("int8", 4, 20, 4, 128, 16, [3000, 1500, 64, 4097], 64),
+    ("int4", 4, 32, 4, 128, 16, [3000, 1500, 64, 4097], 32),
+    ("int8", 4, 16, 2, 64, 16, [3000, 1500, 64, 4097], 16),
 ]
 
 
@@ -186,7 +193,7 @@ def test_nan_codes_past_the_context_do_not_leak():
 
 
 @pytest.mark.parametrize("fmt,group,hq", [("int8", 0, 4), ("int4", 0, 4), ("int4", 32, 4), ("int8", 32, 16),
-                                          ("int8", 64, 16)])
+                                          ("int8", 64, 16), ("int4", 32, 16), ("int4", 64, 16)])
 def test_nan_scales_past_the_context_do_not_leak(fmt, group, hq):
     """Scale slots of rows past the context that were never written hold NaN
     (the caller's memory is not cleared): the masked tokens' weights stay 0.
@@ -247,7 +254,8 @@ def test_workspace_too_small_and_empty_batch():
                                        ("llama2-13b-int4", [0, 64, 127]),
                                        ("llama2-13b-int4-g32", [0, 50, 127]),
                                        ("llama3-70b", [0, 255]),
-                                       ("llama3-70b-int8-g32", [0, 131, 255])])
+                                       ("llama3-70b-int8-g32", [0, 131, 255]),
+                                       ("llama3-70b-int4-g32", [0, 97, 255])])
 def test_decode_workload_sampled(name, seqs):
     wl = W.WORKLOADS[name]
     dw = DeviceWorkload(wl)

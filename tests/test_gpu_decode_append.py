@@ -91,6 +91,8 @@ CASES = [
     ("int8", 3, 16, 2, 128, 32, [500, 1, 64], 32),
     ("int8", 3, 40, 8, 128, 16, [300, 1, 77], 64),
     ("int4", 2, 8, 1, 64, 16, [129, 48], 16),
+    ("int4", 3, 32, 4, 128, 16, [300, 1, 77], 32),
+    ("int4", 3, 16, 2, 64, 32, [129, 0, 64], 32),
 ]
 
 

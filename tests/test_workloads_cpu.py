@@ -23,6 +23,8 @@ def test_decode_bytes_of_the_fixed_context_workloads():
         # four fp32 scales per (token, kv-head) row of K and of V
         "llama3-70b-int8-g32": 17_179_869_184 + 2 * 256 * 32768 * 8 * 4 * 4 + 2 * 4_194_304 + 256 * 2048 * 4
                                + 256 * 4,
+        "llama3-70b-int4-g32": 8_589_934_592 + 2 * 256 * 32768 * 8 * 4 * 4 + 2 * 4_194_304 + 256 * 2048 * 4
+                               + 256 * 4,
     }
     for name, total in want.items():
         wl = W.WORKLOADS[name]
