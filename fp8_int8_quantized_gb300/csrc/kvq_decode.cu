@@ -391,7 +391,7 @@ struct MmaConsumer {
     static constexpr int DC = D / 4;    // K codes per thread per token row
     static constexpr int KW = I4 ? DC / 8 : DC / 4;   // ... as 32-bit words (== KS for 8-bit codes)
     static constexpr int DV = D / 8;    // V codes per thread per token row
-    static constexpr int VW = I4 ? DV / 8 : DV / 4;
+    static constexpr int VW = DV / 4;   // ... as 32-bit words (8-bit codes; INT4 V is read by ldmatrix.trans)
     static constexpr int MT = D / 16;   // m-tiles of PV (head_dim / 16)
     // Operand rows (q-head, scale group pairs) per pass: 8, or 16 with R16.
     // QK^T's m16 tile has 16 rows; the 8-row consumer fills rows 0-7 (this
@@ -471,8 +471,10 @@ struct MmaConsumer {
     float qk_scale;
     // this lane's byte offsets inside a stage tile (the 128-byte swizzle folded
     // in): K row g at chunks 2c, 2c+1 (row 8+g is 8 rows further), V rows 2c
-    // and 2c+1 at chunk g (rows 8+2c, 9+2c are 8 rows further); INT4 rows
-    // hold the same codes at half the bytes (64-byte swizzle at head_dim 128)
+    // and 2c+1 at chunk g (rows 8+2c, 9+2c are 8 rows further).  INT4 rows
+    // hold the codes at half the bytes (64-byte swizzle at head_dim 128): K row
+    // g at chunk c, and v_off0 / v_off1 are this lane's row addresses for the
+    // two ldmatrix.trans of a box's V
     uint32_t k_off0, k_off1, v_off0, v_off1;
 
     __device__ void init(int G_, float qks, int ng_) {
@@ -595,14 +597,7 @@ struct MmaConsumer {
 
     // V words of a row: the thread's DV contiguous codes at DV*g.
     __device__ __forceinline__ void load_v(uint32_t a, uint32_t (&w)[VW]) {
-        if (I4) {
-            if (D == 128) {
-                const uint2 x = lds64(a);
-                w[0] = x.x; w[VW > 1 ? 1 : 0] = x.y;
-            } else {
-                w[0] = lds32(a);
-            }
-        } else if (D == 128) {
+        if (D == 128) {
             const uint4 x = lds128(a);
             w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
         } else {
@@ -996,7 +991,7 @@ struct MmaConsumer {
 //   weights P * s_V[t][gi] (fp16 hi and residual, two MMAs per m-tile).
 // The 16-row multi-pass alternative read the cache once per 16 (q-head, group)
 // pairs: twice for Llama-3-70B's G = 8 with 32-channel groups.
-template <int FMT, int D, int NG>
+template <int FMT, int D, int NG, bool NARROW = false>
 struct MmaGroupConsumer {
     static constexpr bool I4 = FMT == INT4;
     static constexpr int RB = row_bytes(FMT, D);  // bytes of one cached row
@@ -1012,9 +1007,12 @@ struct MmaGroupConsumer {
     // 8-head query rows take ~21 KB per warp; 206 registers).  INT4 stages are
     // half the bytes and the consumer is bound by instruction issue: one CTA of
     // 16 warps per SM with registers capped at 128 (a few spilled) is 3% faster
-    // than two CTAs of 8 and 7% faster than three of 4 at 168 registers
-    static constexpr int kMinCtas = I4 ? KVQ_GA4_CTAS : kMinBlocks;
-    static constexpr int kWarps = I4 ? KVQ_GA4_WARPS : KVQ_GA_WARPS;
+    // than two CTAs of 8 and 7% faster than three of 4 at 168 registers.
+    // NARROW: INT4 in INT8's 4-warp CTAs, for batches whose context-length
+    // scan leaves no room for 16 warps' stages in one CTA
+    static constexpr bool kWide4 = I4 && !NARROW;
+    static constexpr int kMinCtas = kWide4 ? KVQ_GA4_CTAS : kMinBlocks;
+    static constexpr int kWarps = kWide4 ? KVQ_GA4_WARPS : KVQ_GA_WARPS;
     static constexpr float kUnit = 5.9604644775390625e-08f;      // operand value of one code step (2^-24)
     static constexpr float kBias = (I4 ? 8.f : 128.f) * kUnit;   // K operand - code * kUnit
     static constexpr float kLogF = I4 ? 2.f : 6.f;               // weights carry 2^kLogF (cancels in acc / l)
@@ -1904,9 +1902,22 @@ cudaError_t launch_fmt_d(const CUtensorMap& tk, const CUtensorMap& tv, const Dec
             // one pass, a scale group per contraction slice and output m-tile
             // (groups are whole 16-byte chunks of a row: 16 INT8 or 32 INT4 channels)
             e = cudaErrorInvalidValue;
-            if constexpr (FMT == INT8 || FMT == INT4) {
+            if constexpr (FMT == INT8) {
                 if (ng == 2) e = launch_stream<FMT, D, MmaGroupConsumer<FMT, D, 2>>(tk, tv, p, s);
-                else if constexpr (FMT == INT8 || D >= 128) e = launch_stream<FMT, D, MmaGroupConsumer<FMT, D, 4>>(tk, tv, p, s);
+                else e = launch_stream<FMT, D, MmaGroupConsumer<FMT, D, 4>>(tk, tv, p, s);
+            } else if constexpr (FMT == INT4) {
+                // 16-warp CTAs while their shared memory fits (it grows with the
+                // batch: a fused call with four groups over more than ~3300
+                // sequences does not fit), else 4-warp ones
+                const bool narrow = Layout(KVQ_GA4_WARPS, row_bytes(FMT, D), D, G, a.batch, true, a.k_new != nullptr,
+                                           ng).total + 1024 > 227 * 1024;
+                if (ng == 2) {
+                    e = narrow ? launch_stream<FMT, D, MmaGroupConsumer<FMT, D, 2, true>>(tk, tv, p, s)
+                               : launch_stream<FMT, D, MmaGroupConsumer<FMT, D, 2>>(tk, tv, p, s);
+                } else if constexpr (D >= 128) {
+                    e = narrow ? launch_stream<FMT, D, MmaGroupConsumer<FMT, D, 4, true>>(tk, tv, p, s)
+                               : launch_stream<FMT, D, MmaGroupConsumer<FMT, D, 4>>(tk, tv, p, s);
+                }
             }
         } else if constexpr (FMT == INT4 && D == 64) {
             const int per = 16 / ng;

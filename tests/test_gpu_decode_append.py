@@ -125,6 +125,32 @@ def test_fused_equals_append_then_decode(case, kernel, partition):
     assert e <= ATOL_REL, e
 
 
+def test_fused_grouped_int4_large_batch():
+    """INT4 with four scale groups at G = 8 runs 16-warp CTAs while their
+    shared memory fits.  It grows with the batch (the context-length scan):
+    a fused call over 3400 sequences takes 4-warp CTAs instead, the plain
+    decode of the same batch still the 16-warp ones.  The caches are
+    identical, and both outputs match the oracle on sampled sequences (the
+    two grids split the contexts differently, so the outputs may differ in
+    their last bits)."""
+    B = 3400
+    ctx = [1 + (i * 37) % 96 for i in range(B)]
+    dw = small("int4", B, 8, 1, 128, 16, ctx, seed=11, group=32)
+    g = torch.Generator(device="cpu").manual_seed(77)
+    k_new = (torch.randn((B, 1, 128), generator=g) * 2).to(torch.float16).to(dw.device)
+    v_new = (torch.randn((B, 1, 128), generator=g) * 2).to(torch.float16).to(dw.device)
+    kvq.set_decode_kernel(kvq.KERNEL_AUTO)
+    (c1, o1, st1), (c2, o2, st2) = both_paths(dw, k_new, v_new, dw.block_tables, 0)
+    assert st1[0] == 0 and st2[0] == 0
+    assert_same_cache(c1, c2)
+    dw.cache = c2
+    seqs = [0, 1, 95, 1700, B - 1]
+    ref = dw.oracle_decode(seqs)
+    for o in (o1, o2):
+        assert rel_err(o[seqs].float().cpu().numpy(), ref) <= ATOL_REL
+    assert rel_err(o2.float().cpu().numpy(), o1.float().cpu().numpy().astype(np.float64)) <= ATOL_REL
+
+
 def test_fused_bad_block_id_is_reported_and_not_written():
     dw = small("e4m3", 3, 4, 2, 128, 16, [40, 100, 7], seed=5)
     bt = dw.block_tables.clone()
