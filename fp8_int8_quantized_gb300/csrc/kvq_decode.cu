@@ -221,6 +221,7 @@ struct SimtConsumer {
     static constexpr int PASSES = kBox / TPP;
     static constexpr int kMinCtas = GM == 4 ? 3 : kMinBlocks;  // 4 query rows need more registers
     static constexpr int kWarps = 6;
+    static constexpr bool kQGlobal = false;   // query rows staged in shared memory
     uint32_t qh[GM][8];
     float m[GM], l[GM], acc[GM][16];
     int lane, j, grp, G, ng, gi;   // INT8: ng scales per row; this lane's 16 dims lie in group gi
@@ -418,6 +419,7 @@ struct MmaConsumer {
     // the stages fit: +0.7% on the Llama-3-70B batch; neutral to -0.3% for
     // the smaller groups, which keep two CTAs)
     static constexpr int kWarps = R16 ? KVQ_R16_WARPS : (I4 ? KVQ_INT4_WARPS : (WIDE ? 2 * KVQ_MMA_WARPS : KVQ_MMA_WARPS));
+    static constexpr bool kQGlobal = false;   // query rows staged in shared memory
     // INT8 codes enter the tensor cores as fp16 subnormals, code * 2^-24, and
     // INT4 codes the same, or 16x that where the nibble is left in mantissa
     // bits 4..7 -- the high nibble of a byte is masked in place, which saves
@@ -1013,6 +1015,13 @@ struct MmaGroupConsumer {
     static constexpr bool kWide4 = I4 && !NARROW;
     static constexpr int kMinCtas = kWide4 ? KVQ_GA4_CTAS : kMinBlocks;
     static constexpr int kWarps = kWide4 ? KVQ_GA4_WARPS : KVQ_GA_WARPS;
+    // The query rows are read from global memory when a pair starts (set_q)
+    // instead of being staged in shared memory with its first tile, so a new
+    // pair's first tile need not wait for the previous pair's to be consumed
+    // (+1% on the Llama-3-70B shapes for both formats; the 2 KB per warp this
+    // frees at G = 8 would let three INT8 CTAs fit an SM, which measured 6%
+    // slower than two)
+    static constexpr bool kQGlobal = true;
     static constexpr float kUnit = 5.9604644775390625e-08f;      // operand value of one code step (2^-24)
     static constexpr float kBias = (I4 ? 8.f : 128.f) * kUnit;   // K operand - code * kUnit
     static constexpr float kLogF = I4 ? 2.f : 6.f;               // weights carry 2^kLogF (cancels in acc / l)
@@ -1481,7 +1490,8 @@ __global__ void __launch_bounds__(Consumer::kWarps * 32, Consumer::kMinCtas)
     constexpr int RB = row_bytes(FMT, D);
     const int ng = a.cache.ngroups;
     constexpr int kConsumers = Consumer::kWarps, kThreads = kConsumers * 32;
-    const Layout L(kConsumers, RB, D, G, B, kRowScaled, append, ng);
+    constexpr bool kQGlobal = Consumer::kQGlobal;
+    const Layout L(kConsumers, RB, D, kQGlobal ? 0 : G, B, kRowScaled, append, ng);
     const uint32_t sc_stage = 2 * kTile * 4 * ng;  // bytes of a stage's K and V scales
     int* S = reinterpret_cast<int*>(smem + L.scan);
     int* ctx_s = S + B + 1;
@@ -1561,7 +1571,7 @@ __global__ void __launch_bounds__(Consumer::kWarps * 32, Consumer::kMinCtas)
     const uint64_t pol = policy_evict_first();
     const uint32_t box_tx = 2 * kBox * RB + (kRowScaled ? 2 * kBox * 4 * ng : 0);
     const bool big_box = BS >= kTile;  // a tile lies in one block: one 32-row box per tensor
-    const uint32_t q_tx = G * D * 2;
+    const uint32_t q_tx = kQGlobal ? 0u : (uint32_t)(G * D * 2);
 
     const float s_fp8 = (!kRowScaled && a.scale) ? __ldg(a.scale) : 1.0f;
     const float s_out = kRowScaled ? 1.0f : s_fp8;
@@ -1596,7 +1606,7 @@ __global__ void __launch_bounds__(Consumer::kWarps * 32, Consumer::kMinCtas)
         while (fi < hi && fi - fc < kSpw) {
             const int rel = fi - lo;
             const bool new_pair = iw.t == 0 || rel == 0;
-            if (new_pair && pend >= fc) break;
+            if (!kQGlobal && new_pair && pend >= fc) break;
             const bool ends = append && iw.t == iw.n - 1;
             if (ends && lpend >= fc) break;
             const int id0 = __shfl_sync(0xFFFFFFFFu, idc, (2 * rel) & 31);
@@ -1637,7 +1647,7 @@ __global__ void __launch_bounds__(Consumer::kWarps * 32, Consumer::kMinCtas)
                     bulk_load_u32(dst, (which ? a.cache.v_scales : a.cache.k_scales) + (int64_t)row * ng, sb, fb, pol);
                 }
             }
-            if (new_pair && lane == 8)
+            if (!kQGlobal && new_pair && lane == 8)
                 bulk_load(qbuf, a.q + ((int64_t)iw.b * a.num_q_heads + (int64_t)iw.kvh * Gall + h0) * D, q_tx, fb, pol);
             if (ends && (lane == 9 || lane == 10)) {
                 const int64_t row = ((int64_t)iw.b * Hkv + iw.kvh) * D;
@@ -1664,7 +1674,12 @@ __global__ void __launch_bounds__(Consumer::kWarps * 32, Consumer::kMinCtas)
             failed = true;
             break;
         }
-        if (cw.t == 0 || fc == lo) cons.set_q(reinterpret_cast<const uint16_t*>(qbuf));  // came with this tile
+        if (cw.t == 0 || fc == lo) {  // staged with this tile, or read from global memory
+            if (kQGlobal)
+                cons.set_q(a.q + ((int64_t)cw.b * a.num_q_heads + (int64_t)cw.kvh * Gall + h0) * D);
+            else
+                cons.set_q(reinterpret_cast<const uint16_t*>(qbuf));
+        }
         if (append && cw.t == cw.n - 1)
             append_newest<FMT, D>(nkv, *patch_blk, ctx_s[cw.b] - 1, cw.t * kTile, cw.kvh, a, s_fp8,
                                   tiles_u32 + cst * (2 * L.tile_bytes), L.tile_bytes,
@@ -1839,7 +1854,7 @@ template <int FMT, int D, class Consumer>
 cudaError_t launch_stream(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& a, cudaStream_t s) {
     auto kern = decode_stream_kernel<FMT, D, Consumer>;
     constexpr int kConsumers = Consumer::kWarps, kThreads = kConsumers * 32;
-    const int smem = Layout(kConsumers, row_bytes(FMT, D), D, a.heads, a.batch,
+    const int smem = Layout(kConsumers, row_bytes(FMT, D), D, Consumer::kQGlobal ? 0 : a.heads, a.batch,
                             FMT == INT8 || FMT == INT4, a.k_new != nullptr, a.cache.ngroups).total + 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -1909,7 +1924,7 @@ cudaError_t launch_fmt_d(const CUtensorMap& tk, const CUtensorMap& tv, const Dec
                 // 16-warp CTAs while their shared memory fits (it grows with the
                 // batch: a fused call with four groups over more than ~3300
                 // sequences does not fit), else 4-warp ones
-                const bool narrow = Layout(KVQ_GA4_WARPS, row_bytes(FMT, D), D, G, a.batch, true, a.k_new != nullptr,
+                const bool narrow = Layout(KVQ_GA4_WARPS, row_bytes(FMT, D), D, 0, a.batch, true, a.k_new != nullptr,
                                            ng).total + 1024 > 227 * 1024;
                 if (ng == 2) {
                     e = narrow ? launch_stream<FMT, D, MmaGroupConsumer<FMT, D, 2, true>>(tk, tv, p, s)
