@@ -419,7 +419,11 @@ struct MmaConsumer {
     // the stages fit: +0.7% on the Llama-3-70B batch; neutral to -0.3% for
     // the smaller groups, which keep two CTAs)
     static constexpr int kWarps = R16 ? KVQ_R16_WARPS : (I4 ? KVQ_INT4_WARPS : (WIDE ? 2 * KVQ_MMA_WARPS : KVQ_MMA_WARPS));
-    static constexpr bool kQGlobal = false;   // query rows staged in shared memory
+    // INT8 / INT4 read a pair's query rows from global memory when it starts
+    // (set_q), FP8 has them staged in shared memory with the pair's first
+    // tile: the global reads measured +2% on the Llama-2-13B INT8 and INT4
+    // shapes and -0.4% on FP8's (same box)
+    static constexpr bool kQGlobal = kRowScaled;
     // INT8 codes enter the tensor cores as fp16 subnormals, code * 2^-24, and
     // INT4 codes the same, or 16x that where the nibble is left in mantissa
     // bits 4..7 -- the high nibble of a byte is masked in place, which saves
@@ -1904,7 +1908,8 @@ cudaError_t launch_fmt_d(const CUtensorMap& tk, const CUtensorMap& tv, const Dec
         if (G * ng <= 8) {
             if constexpr (FMT != INT4) {
                 // one CTA of 12 warps per SM for 8-head groups when its shared memory fits
-                const int wide_smem = Layout(2 * KVQ_MMA_WARPS, row_bytes(FMT, D), D, G, a.batch, FMT == INT8,
+                const int wide_smem = Layout(2 * KVQ_MMA_WARPS, row_bytes(FMT, D), D,
+                                             MmaConsumer<FMT, D, false, true>::kQGlobal ? 0 : G, a.batch, FMT == INT8,
                                              a.k_new != nullptr, ng).total + 1024;
                 if (G == 8 && wide_smem <= 227 * 1024)
                     e = launch_stream<FMT, D, MmaConsumer<FMT, D, false, true>>(tk, tv, p, s);
