@@ -87,8 +87,9 @@ enum { kKindSimt = 1, kKindMma = 2 };
 
 // Shared-memory layout of one CTA (bytes from a 1024-aligned base).  Tiles
 // first (1024-aligned for the 128-byte swizzle), then per warp its INT8 row
-// scales, its stage barriers and the query rows of the (sequence, kv-head)
-// pair it is on; when the launch appends the newest tokens, per warp the fp16
+// scales, its stage barriers and (consumers that stage them: G > 0) the
+// query rows of the (sequence, kv-head) pair it is on; when the launch
+// appends the newest tokens, per warp the fp16
 // K and V rows of the token that ends the pending pair and the block id its
 // row goes to; then the scan of tiles per sequence and the clamped context
 // lengths.
