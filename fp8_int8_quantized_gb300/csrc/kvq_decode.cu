@@ -1010,8 +1010,8 @@ struct MmaGroupConsumer {
     static constexpr int NLK = I4 ? 1 : NCH / 4;  // K: ldmatrix per half box (.x4; INT4 at head_dim 64: .x2)
     static constexpr int NLV = NCH / 2;           // V: ldmatrix.x4.trans per box (two chunks each)
     static_assert(CPG >= 1 && GS % (I4 ? 32 : 16) == 0, "groups of whole 16-byte chunks");
-    // INT8: 4 warps per CTA, two CTAs per SM (the stages, group scales and
-    // 8-head query rows take ~21 KB per warp; 206 registers).  INT4 stages are
+    // INT8: 4 warps per CTA, two CTAs per SM (the stages and group scales take
+    // ~17 KB per warp; 206 registers).  INT4 stages are
     // half the bytes and the consumer is bound by instruction issue: one CTA of
     // 16 warps per SM with registers capped at 128 (a few spilled) is 3% faster
     // than two CTAs of 8 and 7% faster than three of 4 at 168 registers.
