@@ -75,3 +75,20 @@ def test_source_hash_ignores_comments_only():
     assert '"a // b /* c */"' in bench.strip_comments(code)
     # the committed traffic figures are keyed by the current decode sources
     assert bench.recorded_traffic("llama2-7b") is not None
+
+
+def test_every_decode_workload_has_traffic_on_the_current_sources():
+    """Each workload the benchmark times (all but the tiny one, which fits in
+    L2) has a DRAM-traffic line captured on the current decode sources, within
+    a few percent above its algorithmic bytes (the excess: the newest rows
+    appended in the launch and the chunk partials written)."""
+    import bench
+    from fp8_int8_quantized_gb300 import workloads as W
+    for name in bench.DEFAULT_STEPS:
+        if name == "tiny":
+            continue
+        t = bench.recorded_traffic(name)
+        assert t is not None, name
+        wl = W.WORKLOADS[name]
+        alg = W.decode_bytes(wl, W.context_lens(wl))["total"]
+        assert 1.0 <= t / alg < 1.03, (name, t / alg)
