@@ -151,6 +151,31 @@ def test_fused_grouped_int4_large_batch():
     assert rel_err(o2.float().cpu().numpy(), o1.float().cpu().numpy().astype(np.float64)) <= ATOL_REL
 
 
+@pytest.mark.parametrize("fmt,group", [("e4m3", 0), ("e5m2", 0), ("int8", 0), ("int4", 0), ("int8", 32),
+                                       ("int4", 32), ("int4", 64)])
+def test_fused_at_the_batch_limit(fmt, group):
+    """4096 sequences (the library's batch limit) of 8 q-heads over one
+    kv-head: every consumer's shared memory, which grows with the batch (the
+    context-length scan), still fits or falls back to a smaller CTA; the fused
+    and the two-call paths leave the same cache, and sampled sequences match
+    the oracle."""
+    B = 4096
+    ctx = [1 + (i * 13) % 40 for i in range(B)]
+    dw = small(fmt, B, 8, 1, 128, 16, ctx, seed=21, group=group)
+    g = torch.Generator(device="cpu").manual_seed(5)
+    k_new = (torch.randn((B, 1, 128), generator=g) * 2).to(torch.float16).to(dw.device)
+    v_new = (torch.randn((B, 1, 128), generator=g) * 2).to(torch.float16).to(dw.device)
+    kvq.set_decode_kernel(kvq.KERNEL_AUTO)
+    (c1, o1, st1), (c2, o2, st2) = both_paths(dw, k_new, v_new, dw.block_tables, 0)
+    assert st1[0] == 0 and st2[0] == 0
+    assert_same_cache(c1, c2)
+    dw.cache = c2
+    seqs = [0, 1, 2047, B - 1]
+    ref = dw.oracle_decode(seqs)
+    for o in (o1, o2):
+        assert rel_err(o[seqs].float().cpu().numpy(), ref) <= ATOL_REL
+
+
 def test_fused_bad_block_id_is_reported_and_not_written():
     dw = small("e4m3", 3, 4, 2, 128, 16, [40, 100, 7], seed=5)
     bt = dw.block_tables.clone()
